@@ -1,0 +1,73 @@
+"""Oracle pins: the split-KV planners (CPU only)."""
+
+import numpy as np
+import pytest
+
+from oracle import plan as op
+from oracle_pins import load_golden
+
+
+def test_dynamic_plan_hand_example():
+    g = load_golden("plan_hand_example.json")["dynamic"]
+    items, cta_ptr, seg_ptr = op.plan_dynamic(g["seq_lens"], g["num_ctas"], g["min_tiles"])
+    assert [list(i) for i in items] == g["items"]
+    assert cta_ptr == g["cta_ptr"]
+    assert seg_ptr == g["seg_ptr"]
+
+
+def test_static_plan_hand_example():
+    g = load_golden("plan_hand_example.json")["static"]
+    items, cta_ptr, seg_ptr, num_ctas = op.plan_static(g["seq_lens"], g["splits"])
+    assert [list(i) for i in items] == g["items"]
+    assert num_ctas == g["num_ctas"]
+    assert seg_ptr == g["seg_ptr"]
+    assert cta_ptr == [min(c, len(items)) for c in range(num_ctas + 1)]
+
+
+def _length_mixes(rng):
+    yield [1, 63, 64, 300]
+    yield [4096] * 32
+    yield [131072] + [4096] * 31
+    yield [0, 5, 0, 64 * 7 + 1]
+    yield [0, 0, 0]
+    yield list(rng.integers(1, 5000, size=50))
+    yield list(np.exp(rng.uniform(np.log(128), np.log(262144), 64)).astype(int))
+
+
+@pytest.mark.parametrize("C", [1, 7, 152, 304, 1000])
+def test_dynamic_plan_covers_and_balances(C):
+    rng = np.random.default_rng(C)
+    for lens in _length_mixes(rng):
+        for min_tiles in (1, 4):
+            items, cta_ptr, seg_ptr = op.plan_dynamic(lens, C, min_tiles)
+            n = op.check_coverage(lens, items, cta_ptr, seg_ptr)
+            B = len(lens)
+            assert n <= C + 8 * B, "capacity bound"
+            T = 8 * sum(op.num_tiles(L) for L in lens)
+            q = max(min_tiles, -(-T // C)) if T else min_tiles
+            per_cta = [sum(items[i][3] - items[i][2] for i in range(cta_ptr[c], cta_ptr[c + 1]))
+                       for c in range(C)]
+            assert sum(per_cta) == T
+            # every unit gets exactly q tiles except the tail ones
+            full = T // q
+            assert per_cta[:full] == [q] * full
+            assert all(x == 0 for x in per_cta[full + 1:])
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 64])
+def test_static_plan_covers(S):
+    rng = np.random.default_rng(S)
+    for lens in _length_mixes(rng):
+        items, cta_ptr, seg_ptr, C = op.plan_static(lens, S)
+        op.check_coverage(lens, items, cta_ptr, seg_ptr)
+        assert len(items) <= C
+        # every segment's chunks differ in size by at most one chunk remainder
+        for s in range(len(lens) * 8):
+            sizes = [items[i][3] - items[i][2] for i in range(seg_ptr[s], seg_ptr[s + 1])]
+            assert len(sizes) <= S
+            if sizes:
+                assert all(x == sizes[0] for x in sizes[:-1]) and sizes[-1] <= sizes[0]
+
+
+def test_tiles_of_ragged_lengths():
+    assert [op.num_tiles(L) for L in (0, 1, 63, 64, 65, 128, 129)] == [0, 1, 1, 1, 2, 2, 3]
