@@ -1,0 +1,476 @@
+"""Benchmark of the GB300 paged GQA decode step.
+
+One step = the whole hot path on one batch: fused RoPE/RMSNorm/KV-write
+prologue -> length-proportional split-KV plan -> paged GQA decode attention
+-> log-sum-exp merge.  The workload is the mixed-length decode batch
+(1 x 131072 + 31 x 4096 tokens, 64 q heads / 8 KV heads, head_dim 128, BF16
+KV in 64-token pages), whose KV (1.06 GB) is larger than L2, so no flush is
+needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-static] [--no-cpu]
+
+Prints ONE JSON line on rank 0.  ``value`` is the KV+Q+O bytes of all ranks'
+batches divided by the max-over-ranks device time of K steps (TB/s);
+``ms_per_step`` is that time per step.  Under torchrun every rank runs its own
+batch (weak scaling: the path shards by sequence with no collective).
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload (the slow baseline), on rank 0 only.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn µs/layer-step & KV-read TB/s vs HBM peak on mixed-length batches"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_traffic.json")
+ATTN_SRC = os.path.join(ROOT, "paged_gqa_decode_rope_gb300", "csrc", "attn.cu")
+
+
+def _parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="mixed")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-static", action="store_true", help="skip the static-schedule comparison")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ clocks ---------
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows[-3:]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------ CPU oracle -----
+
+def _cpu_worker(spec_path):
+    """Run the float64 oracle (prologue + attention of each listed sequence) on
+    the host, one thread.  Each entry of spec["steps"] is a list of sequences;
+    a step stops early once spec["seconds"] (if > 0) of work is done.  Prints
+    per-step bytes, seconds, tokens and sequence counts as JSON."""
+    import pickle
+    from oracle import decode as od
+    with open(spec_path, "rb") as f:
+        spec = pickle.load(f)
+    elem = 2 if spec["kv_dtype"] == 0 else 1
+    res = []
+    for step in spec["steps"]:
+        done_bytes = done_tok = seqs = 0
+        t_total = 0.0
+        for item in step:
+            t0 = time.perf_counter()
+            od.decode_step(item["q"], item["k"], item["v"], [item["L"] - 1], item["qw"], item["kw"],
+                           item["cache"], item["row"][None, :], [item["L"]], [item["L"] - 1],
+                           spec["kv_dtype"], spec["scale"])
+            t_total += time.perf_counter() - t0
+            done_tok += item["L"]
+            done_bytes += item["L"] * 8 * 128 * 2 * elem
+            seqs += 1
+            if 0 < spec["seconds"] <= t_total:
+                break
+        res.append({"bytes": done_bytes, "seconds": t_total, "tokens": done_tok, "seqs": seqs})
+    print(json.dumps(res))
+
+
+def _oracle_item(wl, b, host):
+    import gpu_util as gu
+    L = int(wl.lengths[b])
+    sub, row = gu.seq_view(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
+    q, k, v, qw, kw = host
+    return {"q": q[b:b + 1], "k": k[b:b + 1], "v": v[b:b + 1], "qw": qw, "kw": kw,
+            "cache": sub, "row": row, "L": L}
+
+
+def run_oracle_steps(wl, steps, seconds):
+    """Time the oracle on host cores over ``steps`` (lists of sequence ids)."""
+    import pickle
+    import tempfile
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import gpu_util as gu
+    host = (gu.bf16_host(wl.q), gu.bf16_host(wl.k), gu.bf16_host(wl.v),
+            gu.bf16_host(wl.q_norm_w), gu.bf16_host(wl.k_norm_w))
+    cache = {}
+    spec_steps = []
+    for ids in steps:
+        items = []
+        for b in ids:
+            if int(wl.lengths[b]) == 0:
+                continue
+            if b not in cache:
+                cache[b] = _oracle_item(wl, b, host)
+            items.append(cache[b])
+        spec_steps.append(items)
+    spec = {"steps": spec_steps, "kv_dtype": wl.kv_dtype, "seconds": seconds,
+            "scale": wl.kv_scale.cpu().numpy().astype(np.float64)}
+    with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
+        pickle.dump(spec, f)
+        path = f.name
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", path],
+                             capture_output=True, text=True, env=env, timeout=900)
+    finally:
+        os.unlink(path)
+    if out.returncode != 0:
+        raise RuntimeError("oracle worker failed: " + out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle on a bounded, seeded random sample of the workload's
+    sequences, about ``seconds`` of single-thread CPU work."""
+    order = np.random.default_rng(123).permutation(wl.batch).tolist()
+    picked, est = [], 0
+    for b in order:                  # enough sequences for the time budget
+        picked.append(b)
+        est += int(wl.lengths[b])
+        if est > 400000:
+            break
+    return run_oracle_steps(wl, [picked], seconds)[0]
+
+
+# ------------------------------------------------------------ helpers --------
+
+def _load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _traffic_record():
+    """Per-launch DRAM bytes of the attention kernel from the committed ncu
+    summary, if it was taken on the current attn.cu; else None."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    with open(ATTN_SRC, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    if rec.get("attn_cu_sha256") != h:
+        return None
+    return rec
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ reference ------
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = Workload(args.workload, seed=args.seed, device=dev)
+    # each step: the oracle on one bounded slice of the workload, one sequence
+    # of at most 8192 tokens, round-robin (float64, one thread)
+    short = [b for b in range(wl.batch) if 0 < wl.lengths[b] <= 8192] or [int(np.argmin(wl.lengths))]
+    steps = [[short[s % len(short)]] for s in range(args.warmup + args.steps)]
+    res = run_oracle_steps(wl, steps, 0.0)[args.warmup:]
+    t = sum(r["seconds"] for r in res)
+    value = sum(r["bytes"] for r in res) / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload + ": " + _describe(wl),
+                       "sample": "one sequence of <= 8192 tokens per step"},
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one <=8192-token sequence per step, prologue + attention"},
+            "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------ ours -----------
+
+def run_ours(args):
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from paged_gqa_decode_rope_gb300.build import build_library
+    build_library()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+
+    wl = Workload(args.workload, seed=args.seed + rank)
+    cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+    stream = torch.cuda.current_stream()
+    algo_bytes = wl.kv_bytes() + wl.qo_bytes()
+
+    def one_step(ev=None):
+        ops.rope_norm_kvwrite(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w,
+                              wl.cache, wl.kv_dtype, wl.slot_mapping, wl.kv_scale, step.q_out,
+                              step.status)
+        step.plan_step(wl.seq_lens)
+        if ev is not None:
+            ev[0].record(stream)
+        ops.decode_attn(step.q_out, wl.cache, wl.kv_dtype, wl.kv_scale, wl.block_table,
+                        wl.seq_lens, step.plan, step.partial_o, step.partial_lse, step.status)
+        if ev is not None:
+            ev[1].record(stream)
+        ops.merge(step.partial_o, step.partial_lse, step.plan, step.out)
+
+    for _ in range(max(3, args.warmup)):
+        one_step()
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError("device status %d during warm-up" % int(step.status.item()))
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for s in range(args.steps):
+        one_step(attn_ev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if ws > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    if int(step.status.item()) != 0:
+        raise RuntimeError("device status %d during timing" % int(step.status.item()))
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(wall0, wall1)
+    # max over ranks
+    if ws > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = ws * algo_bytes * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the four calls, D2H of the output
+    host_in = {n: getattr(wl, n).cpu().pin_memory() for n in
+               ("q", "k", "v", "positions", "slot_mapping", "seq_lens", "block_table")}
+    dev_in = {n: getattr(wl, n) for n in host_in}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    out_host = torch.empty_like(step.out, device="cpu").pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(10, min(args.steps, 500))
+
+    def e2e_step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        out = step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
+                   wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = ws * algo_bytes / (e2e_ms * 1e-3) / 1e12
+
+    # dynamic vs static equal split on the same kernels (attention + merge)
+    sched = None
+    if rank == 0 and not args.no_static:
+        sched = schedule_comparison(ops, wl, stream)
+
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+
+    peak_gbs, peak_kind = _load_peaks()
+    achieved_gbs = algo_bytes / (attn_ms * 1e-3) / 1e9
+    rec = _traffic_record()
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak_gbs, "unit": "GB/s",
+                "frac": round(achieved_gbs / peak_gbs, 4),
+                "traffic": rec["bytes_per_launch"] if rec else None,
+                "peak_kind": peak_kind, "kernel": "decode_attn_kernel<bf16>" if wl.kv_dtype == 0 else "decode_attn_kernel<fp8>",
+                "algorithmic_bytes_per_launch": algo_bytes, "attn_us": round(attn_ms * 1e3, 2),
+                "frac_of_8TBps": round(achieved_gbs / 8000.0, 4)}
+    cpu = None
+    if ws == 1 and not args.no_cpu:
+        r = cpu_baseline(wl, args.cpu_seconds)
+        cpu_tbps = r["bytes"] / r["seconds"] / 1e12
+        cpu = {"value": cpu_tbps, "unit": "TB/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d sequences (%d tokens), float64 prologue + attention, one thread"
+                         % (r["seqs"], wl.batch, r["tokens"]),
+               "seconds": round(r["seconds"], 2),
+               "us_per_layer_step_extrapolated": round(wl.kv_bytes() / (r["bytes"] / r["seconds"]) * 1e6, 1)}
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == 0 else "fp8_e4m3",
+        "data": "synthetic (seeded N(0,1) q/k/v and history, random page permutation, NaN-filled unused slots)",
+        "config": {"workload": args.workload + ": " + _describe(wl), "global_batch": wl.batch * ws,
+                   "tokens": wl.tokens, "kv_bytes": wl.kv_bytes(), "l2": "inputs larger than L2 (no flush)",
+                   "step": "prologue + plan + attn + merge", "parallelism": "dp%d (sequences per GPU)" % ws},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "schedules": sched,
+    }
+    print(json.dumps(line))
+
+
+def _describe(wl):
+    L = wl.lengths
+    kv = "BF16" if wl.kv_dtype == 0 else "FP8-E4M3"
+    if len(set(L.tolist())) <= 2:
+        parts = []
+        for x in sorted(set(L.tolist()), reverse=True):
+            parts.append("%dx%d" % (int((L == x).sum()), x))
+        return " + ".join(parts) + " tokens, 64q/8kv, d128, %s KV, 64-token pages" % kv
+    return "%d seqs, %d tokens, 64q/8kv, d128, %s KV, 64-token pages" % (wl.batch, wl.tokens, kv)
+
+
+def schedule_comparison(ops, wl, stream):
+    """Attention + merge under the dynamic plan and static equal splits."""
+    import torch
+
+    def time_step(step, reps=30):
+        step.plan_step(wl.seq_lens)
+        for _ in range(5):
+            step.attend(step_q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            step.attend(step_q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        return a.elapsed_time(b) / reps * 1e3
+
+    step_q = wl.q
+    dyn = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+    t_dyn = time_step(dyn)
+    n_ctas = ops.num_ctas(wl.kv_dtype)
+    heuristic = max(1, -(-n_ctas // (wl.batch * 8)))
+    sweep = {}
+    for S in sorted({1, 2, 4, 8, 16, 32, 64, heuristic}):
+        st = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=("static", S))
+        sweep[S] = round(time_step(st), 2)
+        del st
+    best_S = min(sweep, key=sweep.get)
+    return {"unit": "us (attn + merge)", "dynamic": round(t_dyn, 2),
+            "static_heuristic_splits": heuristic, "static_heuristic": sweep[heuristic],
+            "static_best_splits": best_S, "static_best": sweep[best_S],
+            "speedup_vs_heuristic": round(sweep[heuristic] / t_dyn, 3),
+            "speedup_vs_best_static": round(sweep[best_S] / t_dyn, 3),
+            "static_sweep": {str(k): v for k, v in sweep.items()}}
+
+
+def main():
+    args = _parse()
+    if args.cpu_worker:
+        _cpu_worker(args.cpu_worker)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * hpc_decode.h -- C ABI of the GB300 (sm_103a) paged GQA decode step.
+ *
+ * One decode step of an attention layer with 64 query heads, 8 KV heads and
+ * head_dim 128 over a paged KV cache of 64-token blocks, in four calls:
+ *
+ *   1. hpc_rope_norm_kvwrite  fused prologue: RoPE -> per-head QK RMSNorm ->
+ *                             BF16 q output + K/V write into the paged cache
+ *   2. hpc_decode_plan        per-step split-KV plan dealing 64-token tiles to
+ *                             CTAs in proportion to each sequence's length
+ *   3. hpc_decode_attn        split-KV paged GQA decode attention -> partials
+ *   4. hpc_merge              log-sum-exp merge of the partials -> BF16 output
+ *
+ * Sources: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper" (24-ai.news, 2026-07-06), intro of "Two new HPC backends in the vLLM
+ * ecosystem" (model shape) and "Why does dynamic scheduling matter for
+ * attention?" (static split-KV, the per-step length-proportional scheduler of
+ * 64-token tiles, the fused RoPE / QK-Norm / KV-write prologue, BF16 and FP8);
+ * page "[vllm] Introducing the HPC-Ops attention backend" (analysis of vLLM PR
+ * #46020), "Code analysis" section 2 (a fused custom op that writes into a
+ * caller-provided output and enters CUDA directly, which keeps it usable
+ * inside CUDA graphs).
+ *
+ * Conventions for every call below:
+ *   - Pointers marked (device) are device pointers; the caller owns all
+ *     memory.  The library never allocates, frees or synchronises; every call
+ *     enqueues its kernel(s) on `stream` and returns.  Kernel arguments are
+ *     passed by value, so the calls can be captured in a CUDA graph, provided
+ *     one call of each kind was made on the device before capture (the first
+ *     call sets a kernel attribute and resolves a driver entry point).
+ *   - Tensors are dense row-major with the shapes given.  "bf16" buffers hold
+ *     IEEE bfloat16 bit patterns (uint16); "e4m3" buffers hold OCP FP8 E4M3
+ *     codes (uint8).
+ *   - The return value reports host-side argument checks and launch errors
+ *     only: HPC_OK, HPC_ERR_INVALID_ARG (null pointer, negative or
+ *     inconsistent size), HPC_ERR_UNSUPPORTED (a size beyond a stated limit,
+ *     an unknown dtype), HPC_ERR_CUDA (a CUDA runtime error at launch; the
+ *     error is left for cudaGetLastError to report).
+ *   - Bad indices found on the device (a block id, a slot, a position, a
+ *     length out of range, a plan that does not fit its buffers) never trap:
+ *     the kernel ORs a HPC_STATUS_* bit into *status (device int32, zeroed by
+ *     the caller), skips the offending item, and the step completes.
+ */
+#ifndef HPC_DECODE_H
+#define HPC_DECODE_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HPC_NUM_Q_HEADS 64
+#define HPC_NUM_KV_HEADS 8
+#define HPC_HEAD_DIM 128
+#define HPC_PAGE_TOKENS 64
+#define HPC_MAX_BATCH 8192          /* planner limit on the batch size */
+#define HPC_MAX_NUM_BLOCKS 2097151  /* cache blocks addressable by the TMA map */
+
+typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
+
+enum {
+  HPC_OK = 0,
+  HPC_ERR_INVALID_ARG = -1,
+  HPC_ERR_UNSUPPORTED = -2,
+  HPC_ERR_CUDA = -3
+};
+
+/* Bits a kernel ORs into *status. */
+enum {
+  HPC_STATUS_BAD_BLOCK = 1,      /* block_table entry outside [0, num_blocks) */
+  HPC_STATUS_BAD_SLOT = 2,       /* slot_mapping entry >= num_blocks * 64 */
+  HPC_STATUS_BAD_SEQ_LEN = 4,    /* seq_len < 0 or > max_blocks * 64 */
+  HPC_STATUS_BAD_POSITION = 8,   /* position outside [0, max_pos) */
+  HPC_STATUS_PLAN_OVERFLOW = 16, /* the plan needs more items than capacity */
+  HPC_STATUS_WAIT_TIMEOUT = 32,  /* a pipeline wait ran out its time limit */
+  HPC_STATUS_BAD_PLAN = 64       /* a work item that does not fit the batch */
+};
+
+/* One work item: KV head `kv_head` of sequence `seq`, 64-token tiles
+ * [tile_begin, tile_end) (tile t holds tokens 64t .. 64t+63). */
+typedef struct {
+  int32_t seq;
+  int32_t kv_head;
+  int32_t tile_begin;
+  int32_t tile_end;
+} hpc_work_item;
+
+/* A split-KV plan.  The struct itself lives in host memory; its arrays are
+ * device buffers owned by the caller:
+ *   items    [capacity]        work items, ordered by CTA, then by
+ *                              (seq, kv_head, tile): the items of one
+ *                              (seq, kv_head) segment are contiguous
+ *   cta_ptr  [num_ctas + 1]    CTA c runs items cta_ptr[c] .. cta_ptr[c+1]-1
+ *   seg_ptr  [batch * 8 + 1]   segment s = seq*8 + kv_head owns items
+ *                              seg_ptr[s] .. seg_ptr[s+1]-1
+ * num_ctas is the grid of hpc_decode_attn; for the length-proportional plan
+ * use hpc_decode_num_ctas().  A length-proportional plan needs
+ * capacity >= num_ctas + 8 * batch (hpc_plan_capacity). */
+typedef struct {
+  hpc_work_item* items;
+  int32_t* cta_ptr;
+  int32_t* seg_ptr;
+  int32_t capacity;
+  int32_t num_ctas;
+} hpc_plan;
+
+/* Fill the RoPE table cos_sin[pos][i] = cos(pos * theta^(-2i/128)) for
+ * i < 64 and cos_sin[pos][64 + i] = sin(same angle), pos in [0, max_pos).
+ * The angle and its sine and cosine are formed in float64 and rounded to
+ * float32.
+ *   cos_sin  (device) float32 [max_pos, 128], written.
+ * Errors: HPC_ERR_INVALID_ARG if cos_sin is null, max_pos <= 0 or theta <= 0. */
+int hpc_rope_cos_sin_cache(double theta, int32_t max_pos, float* cos_sin, cudaStream_t stream);
+
+/* Fused prologue, one pass per sequence b in [0, batch):
+ *   q'  = RMSNorm(RoPE(q[b], positions[b]), q_norm_w)   for each of 64 heads
+ *   k'  = RMSNorm(RoPE(k[b], positions[b]), k_norm_w)   for each of 8 heads
+ *   q_out[b] = bf16(q')                  (round to nearest even)
+ *   cache K/V at slot_mapping[b] = k', v[b]  (bf16 RNE, or e4m3 of x / scale,
+ *                                        round to nearest even, saturating)
+ * RoPE is the NeoX half rotation: element i pairs with i + 64 and turns by the
+ * table angle of cos_sin[positions[b]].  RMSNorm: x / sqrt(mean(x^2) + eps) * w,
+ * in float32.  v gets neither RoPE nor the norm.
+ *   q             (device) bf16 [batch, 64, 128]
+ *   k, v          (device) bf16 [batch, 8, 128]
+ *   positions     (device) int32 [batch]
+ *   cos_sin       (device) float32 [max_pos, 128] (hpc_rope_cos_sin_cache)
+ *   q_norm_w, k_norm_w (device) bf16 [128]
+ *   kv_cache      (device) [num_blocks][2 (K, V)][8][64][128] of bf16 or e4m3;
+ *                 only the slots named by slot_mapping are written
+ *   slot_mapping  (device) int64 [batch]; slot = block * 64 + offset; a
+ *                 negative slot skips the cache write of that sequence
+ *   kv_scale      (device) float32 [2] = {k_scale, v_scale}; required for
+ *                 e4m3, ignored (may be NULL) for bf16
+ *   q_out         (device) bf16 [batch, 64, 128]; may alias q
+ *   status        (device) int32; BAD_POSITION skips the sequence entirely,
+ *                 BAD_SLOT skips its cache write
+ * Errors: HPC_ERR_INVALID_ARG for a null required pointer, batch < 0,
+ * max_pos <= 0 or num_blocks <= 0; HPC_ERR_UNSUPPORTED for an unknown dtype. */
+int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
+                          const int32_t* positions, const float* cos_sin, int32_t max_pos,
+                          const void* q_norm_w, const void* k_norm_w, float eps,
+                          void* kv_cache, int32_t kv_dtype, int32_t num_blocks,
+                          const int64_t* slot_mapping, const float* kv_scale,
+                          void* q_out, int32_t batch, int32_t* status, cudaStream_t stream);
+
+/* Length-proportional split-KV plan (one CTA, on the device).
+ * With n_b = ceil(seq_lens[b] / 64) tiles per (b, kv_head) and
+ * T = 8 * sum_b n_b, every CTA c < num_ctas owns the flat tile range
+ * [c*q, min((c+1)*q, T)) of the (seq, kv_head, tile) order, where
+ * q = max(min_tiles, ceil(T / num_ctas)); its work items are that range cut
+ * at (seq, kv_head) boundaries.  Writes plan->items, cta_ptr, seg_ptr.
+ *   seq_lens   (device) int32 [batch], tokens per sequence including the new
+ *              one; 0 is an empty sequence; < 0 or > max_blocks * 64 sets
+ *              BAD_SEQ_LEN and the sequence is treated as empty
+ *   plan       (host) plan->num_ctas and capacity set by the caller; if the
+ *              items do not fit, PLAN_OVERFLOW is set and the plan is empty
+ * Errors: HPC_ERR_INVALID_ARG for null pointers, batch < 0, max_blocks < 1,
+ * min_tiles < 1 or num_ctas < 1; HPC_ERR_UNSUPPORTED for batch > 8192. */
+int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
+                    int32_t min_tiles, hpc_plan* plan, int32_t* status, cudaStream_t stream);
+
+/* Static equal-split plan, the comparator of hpc_decode_plan: every
+ * (seq, kv_head) is cut into `splits` chunks of ceil(n_b / splits) tiles
+ * whatever its length, one chunk per CTA (item c runs on CTA c).
+ * Requires plan->num_ctas == batch * 8 * splits and capacity >= num_ctas.
+ * Same buffers, status bits and errors as hpc_decode_plan. */
+int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
+                           int32_t splits, hpc_plan* plan, int32_t* status, cudaStream_t stream);
+
+/* Split-KV paged GQA decode attention.  For every work item i =
+ * (b, h, t0, t1) and each of the 8 query heads j = 8h .. 8h+7:
+ *   s_t   = sm_scale * k_scale * q[b][j] . K[b][h][t]   for tokens t in tiles
+ *           [t0, t1) with t < seq_lens[b]
+ *   partial_o[i][j - 8h]   = v_scale * sum_t softmax(s)_t V[b][h][t]
+ *   partial_lse[i][j - 8h] = log(sum_t exp(s_t))        (natural log)
+ * Each 64-token K and V page is read from HBM once for all 8 query heads.
+ *   q            (device) bf16 [batch, 64, 128] (q_out of the prologue)
+ *   kv_cache     (device) as in hpc_rope_norm_kvwrite, 16-byte aligned
+ *   kv_scale     (device) float32 [2]; required for e4m3, ignored for bf16
+ *   block_table  (device) int32 [batch, max_blocks]; entry [b][t] is the cache
+ *                block of tile t of sequence b (BAD_BLOCK if out of range:
+ *                the tile is skipped)
+ *   seq_lens     (device) int32 [batch]
+ *   plan         (host) plan written by hpc_decode_plan / _static for the same
+ *                seq_lens; its num_ctas is the grid
+ *   partial_o    (device) float32 [plan->capacity, 8, 128], written per item
+ *   partial_lse  (device) float32 [plan->capacity, 8], written per item
+ * Errors: HPC_ERR_INVALID_ARG for null pointers or bad sizes;
+ * HPC_ERR_UNSUPPORTED for num_blocks > HPC_MAX_NUM_BLOCKS or unknown dtype. */
+int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, const float* kv_scale,
+                    int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,
+                    const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
+                    float* partial_o, float* partial_lse, float sm_scale,
+                    int32_t* status, cudaStream_t stream);
+
+/* Log-sum-exp merge: for each segment s = b*8 + h with items K_s =
+ * seg_ptr[s] .. seg_ptr[s+1]-1, in item order,
+ *   M = max_k lse_k,  w_k = exp(lse_k - M),
+ *   out[b][8h + r] = bf16( sum_k w_k partial_o[k][r] / sum_k w_k )
+ * A segment with no items (an empty sequence) gets zeros.
+ *   out  (device) bf16 [batch, 64, 128], written.
+ * Errors: HPC_ERR_INVALID_ARG for null pointers or batch < 0. */
+int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+              int32_t batch, void* out, cudaStream_t stream);
+
+/* Persistent grid of hpc_decode_attn on the current device (SM count times
+ * resident CTAs per SM) for the given KV dtype: the num_ctas to plan for. */
+int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
+
+/* Items a length-proportional plan may need: num_ctas + 8 * batch. */
+int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HPC_DECODE_H */

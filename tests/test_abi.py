@@ -1,0 +1,80 @@
+"""The C-ABI library loads and exports every symbol include/hpc_decode.h
+declares; host-side argument checks work without a GPU (no kernel runs)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hpc_decode.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:int|int32_t)\s+(hpc_\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_gqa_decode_rope_gb300.build import build_library
+    build_library()
+    from paged_gqa_decode_rope_gb300 import _lib
+    return _lib.lib()
+
+
+def test_header_declares_the_four_calls():
+    names = header_functions()
+    for n in ("hpc_rope_norm_kvwrite", "hpc_decode_plan", "hpc_decode_attn", "hpc_merge"):
+        assert n in names
+
+
+def test_binding_covers_the_header():
+    from paged_gqa_decode_rope_gb300 import _lib
+    assert set(header_functions()) == set(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_argument_checks(lib):
+    from paged_gqa_decode_rope_gb300._lib import Plan, HPC_ERR_INVALID_ARG, HPC_ERR_UNSUPPORTED
+    NULL = None
+    fake = ctypes.c_void_p(4096)       # never dereferenced on the host
+    assert lib.hpc_plan_capacity(32, 152) == 152 + 256
+    assert lib.hpc_rope_cos_sin_cache(1e6, 0, fake, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_rope_cos_sin_cache(1e6, 10, NULL, NULL) == HPC_ERR_INVALID_ARG
+    # unknown KV dtype, null pointers, negative batch
+    args = [fake] * 5 + [16, fake, fake, 1e-6, fake, 7, 4, fake, fake, fake, 1, fake, NULL]
+    assert lib.hpc_rope_norm_kvwrite(*args) == HPC_ERR_UNSUPPORTED
+    args[10] = 0
+    args[0] = NULL
+    assert lib.hpc_rope_norm_kvwrite(*args) == HPC_ERR_INVALID_ARG
+    args[0] = fake
+    args[15] = -1
+    assert lib.hpc_rope_norm_kvwrite(*args) == HPC_ERR_INVALID_ARG
+    args[15] = 0
+    assert lib.hpc_rope_norm_kvwrite(*args) == 0          # empty batch: nothing to launch
+    plan = Plan(4096, 4096, 4096, 100, 10)
+    st = fake
+    assert lib.hpc_decode_plan(fake, 4, 8, 0, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_plan(fake, 9000, 8, 1, ctypes.byref(plan), st, NULL) == HPC_ERR_UNSUPPORTED
+    assert lib.hpc_decode_plan(NULL, 4, 8, 1, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    # static plan: num_ctas must be batch * 8 * splits
+    assert lib.hpc_decode_plan_static(fake, 4, 8, 2, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    # attention: misaligned cache, too many blocks, unknown dtype
+    a = [fake, ctypes.c_void_p(4097), 0, fake, 100, fake, 8, fake, 4, ctypes.byref(plan),
+         fake, fake, 0.088, st, NULL]
+    assert lib.hpc_decode_attn(*a) == HPC_ERR_INVALID_ARG
+    a[1] = fake
+    a[4] = 1 << 22
+    assert lib.hpc_decode_attn(*a) == HPC_ERR_UNSUPPORTED
+    a[4] = 100
+    a[2] = 3
+    assert lib.hpc_decode_attn(*a) == HPC_ERR_UNSUPPORTED
+    assert lib.hpc_merge(NULL, fake, ctypes.byref(plan), 4, fake, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_merge(fake, fake, ctypes.byref(plan), 0, fake, NULL) == 0

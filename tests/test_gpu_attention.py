@@ -1,0 +1,142 @@
+"""GPU split-KV decode attention + merge vs the float64 oracle.
+
+Every workload runs at its full size in the launch configuration the
+benchmark uses (persistent grid, length-proportional plan); the oracle
+recomputes sampled output rows one by one from host copies of the same cache
+pages.  Unused cache entries are NaN, so any read past a sequence's length or
+any 0 * NaN in the PV product shows up as a non-finite output.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as od
+from oracle import numerics as nx
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, schedule="dynamic", n_ctas=None, min_tiles=1):
+    from paged_gqa_decode_rope_gb300 import ops
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=schedule,
+                          n_ctas=n_ctas, min_tiles=min_tiles)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    return out.clone(), int(step.status.item())
+
+
+def _sample(wl, k=3, seed=0):
+    L = wl.lengths
+    rng = np.random.default_rng(seed)
+    picks = {int(np.argmax(L)), int(np.argmin(L))}
+    picks |= set(rng.choice(len(L), size=min(k, len(L)), replace=False).tolist())
+    return sorted(picks)
+
+
+def _tol(wl):
+    return (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if wl.kv_dtype == od.KV_BF16 else (gu.TOL_FP8_MAX, None)
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform", "mixed", "mixed_fp8", "heavy_tail"])
+def test_attention_matches_oracle(name):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload(name, seed=0, include_new_token=True)
+    out, st = _run(wl)
+    assert st == 0, st
+    got = gu.bf16_host(out)
+    seqs = list(range(wl.batch)) if name == "tiny" else _sample(wl)
+    for b in seqs:
+        heads = None if wl.lengths[b] <= 65536 else list(range(0, 64, 9))   # one per KV head
+        want = gu.oracle_outputs(wl, wl.q, [b], heads=heads)[0]
+        mx, mean = gu.compare(got[b], want, *_tol(wl), label="%s seq %d (L=%d)" % (name, b, wl.lengths[b]))
+    assert np.all(np.isfinite(got)), "NaN/inf in outputs (read past a length?)"
+
+
+@pytest.mark.parametrize("lengths", [
+    [1], [63], [64], [65], [0, 1, 0], [129, 1, 2, 3, 640, 641, 639],
+    list(np.random.default_rng(9).integers(1, 300, 1024)),
+])
+@pytest.mark.parametrize("kv", [0, 1])
+def test_attention_edge_lengths(lengths, kv):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=11, lengths=lengths, kv_dtype=kv, include_new_token=True)
+    out, st = _run(wl)
+    assert st == 0
+    got = gu.bf16_host(out)
+    seqs = range(wl.batch) if wl.batch <= 16 else _sample(wl, k=12)
+    want = gu.oracle_outputs(wl, wl.q, list(seqs))
+    for i, b in enumerate(seqs):
+        if wl.lengths[b] == 0:
+            assert np.all(got[b] == 0.0), "an empty sequence gives zeros"
+        else:
+            gu.compare(got[b], want[i], *_tol(wl), label="L=%d" % wl.lengths[b])
+
+
+@pytest.mark.parametrize("name", ["mixed", "mixed_fp8"])
+def test_schedules_agree_and_are_deterministic(name):
+    """Static and dynamic plans, any grid, any quota: the same attention up to
+    float32 reordering; the same plan twice: bit-identical output."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload(name, seed=1, include_new_token=True)
+    ref, st = _run(wl)
+    again, st2 = _run(wl)
+    assert st == 0 and st2 == 0
+    assert torch.equal(ref.view(torch.int16), again.view(torch.int16)), "run-to-run bit-identical"
+    r = ref.float()
+    for schedule, n_ctas, mt in ((("static", 1), None, 1), (("static", 8), None, 1),
+                                 ("dynamic", 7, 1), ("dynamic", 304, 1), ("dynamic", None, 64)):
+        out, st = _run(wl, schedule, n_ctas, mt)
+        assert st == 0
+        d = (out.float() - r).abs()
+        # two bf16 roundings of values that differ only by float32 reordering
+        tol = 2.0 ** -7 * r.abs() + 1e-5
+        assert bool((d <= tol).all()), (schedule, n_ctas, mt, float(d.max()))
+
+
+def test_fp8_against_oracle_quantised_history():
+    """Second, independent FP8 check: the oracle quantises the unquantised
+    history itself (its own E4M3 encoder) and attends over those values."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload, history_values
+    wl = Workload("mixed_fp8", seed=2, include_new_token=True)
+    out, st = _run(wl)
+    assert st == 0
+    got = gu.bf16_host(out)
+    scale = wl.kv_scale.cpu().numpy().astype(np.float64)
+    for b in (0, 17):
+        L = int(wl.lengths[b])
+        n = -(-L // 64)
+        sub = np.full((n, 2, 8, 64, 128), 0x7F, np.uint8)
+        for w in (0, 1):
+            x = history_values(b, L, w, seed=2).cpu().numpy().astype(np.float64)   # [n*64, 8, 128]
+            codes = od.encode_kv(np.nan_to_num(x[:L]), od.KV_FP8, scale[w])
+            pad = np.full((n * 64, 8, 128), 0x7F, np.uint8)
+            pad[:L] = codes
+            sub[:, w] = pad.reshape(n, 64, 8, 128).transpose(0, 2, 1, 3)
+        gpu_raw, _ = gu.seq_view(wl.cache, wl.block_table_np[b], L, od.KV_FP8)
+        diff = np.count_nonzero(gpu_raw[:, :, :, :, :][..., :] != sub)
+        assert diff <= max(8, sub.size // 10000), "history codes differ at %d places" % diff
+        heads = list(range(0, 64, 9)) if L > 65536 else None
+        q = gu.bf16_host(wl.q)[b]
+        want = od.decode_attention(q, sub, np.arange(n), L, od.KV_FP8, scale[0], scale[1], heads=heads)
+        gu.compare(got[b], want, gu.TOL_FP8_MAX, label="seq %d" % b)
+
+
+def test_bad_block_is_reported_and_skipped():
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=5, lengths=[300, 200, 100], kv_dtype=0, include_new_token=True)
+    wl.block_table[1, 2] = wl.num_blocks + 5          # tile 2 of sequence 1 points past the cache
+    out, st = _run(wl)
+    assert st & 1, "BAD_BLOCK"
+    got = gu.bf16_host(out)
+    want = gu.oracle_outputs(wl, wl.q, [0, 2])
+    gu.compare(got[0], want[0], *_tol(wl))
+    gu.compare(got[2], want[1], *_tol(wl))
+    assert np.all(np.isfinite(got[1]))

@@ -1,0 +1,97 @@
+"""GPU planner vs the oracle planner: bit-exact work lists and coverage."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import plan as op
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _mixes():
+    rng = np.random.default_rng(5)
+    yield [1, 63, 64, 300]
+    yield [4096] * 32
+    yield [131072] + [4096] * 31
+    yield [0, 5, 0, 64 * 7 + 1]
+    yield [0, 0, 0]
+    yield [65, 1]
+    yield list(rng.integers(1, 5000, size=50))
+    yield list(np.floor(np.exp(rng.uniform(np.log(128), np.log(262144), 64))).astype(int))
+    yield list(rng.integers(0, 200, size=3000))            # many sequences, > 1 per thread
+
+
+def _run_dynamic(lens, C, min_tiles, capacity=None):
+    from paged_gqa_decode_rope_gb300 import ops
+    B = len(lens)
+    max_blocks = max(1, max(-(-L // 64) for L in lens))
+    plan = ops.DecodePlan(B, C, C + 8 * B if capacity is None else capacity, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.decode_plan(torch.tensor(lens, dtype=torch.int32, device="cuda"), max_blocks, plan,
+                    status, min_tiles)
+    torch.cuda.synchronize()
+    return plan, int(status.item())
+
+
+def _host(plan, n_items):
+    items = [tuple(x) for x in plan.items[:n_items].cpu().tolist()]
+    return items, plan.cta_ptr.cpu().tolist(), plan.seg_ptr.cpu().tolist()
+
+
+@pytest.mark.parametrize("C", [1, 7, 152, 304, 1000])
+def test_dynamic_plan_bit_exact(C):
+    gu.require_gpu()
+    for lens in _mixes():
+        for min_tiles in (1, 4):
+            plan, st = _run_dynamic(lens, C, min_tiles)
+            assert st == 0
+            want = op.plan_dynamic(lens, C, min_tiles)
+            got = _host(plan, len(want[0]))
+            assert got[1] == want[1], "cta_ptr"
+            assert got[2] == want[2], "seg_ptr"
+            assert got[0] == [tuple(i) for i in want[0]], "items"
+            op.check_coverage(lens, *got)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 64])
+def test_static_plan_bit_exact(S):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    for lens in _mixes():
+        B = len(lens)
+        if B * 8 * S > 400000:
+            continue
+        max_blocks = max(1, max(-(-L // 64) for L in lens))
+        plan = ops.DecodePlan.static(B, S, "cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.decode_plan_static(torch.tensor(lens, dtype=torch.int32, device="cuda"), max_blocks,
+                               S, plan, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        items, cta_ptr, seg_ptr, C = op.plan_static(lens, S)
+        got = _host(plan, len(items))
+        assert got[0] == [tuple(i) for i in items]
+        assert got[1] == cta_ptr and got[2] == seg_ptr
+        op.check_coverage(lens, *got)
+
+
+def test_plan_overflow_and_bad_lengths_set_status():
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lens = [4096] * 32
+    plan, st = _run_dynamic(lens, 152, 1, capacity=10)
+    assert st & 16, "PLAN_OVERFLOW"
+    assert plan.cta_ptr.cpu().tolist() == [0] * 153      # empty plan
+    # a length beyond max_blocks*64 and a negative one are treated as empty
+    B = 3
+    plan = ops.DecodePlan(B, 16, 16 + 24, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.decode_plan(torch.tensor([100, 10 ** 6, -5], dtype=torch.int32, device="cuda"), 4, plan,
+                    status, 1)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 4, "BAD_SEQ_LEN"
+    want = op.plan_dynamic([100, 0, 0], 16, 1)
+    got = _host(plan, len(want[0]))
+    assert got[0] == [tuple(i) for i in want[0]] and got[1] == want[1] and got[2] == want[2]

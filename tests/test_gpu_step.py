@@ -1,0 +1,41 @@
+"""End to end: fused prologue -> plan -> attention -> merge vs the oracle's own
+prologue, cache write and attention (on host copies taken before the step)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as od
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixed", "heavy_tail"])
+def test_decode_step_end_to_end(name):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload(name, seed=0)                 # history holds tokens 0 .. L-2
+    seqs = list(range(wl.batch)) if name == "tiny" else [int(np.argmax(wl.lengths)), 3, 9]
+    views = {b: gu.seq_view(wl.cache, wl.block_table_np[b], int(wl.lengths[b]), wl.kv_dtype)
+             for b in seqs}
+    cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+    out = step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
+               wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    got = gu.bf16_host(out)
+    q, k, v = gu.bf16_host(wl.q), gu.bf16_host(wl.k), gu.bf16_host(wl.v)
+    qw, kw = gu.bf16_host(wl.q_norm_w), gu.bf16_host(wl.k_norm_w)
+    scale = wl.kv_scale.cpu().numpy().astype(np.float64)
+    tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if wl.kv_dtype == od.KV_BF16 else (gu.TOL_FP8_MAX, None)
+    for b in seqs:
+        L = int(wl.lengths[b])
+        sub, row = views[b]
+        slot = (L - 1) // 64 * 64 + (L - 1) % 64          # the new token's slot in the view
+        heads = list(range(0, 64, 9)) if L > 65536 else None
+        q_out, want = od.decode_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], [L - 1], qw, kw, sub,
+                                     row[None, :], [L], [slot], wl.kv_dtype, scale, heads=heads)
+        gu.compare(got[b], want[0], *tol, label="%s seq %d" % (name, b))
