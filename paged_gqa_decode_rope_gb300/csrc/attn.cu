@@ -20,7 +20,7 @@
 //  * Four consumer warps split each tile's 64 tokens, 16 each, and keep their
 //    own online-softmax state (running max m, sum l, output O) for the
 //    current item; at the end of an item the four states are merged in shared
-//    memory and written as one partial (O, lse).
+//    memory, in a fixed warp order, and written as one partial (O, lse).
 //  * Tensor cores at q_len = 1 without padding: S^T[16 tok x 8 heads] =
 //    K[16 x 128] . Q^T[128 x 8] (m16n8k16, tokens on M, heads on N), then
 //    O^T[128 x 8] += V^T[128 x 16 tok] . P^T[16 x 8] (d on M, heads on N).
@@ -55,8 +55,8 @@ struct AttnTraits {
   static constexpr int kConsumerWarps = 4;                    // 16 tokens of a tile each
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
-  static constexpr int kOffO = kStages * kStageBytes;
-  static constexpr int kOffM = kOffO + kGroup * kOStride * 4;
+  static constexpr int kOffO = kStages * kStageBytes;                 // [warps][8][kOStride]
+  static constexpr int kOffM = kOffO + kConsumerWarps * kGroup * kOStride * 4;
   static constexpr int kOffL = kOffM + kConsumerWarps * kGroup * 4;
   static constexpr int kOffBar = kOffL + kConsumerWarps * kGroup * 4;
   static constexpr int kOffOk = kOffBar + 2 * kStages * 8;
@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     *abort_flag = 0;
     mbar_fence_init();
   }
-  for (int e = threadIdx.x; e < kGroup * T::kOStride; e += blockDim.x) sm_o[e] = 0.f;
   __syncthreads();
 
   // ------------------------------------------------------------ producer
@@ -387,17 +386,19 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       }
       const float f0 = L0 > 0.f ? exp2f(m0 - Ms0) / L0 * v_scale : 0.f;
       const float f1 = L1 > 0.f ? exp2f(m1 - Ms1) / L1 * v_scale : 0.f;
-      float* o_h0 = sm_o + (2 * c) * T::kOStride;
+      // this warp's share, scaled to the merged normaliser, into its own slice
+      // (summed below in a fixed warp order: the result is bit-reproducible)
+      float* o_h0 = sm_o + (warp * kGroup + 2 * c) * T::kOStride;
       float* o_h1 = o_h0 + T::kOStride;
 #pragma unroll
       for (int mi = 0; mi < 8; ++mi) {
         // rows of the O^T fragment: d_a for o[mi][0..1], d_b for o[mi][2..3]
         const int d_a = kFp8 ? 16 * mi + 2 * r : 16 * mi + r;
         const int d_b = kFp8 ? d_a + 1 : d_a + 8;
-        red_add_shared(o_h0 + d_a, f0 * o[mi][0]);
-        red_add_shared(o_h1 + d_a, f1 * o[mi][1]);
-        red_add_shared(o_h0 + d_b, f0 * o[mi][2]);
-        red_add_shared(o_h1 + d_b, f1 * o[mi][3]);
+        o_h0[d_a] = f0 * o[mi][0];
+        o_h1[d_a] = f1 * o[mi][1];
+        o_h0[d_b] = f0 * o[mi][2];
+        o_h1[d_b] = f1 * o[mi][3];
       }
     }
     named_bar_sync(1, 32 * T::kConsumerWarps);
@@ -406,9 +407,17 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       float* dst = partial_o + static_cast<int64_t>(i) * kGroup * kD;
 #pragma unroll
       for (int e = ct * 4; e < kGroup * kD; e += 32 * T::kConsumerWarps * 4) {
-        float* src = sm_o + (e >> 7) * T::kOStride + (e & 127);
-        *reinterpret_cast<float4*>(dst + e) = *reinterpret_cast<float4*>(src);
-        *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int off = (e >> 7) * T::kOStride + (e & 127);
+        float4 acc = *reinterpret_cast<const float4*>(sm_o + off);
+#pragma unroll
+        for (int w = 1; w < T::kConsumerWarps; ++w) {
+          const float4 x = *reinterpret_cast<const float4*>(sm_o + w * kGroup * T::kOStride + off);
+          acc.x += x.x;
+          acc.y += x.y;
+          acc.z += x.z;
+          acc.w += x.w;
+        }
+        *reinterpret_cast<float4*>(dst + e) = acc;
       }
       if (ct < kGroup) {
         float M = -INFINITY;
