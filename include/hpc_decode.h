@@ -206,6 +206,34 @@ int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, const
 int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
               int32_t batch, void* out, cudaStream_t stream);
 
+/* No counterpart in the paper.  hpc_decode_attn followed by hpc_merge, for
+ * callers that cannot allocate device memory (a fixed memory pool they may not
+ * grow, another framework's allocator or graph hooks, an embedder that hands
+ * over only its inputs and outputs): the fp32 partials live in a file-scope
+ * device array of the library instead of caller buffers.  No allocation of
+ * any kind is made.
+ *   Arguments as in hpc_decode_attn, plus
+ *   out  (device) bf16 [batch, 64, 128], written as by hpc_merge.
+ * Limits and behaviour:
+ *   - plan->capacity must be <= HPC_NOALLOC_MAX_ITEMS (2048 work items, an
+ *     8.5 MB array that every GPU loading the library holds until exit);
+ *     a larger plan returns HPC_ERR_UNSUPPORTED and launches nothing.  A
+ *     length-proportional plan on 152 CTAs fits batches up to 237 sequences.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     every item of a valid plan is rewritten before it is read, so nothing
+ *     needs clearing.  Calls that overlap on the GPU (other streams, other
+ *     threads) race on the array: serialise them.
+ * Errors: as hpc_decode_attn and hpc_merge, plus the capacity limit above. */
+#define HPC_NOALLOC_MAX_ITEMS 2048
+int hpc_decode_attn_merge_noalloc(const void* q, const void* kv_cache, int32_t kv_dtype,
+                                  const float* kv_scale, int32_t num_blocks,
+                                  const int32_t* block_table, int32_t max_blocks,
+                                  const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
+                                  void* out, float sm_scale, int32_t* status, cudaStream_t stream);
+
 /* Persistent grid of hpc_decode_attn on the current device (SM count times
  * resident CTAs per SM) for the given KV dtype: the num_ctas to plan for. */
 int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
