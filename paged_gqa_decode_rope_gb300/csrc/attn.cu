@@ -17,10 +17,12 @@
 //    stage is one tile = the K page + the V page of one (block, kv_head).
 //    Block ids are fetched 32 at a time by the whole warp, so the issue loop
 //    never waits on a global load per tile.
-//  * Four consumer warps split each tile's 64 tokens, 16 each, and keep their
-//    own online-softmax state (running max m, sum l, output O) for the
-//    current item; at the end of an item the four states are merged in shared
-//    memory, in a fixed warp order, and written as one partial (O, lse).
+//  * Two groups of four consumer warps take alternate tiles, so two tiles are
+//    in flight through the math at once; inside a group the four warps split
+//    the tile's 64 tokens, 16 each.  Every warp keeps its own online-softmax
+//    state (running max m, sum l, output O) for the current item; at the end
+//    of an item the eight states are merged in shared memory, in a fixed warp
+//    order, and written as one partial (O, lse).
 //  * Tensor cores at q_len = 1 without padding: S^T[16 tok x 8 heads] =
 //    K[16 x 128] . Q^T[128 x 8] (m16n8k16, tokens on M, heads on N), then
 //    O^T[128 x 8] += V^T[128 x 16 tok] . P^T[16 x 8] (d on M, heads on N).
@@ -51,8 +53,10 @@ struct AttnTraits {
   static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
   static constexpr int kStageBytes = 2 * kPageBytes;          // K page + V page
-  static constexpr int kStages = kFp8 ? 12 : 6;
-  static constexpr int kConsumerWarps = 4;                    // 16 tokens of a tile each
+  static constexpr int kStages = kFp8 ? 10 : 6;
+  static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
+  static constexpr int kGroups = 2;                           // groups take alternate tiles
+  static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
   static constexpr int kOffO = kStages * kStageBytes;                 // [warps][8][kOStride]
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), T::kConsumerWarps);
+      mbar_init(smem_u32(&empty[s]), T::kWarpsPerGroup);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -204,7 +208,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   }
 
   // ------------------------------------------------------------ consumers
-  const int wq = warp;                 // token quarter of each tile
+  const uint32_t grp = warp / T::kWarpsPerGroup;   // this warp's tiles: g % kGroups == grp
+  const int wq = warp % T::kWarpsPerGroup;         // token quarter of each tile
   const int r = lane >> 2, c = lane & 3;
   const float k_scale = kFp8 ? kv_scale[0] : 1.f;
   const float v_scale = kFp8 ? kv_scale[1] : 1.f;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       }
 
       for (int t = it.t0; t < it.t1; ++t, ++g) {
-        if (dead) continue;
+        if (dead || g % T::kGroups != grp) continue;
         const int s = static_cast<int>(g % S);
         const uint32_t use = g / S;
         bool ok = !*abort_flag && mbar_wait(smem_u32(&full[s]), use & 1, status);
