@@ -278,18 +278,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     algo_bytes = wl.kv_bytes() + wl.qo_bytes()
 
-    def one_step(ev=None):
-        ops.rope_norm_kvwrite(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w,
-                              wl.cache, wl.kv_dtype, wl.slot_mapping, wl.kv_scale, step.q_out,
-                              step.status)
-        step.plan_step(wl.seq_lens)
-        if ev is not None:
-            ev[0].record(stream)
-        ops.decode_attn(step.q_out, wl.cache, wl.kv_dtype, wl.kv_scale, wl.block_table,
-                        wl.seq_lens, step.plan, step.partial_o, step.partial_lse, step.status)
-        if ev is not None:
-            ev[1].record(stream)
-        ops.merge(step.partial_o, step.partial_lse, step.plan, step.out)
+    def one_step():
+        # the whole path in two launches: prologue + plan, then attention with
+        # the merge fused in (a programmatic dependent of the first)
+        step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
+             wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
 
     for _ in range(max(3, args.warmup)):
         one_step()
@@ -301,8 +294,6 @@ def run_ours(args):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
@@ -310,14 +301,22 @@ def run_ours(args):
     wall0 = time.time()
     t_start.record(stream)
     for s in range(args.steps):
-        one_step(attn_ev[s])
+        one_step()
     t_end.record(stream)
+    torch.cuda.synchronize()
+    # the dominant kernel alone (attention + fused merge), same stream and
+    # inputs, K launches back to back: its mean duration per launch
+    a_start, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_start.record(stream)
+    for s in range(args.steps):
+        step.attend(step.q_out, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    a_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
     if ws > 1:
         torch.distributed.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    attn_ms = a_start.elapsed_time(a_end) / args.steps
     if int(step.status.item()) != 0:
         raise RuntimeError("device status %d during timing" % int(step.status.item()))
     if sampler:
@@ -380,7 +379,8 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak_gbs, "unit": "GB/s",
                 "frac": round(achieved_gbs / peak_gbs, 4),
                 "traffic": rec["bytes_per_launch"] if rec else None,
-                "peak_kind": peak_kind, "kernel": "decode_attn_kernel<bf16>" if wl.kv_dtype == 0 else "decode_attn_kernel<fp8>",
+                "peak_kind": peak_kind,
+                "kernel": "decode_attn_kernel<%s> (merge fused)" % ("bf16" if wl.kv_dtype == 0 else "fp8"),
                 "algorithmic_bytes_per_launch": algo_bytes, "attn_us": round(attn_ms * 1e3, 2),
                 "frac_of_8TBps": round(achieved_gbs / 8000.0, 4)}
     cpu = None
@@ -401,12 +401,13 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) q/k/v and history, random page permutation, NaN-filled unused slots)",
         "config": {"workload": args.workload + ": " + _describe(wl), "global_batch": wl.batch * ws,
                    "tokens": wl.tokens, "kv_bytes": wl.kv_bytes(), "l2": "inputs larger than L2 (no flush)",
-                   "step": "prologue + plan + attn + merge", "parallelism": "dp%d (sequences per GPU)" % ws},
+                   "step": "prologue + plan (one launch) -> attention + merge (PDL launch)",
+                   "parallelism": "dp%d (sequences per GPU)" % ws},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "schedules": sched,
     }
@@ -442,23 +443,41 @@ def schedule_comparison(ops, wl, stream):
         assert int(step.status.item()) == 0
         return a.elapsed_time(b) / reps * 1e3
 
+    def occupancy(step):
+        clock = torch.zeros((step.plan.num_ctas, 3), dtype=torch.int64, device="cuda")
+        ops.decode_attn_profiled(step_q, wl.cache, wl.kv_dtype, wl.kv_scale, wl.block_table,
+                                 wl.seq_lens, step.plan, step.partial_o, step.partial_lse,
+                                 step.status, clock)
+        torch.cuda.synchronize()
+        return ops.cta_occupancy(clock)
+
     step_q = wl.q
     dyn = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
     t_dyn = time_step(dyn)
+    occ = {"dynamic": occupancy(dyn)}
+    nopool = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, pool_chunks=0)
+    t_nopool = time_step(nopool)
+    occ["dynamic, no pool"] = occupancy(nopool)
+    del nopool
     n_ctas = ops.num_ctas(wl.kv_dtype)
     heuristic = max(1, -(-n_ctas // (wl.batch * 8)))
     sweep = {}
     for S in sorted({1, 2, 4, 8, 16, 32, 64, heuristic}):
         st = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=("static", S))
         sweep[S] = round(time_step(st), 2)
+        occ["static S=%d" % S] = occupancy(st)
         del st
     best_S = min(sweep, key=sweep.get)
+    occ = {k: v for k, v in occ.items()
+           if k in ("dynamic", "dynamic, no pool", "static S=%d" % heuristic, "static S=%d" % best_S)}
     return {"unit": "us (attn + merge)", "dynamic": round(t_dyn, 2),
+            "dynamic_no_pool": round(t_nopool, 2), "pool_chunks": ops.POOL_CHUNKS,
             "static_heuristic_splits": heuristic, "static_heuristic": sweep[heuristic],
             "static_best_splits": best_S, "static_best": sweep[best_S],
             "speedup_vs_heuristic": round(sweep[heuristic] / t_dyn, 3),
             "speedup_vs_best_static": round(sweep[best_S] / t_dyn, 3),
-            "static_sweep": {str(k): v for k, v in sweep.items()}}
+            "static_sweep": {str(k): v for k, v in sweep.items()},
+            "occupancy": occ}
 
 
 def main():

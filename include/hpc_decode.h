@@ -89,22 +89,54 @@ typedef struct {
 
 /* A split-KV plan.  The struct itself lives in host memory; its arrays are
  * device buffers owned by the caller:
- *   items    [capacity]        work items, ordered by CTA, then by
- *                              (seq, kv_head, tile): the items of one
- *                              (seq, kv_head) segment are contiguous
- *   cta_ptr  [num_ctas + 1]    CTA c runs items cta_ptr[c] .. cta_ptr[c+1]-1
+ *   items    [capacity]        work items in flat (seq, kv_head, tile) order:
+ *                              the items of one (seq, kv_head) segment are
+ *                              contiguous
+ *   cta_ptr  [num_ctas + 1]    CTA c's range holds items cta_ptr[c] ..
+ *                              cta_ptr[c+1]-1
+ *   home_end [num_ctas]        CTA c runs items cta_ptr[c] .. home_end[c]-1
+ *                              itself; the rest of its range is pooled
+ *   pool     [3 + capacity]    pool[0]: next claim, pool[1]: CTAs done
+ *                              claiming (both zeroed by the planner and reset
+ *                              by the attention kernel's last CTA, so a plan
+ *                              can be run again), pool[2]: pool length,
+ *                              pool[3..]: pooled item indices in claim order;
+ *                              a CTA that has finished its home items claims
+ *                              the next one
  *   seg_ptr  [batch * 8 + 1]   segment s = seq*8 + kv_head owns items
  *                              seg_ptr[s] .. seg_ptr[s+1]-1
+ *   seg_done [batch * 8]       per-segment count of finished items, used by
+ *                              hpc_decode_attn_merge (zeroed by the planner,
+ *                              left at zero by every run)
  * num_ctas is the grid of hpc_decode_attn; for the length-proportional plan
- * use hpc_decode_num_ctas().  A length-proportional plan needs
- * capacity >= num_ctas + 8 * batch (hpc_plan_capacity). */
+ * use hpc_decode_num_ctas().  A length-proportional plan with J pool chunks
+ * needs capacity >= num_ctas * (1 + J) + 8 * batch (hpc_plan_capacity).
+ * items must be 16-byte aligned. */
 typedef struct {
   hpc_work_item* items;
   int32_t* cta_ptr;
   int32_t* seg_ptr;
+  int32_t* home_end;
+  int32_t* pool;
+  int32_t* seg_done;
   int32_t capacity;
   int32_t num_ctas;
 } hpc_plan;
+
+/* Knobs of the length-proportional planner (hpc_decode_plan):
+ *   min_tiles       lower bound of the per-CTA quota q (>= 1)
+ *   pool_chunks     J: pooled tail chunks per CTA range, 0..64 (0 = no pool)
+ *   pool_min_tiles  shortest pooled chunk worth dealing at run time, in
+ *                   tiles (>= 1); shorter chunks mean no pool
+ * A NULL params pointer means {1, HPC_DEFAULT_POOL_CHUNKS,
+ * HPC_DEFAULT_POOL_MIN_TILES}. */
+typedef struct {
+  int32_t min_tiles;
+  int32_t pool_chunks;
+  int32_t pool_min_tiles;
+} hpc_plan_params;
+#define HPC_DEFAULT_POOL_CHUNKS 4
+#define HPC_DEFAULT_POOL_MIN_TILES 16
 
 /* Fill the RoPE table cos_sin[pos][i] = cos(pos * theta^(-2i/128)) for
  * i < 64 and cos_sin[pos][64 + i] = sin(same angle), pos in [0, max_pos).
@@ -151,20 +183,28 @@ int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
  * T = 8 * sum_b n_b, every CTA c < num_ctas owns the flat tile range
  * [c*q, min((c+1)*q, T)) of the (seq, kv_head, tile) order, where
  * q = max(min_tiles, ceil(T / num_ctas)); its work items are that range cut
- * at (seq, kv_head) boundaries.  Writes plan->items, cta_ptr, seg_ptr.
+ * at (seq, kv_head) boundaries.  With pool_chunks = J > 0 the last
+ * P = floor(q / 8) tiles of every range are cut into J chunks of
+ * ceil(P / J) tiles and pooled, provided that is at least pool_min_tiles: a
+ * CTA runs its home part, then claims pool chunks at run time until none is
+ * left, so SMs that stream faster take more of the tail.  J = 0 (or chunks
+ * below pool_min_tiles) deals everything statically.
+ * Writes plan->items, cta_ptr, home_end, pool, seg_ptr.
  *   seq_lens   (device) int32 [batch], tokens per sequence including the new
  *              one; 0 is an empty sequence; < 0 or > max_blocks * 64 sets
  *              BAD_SEQ_LEN and the sequence is treated as empty
  *   plan       (host) plan->num_ctas and capacity set by the caller; if the
  *              items do not fit, PLAN_OVERFLOW is set and the plan is empty
+ *   params     (host) planner knobs, or NULL for the defaults
  * Errors: HPC_ERR_INVALID_ARG for null pointers, batch < 0, max_blocks < 1,
- * min_tiles < 1 or num_ctas < 1; HPC_ERR_UNSUPPORTED for batch > 8192. */
+ * knobs out of range or num_ctas < 1; HPC_ERR_UNSUPPORTED for batch > 8192. */
 int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
-                    int32_t min_tiles, hpc_plan* plan, int32_t* status, cudaStream_t stream);
+                    const hpc_plan_params* params, hpc_plan* plan, int32_t* status,
+                    cudaStream_t stream);
 
 /* Static equal-split plan, the comparator of hpc_decode_plan: every
  * (seq, kv_head) is cut into `splits` chunks of ceil(n_b / splits) tiles
- * whatever its length, one chunk per CTA (item c runs on CTA c).
+ * whatever its length, one chunk per CTA (item c runs on CTA c; no pool).
  * Requires plan->num_ctas == batch * 8 * splits and capacity >= num_ctas.
  * Same buffers, status bits and errors as hpc_decode_plan. */
 int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
@@ -185,7 +225,9 @@ int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_b
  *                the tile is skipped)
  *   seq_lens     (device) int32 [batch]
  *   plan         (host) plan written by hpc_decode_plan / _static for the same
- *                seq_lens; its num_ctas is the grid
+ *                seq_lens; its num_ctas is the grid.  A plan may be run any
+ *                number of times, but launches that share one plan must not
+ *                overlap on the GPU (they share its pool counters).
  *   partial_o    (device) float32 [plan->capacity, 8, 128], written per item
  *   partial_lse  (device) float32 [plan->capacity, 8], written per item
  * Errors: HPC_ERR_INVALID_ARG for null pointers or bad sizes;
@@ -195,6 +237,35 @@ int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, const
                     const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
                     float* partial_o, float* partial_lse, float sm_scale,
                     int32_t* status, cudaStream_t stream);
+
+/* hpc_decode_attn with the log-sum-exp merge fused in: writes out (bf16
+ * [batch, 64, 128], as hpc_merge would) in the same kernel.  A segment whose
+ * tiles form one work item is normalised and written straight from the
+ * item's epilogue; a segment of several items is merged by the CTA that
+ * finishes its last item (plan->seg_done counts finished items; that CTA
+ * resets the count), reading the other items' partials through L2.  The
+ * partial buffers are still needed for segments of several items.
+ * Same source passages as hpc_decode_attn and hpc_merge.
+ * Errors: as hpc_decode_attn, and HPC_ERR_INVALID_ARG for a null out,
+ * plan->seg_ptr or plan->seg_done. */
+int hpc_decode_attn_merge(const void* q, const void* kv_cache, int32_t kv_dtype,
+                          const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
+                          int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                          const hpc_plan* plan, float* partial_o, float* partial_lse, void* out,
+                          float sm_scale, int32_t* status, cudaStream_t stream);
+
+/* Diagnostic variant of hpc_decode_attn: the same kernel, which also writes
+ * for every CTA c of the grid cta_clock[3c] = start and cta_clock[3c+1] = end
+ * (the GPU's global timer, ns) and cta_clock[3c+2] = the SM it ran on.  Used to
+ * measure SM occupancy and tail idle time of a schedule.
+ *   cta_clock  (device) uint64 [plan->num_ctas * 3], written.
+ * Errors: as hpc_decode_attn, and HPC_ERR_INVALID_ARG if cta_clock is null. */
+int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int32_t kv_dtype,
+                             const float* kv_scale, int32_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
+                             float* partial_o, float* partial_lse, float sm_scale,
+                             int32_t* status, unsigned long long* cta_clock, cudaStream_t stream);
 
 /* Log-sum-exp merge: for each segment s = b*8 + h with items K_s =
  * seg_ptr[s] .. seg_ptr[s+1]-1, in item order,
@@ -218,7 +289,8 @@ int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* 
  *   - plan->capacity must be <= HPC_NOALLOC_MAX_ITEMS (2048 work items, an
  *     8.5 MB array that every GPU loading the library holds until exit);
  *     a larger plan returns HPC_ERR_UNSUPPORTED and launches nothing.  A
- *     length-proportional plan on 152 CTAs fits batches up to 237 sequences.
+ *     length-proportional plan on 152 CTAs with the default 4 pool chunks
+ *     fits batches up to 161 sequences.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call before any
  *     stream capture.
@@ -234,12 +306,35 @@ int hpc_decode_attn_merge_noalloc(const void* q, const void* kv_cache, int32_t k
                                   const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
                                   void* out, float sm_scale, int32_t* status, cudaStream_t stream);
 
+/* The whole decode step in two launches: hpc_rope_norm_kvwrite and
+ * hpc_decode_plan run in one kernel (one block plans while the others run
+ * the prologue: they touch disjoint data), then hpc_decode_attn_merge is
+ * launched as a programmatic dependent of it, so its CTAs are resident and
+ * their pipelines set up when the plan and q become ready.  The result is the
+ * same as the four calls in order (with the fused merge).
+ * Arguments: those of hpc_rope_norm_kvwrite, hpc_decode_plan (params may be
+ * NULL) and hpc_decode_attn_merge; q_out is the prologue's output and the
+ * attention's q.  Same checks and errors as those calls.
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", "Why does dynamic scheduling matter for attention?" (per-step
+ * scheduler, fused prologue) and "FP8 MoE pipeline as a single execution
+ * path" (kernels chained with Programmatic Dependent Launch). */
+int hpc_decode_step(const void* q, const void* k, const void* v, const int32_t* positions,
+                    const float* cos_sin, int32_t max_pos, const void* q_norm_w,
+                    const void* k_norm_w, float eps, void* kv_cache, int32_t kv_dtype,
+                    int32_t num_blocks, const int64_t* slot_mapping, const float* kv_scale,
+                    const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                    int32_t batch, const hpc_plan_params* params, hpc_plan* plan,
+                    float* partial_o, float* partial_lse, void* q_out, void* out, float sm_scale,
+                    int32_t* status, cudaStream_t stream);
+
 /* Persistent grid of hpc_decode_attn on the current device (SM count times
  * resident CTAs per SM) for the given KV dtype: the num_ctas to plan for. */
 int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
 
-/* Items a length-proportional plan may need: num_ctas + 8 * batch. */
-int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas);
+/* Items a length-proportional plan may need:
+ * num_ctas * (1 + pool_chunks) + 8 * batch. */
+int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas, int32_t pool_chunks);
 
 #ifdef __cplusplus
 }

@@ -10,10 +10,18 @@ compute units idle on mixed batches; the HPC_ATTN scheduler instead deals
 length at every step.
 
 Reading (the pages give no formula): flatten every (sequence, KV head) tile in
-(sequence, kv_head, tile) order; give compute unit c the contiguous flat range
-[c*q, min((c+1)*q, T)) with q = max(min_tiles, ceil(T / C)); a work item is that
-range cut at (sequence, kv_head) boundaries.  Each unit then streams the same
-number of tiles (up to the last one), so work is proportional to length.
+(sequence, kv_head, tile) order; compute unit c is given the contiguous flat
+range [c*q, min((c+1)*q, T)) with q = max(min_tiles, ceil(T / C)); a work item
+is a piece of that range cut at (sequence, kv_head) boundaries.  Each unit then
+streams the same number of tiles, so work is proportional to length.
+
+Runtime dealing of the tail (``pool_chunks`` = J > 0): units do not run at
+exactly the same speed, so the last P = floor(q / 8) tiles of every unit's
+range are cut into chunks of k = ceil(P / J) tiles and pooled; a unit that
+has finished its home part [c*q, c*q + q - P) claims pool chunks, in pool
+order, until none is left.  Chunks shorter than ``pool_min_tiles`` are not
+worth dealing at run time: then nothing is pooled.  Every tile is still dealt
+exactly once.  J = 0 gives the plain plan above.
 
 The static comparator splits every (sequence, kv_head) into S chunks of
 ceil(n/S) tiles, one chunk per compute unit, whatever the length.
@@ -30,48 +38,66 @@ def num_tiles(length):
     return -(-int(length) // PAGE) if length > 0 else 0
 
 
-def plan_dynamic(seq_lens, num_ctas, min_tiles=1):
+def plan_dynamic(seq_lens, num_ctas, min_tiles=1, pool_chunks=0, pool_min_tiles=1):
     """Length-proportional plan.
 
-    Returns (items, cta_ptr, seg_ptr): ``items`` a list of 4-tuples ordered by
-    compute unit (and so by segment and tile), ``cta_ptr`` [C+1] the first item
-    of each unit, ``seg_ptr`` [B*8+1] the first item of each (seq, kv_head)
-    segment (segment s = seq * 8 + kv_head).
+    Returns (items, cta_ptr, seg_ptr, home_end, pool):
+      items     4-tuples in flat (seq, kv_head, tile) order
+      cta_ptr   [C+1]: unit c's range holds items cta_ptr[c] .. cta_ptr[c+1]-1
+      seg_ptr   [B*8+1]: segment s = seq*8 + kv_head owns items
+                seg_ptr[s] .. seg_ptr[s+1]-1
+      home_end  [C]: unit c runs items cta_ptr[c] .. home_end[c]-1 itself;
+                items home_end[c] .. cta_ptr[c+1]-1 go to the pool
+      pool      pooled item indices, in claim order (unit order, then item)
     """
     B = len(seq_lens)
     n = [num_tiles(L) for L in seq_lens]
     T = HKV * sum(n)
     q = max(int(min_tiles), -(-T // num_ctas)) if T > 0 else max(int(min_tiles), 1)
+    P = q // 8 if pool_chunks > 0 else 0
+    k = -(-P // pool_chunks) if P > 0 else 1
+    if k < pool_min_tiles:                     # chunks too short to deal
+        P, k = 0, 1
+    h = q - P                                  # home tiles of every unit
 
-    # segments in flat order, with their start offsets
-    segments = []
-    start = 0
-    for b in range(B):
-        for h in range(HKV):
-            segments.append((b, h, start, start + n[b]))
-            start += n[b]
+    def piece(f):
+        """(unit, piece) that owns flat tile f; piece 0 is the home part."""
+        c, r = divmod(f, q)
+        return (c, 0) if r < h else (c, 1 + (r - h) // k)
+
+    def piece_end(c, j):
+        return c * q + (h if j == 0 else min(q, h + j * k))
 
     items, owner = [], []
-    cta_ptr = [0] * (num_ctas + 1)
-    seg_first = []
-    for (b, h, s0, s1) in segments:
-        seg_first.append(len(items))
-        t = s0
-        while t < s1:
-            c = t // q                       # the unit that owns flat tile t
-            end = min(s1, (c + 1) * q)
-            items.append((b, h, t - s0, end - s0))
-            owner.append(c)
-            t = end
-    seg_ptr = seg_first + [len(items)]
+    start = 0
+    seg_ptr = []
+    for b in range(B):
+        for hh in range(HKV):
+            s0, s1 = start, start + n[b]
+            seg_ptr.append(len(items))
+            t = s0
+            while t < s1:
+                c, j = piece(t)
+                end = min(s1, piece_end(c, j))
+                items.append((b, hh, t - s0, end - s0))
+                owner.append((c, j))
+                t = end
+            start = s1
+    seg_ptr.append(len(items))
 
-    # cta_ptr[c] = index of the first item owned by a unit >= c
+    cta_ptr, home_end = [], []
     i = 0
     for c in range(num_ctas + 1):
-        while i < len(items) and owner[i] < c:
+        while i < len(items) and owner[i][0] < c:
             i += 1
-        cta_ptr[c] = i
-    return items, cta_ptr, seg_ptr
+        cta_ptr.append(i)
+    for c in range(num_ctas):
+        i = cta_ptr[c]
+        while i < cta_ptr[c + 1] and owner[i][1] == 0:
+            i += 1
+        home_end.append(i)
+    pool = [i for c in range(num_ctas) for i in range(home_end[c], cta_ptr[c + 1])]
+    return items, cta_ptr, seg_ptr, home_end, pool
 
 
 def plan_static(seq_lens, splits):
@@ -95,8 +121,8 @@ def plan_static(seq_lens, splits):
     return items, cta_ptr, seg_ptr, num_ctas
 
 
-def check_coverage(seq_lens, items, cta_ptr, seg_ptr):
-    """Assert that a plan covers every (seq, kv_head, tile) exactly once and
+def check_coverage(seq_lens, items, cta_ptr, seg_ptr, home_end=None, pool=None):
+    """Assert that a plan deals every (seq, kv_head, tile) exactly once and
     that its index arrays are consistent.  Returns the number of items."""
     B = len(seq_lens)
     want = {}
@@ -118,4 +144,12 @@ def check_coverage(seq_lens, items, cta_ptr, seg_ptr):
         # items of a segment are in tile order and contiguous
         ts = [items[i][2:] for i in range(seg_ptr[s], seg_ptr[s + 1])]
         assert all(a[1] == b[0] for a, b in zip(ts, ts[1:]))
+    if home_end is not None:
+        # each item is run exactly once: by its home unit or from the pool
+        runs = []
+        for c in range(len(cta_ptr) - 1):
+            assert cta_ptr[c] <= home_end[c] <= cta_ptr[c + 1]
+            runs += list(range(cta_ptr[c], home_end[c]))
+        runs += list(pool)
+        assert sorted(runs) == list(range(len(items))), "an item is run twice or never"
     return len(items)

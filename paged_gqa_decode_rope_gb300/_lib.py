@@ -29,8 +29,12 @@ class WorkItem(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("items", _c_p), ("cta_ptr", _c_p), ("seg_ptr", _c_p),
-                ("capacity", _c_i32), ("num_ctas", _c_i32)]
+    _fields_ = [("items", _c_p), ("cta_ptr", _c_p), ("seg_ptr", _c_p), ("home_end", _c_p),
+                ("pool", _c_p), ("seg_done", _c_p), ("capacity", _c_i32), ("num_ctas", _c_i32)]
+
+
+class PlanParams(ctypes.Structure):
+    _fields_ = [("min_tiles", _c_i32), ("pool_chunks", _c_i32), ("pool_min_tiles", _c_i32)]
 
 
 # name -> (restype, argtypes); the order follows include/hpc_decode.h
@@ -39,17 +43,28 @@ SIGNATURES = {
     "hpc_rope_norm_kvwrite": (ctypes.c_int, [
         _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p, ctypes.c_float,
         _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p]),
-    "hpc_decode_plan": (ctypes.c_int, [_c_p, _c_i32, _c_i32, _c_i32, ctypes.POINTER(Plan), _c_p, _c_p]),
+    "hpc_decode_plan": (ctypes.c_int, [_c_p, _c_i32, _c_i32, ctypes.POINTER(PlanParams),
+                                       ctypes.POINTER(Plan), _c_p, _c_p]),
     "hpc_decode_plan_static": (ctypes.c_int, [_c_p, _c_i32, _c_i32, _c_i32, ctypes.POINTER(Plan), _c_p, _c_p]),
     "hpc_decode_attn": (ctypes.c_int, [
         _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(Plan),
         _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_decode_attn_merge": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(Plan),
+        _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_decode_attn_profiled": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(Plan),
+        _c_p, _c_p, ctypes.c_float, _c_p, _c_p, _c_p]),
     "hpc_merge": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(Plan), _c_i32, _c_p, _c_p]),
     "hpc_decode_attn_merge_noalloc": (ctypes.c_int, [
         _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(Plan),
         _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_decode_step": (ctypes.c_int, [
+        _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p, ctypes.c_float, _c_p, _c_i32, _c_i32,
+        _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(PlanParams), ctypes.POINTER(Plan),
+        _c_p, _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
     "hpc_decode_num_ctas": (ctypes.c_int, [_c_i32, ctypes.POINTER(_c_i32)]),
-    "hpc_plan_capacity": (_c_i32, [_c_i32, _c_i32]),
+    "hpc_plan_capacity": (_c_i32, [_c_i32, _c_i32, _c_i32]),
 }
 
 _lib = None

@@ -19,10 +19,10 @@
 //    never waits on a global load per tile.
 //  * Two groups of four consumer warps take alternate tiles, so two tiles are
 //    in flight through the math at once; inside a group the four warps split
-//    the tile's 64 tokens, 16 each.  Every warp keeps its own online-softmax
-//    state (running max m, sum l, output O) for the current item; at the end
-//    of an item the eight states are merged in shared memory, in a fixed warp
-//    order, and written as one partial (O, lse).
+//    the tile's 64 tokens, 16 each.  Every warp keeps its own
+//    online-softmax state (running max m, sum l, output O) for the current
+//    item; at the end of an item the states are merged in shared memory, in a
+//    fixed warp order, and written as one partial (O, lse).
 //  * Tensor cores at q_len = 1 without padding: S^T[16 tok x 8 heads] =
 //    K[16 x 128] . Q^T[128 x 8] (m16n8k16, tokens on M, heads on N), then
 //    O^T[128 x 8] += V^T[128 x 16 tok] . P^T[16 x 8] (d on M, heads on N).
@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "internal.h"
 
 namespace hpc {
 namespace {
@@ -63,11 +64,21 @@ struct AttnTraits {
   static constexpr int kOffM = kOffO + kConsumerWarps * kGroup * kOStride * 4;
   static constexpr int kOffL = kOffM + kConsumerWarps * kGroup * 4;
   static constexpr int kOffBar = kOffL + kConsumerWarps * kGroup * 4;
-  static constexpr int kOffOk = kOffBar + 2 * kStages * 8;
-  static constexpr int kOffAbort = kOffOk + kStages * 4;
+  static constexpr int kItemRing = 4;                         // items queued ahead
+  // barriers: full[S], empty[S], item_full[R], item_empty[R], consumer barrier
+  static constexpr int kNumBars = 2 * kStages + 2 * kItemRing + 1;
+  static constexpr int kOffOk = kOffBar + kNumBars * 8;
+  static constexpr int kOffRing = kOffOk + kStages * 4;
+  static constexpr int kOffAbort = kOffRing + kItemRing * 4;
   static constexpr int kSmemUsed = kOffAbort + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;         // slack for 1024-byte alignment
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
+  // A consumer waits on full[s] by the parity of its use (g / kStages) & 1,
+  // which names the right phase only if the same warp saw the stage's previous
+  // phase complete.  That holds when every use of a stage belongs to one group,
+  // i.e. kStages % kGroups == 0; otherwise a warp can pass its wait while the
+  // stage's previous copy (another group's tile) is still in flight.
+  static_assert(kStages % kGroups == 0, "each stage must always serve the same group");
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
 };
 
@@ -78,7 +89,7 @@ struct Item {
 
 __device__ __forceinline__ Item load_item(const hpc_work_item* items, int i,
                                           const int32_t* seq_lens, int batch, int max_blocks) {
-  const int4 w = __ldg(reinterpret_cast<const int4*>(items) + i);
+  const int4 w = reinterpret_cast<const int4*>(items)[i];
   Item it{w.x, w.y, w.z, w.w, 0, false};
   if (it.seq >= 0 && it.seq < batch && it.h >= 0 && it.h < kHkv) {
     const int L = __ldg(seq_lens + it.seq);
@@ -93,16 +104,73 @@ __device__ __forceinline__ Item load_item(const hpc_work_item* items, int i,
   return it;
 }
 
+// Diagnostic record of one CTA: [start ns, end ns, SM id] (globaltimer).
+__device__ __forceinline__ void record_cta_clock(unsigned long long* cta_clock,
+                                                 unsigned long long t_start) {
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  cta_clock[3 * blockIdx.x + 0] = t_start;
+  cta_clock[3 * blockIdx.x + 1] = globaltimer_ns();
+  cta_clock[3 * blockIdx.x + 2] = smid;
+}
+
+// O^T += V^T P^T for one warp's 16 tokens (rows: d, cols: 8 heads).  With
+// kMask, V entries of tokens past the length are zeroed first (mask01 covers
+// the fragment's tokens 2c, 2c+1; mask23 tokens 2c+8, 2c+9).
+template <bool kFp8, bool kMask>
+__device__ __forceinline__ void pv_tile(uint32_t vb, int row, int vtok_bf16, int vsel_bf16, int hi,
+                                        int sw, uint32_t pb0, uint32_t pb1, uint32_t mask01,
+                                        uint32_t mask23, float (&o)[8][4]) {
+  if constexpr (kFp8) {
+#pragma unroll
+    for (int mp = 0; mp < 4; ++mp) {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(vb + row * 128 + ((((2 * mp + hi) & 7) ^ sw) << 4), r0, r1, r2, r3);
+      // r0: tokens 2c, 2c+1 at d 2r, 2r+1 (bytes t0d0, t0d1, t1d0, t1d1); the
+      // byte shuffle pairs the two tokens of one d for each f16x2
+      const uint32_t x = prmt(r0, 0, 0x3120), y = prmt(r1, 0, 0x3120);
+      const uint32_t z = prmt(r2, 0, 0x3120), w = prmt(r3, 0, 0x3120);
+      uint32_t a[8] = {e4m3x2_to_f16x2(x & 0xffff), e4m3x2_to_f16x2(x >> 16),
+                       e4m3x2_to_f16x2(y & 0xffff), e4m3x2_to_f16x2(y >> 16),
+                       e4m3x2_to_f16x2(z & 0xffff), e4m3x2_to_f16x2(z >> 16),
+                       e4m3x2_to_f16x2(w & 0xffff), e4m3x2_to_f16x2(w >> 16)};
+      if constexpr (kMask) {
+        a[0] &= mask01; a[1] &= mask01; a[2] &= mask23; a[3] &= mask23;
+        a[4] &= mask01; a[5] &= mask01; a[6] &= mask23; a[7] &= mask23;
+      }
+      mma_f16(o[2 * mp], a[0], a[1], a[2], a[3], pb0, pb1);
+      mma_f16(o[2 * mp + 1], a[4], a[5], a[6], a[7], pb0, pb1);
+    }
+  } else {
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vb + (mi >> 2) * (64 * 128) + vtok_bf16 * 128 + ((((2 * mi + vsel_bf16) & 7) ^ sw) << 4),
+                a0, a1, a2, a3);
+      if constexpr (kMask) {
+        a0 &= mask01; a1 &= mask01; a2 &= mask23; a3 &= mask23;
+      }
+      mma_bf16(o[mi], a0, a1, a2, a3, pb0, pb1);
+    }
+  }
+}
+
 template <bool kFp8>
 __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_kernel(
-    const __grid_constant__ CUtensorMap kv_map, const uint16_t* __restrict__ q,
+    // q, the plan arrays and the cache may be written by the kernel this one
+    // is a programmatic dependent of: they are read with plain (coherent)
+    // loads, never as restrict/read-only data, so that no load of them can be
+    // hoisted above the grid-dependency wait
+    const __grid_constant__ CUtensorMap kv_map, const uint16_t* q,
     const float* __restrict__ kv_scale, const int32_t* __restrict__ block_table, int32_t max_blocks,
     int32_t num_blocks, const int32_t* __restrict__ seq_lens, int32_t batch,
-    const hpc_work_item* __restrict__ items, const int32_t* __restrict__ cta_ptr, int32_t capacity,
-    float* __restrict__ partial_o, float* __restrict__ partial_lse, float sm_scale,
-    int32_t* __restrict__ status) {
+    const hpc_work_item* items, const int32_t* cta_ptr, const int32_t* home_end, int32_t* pool,
+    int32_t capacity, float* __restrict__ partial_o, float* __restrict__ partial_lse,
+    float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
+    const int32_t* seg_ptr, int32_t* seg_done, uint16_t* __restrict__ out) {
   using T = AttnTraits<kFp8>;
   constexpr int S = T::kStages;
+  constexpr int R = T::kItemRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -111,41 +179,140 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   float* sm_l = reinterpret_cast<float*>(smem + T::kOffL);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
   uint64_t* empty = full + S;
+  uint64_t* item_full = empty + S;
+  uint64_t* item_empty = item_full + R;
+  uint64_t* cons_bar = item_empty + R;
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + T::kOffOk);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + T::kOffRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kOffAbort);
+  volatile int* merge_flag = abort_flag + 1;
+  const bool fuse = out != nullptr;   // merge the partials in this kernel
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int it_begin = cta_ptr[blockIdx.x];
-  const int it_end = cta_ptr[blockIdx.x + 1];
-  if (it_begin < 0 || it_end < it_begin || it_end > capacity) {
-    if (threadIdx.x == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
-    return;
-  }
-  if (it_begin == it_end) return;
-
+  const unsigned long long t_start = cta_clock != nullptr ? globaltimer_ns() : 0ull;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), T::kWarpsPerGroup);
     }
+    for (int r = 0; r < R; ++r) {
+      mbar_init(smem_u32(&item_full[r]), 1);
+      mbar_init(smem_u32(&item_empty[r]), T::kConsumerWarps);
+    }
+    mbar_init(smem_u32(cons_bar), 32 * T::kConsumerWarps);
     *abort_flag = 0;
     mbar_fence_init();
   }
+  if (warp == T::kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
+  // everything above is independent of the previous kernel on the stream;
+  // from here on the plan, q and the cache are read
+  pdl_wait();
+
+  // The pool counters are pool[0] (next claim) and pool[1] (CTAs done
+  // claiming); the last CTA to finish claiming resets both, so the same plan
+  // can be run again.
+  auto finish_claims = [&]() {
+    if (atomicAdd(&pool[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      pool[0] = 0;
+      pool[1] = 0;
+    }
+  };
+
+  const int home_begin = cta_ptr[blockIdx.x];
+  const int home_stop = home_end[blockIdx.x];
+  const int pool_len = pool[2];
+  const bool bad_range = home_begin < 0 || home_stop < home_begin || home_stop > capacity ||
+                         pool_len < 0 || pool_len > capacity;
+  if (bad_range) {
+    if (threadIdx.x == 0) {
+      atomicOr(status, HPC_STATUS_BAD_PLAN);
+      finish_claims();
+      if (cta_clock != nullptr) record_cta_clock(cta_clock, t_start);
+    }
+    return;
+  }
+
   __syncthreads();
 
   // ------------------------------------------------------------ producer
   if (warp == T::kConsumerWarps) {
-    if (lane == 0) tma_prefetch_desc(&kv_map);
     const uint64_t policy = l2_evict_first_policy();
     const uint32_t stage0 = smem_u32(smem);
     uint32_t g = 0;          // tiles issued so far by this CTA
+    uint32_t n_pushed = 0;   // items handed to the consumers so far
+    int next_home = home_begin;
+    bool claiming = true;    // still taking items (home, then pool)
     bool alive = true;
-    for (int i = it_begin; i < it_end && alive; ++i) {
-      const Item it = load_item(items, i, seq_lens, batch, max_blocks);
+    while (alive) {
+      // next item: the home part first, then claims from the pool; -1 ends
+      int idx = -1;
+      if (next_home < home_stop) {
+        idx = next_home++;
+      } else if (claiming) {
+        int k = 0;
+        if (lane == 0) k = atomicAdd(&pool[0], 1);
+        k = __shfl_sync(0xffffffffu, k, 0);
+        if (k < pool_len) {
+          idx = pool[3 + k];
+          if (idx < 0 || idx >= capacity) {
+            if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
+            continue;
+          }
+        } else {
+          claiming = false;
+          if (lane == 0) finish_claims();
+        }
+      }
+      // hand the item (or the end mark) to the consumers
+      int ok = 1;
+      if (lane == 0) {
+        const int r = static_cast<int>(n_pushed % R);
+        const uint32_t use = n_pushed / R;
+        if (*abort_flag) {
+          ok = 0;
+        } else if (use > 0 && !mbar_wait(smem_u32(&item_empty[r]), (use - 1) & 1, status)) {
+          *abort_flag = 1;
+          ok = 0;
+        }
+        if (ok) {
+          ring[r] = idx;
+          mbar_arrive(smem_u32(&item_full[r]));
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      ++n_pushed;
+      if (idx < 0) break;
+
+      const Item it = load_item(items, idx, seq_lens, batch, max_blocks);
       if (!it.ok) {
         if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
         continue;
+      }
+      // start the item on a slot of group 0 (padding slots carry no data), so
+      // tile t of the item always goes to group (t - t0) % kGroups, whichever
+      // CTA runs it: the output does not depend on the schedule's run order
+      while (g % T::kGroups != 0) {
+        int tok = 1;
+        if (lane == 0) {
+          const int s = static_cast<int>(g % S);
+          const uint32_t use = g / S;
+          if (*abort_flag) {
+            tok = 0;
+          } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
+            *abort_flag = 1;
+            tok = 0;
+          }
+          if (tok) {
+            stage_ok[s] = 0;
+            mbar_arrive(smem_u32(&full[s]));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, tok, 0)) {
+          alive = false;
+          break;
+        }
+        ++g;
       }
       const int32_t* bt_row = block_table + static_cast<int64_t>(it.seq) * max_blocks;
       for (int tb = it.t0; tb < it.t1 && alive; tb += 32) {
@@ -153,17 +320,17 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         const int my_bid = lane < nt ? __ldg(bt_row + tb + lane) : 0;
         for (int j = 0; j < nt; ++j) {
           const int bid = __shfl_sync(0xffffffffu, my_bid, j);
-          int ok = 1;
+          int tok = 1;
           if (lane == 0) {
             const int s = static_cast<int>(g % S);
             const uint32_t use = g / S;
             if (*abort_flag) {
-              ok = 0;
+              tok = 0;
             } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
               *abort_flag = 1;
-              ok = 0;
+              tok = 0;
             }
-            if (ok) {
+            if (tok) {
               const uint32_t fb = smem_u32(&full[s]);
               if (bid >= 0 && bid < num_blocks) {
                 stage_ok[s] = 1;
@@ -187,8 +354,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
               }
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
+          if (!__shfl_sync(0xffffffffu, tok, 0)) {
             alive = false;
             break;
           }
@@ -196,6 +362,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         }
       }
     }
+    if (claiming && lane == 0) finish_claims();   // stopped early by a fault
     // After a fault, copies may still be landing in stages nobody will wait
     // on: wait for the last one issued into every stage before exiting.
     if (lane == 0 && *abort_flag) {
@@ -221,9 +388,43 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   const int vtok_bf16 = 16 * wq + (lane & 7) + hi * 8;             // V^T .trans row (token)
   const int vsel_bf16 = (lane >> 3) & 1;                           // V^T d half
   uint32_t g = 0;
+  uint32_t bar_phase = 0;
   bool dead = false;
 
-  for (int i = it_begin; i < it_end; ++i) {
+  // all consumer threads meet; bounded, so a stuck peer ends in a timeout
+  auto cons_sync = [&]() -> bool {
+    mbar_arrive(smem_u32(cons_bar));
+    bool ok = !*abort_flag && mbar_wait(smem_u32(cons_bar), bar_phase & 1, status);
+    ++bar_phase;
+    ok = __all_sync(0xffffffffu, ok);   // the same answer for the whole warp
+    if (!ok && lane == 0) *abort_flag = 1;
+    return ok;
+  };
+
+  // with the merge fused in, the rows of empty sequences (no items) are
+  // zeroed here, the segments spread over the CTAs of the grid
+  if (fuse) {
+    for (int sg = blockIdx.x; sg < batch * kHkv; sg += gridDim.x) {
+      if (seg_ptr[sg + 1] != seg_ptr[sg]) continue;
+      for (int e = threadIdx.x * 4; e < kGroup * kD; e += 32 * T::kConsumerWarps * 4)
+        *reinterpret_cast<uint2*>(out + static_cast<int64_t>(sg) * kGroup * kD + e) = make_uint2(0u, 0u);
+    }
+  }
+
+  for (uint32_t n = 0;; ++n) {
+    // next item from the producer
+    const int rslot = static_cast<int>(n % R);
+    bool ok = !*abort_flag && mbar_wait(smem_u32(&item_full[rslot]), (n / R) & 1, status);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      if (lane == 0) *abort_flag = 1;
+      break;
+    }
+    const int i = ring[rslot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
+    if (i < 0) break;
+
     const Item it = load_item(items, i, seq_lens, batch, max_blocks);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2c, 2c+1
     float o[8][4];
@@ -237,22 +438,36 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         if constexpr (kFp8) {
-          const uint2 x = __ldg(reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c));
+          const uint2 x = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
           bq[ks][0] = pack_f16(bf16_lo(x.x), bf16_hi(x.x));
           bq[ks][1] = pack_f16(bf16_lo(x.y), bf16_hi(x.y));
         } else {
-          bq[ks][0] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c));
-          bq[ks][1] = __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c));
+          bq[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
+          bq[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c);
         }
       }
 
+      // the producer's padding slots: wait for them and hand them back
+      for (; g % T::kGroups != 0; ++g) {
+        if (dead || g % T::kGroups != grp) continue;
+        const int s = static_cast<int>(g % S);
+        bool tok = !*abort_flag && mbar_wait(smem_u32(&full[s]), (g / S) & 1, status);
+        tok = __all_sync(0xffffffffu, tok);
+        if (!tok) {
+          if (lane == 0) *abort_flag = 1;
+          dead = true;
+          continue;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      }
       for (int t = it.t0; t < it.t1; ++t, ++g) {
         if (dead || g % T::kGroups != grp) continue;
         const int s = static_cast<int>(g % S);
         const uint32_t use = g / S;
-        bool ok = !*abort_flag && mbar_wait(smem_u32(&full[s]), use & 1, status);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) {
+        bool tok = !*abort_flag && mbar_wait(smem_u32(&full[s]), use & 1, status);
+        tok = __all_sync(0xffffffffu, tok);
+        if (!tok) {
           if (lane == 0) *abort_flag = 1;
           dead = true;
           continue;
@@ -305,19 +520,23 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
           const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
           const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-          const float al0 = exp2f(m0 - ms0), al1 = exp2f(m1 - ms1);
-          const float p0 = exp2f(x0 - ms0), p1 = exp2f(x1 - ms1);
-          const float p2 = exp2f(x2 - ms0), p3 = exp2f(x3 - ms1);
+          const float al0 = exp2_ftz(m0 - ms0), al1 = exp2_ftz(m1 - ms1);
+          const float p0 = exp2_ftz(x0 - ms0), p1 = exp2_ftz(x1 - ms1);
+          const float p2 = exp2_ftz(x2 - ms0), p3 = exp2_ftz(x3 - ms1);
           l0 = l0 * al0 + (p0 + p2);
           l1 = l1 * al1 + (p1 + p3);
           m0 = mn0;
           m1 = mn1;
+          // the running max rarely moves after the first tiles: skip the
+          // (exact, multiply-by-one) rescale when no lane needs it
+          if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
 #pragma unroll
-          for (int mi = 0; mi < 8; ++mi) {
-            o[mi][0] *= al0;
-            o[mi][1] *= al1;
-            o[mi][2] *= al0;
-            o[mi][3] *= al1;
+            for (int mi = 0; mi < 8; ++mi) {
+              o[mi][0] *= al0;
+              o[mi][1] *= al1;
+              o[mi][2] *= al0;
+              o[mi][3] *= al1;
+            }
           }
           // P^T fragment -> B operand (k = token, n = head) by an 8x8 transpose
           uint32_t pb0, pb1;
@@ -329,39 +548,21 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
             pb1 = movmatrix_t(pack_bf16(p2, p3));
           }
 
-          // O^T += V^T P^T  (rows: d, cols: 8 heads)
-          if constexpr (kFp8) {
-#pragma unroll
-            for (int mp = 0; mp < 4; ++mp) {
-              uint32_t r0, r1, r2, r3;
-              ldsm_x4_t(vb + row * 128 + ((((2 * mp + hi) & 7) ^ sw) << 4), r0, r1, r2, r3);
-              // r0: tokens 2c, 2c+1 at d 2r, 2r+1 (bytes t0d0, t0d1, t1d0, t1d1)
-              const uint32_t x = prmt(r0, 0, 0x3120), y = prmt(r1, 0, 0x3120);
-              const uint32_t z = prmt(r2, 0, 0x3120), w = prmt(r3, 0, 0x3120);
-              mma_f16(o[2 * mp], e4m3x2_to_f16x2(x & 0xffff) & mask01,
-                      e4m3x2_to_f16x2(x >> 16) & mask01, e4m3x2_to_f16x2(y & 0xffff) & mask23,
-                      e4m3x2_to_f16x2(y >> 16) & mask23, pb0, pb1);
-              mma_f16(o[2 * mp + 1], e4m3x2_to_f16x2(z & 0xffff) & mask01,
-                      e4m3x2_to_f16x2(z >> 16) & mask01, e4m3x2_to_f16x2(w & 0xffff) & mask23,
-                      e4m3x2_to_f16x2(w >> 16) & mask23, pb0, pb1);
-            }
-          } else {
-#pragma unroll
-            for (int mi = 0; mi < 8; ++mi) {
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4_t(vb + (mi >> 2) * T::kBoxBytes + vtok_bf16 * 128 +
-                            ((((2 * mi + vsel_bf16) & 7) ^ sw) << 4),
-                        a0, a1, a2, a3);
-              mma_bf16(o[mi], a0 & mask01, a1 & mask01, a2 & mask23, a3 & mask23, pb0, pb1);
-            }
-          }
+          if (nvalid < 16)
+            pv_tile<kFp8, true>(vb, row, vtok_bf16, vsel_bf16, hi, sw, pb0, pb1, mask01, mask23, o);
+          else
+            pv_tile<kFp8, false>(vb, row, vtok_bf16, vsel_bf16, hi, sw, pb0, pb1, mask01, mask23, o);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
       }
     }
+    if (dead) break;
 
-    // ---- merge the four warps' states and write the item's partial
+    // ---- merge the warps' states and write the item's partial: every warp
+    // stores its raw (m, l, O) in its own slice; after one barrier each
+    // output element is combined over the warps in a fixed order (the result
+    // is bit-reproducible) with the log-sum-exp weights of its head
     l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
@@ -374,25 +575,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       sm_l[warp * kGroup + 2 * c] = l0;
       sm_l[warp * kGroup + 2 * c + 1] = l1;
     }
-    named_bar_sync(1, 32 * T::kConsumerWarps);
     {
-      float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < T::kConsumerWarps; ++w) {
-        M0 = fmaxf(M0, sm_m[w * kGroup + 2 * c]);
-        M1 = fmaxf(M1, sm_m[w * kGroup + 2 * c + 1]);
-      }
-      const float Ms0 = M0 == -INFINITY ? 0.f : M0, Ms1 = M1 == -INFINITY ? 0.f : M1;
-      float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < T::kConsumerWarps; ++w) {
-        L0 += sm_l[w * kGroup + 2 * c] * exp2f(sm_m[w * kGroup + 2 * c] - Ms0);
-        L1 += sm_l[w * kGroup + 2 * c + 1] * exp2f(sm_m[w * kGroup + 2 * c + 1] - Ms1);
-      }
-      const float f0 = L0 > 0.f ? exp2f(m0 - Ms0) / L0 * v_scale : 0.f;
-      const float f1 = L1 > 0.f ? exp2f(m1 - Ms1) / L1 * v_scale : 0.f;
-      // this warp's share, scaled to the merged normaliser, into its own slice
-      // (summed below in a fixed warp order: the result is bit-reproducible)
       float* o_h0 = sm_o + (warp * kGroup + 2 * c) * T::kOStride;
       float* o_h1 = o_h0 + T::kOStride;
 #pragma unroll
@@ -400,46 +583,123 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         // rows of the O^T fragment: d_a for o[mi][0..1], d_b for o[mi][2..3]
         const int d_a = kFp8 ? 16 * mi + 2 * r : 16 * mi + r;
         const int d_b = kFp8 ? d_a + 1 : d_a + 8;
-        o_h0[d_a] = f0 * o[mi][0];
-        o_h1[d_a] = f1 * o[mi][1];
-        o_h0[d_b] = f0 * o[mi][2];
-        o_h1[d_b] = f1 * o[mi][3];
+        o_h0[d_a] = o[mi][0];
+        o_h1[d_a] = o[mi][1];
+        o_h0[d_b] = o[mi][2];
+        o_h1[d_b] = o[mi][3];
       }
     }
-    named_bar_sync(1, 32 * T::kConsumerWarps);
+    if (!cons_sync()) break;
+    // with the merge fused in: a segment of one item is final here; a segment
+    // of several items is merged by the CTA that finishes its last item
+    const int seg = it.seq * kHkv + it.h;
+    const int seg_items = fuse && it.ok ? seg_ptr[seg + 1] - seg_ptr[seg] : 0;
+    const bool direct = fuse && it.ok && seg_items == 1;
     {
-      const int ct = threadIdx.x;   // 0 .. 127
+      const int ct = threadIdx.x;   // consumer thread
       float* dst = partial_o + static_cast<int64_t>(i) * kGroup * kD;
 #pragma unroll
       for (int e = ct * 4; e < kGroup * kD; e += 32 * T::kConsumerWarps * 4) {
-        const int off = (e >> 7) * T::kOStride + (e & 127);
-        float4 acc = *reinterpret_cast<const float4*>(sm_o + off);
-#pragma unroll
-        for (int w = 1; w < T::kConsumerWarps; ++w) {
-          const float4 x = *reinterpret_cast<const float4*>(sm_o + w * kGroup * T::kOStride + off);
-          acc.x += x.x;
-          acc.y += x.y;
-          acc.z += x.z;
-          acc.w += x.w;
-        }
-        *reinterpret_cast<float4*>(dst + e) = acc;
-      }
-      if (ct < kGroup) {
+        const int hh = e >> 7;      // head of these 4 outputs
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < T::kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kGroup + ct]);
+        for (int w = 0; w < T::kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kGroup + hh]);
+        const float Ms = M == -INFINITY ? 0.f : M;
         float L = 0.f;
-        if (M != -INFINITY) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int w = 0; w < T::kConsumerWarps; ++w)
-            L += sm_l[w * kGroup + ct] * exp2f(sm_m[w * kGroup + ct] - M);
+        for (int w = 0; w < T::kConsumerWarps; ++w) {
+          const float wt = exp2_ftz(sm_m[w * kGroup + hh] - Ms);
+          L += wt * sm_l[w * kGroup + hh];
+          const float4 x =
+              *reinterpret_cast<const float4*>(sm_o + (w * kGroup + hh) * T::kOStride + (e & 127));
+          acc.x += wt * x.x;
+          acc.y += wt * x.y;
+          acc.z += wt * x.z;
+          acc.w += wt * x.w;
         }
-        partial_lse[static_cast<int64_t>(i) * kGroup + ct] =
-            L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        const float inv = L > 0.f ? v_scale / L : 0.f;
+        if (direct) {
+          uint2 packed;
+          packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+          packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+          // segment s holds rows s*8 .. s*8+7 of the [batch*64, 128] output
+          *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
+        } else {
+          *reinterpret_cast<float4*>(dst + e) =
+              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          if ((e & 127) == 0)
+            partial_lse[static_cast<int64_t>(i) * kGroup + hh] =
+                L > 0.f ? (Ms + log2f(L)) * 0.6931471805599453f : -INFINITY;
+        }
       }
     }
-    named_bar_sync(1, 32 * T::kConsumerWarps);
+    if (fuse && it.ok && !direct) {
+      __threadfence();             // this CTA's partial is visible device-wide...
+      if (!cons_sync()) break;     // ...for every writer, before the count
+      if (threadIdx.x == 0) {
+        const int done = atomicAdd(&seg_done[seg], 1);
+        *merge_flag = done == seg_items - 1;
+        if (done == seg_items - 1) {
+          seg_done[seg] = 0;       // reset for the next run of this plan
+          __threadfence();
+        }
+      }
+      if (!cons_sync()) break;
+      if (*merge_flag) {
+        // the last item of the segment: merge its partials.  The lse values
+        // are staged in shared memory (the merge slices are free now) by one
+        // parallel load, so the per-thread loop is a single pass of
+        // independent float4 loads through L2; segments of more than
+        // kMergeChunk items are taken chunk by chunk with an online rescale.
+        constexpr int kMergeChunk = 1024;
+        static_assert(kMergeChunk * kGroup <= T::kConsumerWarps * kGroup * T::kOStride,
+                      "the lse staging area must fit in the merge slices");
+        static_assert(32 * T::kConsumerWarps * 4 == kGroup * kD, "one float4 of output per thread");
+        float* lse_s = sm_o;
+        const int i0 = seg_ptr[seg];
+        const int e = threadIdx.x * 4;
+        const int hh = e >> 7;
+        float M = -INFINITY, W = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool synced = true;
+        for (int base = 0; base < seg_items && synced; base += kMergeChunk) {
+          const int m = min(kMergeChunk, seg_items - base);
+          for (int x = threadIdx.x; x < m * kGroup; x += 32 * T::kConsumerWarps)
+            lse_s[x] = __ldcg(partial_lse + static_cast<int64_t>(i0 + base) * kGroup + x);
+          if (!(synced = cons_sync())) break;
+          float Mn = M;
+          for (int k = 0; k < m; ++k) Mn = fmaxf(Mn, lse_s[k * kGroup + hh]);
+          if (Mn != -INFINITY) {
+            const float sc = __expf(M - Mn);   // 0 while M is still -inf
+            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+            W *= sc;
+            const float* po = partial_o + static_cast<int64_t>(i0 + base) * kGroup * kD + e;
+#pragma unroll 8
+            for (int k = 0; k < m; ++k) {
+              const float w = __expf(lse_s[k * kGroup + hh] - Mn);
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * kGroup * kD));
+              acc.x += w * x.x;
+              acc.y += w * x.y;
+              acc.z += w * x.z;
+              acc.w += w * x.w;
+              W += w;
+            }
+            M = Mn;
+          }
+          synced = cons_sync();   // before the staging area is overwritten
+        }
+        if (!synced) break;
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        uint2 packed;
+        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
+      }
+    }
+    if (!cons_sync()) break;
   }
+  if (cta_clock != nullptr && threadIdx.x == 0) record_cta_clock(cta_clock, t_start);
 }
 
 // ------------------------------------------------------------ host side
@@ -478,7 +738,8 @@ template <bool kFp8>
 int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int32_t num_blocks,
                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
                 int32_t batch, const hpc_plan* plan, float* partial_o, float* partial_lse,
-                float sm_scale, int32_t* status, cudaStream_t stream) {
+                float sm_scale, int32_t* status, unsigned long long* cta_clock, uint16_t* out,
+                bool pdl, cudaStream_t stream) {
   using T = AttnTraits<kFp8>;
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
@@ -495,14 +756,56 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
-  decode_attn_kernel<kFp8><<<plan->num_ctas, T::kThreads, T::kSmemBytes, stream>>>(
-      map, static_cast<const uint16_t*>(q), kv_scale, block_table, max_blocks, num_blocks, seq_lens,
-      batch, plan->items, plan->cta_ptr, plan->capacity, partial_o, partial_lse, sm_scale, status);
-  return HPC_LAUNCH_STATUS();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan->num_ctas);
+  cfg.blockDim = dim3(T::kThreads);
+  cfg.dynamicSmemBytes = T::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, decode_attn_kernel<kFp8>, map, static_cast<const uint16_t*>(q), kv_scale, block_table,
+      max_blocks, num_blocks, seq_lens, batch, static_cast<const hpc_work_item*>(plan->items),
+      static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
+      plan->pool, plan->capacity, partial_o, partial_lse, sm_scale, status, cta_clock,
+      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out);
+  return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
 
 }  // namespace
 }  // namespace hpc
+
+int hpc::launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
+                            const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
+                            int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                            const hpc_plan* plan, float* partial_o, float* partial_lse,
+                            float sm_scale, int32_t* status, unsigned long long* cta_clock,
+                            void* out, bool pdl, cudaStream_t stream) {
+  HPC_CHECK_ARG(q && kv_cache && block_table && seq_lens && plan && partial_o && partial_lse &&
+                status && plan->items && plan->cta_ptr && plan->home_end && plan->pool);
+  HPC_CHECK_ARG(num_blocks > 0 && max_blocks >= 1 && batch >= 0 && plan->num_ctas >= 1 &&
+                plan->capacity >= 0);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
+  if (out != nullptr) HPC_CHECK_ARG(plan->seg_ptr && plan->seg_done);
+  if (num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
+  if (plan->num_ctas > 0x7fffffff - 1) return HPC_ERR_UNSUPPORTED;
+  if (kv_dtype == HPC_KV_BF16)
+    return hpc::launch_attn<false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                   seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
+                                   cta_clock, static_cast<uint16_t*>(out), pdl, stream);
+  if (kv_dtype == HPC_KV_FP8_E4M3) {
+    HPC_CHECK_ARG(kv_scale != nullptr);
+    return hpc::launch_attn<true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                  seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
+                                  cta_clock, static_cast<uint16_t*>(out), pdl, stream);
+  }
+  return HPC_ERR_UNSUPPORTED;
+}
 
 extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
                                const float* kv_scale, int32_t num_blocks,
@@ -510,26 +813,34 @@ extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_d
                                const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
                                float* partial_o, float* partial_lse, float sm_scale,
                                int32_t* status, cudaStream_t stream) {
-  HPC_CHECK_ARG(q && kv_cache && block_table && seq_lens && plan && partial_o && partial_lse &&
-                status && plan->items && plan->cta_ptr);
-  HPC_CHECK_ARG(num_blocks > 0 && max_blocks >= 1 && batch >= 0 && plan->num_ctas >= 1 &&
-                plan->capacity >= 0);
-  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
-  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
-  if (num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
-  if (plan->num_ctas > 0x7fffffff - 1) return HPC_ERR_UNSUPPORTED;
-  if (kv_dtype == HPC_KV_BF16)
-    return hpc::launch_attn<false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                   seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
-                                   stream);
-  if (kv_dtype == HPC_KV_FP8_E4M3) {
-    HPC_CHECK_ARG(kv_scale != nullptr);
-    return hpc::launch_attn<true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                  seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
-                                  stream);
-  }
-  return HPC_ERR_UNSUPPORTED;
+  return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 sm_scale, status, nullptr, nullptr, false, stream);
+}
+
+extern "C" int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int32_t kv_dtype,
+                                        const float* kv_scale, int32_t num_blocks,
+                                        const int32_t* block_table, int32_t max_blocks,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        const hpc_plan* plan, float* partial_o,
+                                        float* partial_lse, float sm_scale, int32_t* status,
+                                        unsigned long long* cta_clock, cudaStream_t stream) {
+  HPC_CHECK_ARG(cta_clock != nullptr);
+  return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 sm_scale, status, cta_clock, nullptr, false, stream);
+}
+
+extern "C" int hpc_decode_attn_merge(const void* q, const void* kv_cache, int32_t kv_dtype,
+                                     const float* kv_scale, int32_t num_blocks,
+                                     const int32_t* block_table, int32_t max_blocks,
+                                     const int32_t* seq_lens, int32_t batch, const hpc_plan* plan,
+                                     float* partial_o, float* partial_lse, void* out,
+                                     float sm_scale, int32_t* status, cudaStream_t stream) {
+  HPC_CHECK_ARG(out != nullptr);
+  return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 sm_scale, status, nullptr, out, false, stream);
 }
 
 extern "C" int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas) {

@@ -172,11 +172,28 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   return y;
 }
 
+// 2^x for x <= 0 (softmax weights): the hardware approximation, results
+// below 2^-126 flushed to zero, 2^-inf = 0.
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
+
+// Programmatic dependent launch: the primary grid lets its dependent grid be
+// scheduled early (trigger); the dependent waits for the primary grid to have
+// completed and its memory to be visible before touching its outputs (wait).
+// Without a programmatic launch both are no-ops.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Named barrier among `nthreads` threads (a multiple of 32), id >= 1.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -31,10 +31,14 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   if (i1 - i0 == 1) {
     acc = *reinterpret_cast<const float4*>(partial_o + (static_cast<int64_t>(i0) * kGroup + r) * kD + d);
   } else if (i1 > i0) {
+    // both loops are unrolled so that several partials are in flight at once
+    // (a long sequence's segment holds tens of items)
     float M = -INFINITY;
+#pragma unroll 8
     for (int i = i0; i < i1; ++i) M = fmaxf(M, partial_lse[static_cast<int64_t>(i) * kGroup + r]);
     if (M != -INFINITY) {
       float wsum = 0.f;
+#pragma unroll 8
       for (int i = i0; i < i1; ++i) {
         const float w = expf(partial_lse[static_cast<int64_t>(i) * kGroup + r] - M);
         const float4 o =

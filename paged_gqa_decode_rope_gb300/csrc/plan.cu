@@ -17,154 +17,48 @@
 // on CTA floor(S0 / q) + j, and the first item of CTA c is the one that holds
 // flat tile c*q.  Two block-wide scans (tiles, then items) give every index in
 // closed form; no thread walks another thread's data.
-#include "common.cuh"
+//
+// Runtime dealing of the tail (pool_chunks = J > 0): SMs do not stream at
+// exactly the same rate, so equal ranges finish apart.  The last
+// P = floor(q / 8) tiles of every range are cut into chunks of ceil(P / J)
+// tiles (no pool at all when that is below pool_min_tiles: short chunks cost
+// more in per-item work than they save); the planner lists them, in CTA
+// order, in a pool.  A CTA first runs
+// its home part [c*q, c*q + q - P), then claims pool chunks through one
+// atomic counter until the pool is empty.  Cutting at the piece boundaries
+// just refines the cuts above, so the items stay in flat order and every
+// (seq, kv_head) segment's items stay contiguous for the merge.
+#include <mutex>
+
+
+#include "plan_body.cuh"
 
 namespace hpc {
 namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Exclusive scan of one int per thread over the CTA; *total gets the sum.
-__device__ int cta_exclusive_scan(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int s = lane < (kPlanThreads / 32) ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    warp_sums[lane] = s;
-  }
-  __syncthreads();
-  const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
-  *total = warp_sums[31];
-  __syncthreads();   // warp_sums is reused by the next scan
-  return excl;
-}
-
-__device__ __forceinline__ int tiles_of(const int32_t* seq_lens, int b, int max_blocks,
-                                        int32_t* status) {
-  const int L = seq_lens[b];
-  if (L < 0 || L > max_blocks * kPage) {
-    atomicOr(status, HPC_STATUS_BAD_SEQ_LEN);
-    return 0;
-  }
-  return (L + kPage - 1) / kPage;
-}
-
-__device__ void write_empty_plan(int batch, int num_ctas, int32_t* cta_ptr, int32_t* seg_ptr) {
-  for (int c = threadIdx.x; c <= num_ctas; c += kPlanThreads) cta_ptr[c] = 0;
-  for (int s = threadIdx.x; s <= batch * kHkv; s += kPlanThreads) seg_ptr[s] = 0;
-}
-
 __global__ void __launch_bounds__(kPlanThreads) plan_dynamic_kernel(
-    const int32_t* __restrict__ seq_lens, int batch, int max_blocks, int min_tiles,
-    hpc_work_item* __restrict__ items, int32_t* __restrict__ cta_ptr, int32_t* seg_ptr,
-    int capacity, int num_ctas, int32_t* __restrict__ status) {
-  extern __shared__ int pre_n[];       // [batch + 1]: sum of n_b' for b' < b
-  __shared__ int warp_sums[32];
-  const int per = (batch + kPlanThreads - 1) / kPlanThreads;
-  const int b0 = min(batch, static_cast<int>(threadIdx.x) * per);
-  const int b1 = min(batch, b0 + per);
-
-  // 1. tiles per sequence and their prefix
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += tiles_of(seq_lens, b, max_blocks, status);
-  int total_n;
-  int run = cta_exclusive_scan(local, warp_sums, &total_n);
-  for (int b = b0; b < b1; ++b) {
-    pre_n[b] = run;
-    const int L = seq_lens[b];
-    run += (L < 0 || L > max_blocks * kPage) ? 0 : (L + kPage - 1) / kPage;
-  }
-  if (threadIdx.x == 0) pre_n[batch] = total_n;
-  __syncthreads();
-
-  const int64_t T = static_cast<int64_t>(kHkv) * total_n;
-  const int64_t q = max(static_cast<int64_t>(min_tiles), (T + num_ctas - 1) / num_ctas);
-
-  // 2. items per sequence (its 8 segments) and their prefix
-  local = 0;
-  for (int b = b0; b < b1; ++b) {
-    const int n = pre_n[b + 1] - pre_n[b];
-    if (n == 0) continue;
-    for (int h = 0; h < kHkv; ++h) {
-      const int64_t s0 = static_cast<int64_t>(kHkv) * pre_n[b] + static_cast<int64_t>(h) * n;
-      local += static_cast<int>((s0 + n - 1) / q - s0 / q + 1);
-    }
-  }
-  int total_items;
-  run = cta_exclusive_scan(local, warp_sums, &total_items);
-  if (total_items > capacity) {
-    if (threadIdx.x == 0) atomicOr(status, HPC_STATUS_PLAN_OVERFLOW);
-    write_empty_plan(batch, num_ctas, cta_ptr, seg_ptr);
-    return;
-  }
-
-  // 3. segment offsets and the items themselves
-  for (int b = b0; b < b1; ++b) {
-    const int n = pre_n[b + 1] - pre_n[b];
-    for (int h = 0; h < kHkv; ++h) {
-      seg_ptr[b * kHkv + h] = run;
-      if (n == 0) continue;
-      const int64_t s0 = static_cast<int64_t>(kHkv) * pre_n[b] + static_cast<int64_t>(h) * n;
-      const int64_t s1 = s0 + n;
-      const int64_t c0 = s0 / q;
-      const int cnt = static_cast<int>((s1 - 1) / q - c0 + 1);
-      for (int j = 0; j < cnt; ++j) {
-        const int64_t lo = max(s0, (c0 + j) * q);
-        const int64_t hi = min(s1, (c0 + j + 1) * q);
-        hpc_work_item it;
-        it.seq = b;
-        it.kv_head = h;
-        it.tile_begin = static_cast<int32_t>(lo - s0);
-        it.tile_end = static_cast<int32_t>(hi - s0);
-        items[run + j] = it;
-      }
-      run += cnt;
-    }
-  }
-  if (threadIdx.x == 0) seg_ptr[batch * kHkv] = total_items;
-  __syncthreads();   // seg_ptr is read below by other threads
-
-  // 4. first item of every CTA: the item that holds flat tile c*q
-  for (int c = threadIdx.x; c <= num_ctas; c += kPlanThreads) {
-    const int64_t f = static_cast<int64_t>(c) * q;
-    if (c == num_ctas || f >= T) {
-      cta_ptr[c] = total_items;
-      continue;
-    }
-    // last sequence b with 8*pre_n[b] <= f (it has n_b > 0 because f < T)
-    int lo = 0, hi = batch;   // invariant: 8*pre_n[lo] <= f < 8*pre_n[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (static_cast<int64_t>(kHkv) * pre_n[mid] <= f) lo = mid; else hi = mid;
-    }
-    const int b = lo;
-    const int n = pre_n[b + 1] - pre_n[b];
-    const int h = static_cast<int>((f - static_cast<int64_t>(kHkv) * pre_n[b]) / n);
-    const int64_t s0 = static_cast<int64_t>(kHkv) * pre_n[b] + static_cast<int64_t>(h) * n;
-    cta_ptr[c] = seg_ptr[b * kHkv + h] + static_cast<int>(c - s0 / q);
-  }
+    const int32_t* __restrict__ seq_lens, int batch, int max_blocks, int min_tiles, int pool_chunks,
+    int pool_min_tiles, hpc_work_item* __restrict__ items, int32_t* cta_ptr, int32_t* seg_ptr,
+    int32_t* home_end, int32_t* __restrict__ pool, int32_t* __restrict__ seg_done, int capacity,
+    int num_ctas, int32_t* __restrict__ status) {
+  extern __shared__ int plan_smem[];
+  plan_dynamic_body<kPlanThreads>(seq_lens, batch, max_blocks, min_tiles, pool_chunks, pool_min_tiles,
+                                  items, cta_ptr, seg_ptr, home_end, pool, seg_done, capacity,
+                                  num_ctas, status, plan_smem);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_static_kernel(
     const int32_t* __restrict__ seq_lens, int batch, int max_blocks, int splits,
     hpc_work_item* __restrict__ items, int32_t* __restrict__ cta_ptr, int32_t* __restrict__ seg_ptr,
+    int32_t* __restrict__ home_end, int32_t* __restrict__ pool, int32_t* __restrict__ seg_done,
     int capacity, int num_ctas, int32_t* __restrict__ status) {
   __shared__ int warp_sums[32];
   const int per = (batch + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(batch, static_cast<int>(threadIdx.x) * per);
   const int b1 = min(batch, b0 + per);
+  for (int x = threadIdx.x; x < batch * kHkv; x += kPlanThreads) seg_done[x] = 0;
 
   int local = 0;
   for (int b = b0; b < b1; ++b) {
@@ -174,10 +68,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_static_kernel(
     local += kHkv * ((n + chunk - 1) / chunk);
   }
   int total_items;
-  int run = cta_exclusive_scan(local, warp_sums, &total_items);
+  int run = cta_exclusive_scan<kPlanThreads>(local, warp_sums, &total_items);
+  if (threadIdx.x == 0) pool[0] = pool[1] = pool[2] = 0;   // a static plan has no pool
   if (total_items > capacity) {
     if (threadIdx.x == 0) atomicOr(status, HPC_STATUS_PLAN_OVERFLOW);
-    write_empty_plan(batch, num_ctas, cta_ptr, seg_ptr);
+    write_empty_plan<kPlanThreads>(batch, num_ctas, cta_ptr, seg_ptr);
+    for (int c = threadIdx.x; c < num_ctas; c += kPlanThreads) home_end[c] = 0;
     return;
   }
   for (int b = b0; b < b1; ++b) {
@@ -197,12 +93,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_static_kernel(
     }
   }
   if (threadIdx.x == 0) seg_ptr[batch * kHkv] = total_items;
-  for (int c = threadIdx.x; c <= num_ctas; c += kPlanThreads) cta_ptr[c] = min(c, total_items);
+  for (int c = threadIdx.x; c <= num_ctas; c += kPlanThreads) {
+    cta_ptr[c] = min(c, total_items);
+    if (c < num_ctas) home_end[c] = min(c + 1, total_items);
+  }
+}
+
+// Dynamic shared memory above 48 KB needs a per-device opt-in (batches over
+// 6143 sequences); done once per device with the largest size the batch cap
+// allows.
+cudaError_t plan_smem_optin(size_t) {
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(plan_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(2 * sizeof(int) * (HPC_MAX_BATCH + 1)));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
 }
 
 int check_plan_args(const int32_t* seq_lens, int32_t batch, int32_t max_blocks, const hpc_plan* plan,
                     const int32_t* status) {
-  HPC_CHECK_ARG(seq_lens && plan && status && plan->items && plan->cta_ptr && plan->seg_ptr);
+  HPC_CHECK_ARG(seq_lens && plan && status && plan->items && plan->cta_ptr && plan->seg_ptr &&
+                plan->home_end && plan->pool && plan->seg_done);
   HPC_CHECK_ARG(batch >= 0 && max_blocks >= 1 && plan->num_ctas >= 1 && plan->capacity >= 0);
   if (batch > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
   // keep the flat tile count 8 * sum(n_b) inside int32
@@ -214,20 +131,26 @@ int check_plan_args(const int32_t* seq_lens, int32_t batch, int32_t max_blocks, 
 }  // namespace
 }  // namespace hpc
 
-extern "C" int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas) {
-  return num_ctas + hpc::kHkv * batch;
+extern "C" int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas, int32_t pool_chunks) {
+  return num_ctas * (1 + (pool_chunks > 0 ? pool_chunks : 0)) + hpc::kHkv * batch;
 }
 
 extern "C" int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
-                               int32_t min_tiles, hpc_plan* plan, int32_t* status,
+                               const hpc_plan_params* params, hpc_plan* plan, int32_t* status,
                                cudaStream_t stream) {
   const int rc = hpc::check_plan_args(seq_lens, batch, max_blocks, plan, status);
   if (rc != HPC_OK) return rc;
-  HPC_CHECK_ARG(min_tiles >= 1);
-  const size_t smem = sizeof(int) * (static_cast<size_t>(batch) + 1);
+  const hpc_plan_params def = {1, HPC_DEFAULT_POOL_CHUNKS, HPC_DEFAULT_POOL_MIN_TILES};
+  const hpc_plan_params& pp = params != nullptr ? *params : def;
+  const int min_tiles = pp.min_tiles, pool_chunks = pp.pool_chunks;
+  HPC_CHECK_ARG(min_tiles >= 1 && pool_chunks >= 0 && pool_chunks <= 64 && pp.pool_min_tiles >= 1);
+  const size_t smem = 2 * sizeof(int) * (static_cast<size_t>(batch) + 1);
+  if (smem > 48 * 1024 && hpc::plan_smem_optin(smem) != cudaSuccess) return HPC_ERR_CUDA;
   hpc::plan_dynamic_kernel<<<1, hpc::kPlanThreads, smem, stream>>>(
-      seq_lens, batch, max_blocks, min_tiles, plan->items, plan->cta_ptr, plan->seg_ptr,
-      plan->capacity, plan->num_ctas, status);
+      seq_lens, batch, max_blocks, min_tiles, pool_chunks, pp.pool_min_tiles, plan->items,
+      plan->cta_ptr,
+      plan->seg_ptr, plan->home_end, plan->pool, plan->seg_done, plan->capacity, plan->num_ctas,
+      status);
   return HPC_LAUNCH_STATUS();
 }
 
@@ -241,6 +164,6 @@ extern "C" int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, in
   HPC_CHECK_ARG(plan->capacity >= plan->num_ctas);
   hpc::plan_static_kernel<<<1, hpc::kPlanThreads, 0, stream>>>(
       seq_lens, batch, max_blocks, splits, plan->items, plan->cta_ptr, plan->seg_ptr,
-      plan->capacity, plan->num_ctas, status);
+      plan->home_end, plan->pool, plan->seg_done, plan->capacity, plan->num_ctas, status);
   return HPC_LAUNCH_STATUS();
 }

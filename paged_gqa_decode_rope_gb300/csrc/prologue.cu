@@ -14,7 +14,7 @@
 // 64+2l+1 of its head, so each RoPE pair (i, i+64) lives in one lane and the
 // row loads are two coalesced 128-byte segments.  A head is ~0.5 KB of
 // traffic: the kernel is latency-bound, not bandwidth-bound.
-#include "common.cuh"
+#include "prologue_body.cuh"
 
 namespace hpc {
 namespace {
@@ -41,88 +41,8 @@ __global__ void __launch_bounds__(256) prologue_kernel(
     const uint16_t* __restrict__ q_w, const uint16_t* __restrict__ k_w, float eps,
     uint8_t* __restrict__ kv_cache, int32_t num_blocks, const int64_t* __restrict__ slot_mapping,
     const float* __restrict__ kv_scale, uint16_t* q_out, int32_t* __restrict__ status) {
-  const int b = blockIdx.y;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const bool is_kv = blockIdx.x == kGroup;   // the 9th CTA of a sequence
-
-  const int32_t pos = positions[b];
-  if (pos < 0 || pos >= max_pos) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, HPC_STATUS_BAD_POSITION);
-    return;
-  }
-  const int d0 = 2 * lane;          // this lane's first-half pair index
-  const float2 cs = *reinterpret_cast<const float2*>(cos_sin + static_cast<int64_t>(pos) * kD + d0);
-  const float2 sn = *reinterpret_cast<const float2*>(cos_sin + static_cast<int64_t>(pos) * kD + kD / 2 + d0);
-
-  const uint16_t* src;
-  const uint16_t* w;
-  if (!is_kv) {
-    src = q + (static_cast<int64_t>(b) * kHq + blockIdx.x * kGroup + warp) * kD;
-    w = q_w;
-  } else {
-    src = k + (static_cast<int64_t>(b) * kHkv + warp) * kD;
-    w = k_w;
-  }
-  const uint32_t xa = *reinterpret_cast<const uint32_t*>(src + d0);
-  const uint32_t xb = *reinterpret_cast<const uint32_t*>(src + kD / 2 + d0);
-  const float a0 = bf16_lo(xa), a1 = bf16_hi(xa);   // x[2l], x[2l+1]
-  const float b0 = bf16_lo(xb), b1 = bf16_hi(xb);   // x[64+2l], x[64+2l+1]
-
-  // RoPE: pair (i, i+64) turns by the table angle of row `pos`.
-  const float r0 = a0 * cs.x - b0 * sn.x;
-  const float r1 = a1 * cs.y - b1 * sn.y;
-  const float r2 = b0 * cs.x + a0 * sn.x;
-  const float r3 = b1 * cs.y + a1 * sn.y;
-
-  // RMSNorm over the 128 elements of the head.
-  float ss = r0 * r0 + r1 * r1 + r2 * r2 + r3 * r3;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps);
-  const uint32_t wa = *reinterpret_cast<const uint32_t*>(w + d0);
-  const uint32_t wb = *reinterpret_cast<const uint32_t*>(w + kD / 2 + d0);
-  const float y0 = r0 * inv * bf16_lo(wa), y1 = r1 * inv * bf16_hi(wa);
-  const float y2 = r2 * inv * bf16_lo(wb), y3 = r3 * inv * bf16_hi(wb);
-
-  if (!is_kv) {
-    uint16_t* dst = q_out + (static_cast<int64_t>(b) * kHq + blockIdx.x * kGroup + warp) * kD;
-    *reinterpret_cast<uint32_t*>(dst + d0) = pack_bf16(y0, y1);
-    *reinterpret_cast<uint32_t*>(dst + kD / 2 + d0) = pack_bf16(y2, y3);
-    return;
-  }
-
-  // K and V of KV head `warp` go to the cache slot of this sequence.
-  const int64_t slot = slot_mapping[b];
-  if (slot < 0) return;                                   // padding entry
-  if (slot >= static_cast<int64_t>(num_blocks) * kPage) {
-    if (lane == 0) atomicOr(status, HPC_STATUS_BAD_SLOT);
-    return;
-  }
-  const int64_t blk = slot / kPage;
-  const int off = static_cast<int>(slot % kPage);
-  const int64_t k_row = ((blk * 2 + 0) * kHkv + warp) * kPage + off;   // [blk][0][h][off]
-  const int64_t v_row = ((blk * 2 + 1) * kHkv + warp) * kPage + off;   // [blk][1][h][off]
-  const uint16_t* vsrc = v + (static_cast<int64_t>(b) * kHkv + warp) * kD;
-  const uint32_t va = *reinterpret_cast<const uint32_t*>(vsrc + d0);
-  const uint32_t vb = *reinterpret_cast<const uint32_t*>(vsrc + kD / 2 + d0);
-
-  if constexpr (!kFp8) {
-    uint16_t* kc = reinterpret_cast<uint16_t*>(kv_cache);
-    *reinterpret_cast<uint32_t*>(kc + k_row * kD + d0) = pack_bf16(y0, y1);
-    *reinterpret_cast<uint32_t*>(kc + k_row * kD + kD / 2 + d0) = pack_bf16(y2, y3);
-    *reinterpret_cast<uint32_t*>(kc + v_row * kD + d0) = va;
-    *reinterpret_cast<uint32_t*>(kc + v_row * kD + kD / 2 + d0) = vb;
-  } else {
-    const float ks = kv_scale[0], vs = kv_scale[1];
-    uint8_t* kc = kv_cache;
-    *reinterpret_cast<uint16_t*>(kc + k_row * kD + d0) = f32x2_to_e4m3x2(y0 / ks, y1 / ks);
-    *reinterpret_cast<uint16_t*>(kc + k_row * kD + kD / 2 + d0) = f32x2_to_e4m3x2(y2 / ks, y3 / ks);
-    *reinterpret_cast<uint16_t*>(kc + v_row * kD + d0) =
-        f32x2_to_e4m3x2(bf16_lo(va) / vs, bf16_hi(va) / vs);
-    *reinterpret_cast<uint16_t*>(kc + v_row * kD + kD / 2 + d0) =
-        f32x2_to_e4m3x2(bf16_lo(vb) / vs, bf16_hi(vb) / vs);
-  }
+  prologue_heads<kFp8>(blockIdx.y, blockIdx.x, q, k, v, positions, cos_sin, max_pos, q_w, k_w, eps,
+                       kv_cache, num_blocks, slot_mapping, kv_scale, q_out, status);
 }
 
 }  // namespace

@@ -12,13 +12,15 @@ import math
 import torch
 
 from . import _lib
-from ._lib import Plan, check
+from ._lib import Plan, PlanParams, check
 
 KV_BF16 = 0
 KV_FP8 = 1
 HQ, HKV, D, PAGE = 64, 8, 128, 64
 THETA = 1.0e6
 EPS = 1.0e-6
+POOL_CHUNKS = 4          # tail chunks per CTA range dealt at run time
+POOL_MIN_TILES = 16      # shorter chunks are not worth dealing: no pool then
 
 
 def _p(t):
@@ -64,18 +66,25 @@ def num_ctas(kv_dtype=KV_BF16):
 class DecodePlan:
     """Device buffers of a split-KV plan plus the C struct that points at them."""
 
-    def __init__(self, batch, n_ctas, capacity, device):
+    def __init__(self, batch, n_ctas, capacity, device, pool_chunks=0, pool_min_tiles=POOL_MIN_TILES):
         self.batch, self.num_ctas, self.capacity = batch, n_ctas, capacity
+        self.pool_chunks, self.pool_min_tiles = pool_chunks, pool_min_tiles
         self.items = torch.empty((max(capacity, 1), 4), dtype=torch.int32, device=device)
         self.cta_ptr = torch.empty(n_ctas + 1, dtype=torch.int32, device=device)
         self.seg_ptr = torch.empty(batch * HKV + 1, dtype=torch.int32, device=device)
+        self.home_end = torch.empty(n_ctas, dtype=torch.int32, device=device)
+        self.pool = torch.zeros(3 + max(capacity, 1), dtype=torch.int32, device=device)
+        self.seg_done = torch.zeros(max(batch * HKV, 1), dtype=torch.int32, device=device)
         self.c = Plan(self.items.data_ptr(), self.cta_ptr.data_ptr(), self.seg_ptr.data_ptr(),
+                      self.home_end.data_ptr(), self.pool.data_ptr(), self.seg_done.data_ptr(),
                       capacity, n_ctas)
 
     @classmethod
-    def dynamic(cls, batch, device="cuda", n_ctas=None, kv_dtype=KV_BF16):
+    def dynamic(cls, batch, device="cuda", n_ctas=None, kv_dtype=KV_BF16, pool_chunks=POOL_CHUNKS,
+                pool_min_tiles=POOL_MIN_TILES):
         n_ctas = num_ctas(kv_dtype) if n_ctas is None else n_ctas
-        return cls(batch, n_ctas, _lib.lib().hpc_plan_capacity(batch, n_ctas), device)
+        cap = _lib.lib().hpc_plan_capacity(batch, n_ctas, pool_chunks)
+        return cls(batch, n_ctas, cap, device, pool_chunks, pool_min_tiles)
 
     @classmethod
     def static(cls, batch, splits, device="cuda"):
@@ -119,8 +128,9 @@ def rope_norm_kvwrite(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache,
 def decode_plan(seq_lens, max_blocks, plan, status, min_tiles=1):
     _want(seq_lens, "seq_lens", (torch.int32,), (plan.batch,))
     _want(status, "status", (torch.int32,), (1,))
+    params = PlanParams(int(min_tiles), int(plan.pool_chunks), int(plan.pool_min_tiles))
     check("hpc_decode_plan", _lib.lib().hpc_decode_plan(
-        _p(seq_lens), plan.batch, int(max_blocks), int(min_tiles), ctypes.byref(plan.c),
+        _p(seq_lens), plan.batch, int(max_blocks), ctypes.byref(params), ctypes.byref(plan.c),
         _p(status), _stream()))
 
 
@@ -159,6 +169,76 @@ def decode_attn(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, pa
         ctypes.byref(plan.c), _p(partial_o), _p(partial_lse), scale, _p(status), _stream()))
 
 
+def decode_attn_profiled(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                         partial_lse, status, cta_clock, sm_scale=None):
+    """hpc_decode_attn that also records [start ns, end ns, SM id] per CTA."""
+    B = q.shape[0]
+    _want(cta_clock, "cta_clock", (torch.int64,), (plan.num_ctas, 3))
+    _want(q, "q", _BF16, (B, HQ, D))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    _want(block_table, "block_table", (torch.int32,))
+    _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+    _want(status, "status", (torch.int32,), (1,))
+    if partial_o.numel() < plan.capacity * HKV * D or partial_lse.numel() < plan.capacity * HKV:
+        raise ValueError("partial buffers are smaller than the plan capacity")
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    check("hpc_decode_attn_profiled", _lib.lib().hpc_decode_attn_profiled(
+        _p(q), _p(kv_cache), kv_dtype, _p(kv_scale if kv_dtype == KV_FP8 else None),
+        kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(seq_lens), B,
+        ctypes.byref(plan.c), _p(partial_o), _p(partial_lse), scale, _p(status), _p(cta_clock),
+        _stream()))
+
+
+def cta_occupancy(cta_clock):
+    """SM occupancy and tail idle of one profiled launch.
+
+    From per-CTA [start, end, sm] records: span = last end - first start;
+    occupancy = sum of CTA busy time / (SMs used x span); tail idle = mean
+    over SMs of (last end overall - that SM's last end)."""
+    rec = cta_clock.cpu().numpy()
+    rec = rec[rec[:, 1] > 0]
+    t0, t1 = rec[:, 0].min(), rec[:, 1].max()
+    span = float(t1 - t0)
+    sms = {}
+    for st, en, sm in rec.tolist():
+        b = sms.setdefault(sm, [0, 0])
+        b[0] += en - st
+        b[1] = max(b[1], en)
+    busy = sum(v[0] for v in sms.values())
+    tail = sum(t1 - v[1] for v in sms.values()) / len(sms)
+    return {"span_us": round(span / 1e3, 2), "sms": len(sms),
+            "occupancy": round(busy / (len(sms) * span), 4), "tail_idle_us": round(tail / 1e3, 2),
+            "ctas": int(len(rec))}
+
+
+def decode_attn_merge(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                      partial_lse, out, status, sm_scale=None):
+    """Attention with the log-sum-exp merge fused in: writes ``out`` directly."""
+    B = q.shape[0]
+    _want(q, "q", _BF16, (B, HQ, D))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    if kv_cache.dim() != 5 or tuple(kv_cache.shape[1:]) != (2, HKV, PAGE, D):
+        raise ValueError("kv_cache must be [num_blocks, 2, 8, 64, 128]")
+    if kv_dtype == KV_FP8:
+        _want(kv_scale, "kv_scale", (torch.float32,), (2,))
+    _want(block_table, "block_table", (torch.int32,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if plan.batch != B:
+        raise ValueError("plan was made for batch %d, not %d" % (plan.batch, B))
+    if partial_o.numel() < plan.capacity * HKV * D or partial_lse.numel() < plan.capacity * HKV:
+        raise ValueError("partial buffers are smaller than the plan capacity")
+    _want(out, "out", _BF16, (B, HQ, D))
+    _want(status, "status", (torch.int32,), (1,))
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    check("hpc_decode_attn_merge", _lib.lib().hpc_decode_attn_merge(
+        _p(q), _p(kv_cache), kv_dtype, _p(kv_scale if kv_dtype == KV_FP8 else None),
+        kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(seq_lens), B,
+        ctypes.byref(plan.c), _p(partial_o), _p(partial_lse), _p(out), scale, _p(status),
+        _stream()))
+
+
 def merge(partial_o, partial_lse, plan, out):
     B = plan.batch
     _want(partial_o, "partial_o", (torch.float32,))
@@ -168,20 +248,67 @@ def merge(partial_o, partial_lse, plan, out):
         _p(partial_o), _p(partial_lse), ctypes.byref(plan.c), B, _p(out), _stream()))
 
 
+def decode_step(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, kv_dtype, slot_mapping,
+                kv_scale, block_table, seq_lens, plan, partial_o, partial_lse, q_out, out, status,
+                min_tiles=1, eps=EPS, sm_scale=None):
+    """The whole step in two launches (hpc_decode_step)."""
+    B = q.shape[0]
+    _want(q, "q", _BF16, (B, HQ, D))
+    _want(k, "k", _BF16, (B, HKV, D))
+    _want(v, "v", _BF16, (B, HKV, D))
+    _want(positions, "positions", (torch.int32,), (B,))
+    _want(cos_sin, "cos_sin", (torch.float32,))
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != D:
+        raise ValueError("cos_sin must be [max_pos, 128]")
+    _want(q_norm_w, "q_norm_w", _BF16, (D,))
+    _want(k_norm_w, "k_norm_w", _BF16, (D,))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    if kv_cache.dim() != 5 or tuple(kv_cache.shape[1:]) != (2, HKV, PAGE, D):
+        raise ValueError("kv_cache must be [num_blocks, 2, 8, 64, 128]")
+    _want(slot_mapping, "slot_mapping", (torch.int64,), (B,))
+    if kv_dtype == KV_FP8:
+        _want(kv_scale, "kv_scale", (torch.float32,), (2,))
+    _want(block_table, "block_table", (torch.int32,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if plan.batch != B:
+        raise ValueError("plan was made for batch %d, not %d" % (plan.batch, B))
+    if partial_o.numel() < plan.capacity * HKV * D or partial_lse.numel() < plan.capacity * HKV:
+        raise ValueError("partial buffers are smaller than the plan capacity")
+    _want(q_out, "q_out", _BF16, (B, HQ, D))
+    _want(out, "out", _BF16, (B, HQ, D))
+    _want(status, "status", (torch.int32,), (1,))
+    params = PlanParams(int(min_tiles), int(plan.pool_chunks), int(plan.pool_min_tiles))
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    check("hpc_decode_step", _lib.lib().hpc_decode_step(
+        _p(q), _p(k), _p(v), _p(positions), _p(cos_sin), cos_sin.shape[0], _p(q_norm_w),
+        _p(k_norm_w), float(eps), _p(kv_cache), kv_dtype, kv_cache.shape[0], _p(slot_mapping),
+        _p(kv_scale if kv_dtype == KV_FP8 else None), _p(block_table), block_table.shape[1],
+        _p(seq_lens), B, ctypes.byref(params), ctypes.byref(plan.c), _p(partial_o),
+        _p(partial_lse), _p(q_out), _p(out), scale, _p(status), _stream()))
+
+
 class DecodeStep:
     """All four calls of one decode step, with the plan and partial buffers
     allocated once for a batch size (so the step can be graph-captured).
 
-    ``schedule`` is "dynamic" (length-proportional, the default) or
-    ("static", splits) for the equal-split comparator.
+    ``schedule`` is "dynamic" (length-proportional, the default, with
+    ``pool_chunks`` tail chunks per CTA dealt at run time; 0 = none) or
+    ("static", splits) for the equal-split comparator.  ``fused`` runs the
+    merge inside the attention kernel (hpc_decode_attn_merge) instead of the
+    separate hpc_decode_attn + hpc_merge pair.
     """
 
     def __init__(self, batch, kv_dtype, max_blocks, device="cuda", schedule="dynamic",
-                 min_tiles=1, n_ctas=None):
+                 min_tiles=1, n_ctas=None, pool_chunks=POOL_CHUNKS, fused=True,
+                 pool_min_tiles=POOL_MIN_TILES):
         self.batch, self.kv_dtype, self.max_blocks = batch, kv_dtype, max_blocks
         self.min_tiles = min_tiles
+        self.fused = fused
         if schedule == "dynamic":
-            self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype)
+            self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks,
+                                           pool_min_tiles)
             self.splits = None
         else:
             self.splits = int(schedule[1])
@@ -200,13 +327,25 @@ class DecodeStep:
             decode_plan_static(seq_lens, self.max_blocks, self.splits, self.plan, self.status)
 
     def attend(self, q, kv_cache, kv_scale, block_table, seq_lens):
-        decode_attn(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens, self.plan,
-                    self.partial_o, self.partial_lse, self.status)
-        merge(self.partial_o, self.partial_lse, self.plan, self.out)
+        if self.fused:
+            decode_attn_merge(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens,
+                              self.plan, self.partial_o, self.partial_lse, self.out, self.status)
+        else:
+            decode_attn(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens, self.plan,
+                        self.partial_o, self.partial_lse, self.status)
+            merge(self.partial_o, self.partial_lse, self.plan, self.out)
         return self.out
 
     def __call__(self, q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, slot_mapping,
-                 kv_scale, block_table, seq_lens):
+                 kv_scale, block_table, seq_lens, two_launch=True):
+        """One step.  With the dynamic plan and the fused merge the step runs
+        as two launches (hpc_decode_step) unless ``two_launch`` is False; the
+        other configurations make the four calls in order."""
+        if two_launch and self.fused and self.splits is None:
+            decode_step(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, self.kv_dtype,
+                        slot_mapping, kv_scale, block_table, seq_lens, self.plan, self.partial_o,
+                        self.partial_lse, self.q_out, self.out, self.status, self.min_tiles)
+            return self.out
         rope_norm_kvwrite(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, self.kv_dtype,
                           slot_mapping, kv_scale, self.q_out, self.status)
         self.plan_step(seq_lens)

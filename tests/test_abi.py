@@ -42,10 +42,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_host_argument_checks(lib):
-    from paged_gqa_decode_rope_gb300._lib import Plan, HPC_ERR_INVALID_ARG, HPC_ERR_UNSUPPORTED
+    from paged_gqa_decode_rope_gb300._lib import (Plan, PlanParams, HPC_ERR_INVALID_ARG,
+                                                  HPC_ERR_UNSUPPORTED)
     NULL = None
     fake = ctypes.c_void_p(4096)       # never dereferenced on the host
-    assert lib.hpc_plan_capacity(32, 152) == 152 + 256
+    assert lib.hpc_plan_capacity(32, 152, 0) == 152 + 256
+    assert lib.hpc_plan_capacity(32, 152, 6) == 152 * 7 + 256
     assert lib.hpc_rope_cos_sin_cache(1e6, 0, fake, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_rope_cos_sin_cache(1e6, 10, NULL, NULL) == HPC_ERR_INVALID_ARG
     # unknown KV dtype, null pointers, negative batch
@@ -59,11 +61,16 @@ def test_host_argument_checks(lib):
     assert lib.hpc_rope_norm_kvwrite(*args) == HPC_ERR_INVALID_ARG
     args[15] = 0
     assert lib.hpc_rope_norm_kvwrite(*args) == 0          # empty batch: nothing to launch
-    plan = Plan(4096, 4096, 4096, 100, 10)
+    plan = Plan(4096, 4096, 4096, 4096, 4096, 4096, 100, 10)
     st = fake
-    assert lib.hpc_decode_plan(fake, 4, 8, 0, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
-    assert lib.hpc_decode_plan(fake, 9000, 8, 1, ctypes.byref(plan), st, NULL) == HPC_ERR_UNSUPPORTED
-    assert lib.hpc_decode_plan(NULL, 4, 8, 1, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    P = lambda a, b, c: ctypes.byref(PlanParams(a, b, c))
+    assert lib.hpc_decode_plan(fake, 4, 8, P(0, 0, 1), ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_plan(fake, 4, 8, P(1, 65, 1), ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_plan(fake, 4, 8, P(1, 4, 0), ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_plan(fake, 9000, 8, None, ctypes.byref(plan), st, NULL) == HPC_ERR_UNSUPPORTED
+    assert lib.hpc_decode_plan(NULL, 4, 8, None, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    bad = Plan(4096, 4096, 4096, 0, 4096, 4096, 100, 10)  # no home_end array
+    assert lib.hpc_decode_plan(fake, 4, 8, None, ctypes.byref(bad), st, NULL) == HPC_ERR_INVALID_ARG
     # static plan: num_ctas must be batch * 8 * splits
     assert lib.hpc_decode_plan_static(fake, 4, 8, 2, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
     # attention: misaligned cache, too many blocks, unknown dtype

@@ -18,10 +18,14 @@ import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-def _run(wl, schedule="dynamic", n_ctas=None, min_tiles=1):
+def _run(wl, schedule="dynamic", n_ctas=None, min_tiles=1, fused=True, pool_chunks=None,
+         pool_min_tiles=None):
     from paged_gqa_decode_rope_gb300 import ops
+    kw = {} if pool_chunks is None else {"pool_chunks": pool_chunks}
+    if pool_min_tiles is not None:
+        kw["pool_min_tiles"] = pool_min_tiles
     step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=schedule,
-                          n_ctas=n_ctas, min_tiles=min_tiles)
+                          n_ctas=n_ctas, min_tiles=min_tiles, fused=fused, **kw)
     step.plan_step(wl.seq_lens)
     out = step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
     torch.cuda.synchronize()
@@ -61,11 +65,12 @@ def test_attention_matches_oracle(name):
     list(np.random.default_rng(9).integers(1, 300, 1024)),
 ])
 @pytest.mark.parametrize("kv", [0, 1])
-def test_attention_edge_lengths(lengths, kv):
+@pytest.mark.parametrize("fused", [True, False])
+def test_attention_edge_lengths(lengths, kv, fused):
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300.workloads import Workload
     wl = Workload("custom", seed=11, lengths=lengths, kv_dtype=kv, include_new_token=True)
-    out, st = _run(wl)
+    out, st = _run(wl, fused=fused)
     assert st == 0
     got = gu.bf16_host(out)
     seqs = range(wl.batch) if wl.batch <= 16 else _sample(wl, k=12)
@@ -96,13 +101,17 @@ def test_schedules_agree_and_are_deterministic(name):
     assert st == 0 and st2 == 0
     assert torch.equal(ref.view(torch.int16), again.view(torch.int16)), "run-to-run bit-identical"
     r = ref.float()
-    for schedule, n_ctas, mt in ((("static", 1), None, 1), (("static", 8), None, 1),
-                                 ("dynamic", 7, 1), ("dynamic", 304, 1), ("dynamic", None, 64)):
-        out, st = _run(wl, schedule, n_ctas, mt)
+    for schedule, n_ctas, mt, fused, pc, pk in (
+            (("static", 1), None, 1, True, None, None), (("static", 8), None, 1, True, None, None),
+            ("dynamic", 7, 1, True, None, None), ("dynamic", 304, 1, True, None, None),
+            ("dynamic", None, 64, True, None, None), ("dynamic", None, 1, False, None, None),
+            ("dynamic", None, 1, True, 0, None), ("dynamic", None, 1, False, 6, 1),
+            ("dynamic", None, 1, True, 6, 1), ("dynamic", None, 1, True, 4, 4)):
+        out, st = _run(wl, schedule, n_ctas, mt, fused, pc, pk)
         assert st == 0
         d = (out.float() - r).abs()
         assert float(d.max()) <= 4e-3 and float(d.mean()) <= 2e-4, \
-            (schedule, n_ctas, mt, float(d.max()), float(d.mean()))
+            (schedule, n_ctas, mt, fused, pc, pk, float(d.max()), float(d.mean()))
 
 
 def test_fp8_against_oracle_quantised_history():
@@ -146,3 +155,54 @@ def test_bad_block_is_reported_and_skipped():
     gu.compare(got[0], want[0], *_tol(wl))
     gu.compare(got[2], want[1], *_tol(wl))
     assert np.all(np.isfinite(got[1]))
+
+
+def test_profiled_variant_same_output_and_sane_clocks():
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=6, lengths=[4096, 300, 70, 1], kv_dtype=0, include_new_token=True)
+    ref, st = _run(wl, fused=False)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+    step.plan_step(wl.seq_lens)
+    clock = torch.zeros((step.plan.num_ctas, 3), dtype=torch.int64, device="cuda")
+    ops.decode_attn_profiled(wl.q, wl.cache, wl.kv_dtype, wl.kv_scale, wl.block_table, wl.seq_lens,
+                             step.plan, step.partial_o, step.partial_lse, step.status, clock)
+    ops.merge(step.partial_o, step.partial_lse, step.plan, step.out)
+    torch.cuda.synchronize()
+    assert st == 0 and int(step.status.item()) == 0
+    assert torch.equal(step.out.view(torch.int16), ref.view(torch.int16))
+    rec = clock.cpu().numpy()
+    assert np.all(rec[:, 1] >= rec[:, 0]) and np.all(rec[:, 0] > 0)
+    assert np.all((rec[:, 2] >= 0) & (rec[:, 2] < 1024))
+    occ = ops.cta_occupancy(clock)
+    assert 0.0 < occ["occupancy"] <= 1.0 and occ["span_us"] > 0
+
+
+@pytest.mark.parametrize("kv", [0, 1])
+def test_plan_runs_again_and_pool_counters_reset(kv):
+    """A plan may be run several times: the attention kernel's last CTA puts
+    the pool counters back to zero, so every run deals every pooled item."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=7, lengths=[20000, 4096, 300, 1, 9000], kv_dtype=kv,
+                  include_new_token=True)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, pool_chunks=3, pool_min_tiles=1)
+    step.plan_step(wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.plan.pool[2].item()) > 0, "the plan has pooled items"
+    outs = []
+    for _ in range(3):
+        outs.append(step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens).clone())
+        torch.cuda.synchronize()
+        assert step.plan.pool[:2].cpu().tolist() == [0, 0]
+        assert int(step.plan.seg_done.abs().sum().item()) == 0
+    assert int(step.status.item()) == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    want = gu.oracle_outputs(wl, wl.q, [0, 2, 4])
+    got = gu.bf16_host(outs[0])
+    tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if kv == 0 else (gu.TOL_FP8_MAX, None)
+    for i, b in enumerate([0, 2, 4]):
+        gu.compare(got[b], want[i], *tol)

@@ -23,11 +23,12 @@ def _mixes():
     yield list(rng.integers(0, 200, size=3000))            # many sequences, > 1 per thread
 
 
-def _run_dynamic(lens, C, min_tiles, capacity=None):
+def _run_dynamic(lens, C, min_tiles, capacity=None, J=0, kmin=1):
     from paged_gqa_decode_rope_gb300 import ops
     B = len(lens)
     max_blocks = max(1, max(-(-L // 64) for L in lens))
-    plan = ops.DecodePlan(B, C, C + 8 * B if capacity is None else capacity, "cuda")
+    cap = C * (1 + J) + 8 * B if capacity is None else capacity
+    plan = ops.DecodePlan(B, C, cap, "cuda", pool_chunks=J, pool_min_tiles=kmin)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ops.decode_plan(torch.tensor(lens, dtype=torch.int32, device="cuda"), max_blocks, plan,
                     status, min_tiles)
@@ -40,19 +41,23 @@ def _host(plan, n_items):
     return items, plan.cta_ptr.cpu().tolist(), plan.seg_ptr.cpu().tolist()
 
 
+@pytest.mark.parametrize("J,kmin", [(0, 1), (1, 1), (6, 1), (4, 2), (4, 16)])
 @pytest.mark.parametrize("C", [1, 7, 152, 304, 1000])
-def test_dynamic_plan_bit_exact(C):
+def test_dynamic_plan_bit_exact(C, J, kmin):
     gu.require_gpu()
     for lens in _mixes():
         for min_tiles in (1, 4):
-            plan, st = _run_dynamic(lens, C, min_tiles)
+            plan, st = _run_dynamic(lens, C, min_tiles, J=J, kmin=kmin)
             assert st == 0
-            want = op.plan_dynamic(lens, C, min_tiles)
-            got = _host(plan, len(want[0]))
-            assert got[1] == want[1], "cta_ptr"
-            assert got[2] == want[2], "seg_ptr"
-            assert got[0] == [tuple(i) for i in want[0]], "items"
-            op.check_coverage(lens, *got)
+            items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(lens, C, min_tiles, J, kmin)
+            got = _host(plan, len(items))
+            assert got[1] == cta_ptr, "cta_ptr"
+            assert got[2] == seg_ptr, "seg_ptr"
+            assert got[0] == [tuple(i) for i in items], "items"
+            assert plan.home_end.cpu().tolist() == home_end, "home_end"
+            pl = plan.pool.cpu().tolist()
+            assert pl[:3] == [0, 0, len(pool)] and pl[3:3 + len(pool)] == pool, "pool"
+            op.check_coverage(lens, *got, home_end, pool)
 
 
 @pytest.mark.parametrize("S", [1, 2, 3, 64])
@@ -74,6 +79,8 @@ def test_static_plan_bit_exact(S):
         got = _host(plan, len(items))
         assert got[0] == [tuple(i) for i in items]
         assert got[1] == cta_ptr and got[2] == seg_ptr
+        assert plan.home_end.cpu().tolist() == [min(c + 1, len(items)) for c in range(C)]
+        assert plan.pool.cpu().tolist()[:3] == [0, 0, 0]
         op.check_coverage(lens, *got)
 
 
@@ -86,12 +93,12 @@ def test_plan_overflow_and_bad_lengths_set_status():
     assert plan.cta_ptr.cpu().tolist() == [0] * 153      # empty plan
     # a length beyond max_blocks*64 and a negative one are treated as empty
     B = 3
-    plan = ops.DecodePlan(B, 16, 16 + 24, "cuda")
+    plan = ops.DecodePlan(B, 16, 16 + 24, "cuda")       # no pool chunks
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ops.decode_plan(torch.tensor([100, 10 ** 6, -5], dtype=torch.int32, device="cuda"), 4, plan,
                     status, 1)
     torch.cuda.synchronize()
     assert int(status.item()) & 4, "BAD_SEQ_LEN"
-    want = op.plan_dynamic([100, 0, 0], 16, 1)
+    want = op.plan_dynamic([100, 0, 0], 16, 1)[:3]
     got = _host(plan, len(want[0]))
     assert got[0] == [tuple(i) for i in want[0]] and got[1] == want[1] and got[2] == want[2]

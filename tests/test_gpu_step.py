@@ -11,8 +11,9 @@ import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixed", "heavy_tail"])
-def test_decode_step_end_to_end(name):
+@pytest.mark.parametrize("name,two_launch", [("tiny", True), ("tiny", False), ("mixed", True),
+                                             ("mixed", False), ("heavy_tail", True)])
+def test_decode_step_end_to_end(name, two_launch):
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
@@ -23,7 +24,7 @@ def test_decode_step_end_to_end(name):
     cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
     step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
     out = step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
-               wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
+               wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens, two_launch=two_launch)
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     got = gu.bf16_host(out)

@@ -9,10 +9,21 @@ from oracle_pins import load_golden
 
 def test_dynamic_plan_hand_example():
     g = load_golden("plan_hand_example.json")["dynamic"]
-    items, cta_ptr, seg_ptr = op.plan_dynamic(g["seq_lens"], g["num_ctas"], g["min_tiles"])
+    items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(g["seq_lens"], g["num_ctas"],
+                                                              g["min_tiles"])
     assert [list(i) for i in items] == g["items"]
     assert cta_ptr == g["cta_ptr"]
     assert seg_ptr == g["seg_ptr"]
+    assert home_end == cta_ptr[1:] and pool == [], "no pool without pool chunks"
+
+
+def test_dynamic_plan_with_pool_hand_example():
+    g = load_golden("plan_hand_example.json")["dynamic_pool"]
+    items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(
+        g["seq_lens"], g["num_ctas"], g["min_tiles"], g["pool_chunks"])
+    assert [list(i) for i in items] == g["items"]
+    assert cta_ptr == g["cta_ptr"] and seg_ptr == g["seg_ptr"]
+    assert home_end == g["home_end"] and pool == g["pool"]
 
 
 def test_static_plan_hand_example():
@@ -34,15 +45,16 @@ def _length_mixes(rng):
     yield list(np.exp(rng.uniform(np.log(128), np.log(262144), 64)).astype(int))
 
 
+@pytest.mark.parametrize("J,kmin", [(0, 1), (1, 1), (6, 1), (4, 2), (4, 16)])
 @pytest.mark.parametrize("C", [1, 7, 152, 304, 1000])
-def test_dynamic_plan_covers_and_balances(C):
+def test_dynamic_plan_covers_and_balances(C, J, kmin):
     rng = np.random.default_rng(C)
     for lens in _length_mixes(rng):
         for min_tiles in (1, 4):
-            items, cta_ptr, seg_ptr = op.plan_dynamic(lens, C, min_tiles)
-            n = op.check_coverage(lens, items, cta_ptr, seg_ptr)
+            items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(lens, C, min_tiles, J, kmin)
+            n = op.check_coverage(lens, items, cta_ptr, seg_ptr, home_end, pool)
             B = len(lens)
-            assert n <= C + 8 * B, "capacity bound"
+            assert n <= C * (1 + J) + 8 * B, "capacity bound"
             T = 8 * sum(op.num_tiles(L) for L in lens)
             q = max(min_tiles, -(-T // C)) if T else min_tiles
             per_cta = [sum(items[i][3] - items[i][2] for i in range(cta_ptr[c], cta_ptr[c + 1]))
@@ -71,3 +83,18 @@ def test_static_plan_covers(S):
 
 def test_tiles_of_ragged_lengths():
     assert [op.num_tiles(L) for L in (0, 1, 63, 64, 65, 128, 129)] == [0, 1, 1, 1, 2, 2, 3]
+
+
+def test_pool_min_chunk_hand_example():
+    """seq_lens [700], C = 2, J = 2: P = 5 pooled tiles in chunks of 3.  With
+    the smallest worthwhile chunk at 3 the pool stays (the golden plan); at 4
+    the chunks are too short and the plan is the plain one."""
+    g = load_golden("plan_hand_example.json")
+    with_pool = op.plan_dynamic([700], 2, 1, 2, 3)
+    assert [list(i) for i in with_pool[0]] == g["dynamic_pool"]["items"]
+    assert with_pool[4] == g["dynamic_pool"]["pool"]
+    items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic([700], 2, 1, 2, 4)
+    plain = op.plan_dynamic([700], 2, 1, 0)
+    assert items == plain[0] and cta_ptr == plain[1] and pool == [] and home_end == cta_ptr[1:]
+    # by hand: q = 44, so the plain plan cuts segment 3 ([33,44)) and 7 only at 44
+    assert items[3] == (0, 3, 0, 11) and len(items) == 8
