@@ -69,7 +69,8 @@ struct AttnTraits {
   static constexpr int kNumBars = 2 * kStages + 2 * kItemRing + 1;
   static constexpr int kOffOk = kOffBar + kNumBars * 8;
   static constexpr int kOffRing = kOffOk + kStages * 4;
-  static constexpr int kOffAbort = kOffRing + kItemRing * 4;
+  static constexpr int kRingInts = 8;                         // idx, seq, h, t0, t1, len
+  static constexpr int kOffAbort = kOffRing + kItemRing * kRingInts * 4;
   static constexpr int kSmemUsed = kOffAbort + 16;
   static constexpr int kSmemBytes = kSmemUsed + 1024;         // slack for 1024-byte alignment
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
@@ -87,18 +88,16 @@ struct Item {
   bool ok;
 };
 
-__device__ __forceinline__ Item load_item(const hpc_work_item* items, int i,
-                                          const int32_t* seq_lens, int batch, int max_blocks) {
-  const int4 w = reinterpret_cast<const int4*>(items)[i];
+// The item (w = {seq, kv_head, tile_begin, tile_end}) checked against the
+// batch, with `len` the length of its sequence (-1 if the sequence id is bad).
+__device__ __forceinline__ Item make_item(int4 w, int len, int batch, int max_blocks) {
   Item it{w.x, w.y, w.z, w.w, 0, false};
-  if (it.seq >= 0 && it.seq < batch && it.h >= 0 && it.h < kHkv) {
-    const int L = __ldg(seq_lens + it.seq);
-    if (L >= 0 && L <= max_blocks * kPage) {
-      const int n = (L + kPage - 1) / kPage;
-      if (it.t0 >= 0 && it.t0 < it.t1 && it.t1 <= n) {
-        it.ok = true;
-        it.len = L;
-      }
+  if (it.seq >= 0 && it.seq < batch && it.h >= 0 && it.h < kHkv && len >= 0 &&
+      len <= max_blocks * kPage) {
+    const int n = (len + kPage - 1) / kPage;
+    if (it.t0 >= 0 && it.t0 < it.t1 && it.t1 <= n) {
+      it.ok = true;
+      it.len = len;
     }
   }
   return it;
@@ -236,35 +235,90 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   __syncthreads();
 
   // ------------------------------------------------------------ producer
+  // The producer does not wait on a global load in its issue loop: the home
+  // items' descriptors and lengths arrive 32 at a time (one per lane), the
+  // block ids of the next 32 tiles are fetched while the current 32 are
+  // issued (across item boundaries), and a pool claim is made when an item
+  // starts and resolved during its last chunk.
   if (warp == T::kConsumerWarps) {
     const uint64_t policy = l2_evict_first_policy();
     const uint32_t stage0 = smem_u32(smem);
+    const int4* items4 = reinterpret_cast<const int4*>(items);
     uint32_t g = 0;          // tiles issued so far by this CTA
     uint32_t n_pushed = 0;   // items handed to the consumers so far
-    int next_home = home_begin;
-    bool claiming = true;    // still taking items (home, then pool)
+    bool claiming = true;    // the pool is not known to be empty yet
     bool alive = true;
-    while (alive) {
-      // next item: the home part first, then claims from the pool; -1 ends
-      int idx = -1;
-      if (next_home < home_stop) {
-        idx = next_home++;
-      } else if (claiming) {
-        int k = 0;
-        if (lane == 0) k = atomicAdd(&pool[0], 1);
-        k = __shfl_sync(0xffffffffu, k, 0);
+    int ticket = -1;         // lane 0: an unresolved pool claim (its counter value)
+
+    // home items, 32 at a time: lane j holds item hb_next - hb_cnt + j
+    int hb_next = home_begin, hb_cnt = 0, hb_pos = 0;
+    int4 hw = make_int4(-1, -1, 0, 0);
+    int hlen = -1;
+    auto load_home_batch = [&]() {
+      hb_cnt = min(32, home_stop - hb_next);
+      hb_pos = 0;
+      hw = make_int4(-1, -1, 0, 0);
+      hlen = -1;
+      if (lane < hb_cnt) {
+        hw = items4[hb_next + lane];
+        hlen = (hw.x >= 0 && hw.x < batch) ? __ldg(seq_lens + hw.x) : -1;
+      }
+      hb_next += hb_cnt;
+    };
+    // start a pool claim (lane 0) once the home part is used up
+    auto start_claim = [&]() {
+      if (lane == 0 && claiming && ticket < 0 && hb_pos == hb_cnt && hb_next == home_stop)
+        ticket = atomicAdd(&pool[0], 1);
+    };
+    // next item: {index, descriptor, length}; index -1 when nothing is left
+    struct Next {
+      int idx;
+      int4 w;
+      int len;
+    };
+    auto next_item = [&]() -> Next {
+      while (true) {
+        if (hb_pos == hb_cnt && hb_next < home_stop) load_home_batch();
+        if (hb_pos < hb_cnt) {
+          Next n;
+          n.idx = hb_next - hb_cnt + hb_pos;
+          n.w.x = __shfl_sync(0xffffffffu, hw.x, hb_pos);
+          n.w.y = __shfl_sync(0xffffffffu, hw.y, hb_pos);
+          n.w.z = __shfl_sync(0xffffffffu, hw.z, hb_pos);
+          n.w.w = __shfl_sync(0xffffffffu, hw.w, hb_pos);
+          n.len = __shfl_sync(0xffffffffu, hlen, hb_pos);
+          ++hb_pos;
+          return n;
+        }
+        if (!claiming) return Next{-1, make_int4(-1, -1, 0, 0), -1};
+        start_claim();
+        const int k = __shfl_sync(0xffffffffu, ticket, 0);
+        if (lane == 0) ticket = -1;
         if (k < pool_len) {
-          idx = pool[3 + k];
+          const int idx = pool[3 + k];
           if (idx < 0 || idx >= capacity) {
             if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
             continue;
           }
-        } else {
-          claiming = false;
-          if (lane == 0) finish_claims();
+          Next n;
+          n.idx = idx;
+          n.w = items4[idx];
+          n.len = (n.w.x >= 0 && n.w.x < batch) ? __ldg(seq_lens + n.w.x) : -1;
+          return n;
         }
+        claiming = false;
+        if (lane == 0) finish_claims();
+        return Next{-1, make_int4(-1, -1, 0, 0), -1};
       }
-      // hand the item (or the end mark) to the consumers
+    };
+    // block ids of tiles tb .. tb+31 of an item (lane j: tile tb + j)
+    auto fetch_bids = [&](const Item& it, int tb) -> int {
+      const int t = tb + lane;
+      return (it.ok && t < it.t1) ? __ldg(block_table + static_cast<int64_t>(it.seq) * max_blocks + t)
+                                  : 0;
+    };
+    // hand an item's descriptor (or the end mark) to the consumers
+    auto push_item = [&](int idx, const Item& it) -> bool {
       int ok = 1;
       if (lane == 0) {
         const int r = static_cast<int>(n_pushed % R);
@@ -276,91 +330,103 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           ok = 0;
         }
         if (ok) {
-          ring[r] = idx;
+          volatile int* slot = ring + r * T::kRingInts;
+          slot[0] = idx;
+          slot[1] = it.seq;
+          slot[2] = it.h;
+          slot[3] = it.t0;
+          slot[4] = it.t1;
+          slot[5] = it.ok ? it.len : -1;
           mbar_arrive(smem_u32(&item_full[r]));
         }
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       ++n_pushed;
-      if (idx < 0) break;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    // one stage: a tile (data, block id bid), or a slot without data
+    auto issue = [&](int bid, int h, bool data) -> bool {
+      int tok = 1;
+      if (lane == 0) {
+        const int s = static_cast<int>(g % S);
+        const uint32_t use = g / S;
+        if (*abort_flag) {
+          tok = 0;
+        } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
+          *abort_flag = 1;
+          tok = 0;
+        }
+        if (tok) {
+          const uint32_t fb = smem_u32(&full[s]);
+          if (data && bid >= 0 && bid < num_blocks) {
+            stage_ok[s] = 1;
+            mbar_arrive_expect_tx(fb, T::kStageBytes);
+            const uint32_t dst = stage0 + s * T::kStageBytes;
+            const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
+            const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
+            if constexpr (kFp8) {
+              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
+              tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
+            } else {
+              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
+              tma_load_2d(dst + T::kBoxBytes, &kv_map, 64, yk, fb, policy);
+              tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
+              tma_load_2d(dst + T::kPageBytes + T::kBoxBytes, &kv_map, 64, yv, fb, policy);
+            }
+          } else {
+            if (data) atomicOr(status, HPC_STATUS_BAD_BLOCK);
+            stage_ok[s] = 0;
+            mbar_arrive(fb);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, tok, 0)) return false;
+      ++g;
+      return true;
+    };
 
-      const Item it = load_item(items, idx, seq_lens, batch, max_blocks);
+    Next cur = next_item();
+    Item it = make_item(cur.w, cur.len, batch, max_blocks);
+    int cur_bids = fetch_bids(it, it.t0);
+    while (alive) {
+      if (!push_item(cur.idx, it)) break;
+      if (cur.idx < 0) break;
       if (!it.ok) {
         if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
-        continue;
+      } else {
+        start_claim();
+        // start the item on a slot of group 0 (padding slots carry no data),
+        // so tile t of the item always goes to group (t - t0) % kGroups,
+        // whichever CTA runs it: the output does not depend on run order
+        while (alive && g % T::kGroups != 0) alive = issue(-1, 0, false);
       }
-      // start the item on a slot of group 0 (padding slots carry no data), so
-      // tile t of the item always goes to group (t - t0) % kGroups, whichever
-      // CTA runs it: the output does not depend on the schedule's run order
-      while (g % T::kGroups != 0) {
-        int tok = 1;
-        if (lane == 0) {
-          const int s = static_cast<int>(g % S);
-          const uint32_t use = g / S;
-          if (*abort_flag) {
-            tok = 0;
-          } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
-            *abort_flag = 1;
-            tok = 0;
-          }
-          if (tok) {
-            stage_ok[s] = 0;
-            mbar_arrive(smem_u32(&full[s]));
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, tok, 0)) {
-          alive = false;
-          break;
-        }
-        ++g;
-      }
-      const int32_t* bt_row = block_table + static_cast<int64_t>(it.seq) * max_blocks;
-      for (int tb = it.t0; tb < it.t1 && alive; tb += 32) {
+      Next nxt{-1, make_int4(-1, -1, 0, 0), -1};
+      Item nit{-1, -1, 0, 0, 0, false};
+      int nxt_bids = 0;
+      bool have_next = false;
+      for (int tb = it.t0; it.ok && tb < it.t1 && alive; tb += 32) {
         const int nt = min(32, it.t1 - tb);
-        const int my_bid = lane < nt ? __ldg(bt_row + tb + lane) : 0;
-        for (int j = 0; j < nt; ++j) {
-          const int bid = __shfl_sync(0xffffffffu, my_bid, j);
-          int tok = 1;
-          if (lane == 0) {
-            const int s = static_cast<int>(g % S);
-            const uint32_t use = g / S;
-            if (*abort_flag) {
-              tok = 0;
-            } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
-              *abort_flag = 1;
-              tok = 0;
-            }
-            if (tok) {
-              const uint32_t fb = smem_u32(&full[s]);
-              if (bid >= 0 && bid < num_blocks) {
-                stage_ok[s] = 1;
-                mbar_arrive_expect_tx(fb, T::kStageBytes);
-                const uint32_t dst = stage0 + s * T::kStageBytes;
-                const int yk = ((bid * 2 + 0) * kHkv + it.h) * kPage;   // row of [bid][0][h][0]
-                const int yv = yk + kHkv * kPage;                        // row of [bid][1][h][0]
-                if constexpr (kFp8) {
-                  tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-                  tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
-                } else {
-                  tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-                  tma_load_2d(dst + T::kBoxBytes, &kv_map, 64, yk, fb, policy);
-                  tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
-                  tma_load_2d(dst + T::kPageBytes + T::kBoxBytes, &kv_map, 64, yv, fb, policy);
-                }
-              } else {
-                atomicOr(status, HPC_STATUS_BAD_BLOCK);
-                stage_ok[s] = 0;
-                mbar_arrive(fb);
-              }
-            }
-          }
-          if (!__shfl_sync(0xffffffffu, tok, 0)) {
-            alive = false;
-            break;
-          }
-          ++g;
+        int pre = 0;
+        if (tb + 32 < it.t1) {
+          pre = fetch_bids(it, tb + 32);              // the next chunk of this item
+        } else {
+          nxt = next_item();                          // the next item and its first chunk
+          nit = make_item(nxt.w, nxt.len, batch, max_blocks);
+          nxt_bids = fetch_bids(nit, nit.t0);
+          have_next = true;
         }
+        for (int j = 0; j < nt && alive; ++j)
+          alive = issue(__shfl_sync(0xffffffffu, cur_bids, j), it.h, true);
+        cur_bids = pre;
       }
+      if (!alive) break;
+      if (!have_next) {
+        nxt = next_item();
+        nit = make_item(nxt.w, nxt.len, batch, max_blocks);
+        nxt_bids = fetch_bids(nit, nit.t0);
+      }
+      cur = nxt;
+      it = nit;
+      cur_bids = nxt_bids;
     }
     if (claiming && lane == 0) finish_claims();   // stopped early by a fault
     // After a fault, copies may still be landing in stages nobody will wait
@@ -420,12 +486,13 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       if (lane == 0) *abort_flag = 1;
       break;
     }
-    const int i = ring[rslot];
+    const volatile int* slot = ring + rslot * T::kRingInts;
+    const int i = slot[0];
+    const Item it{slot[1], slot[2], slot[3], slot[4], slot[5], slot[5] >= 0};
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
     if (i < 0) break;
 
-    const Item it = load_item(items, i, seq_lens, batch, max_blocks);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2c, 2c+1
     float o[8][4];
 #pragma unroll
