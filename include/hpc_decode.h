@@ -56,6 +56,7 @@ extern "C" {
 #define HPC_HEAD_DIM 128
 #define HPC_PAGE_TOKENS 64
 #define HPC_MAX_BATCH 8192          /* planner limit on the batch size */
+#define HPC_MAX_PLAN_CTAS 16384     /* length-proportional planner limit on num_ctas */
 #define HPC_MAX_NUM_BLOCKS 2097151  /* cache blocks addressable by the TMA map */
 
 typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
@@ -197,7 +198,8 @@ int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
  *              items do not fit, PLAN_OVERFLOW is set and the plan is empty
  *   params     (host) planner knobs, or NULL for the defaults
  * Errors: HPC_ERR_INVALID_ARG for null pointers, batch < 0, max_blocks < 1,
- * knobs out of range or num_ctas < 1; HPC_ERR_UNSUPPORTED for batch > 8192. */
+ * knobs out of range or num_ctas < 1; HPC_ERR_UNSUPPORTED for batch > 8192,
+ * num_ctas > HPC_MAX_PLAN_CTAS or batch * max_blocks * 8 >= 2^30. */
 int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
                     const hpc_plan_params* params, hpc_plan* plan, int32_t* status,
                     cudaStream_t stream);

@@ -99,10 +99,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_static_kernel(
   }
 }
 
-// Dynamic shared memory above 48 KB needs a per-device opt-in (batches over
-// 6143 sequences); done once per device with the largest size the batch cap
-// allows.
-cudaError_t plan_smem_optin(size_t) {
+// Dynamic shared memory above 48 KB needs a per-device opt-in; done once per
+// device with the largest size the batch and CTA caps allow (160 KB).
+cudaError_t plan_smem_optin() {
   static std::mutex mu;
   static bool done[64] = {};
   int dev = 0;
@@ -111,7 +110,8 @@ cudaError_t plan_smem_optin(size_t) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   e = cudaFuncSetAttribute(plan_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(2 * sizeof(int) * (HPC_MAX_BATCH + 1)));
+                           static_cast<int>(sizeof(int) *
+                                            plan_smem_ints(HPC_MAX_BATCH, HPC_MAX_PLAN_CTAS)));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -122,8 +122,9 @@ int check_plan_args(const int32_t* seq_lens, int32_t batch, int32_t max_blocks, 
                 plan->home_end && plan->pool && plan->seg_done);
   HPC_CHECK_ARG(batch >= 0 && max_blocks >= 1 && plan->num_ctas >= 1 && plan->capacity >= 0);
   if (batch > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
-  // keep the flat tile count 8 * sum(n_b) inside int32
-  if (static_cast<int64_t>(batch) * max_blocks * kHkv >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
+  // keep the flat tile count T = 8 * sum(n_b) below 2^30, so that every flat
+  // position the planner forms (at most T plus one range) fits in int32
+  if (static_cast<int64_t>(batch) * max_blocks * kHkv >= (int64_t{1} << 30)) return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks) * kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
   return HPC_OK;
 }
@@ -144,8 +145,9 @@ extern "C" int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t m
   const hpc_plan_params& pp = params != nullptr ? *params : def;
   const int min_tiles = pp.min_tiles, pool_chunks = pp.pool_chunks;
   HPC_CHECK_ARG(min_tiles >= 1 && pool_chunks >= 0 && pool_chunks <= 64 && pp.pool_min_tiles >= 1);
-  const size_t smem = 2 * sizeof(int) * (static_cast<size_t>(batch) + 1);
-  if (smem > 48 * 1024 && hpc::plan_smem_optin(smem) != cudaSuccess) return HPC_ERR_CUDA;
+  if (plan->num_ctas > HPC_MAX_PLAN_CTAS) return HPC_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(int) * hpc::plan_smem_ints(batch, plan->num_ctas);
+  if (smem > 48 * 1024 && hpc::plan_smem_optin() != cudaSuccess) return HPC_ERR_CUDA;
   hpc::plan_dynamic_kernel<<<1, hpc::kPlanThreads, smem, stream>>>(
       seq_lens, batch, max_blocks, min_tiles, pool_chunks, pp.pool_min_tiles, plan->items,
       plan->cta_ptr,

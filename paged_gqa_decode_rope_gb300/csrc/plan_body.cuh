@@ -58,22 +58,48 @@ __device__ void write_empty_plan(int batch, int num_ctas, int32_t* cta_ptr, int3
   for (int s = threadIdx.x; s <= batch * kHkv; s += kThreads) seg_ptr[s] = 0;
 }
 
-// Pieces of the flat tile order: CTA c's range [c*q, (c+1)*q) is its home
-// part [c*q, c*q + h) followed by npc - 1 pool chunks of k tiles (the last
-// one may be shorter).  Pieces are numbered in flat order, npc per CTA.
+// floor(a * 2^32 / d) for 0 <= a < d <= 2^31 in 32-bit float and integer
+// steps (double precision is slow on this part).  The estimate from a
+// correctly rounded reciprocal carries three roundings of at most 2^-24 on a
+// quotient below 2^32, so it is within 2^10 of the quotient and the exact
+// remainder is below 2^11 d in size; one more estimate from that remainder
+// (its top bits only when it passes 2^31, which needs d > 2^20 and so moves
+// the estimate by less than 2^-8) lands within one of the quotient, and the
+// remainder's sign and size settle the last step.
+__device__ __forceinline__ uint32_t frac_quotient(uint32_t a, uint32_t d) {
+  const float r = __frcp_rn(static_cast<float>(d));
+  uint32_t qe = __float2uint_rz(static_cast<float>(a) * r * 4294967296.0f);
+  const int64_t num = static_cast<int64_t>(a) << 32;
+  int64_t rem = num - static_cast<int64_t>(static_cast<uint64_t>(qe) * d);
+  const float fr = (rem >= INT32_MIN && rem <= INT32_MAX)
+                       ? static_cast<float>(static_cast<int32_t>(rem))
+                       : static_cast<float>(static_cast<int32_t>(rem >> 12)) * 4096.0f;
+  qe += static_cast<uint32_t>(__float2int_rz(fr * r));
+  rem = num - static_cast<int64_t>(static_cast<uint64_t>(qe) * d);
+  while (rem < 0) {
+    --qe;
+    rem += d;
+  }
+  while (rem >= static_cast<int64_t>(d)) {
+    ++qe;
+    rem -= d;
+  }
+  return qe;
+}
+
 // Division of dividends in [0, 2^31) by a divisor fixed for the whole plan,
 // by multiplication: Granlund and Montgomery, "Division by invariant integers
 // using multiplication" (PLDI 1994), with l = ceil(log2 d) and
 // m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(m, n) + n) >> l.  The
-// planner's closed forms divide by q, k and the pieces per range in long
-// dependent chains; a hardware-free quotient keeps them short.
+// planner's closed forms divide by q, k and the pieces per range in dependent
+// chains; a quotient in three instructions keeps them short.
 struct FastDiv {
   uint32_t d, m, l;
+  // d in [1, 2^31]; 2^l - d < d, so m < 2^32
   __device__ __forceinline__ void init(uint32_t div) {
     d = div;
-    l = 0;
-    while ((1u << l) < d) ++l;
-    m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
+    l = div > 1 ? 32 - __clz(div - 1) : 0;
+    m = frac_quotient((1u << l) - div, div) + 1u;
   }
   __device__ __forceinline__ int div(int n) const {
     const uint32_t un = static_cast<uint32_t>(n);
@@ -81,15 +107,31 @@ struct FastDiv {
   }
 };
 
+// Pieces of the flat tile order: CTA c's range [c*q, (c+1)*q) is its home
+// part [c*q, c*q + h) followed by npc - 1 pool chunks of k tiles (the last
+// one may be shorter).  Pieces are numbered in flat order, npc per CTA.
 struct Pieces {
-  // all flat positions are < 2^31: the host checks batch * max_blocks * 8
+  // all flat positions are < 2^31: the host keeps batch * max_blocks * 8
+  // below 2^30, and a piece is formed only when it starts before T
   int q, h, k;
   int npc;   // pieces per CTA range (1 + pool chunks)
   FastDiv dq, dk, dnpc;
+  // the three inverses are set up on lanes 0, 1 and 2 of every warp at once
+  // and broadcast (the whole warp must call this)
   __device__ __forceinline__ void ready() {
-    dq.init(q);
-    dk.init(k);
-    dnpc.init(npc);
+    const int lane = threadIdx.x & 31;
+    FastDiv f;
+    f.init(static_cast<uint32_t>(lane == 0 ? q : (lane == 1 ? k : npc)));
+    const uint32_t m = f.m, l = f.l;
+    dq.d = q;
+    dq.m = __shfl_sync(0xffffffffu, m, 0);
+    dq.l = __shfl_sync(0xffffffffu, l, 0);
+    dk.d = k;
+    dk.m = __shfl_sync(0xffffffffu, m, 1);
+    dk.l = __shfl_sync(0xffffffffu, l, 1);
+    dnpc.d = npc;
+    dnpc.m = __shfl_sync(0xffffffffu, m, 2);
+    dnpc.l = __shfl_sync(0xffffffffu, l, 2);
   }
   // number of piece starts at or before flat tile x (x >= 0)
   __device__ __forceinline__ int starts_upto(int x) const {
@@ -99,58 +141,53 @@ struct Pieces {
     return n;
   }
   __device__ __forceinline__ int id(int f) const { return starts_upto(f) - 1; }
-  __device__ __forceinline__ int begin(int p) const {
-    const int c = dnpc.div(p), j = p - c * npc;
+  // first flat tile of piece p = c*npc + j
+  __device__ __forceinline__ int begin(int c, int j) const {
     return c * q + (j == 0 ? 0 : h + (j - 1) * k);
   }
-  __device__ __forceinline__ int end(int p) const {
-    const int c = dnpc.div(p), j = p - c * npc;
-    return c * q + (j == 0 ? h : min(q, h + j * k));
+  // one past the last flat tile of piece p = c*npc + j (j * k stays below
+  // 2 (q - h), so the sum is formed only once it is at most q)
+  __device__ __forceinline__ int end(int c, int j) const {
+    return c * q + h + (j == 0 ? 0 : min(q - h, j * k));
   }
 };
 
-// Shared-memory view of the plan under construction: pre_n[b] = tiles of
-// sequences before b (per KV head), pre_items[b] = items before sequence b.
-// Every index the planner writes is derived from these two prefixes and the
-// piece arithmetic, so nothing it wrote to global memory is read back.
-struct PlanView {
-  const int* pre_n;
-  const int* pre_items;
-  int batch;
-  Pieces pc;
-  // items of segment (b, h)
-  __device__ __forceinline__ int seg_items(int b, int h) const {
-    const int n = pre_n[b + 1] - pre_n[b];
-    if (n == 0) return 0;
-    const int s0 = kHkv * pre_n[b] + h * n;
-    return pc.id(s0 + n - 1) - pc.id(s0) + 1;
-  }
-  // index of the first item of segment (b, h)
-  __device__ __forceinline__ int seg_first(int b, int h) const {
-    int i = pre_items[b];
-    for (int x = 0; x < h; ++x) i += seg_items(b, x);
-    return i;
-  }
-  // index of the item holding flat tile f (total_items if f >= T)
-  __device__ int item_at(int64_t f, int T, int total_items) const {
-    if (f >= T) return total_items;
-    const int ff = static_cast<int>(f);
-    int lo = 0, hi = batch;   // invariant: 8*pre_n[lo] <= f < 8*pre_n[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (kHkv * pre_n[mid] <= ff) lo = mid; else hi = mid;
+// Shared memory of the planner, in ints: the tile prefix [batch + 1] and the
+// per-CTA item bounds [num_ctas + 1] and [num_ctas].
+__host__ __device__ __forceinline__ size_t plan_smem_ints(int batch, int num_ctas) {
+  return static_cast<size_t>(batch) + 1 + 2 * static_cast<size_t>(num_ctas) + 1;
+}
+
+// Items of one (seq, kv_head) segment: flat tiles [s0, s0 + n) cut at piece
+// starts.  Item j (global index first + j) is piece id(s0) + j clipped to the
+// segment.  An item that begins on a piece start records the CTA bounds that
+// start defines: the start of CTA c's range (piece c*npc) is cta_s[c]; the
+// start of the piece after CTA c's home part (piece c*npc + 1) is home_s[c].
+struct SegItems {
+  int b, h, s0, n, first, p0;
+  __device__ __forceinline__ void write(const Pieces& pc, int j, hpc_work_item* items, int* cta_s,
+                                        int* home_s) const {
+    const int p = p0 + j;
+    const int c = pc.dnpc.div(p), jj = p - c * pc.npc;
+    const int pb = pc.begin(c, jj), pe = pc.end(c, jj);
+    hpc_work_item it;
+    it.seq = b;
+    it.kv_head = h;
+    it.tile_begin = max(pb, s0) - s0;
+    it.tile_end = min(pe, s0 + n) - s0;
+    items[first + j] = it;
+    if (pb >= s0) {   // the item begins on piece p's start
+      if (jj == 0) cta_s[c] = first + j;
+      if (pc.npc == 1 && c > 0) home_s[c - 1] = first + j;
+      if (jj == 1) home_s[c] = first + j;
     }
-    const int b = lo;
-    const int n = pre_n[b + 1] - pre_n[b];   // > 0 because f < 8*pre_n[b+1]
-    const int h = (ff - kHkv * pre_n[b]) / n;
-    const int s0 = kHkv * pre_n[b] + h * n;
-    return seg_first(b, h) + pc.id(ff) - pc.id(s0);
   }
 };
 
 // The length-proportional planner, run by one CTA of kThreads threads.
-// smem points at 2 * (batch + 1) ints of shared memory.  One round trip to
-// global memory (seq_lens); everything else is shared memory and arithmetic.
+// smem points at plan_smem_ints(batch, num_ctas) ints of shared memory.  One
+// round trip to global memory (seq_lens); everything else is shared memory and
+// arithmetic, with four block-wide scans' worth of barriers.
 template <int kThreads>
 __device__ void plan_dynamic_body(
     const int32_t* __restrict__ seq_lens, int batch, int max_blocks, int min_tiles, int pool_chunks,
@@ -158,12 +195,14 @@ __device__ void plan_dynamic_body(
     int32_t* home_end, int32_t* __restrict__ pool, int32_t* __restrict__ seg_done, int capacity,
     int num_ctas, int32_t* __restrict__ status, int* smem) {
   __shared__ int warp_sums[32];
-  int* pre_n = smem;                   // [batch + 1]
-  int* pre_items = smem + batch + 1;   // [batch + 1]
+  const int C = num_ctas;
+  int* pre_n = smem;               // [batch + 1]
+  int* cta_s = smem + batch + 1;   // [C + 1]
+  int* home_s = cta_s + C + 1;     // [C]
+  const int tid = threadIdx.x, lane = tid & 31;
   const int per = (batch + kThreads - 1) / kThreads;
-  const int b0 = min(batch, static_cast<int>(threadIdx.x) * per);
+  const int b0 = min(batch, tid * per);
   const int b1 = min(batch, b0 + per);
-  for (int x = threadIdx.x; x < batch * kHkv; x += kThreads) seg_done[x] = 0;
 
   // 1. tiles per sequence (staged in pre_n), then their exclusive prefix
   int local = 0;
@@ -172,6 +211,7 @@ __device__ void plan_dynamic_body(
     pre_n[b] = n;
     local += n;
   }
+  for (int x = tid; x < batch * kHkv; x += kThreads) seg_done[x] = 0;
   int total_n;
   int run = cta_exclusive_scan<kThreads>(local, warp_sums, &total_n);
   for (int b = b0; b < b1; ++b) {
@@ -179,17 +219,13 @@ __device__ void plan_dynamic_body(
     pre_n[b] = run;
     run += n;
   }
-  if (threadIdx.x == 0) pre_n[batch] = total_n;
-  __syncthreads();
+  if (tid == 0) pre_n[batch] = total_n;
 
+  // 2. the pieces: range q, pooled tiles P in chunks of k, home part h
   const int T = kHkv * total_n;
-  PlanView v;
-  v.pre_n = pre_n;
-  v.pre_items = pre_items;
-  v.batch = batch;
-  Pieces& pc = v.pc;
-  pc.q = max(min_tiles, (T + num_ctas - 1) / num_ctas);
-  int P = pool_chunks > 0 ? pc.q / 8 : 0;                // pooled tiles per CTA range
+  Pieces pc;
+  pc.q = max(min_tiles, (T + C - 1) / C);
+  int P = pool_chunks > 0 ? pc.q / 8 : 0;
   pc.k = P > 0 ? (P + pool_chunks - 1) / pool_chunks : 1;
   if (pc.k < pool_min_tiles) {                           // chunks too short to deal
     P = 0;
@@ -198,86 +234,101 @@ __device__ void plan_dynamic_body(
   pc.h = pc.q - P;
   pc.npc = 1 + (P > 0 ? (P + pc.k - 1) / pc.k : 0);
   pc.ready();
+  __syncthreads();   // pre_n complete
 
-  // 2. items per sequence (its 8 segments) and their prefix
+  // 3. items per segment (segments sper at a time per thread), their prefix
+  const int nseg = batch * kHkv;
+  const int sper = (nseg + kThreads - 1) / kThreads;
+  const int sb = min(nseg, tid * sper), se = min(nseg, sb + sper);
   local = 0;
-  for (int b = b0; b < b1; ++b)
-    for (int h = 0; h < kHkv; ++h) local += v.seg_items(b, h);
+  for (int s = sb; s < se; ++s) {
+    const int b = s >> 3, h = s & 7;
+    const int n = pre_n[b + 1] - pre_n[b];
+    if (n > 0) {
+      const int s0 = kHkv * pre_n[b] + h * n;
+      local += pc.id(s0 + n - 1) - pc.id(s0) + 1;
+    }
+  }
   int total_items;
   run = cta_exclusive_scan<kThreads>(local, warp_sums, &total_items);
   if (total_items > capacity) {
-    if (threadIdx.x == 0) atomicOr(status, HPC_STATUS_PLAN_OVERFLOW);
-    write_empty_plan<kThreads>(batch, num_ctas, cta_ptr, seg_ptr);
-    for (int c = threadIdx.x; c < num_ctas; c += kThreads) home_end[c] = 0;
-    if (threadIdx.x == 0) pool[0] = pool[1] = pool[2] = 0;
+    if (tid == 0) atomicOr(status, HPC_STATUS_PLAN_OVERFLOW);
+    write_empty_plan<kThreads>(batch, C, cta_ptr, seg_ptr);
+    for (int c = tid; c < C; c += kThreads) home_end[c] = 0;
+    if (tid == 0) pool[0] = pool[1] = pool[2] = 0;
     return;
   }
 
-  // 3. segment offsets, and the first item of every sequence (in smem)
-  for (int b = b0; b < b1; ++b) {
-    pre_items[b] = run;
-    for (int h = 0; h < kHkv; ++h) {
-      seg_ptr[b * kHkv + h] = run;
-      run += v.seg_items(b, h);
+  // 4. segment offsets and items.  The items of the 32 segments a warp holds
+  //    at step i are written by the whole warp as one flat range (lane j
+  //    takes every 32nd), so a long segment is not left to one thread.
+  for (int i = 0; i < sper; ++i) {
+    const int s = sb + i;
+    SegItems g{0, 0, 0, 0, run, 0};
+    int cnt = 0;
+    if (s < se) {
+      g.b = s >> 3;
+      g.h = s & 7;
+      g.n = pre_n[g.b + 1] - pre_n[g.b];
+      g.s0 = kHkv * pre_n[g.b] + g.h * g.n;
+      seg_ptr[s] = run;
+      if (g.n > 0) {
+        g.p0 = pc.id(g.s0);
+        cnt = pc.id(g.s0 + g.n - 1) - g.p0 + 1;
+      }
+      run += cnt;
+    }
+    int incl = cnt;   // inclusive scan of the counts over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - cnt;
+    const int wtotal = __shfl_sync(0xffffffffu, incl, 31);
+    for (int base = 0; base < wtotal; base += 32) {
+      const int v = base + lane;
+      // the last lane whose range starts at or before v owns it
+      int src = 0;
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (__shfl_sync(0xffffffffu, excl, src + step) <= v) src += step;
+      SegItems w;
+      w.b = __shfl_sync(0xffffffffu, g.b, src);
+      w.h = __shfl_sync(0xffffffffu, g.h, src);
+      w.s0 = __shfl_sync(0xffffffffu, g.s0, src);
+      w.n = __shfl_sync(0xffffffffu, g.n, src);
+      w.first = __shfl_sync(0xffffffffu, g.first, src);
+      w.p0 = __shfl_sync(0xffffffffu, g.p0, src);
+      const int j = v - __shfl_sync(0xffffffffu, excl, src);
+      if (v < wtotal) w.write(pc, j, items, cta_s, home_s);
     }
   }
-  if (threadIdx.x == 0) {
-    seg_ptr[batch * kHkv] = total_items;
-    pre_items[batch] = total_items;
+  if (tid == 0) seg_ptr[nseg] = total_items;
+  //    bounds that start at or past the last tile hold no item
+  for (int c = tid; c <= C; c += kThreads) {
+    const int64_t f = static_cast<int64_t>(c) * pc.q;
+    if (f >= T) cta_s[c] = total_items;
+    if (c < C && f + (pc.npc > 1 ? pc.h : pc.q) >= T) home_s[c] = total_items;
   }
-  __syncthreads();   // pre_items is read below by other threads
+  __syncthreads();
 
-  //    the items, one per thread: item i lies in the last sequence b with
-  //    pre_items[b] <= i and, inside it, in the segment whose range holds i
-  for (int i = threadIdx.x; i < total_items; i += kThreads) {
-    int lo = 0, hi = batch;   // invariant: pre_items[lo] <= i < pre_items[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (pre_items[mid] <= i) lo = mid; else hi = mid;
-    }
-    const int b = lo;
-    const int n = pre_n[b + 1] - pre_n[b];
-    int h = 0, first = pre_items[b];
-    for (int c = v.seg_items(b, 0); first + c <= i; c = v.seg_items(b, h)) {
-      first += c;
-      ++h;
-    }
-    const int s0 = kHkv * pre_n[b] + h * n;
-    const int p = pc.id(s0) + (i - first);
-    hpc_work_item it;
-    it.seq = b;
-    it.kv_head = h;
-    it.tile_begin = max(s0, pc.begin(p)) - s0;
-    it.tile_end = min(s0 + n, pc.end(p)) - s0;
-    items[i] = it;
-  }
-
-  // 4. each CTA's range (its first item holds flat tile c*q), home part (the
-  //    first pool item holds flat tile c*q + h) and pooled items
+  // 5. each CTA's range and home part; its pooled items
   //    home_end[c] .. cta_ptr[c+1]-1, listed in CTA order
-  const int cper = (num_ctas + kThreads - 1) / kThreads;
-  const int c0 = min(num_ctas, static_cast<int>(threadIdx.x) * cper);
-  const int c1 = min(num_ctas, c0 + cper);
+  const int cper = (C + kThreads - 1) / kThreads;
+  const int c0 = min(C, tid * cper), c1 = min(C, c0 + cper);
   local = 0;
   for (int c = c0; c < c1; ++c) {
-    const int64_t f = static_cast<int64_t>(c) * pc.q;
-    const int first = v.item_at(f, T, total_items);
-    const int home = v.item_at(f + (P > 0 ? pc.h : pc.q), T, total_items);
-    const int next = v.item_at(f + pc.q, T, total_items);
-    cta_ptr[c] = first;
-    home_end[c] = home;
-    local += next - home;
+    cta_ptr[c] = cta_s[c];
+    home_end[c] = home_s[c];
+    local += cta_s[c + 1] - home_s[c];
   }
-  if (threadIdx.x == 0) cta_ptr[num_ctas] = total_items;
+  if (tid == 0) cta_ptr[C] = total_items;
   int pool_len;
   run = cta_exclusive_scan<kThreads>(local, warp_sums, &pool_len);
-  for (int c = c0; c < c1; ++c) {
-    const int64_t f = static_cast<int64_t>(c) * pc.q;
-    const int home = v.item_at(f + (P > 0 ? pc.h : pc.q), T, total_items);
-    const int next = v.item_at(f + pc.q, T, total_items);
-    for (int i = home; i < next; ++i) pool[3 + run++] = i;
-  }
-  if (threadIdx.x == 0) {
+  for (int c = c0; c < c1; ++c)
+    for (int i = home_s[c]; i < cta_s[c + 1]; ++i) pool[3 + run++] = i;
+  if (tid == 0) {
     pool[0] = 0;          // next claim
     pool[1] = 0;          // CTAs done claiming
     pool[2] = pool_len;

@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kStepThreads) prologue_plan_kernel(
   }
 }
 
-// Dynamic shared memory above 48 KB (the planner's two prefix arrays for
-// batches over 6143) needs a per-device opt-in, done once per device.
+// Dynamic shared memory above 48 KB (the planner's arrays for large batches
+// or grids) needs a per-device opt-in, done once per device.
 template <bool kFp8>
 cudaError_t step_smem_optin() {
   static std::mutex mu;
@@ -60,7 +60,8 @@ cudaError_t step_smem_optin() {
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
   e = cudaFuncSetAttribute(prologue_plan_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(2 * sizeof(int) * (HPC_MAX_BATCH + 1)));
+                           static_cast<int>(sizeof(int) *
+                                            plan_smem_ints(HPC_MAX_BATCH, HPC_MAX_PLAN_CTAS)));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
@@ -88,8 +89,8 @@ extern "C" int hpc_decode_step(const void* q, const void* k, const void* v,
   HPC_CHECK_ARG(seq_lens && plan && plan->items && plan->cta_ptr && plan->seg_ptr &&
                 plan->home_end && plan->pool && plan->seg_done);
   HPC_CHECK_ARG(max_blocks >= 1 && plan->num_ctas >= 1 && plan->capacity >= 0);
-  if (batch > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(batch) * max_blocks * hpc::kHkv >= (int64_t{1} << 31))
+  if (batch > HPC_MAX_BATCH || plan->num_ctas > HPC_MAX_PLAN_CTAS) return HPC_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(batch) * max_blocks * hpc::kHkv >= (int64_t{1} << 30))
     return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
   const hpc_plan_params def = {1, HPC_DEFAULT_POOL_CHUNKS, HPC_DEFAULT_POOL_MIN_TILES};
@@ -97,7 +98,7 @@ extern "C" int hpc_decode_step(const void* q, const void* k, const void* v,
   HPC_CHECK_ARG(pp.min_tiles >= 1 && pp.pool_chunks >= 0 && pp.pool_chunks <= 64 &&
                 pp.pool_min_tiles >= 1);
 
-  const size_t smem = 2 * sizeof(int) * (static_cast<size_t>(batch) + 1);
+  const size_t smem = sizeof(int) * hpc::plan_smem_ints(batch, plan->num_ctas);
   const dim3 grid(1 + (hpc::kGroup + 1) * batch);
   auto* cache = static_cast<uint8_t*>(kv_cache);
   auto args = [&](auto kernel) {

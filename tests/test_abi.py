@@ -69,6 +69,8 @@ def test_host_argument_checks(lib):
     assert lib.hpc_decode_plan(fake, 4, 8, P(1, 4, 0), ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_decode_plan(fake, 9000, 8, None, ctypes.byref(plan), st, NULL) == HPC_ERR_UNSUPPORTED
     assert lib.hpc_decode_plan(NULL, 4, 8, None, ctypes.byref(plan), st, NULL) == HPC_ERR_INVALID_ARG
+    wide = Plan(4096, 4096, 4096, 4096, 4096, 4096, 100, 16385)   # above HPC_MAX_PLAN_CTAS
+    assert lib.hpc_decode_plan(fake, 4, 8, None, ctypes.byref(wide), st, NULL) == HPC_ERR_UNSUPPORTED
     bad = Plan(4096, 4096, 4096, 0, 4096, 4096, 100, 10)  # no home_end array
     assert lib.hpc_decode_plan(fake, 4, 8, None, ctypes.byref(bad), st, NULL) == HPC_ERR_INVALID_ARG
     # static plan: num_ctas must be batch * 8 * splits

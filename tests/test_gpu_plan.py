@@ -60,6 +60,33 @@ def test_dynamic_plan_bit_exact(C, J, kmin):
             op.check_coverage(lens, *got, home_end, pool)
 
 
+def test_dynamic_plan_random_configs():
+    """Many seeded (lengths, CTAs, min_tiles, pool) draws: every divisor the
+    planner sets up a multiplicative inverse for (range, chunk, pieces per
+    range) takes many values, including ranges near 2^31 from a huge
+    min_tiles."""
+    gu.require_gpu()
+    rng = np.random.default_rng(11)
+    for trial in range(160):
+        B = int(rng.choice([1, 2, 5, 33, 200]))
+        hi = int(rng.choice([100, 5000, 300000]))
+        lens = [int(x) for x in rng.integers(0, hi, size=B)]
+        C = int(rng.choice([1, 3, 152, 999, 4096]))
+        min_tiles = int(rng.choice([1, 1, 3, 1000003, 2 ** 30 + 12345, 2 ** 31 - 1]))
+        J = int(rng.choice([0, 1, 3, 4, 64]))
+        kmin = int(rng.choice([1, 16]))
+        plan, st = _run_dynamic(lens, C, min_tiles, J=J, kmin=kmin)
+        assert st == 0
+        items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(lens, C, min_tiles, J, kmin)
+        got = _host(plan, len(items))
+        ctx = (trial, B, C, min_tiles, J, kmin)
+        assert got[0] == [tuple(i) for i in items], ctx
+        assert got[1] == cta_ptr and got[2] == seg_ptr, ctx
+        assert plan.home_end.cpu().tolist() == home_end, ctx
+        pl = plan.pool.cpu().tolist()
+        assert pl[:3] == [0, 0, len(pool)] and pl[3:3 + len(pool)] == pool, ctx
+
+
 @pytest.mark.parametrize("S", [1, 2, 3, 64])
 def test_static_plan_bit_exact(S):
     gu.require_gpu()
