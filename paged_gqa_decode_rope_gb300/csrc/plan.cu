@@ -121,6 +121,7 @@ int check_plan_args(const int32_t* seq_lens, int32_t batch, int32_t max_blocks, 
   HPC_CHECK_ARG(seq_lens && plan && status && plan->items && plan->cta_ptr && plan->seg_ptr &&
                 plan->home_end && plan->pool && plan->seg_done);
   HPC_CHECK_ARG(batch >= 0 && max_blocks >= 1 && plan->num_ctas >= 1 && plan->capacity >= 0);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
   if (batch > HPC_MAX_BATCH) return HPC_ERR_UNSUPPORTED;
   // keep the flat tile count T = 8 * sum(n_b) below 2^30, so that every flat
   // position the planner forms (at most T plus one range) fits in int32

@@ -59,15 +59,15 @@ __device__ void write_empty_plan(int batch, int num_ctas, int32_t* cta_ptr, int3
 }
 
 // floor(a * 2^32 / d) for 0 <= a < d <= 2^31 in 32-bit float and integer
-// steps (double precision is slow on this part).  The estimate from a
-// correctly rounded reciprocal carries three roundings of at most 2^-24 on a
-// quotient below 2^32, so it is within 2^10 of the quotient and the exact
-// remainder is below 2^11 d in size; one more estimate from that remainder
-// (its top bits only when it passes 2^31, which needs d > 2^20 and so moves
-// the estimate by less than 2^-8) lands within one of the quotient, and the
-// remainder's sign and size settle the last step.
+// steps (double precision is slow on this part).  The estimate from an
+// approximate reciprocal (relative error at most 2^-23) and two more
+// roundings of at most 2^-24 on a quotient below 2^32 is within 2^10 of the
+// quotient, so the exact remainder is below 2^11 d in size; one more estimate
+// from that remainder (its top bits only when it passes 2^31, which needs
+// d > 2^20 and so moves the estimate by less than 2^-8) lands within one of
+// the quotient, and the remainder's sign and size settle the last step.
 __device__ __forceinline__ uint32_t frac_quotient(uint32_t a, uint32_t d) {
-  const float r = __frcp_rn(static_cast<float>(d));
+  const float r = rcp_approx(static_cast<float>(d));
   uint32_t qe = __float2uint_rz(static_cast<float>(a) * r * 4294967296.0f);
   const int64_t num = static_cast<int64_t>(a) << 32;
   int64_t rem = num - static_cast<int64_t>(static_cast<uint64_t>(qe) * d);
@@ -170,12 +170,9 @@ struct SegItems {
     const int p = p0 + j;
     const int c = pc.dnpc.div(p), jj = p - c * pc.npc;
     const int pb = pc.begin(c, jj), pe = pc.end(c, jj);
-    hpc_work_item it;
-    it.seq = b;
-    it.kv_head = h;
-    it.tile_begin = max(pb, s0) - s0;
-    it.tile_end = min(pe, s0 + n) - s0;
-    items[first + j] = it;
+    // one 16-byte store (the item array is 16-byte aligned)
+    reinterpret_cast<int4*>(items)[first + j] =
+        make_int4(b, h, max(pb, s0) - s0, min(pe, s0 + n) - s0);
     if (pb >= s0) {   // the item begins on piece p's start
       if (jj == 0) cta_s[c] = first + j;
       if (pc.npc == 1 && c > 0) home_s[c - 1] = first + j;
@@ -200,6 +197,9 @@ __device__ void plan_dynamic_body(
   int* cta_s = smem + batch + 1;   // [C + 1]
   int* home_s = cta_s + C + 1;     // [C]
   const int tid = threadIdx.x, lane = tid & 31;
+  // read the scalar arguments into registers up front: their first reads
+  // then overlap the sequence-length loads instead of stalling step 2
+  asm volatile("" ::"r"(C), "r"(min_tiles), "r"(pool_chunks), "r"(pool_min_tiles), "r"(capacity));
   const int per = (batch + kThreads - 1) / kThreads;
   const int b0 = min(batch, tid * per);
   const int b1 = min(batch, b0 + per);
@@ -222,32 +222,43 @@ __device__ void plan_dynamic_body(
   if (tid == 0) pre_n[batch] = total_n;
 
   // 2. the pieces: range q, pooled tiles P in chunks of k, home part h
+  //    (every thread works them out: a shared copy would cost a barrier)
   const int T = kHkv * total_n;
   Pieces pc;
-  pc.q = max(min_tiles, (T + C - 1) / C);
-  int P = pool_chunks > 0 ? pc.q / 8 : 0;
-  pc.k = P > 0 ? (P + pool_chunks - 1) / pool_chunks : 1;
+  const uint32_t uC = static_cast<uint32_t>(C), uJ = static_cast<uint32_t>(pool_chunks);
+  pc.q = max(min_tiles, static_cast<int>((static_cast<uint32_t>(T) + uC - 1u) / uC));
+  uint32_t P = pool_chunks > 0 ? static_cast<uint32_t>(pc.q) / 8u : 0u;
+  pc.k = P > 0 ? static_cast<int>((P + uJ - 1u) / uJ) : 1;
   if (pc.k < pool_min_tiles) {                           // chunks too short to deal
     P = 0;
     pc.k = 1;
   }
-  pc.h = pc.q - P;
-  pc.npc = 1 + (P > 0 ? (P + pc.k - 1) / pc.k : 0);
+  pc.h = pc.q - static_cast<int>(P);
+  pc.npc = 1 + (P > 0 ? static_cast<int>((P + pc.k - 1u) / static_cast<uint32_t>(pc.k)) : 0);
   pc.ready();
   __syncthreads();   // pre_n complete
 
-  // 3. items per segment (segments sper at a time per thread), their prefix
+  // 3. items per segment.  Warp w owns the segments
+  //    [w * 32 * sper, (w + 1) * 32 * sper) and walks them 32 at a time (lane
+  //    j takes the j-th of each group), so its segment offsets and item
+  //    stores are consecutive across the lanes.  The block-wide scan gives
+  //    each warp the items before its segments.
   const int nseg = batch * kHkv;
   const int sper = (nseg + kThreads - 1) / kThreads;
-  const int sb = min(nseg, tid * sper), se = min(nseg, sb + sper);
+  const int wseg0 = (tid >> 5) * 32 * sper;
+  auto seg_at = [&](int s, SegItems& g) -> int {   // fills g but first; returns the count
+    g.b = s >> 3;
+    g.h = s & 7;
+    g.n = pre_n[g.b + 1] - pre_n[g.b];
+    g.s0 = kHkv * pre_n[g.b] + g.h * g.n;
+    g.p0 = g.n > 0 ? pc.id(g.s0) : 0;
+    return g.n > 0 ? pc.id(g.s0 + g.n - 1) - g.p0 + 1 : 0;
+  };
   local = 0;
-  for (int s = sb; s < se; ++s) {
-    const int b = s >> 3, h = s & 7;
-    const int n = pre_n[b + 1] - pre_n[b];
-    if (n > 0) {
-      const int s0 = kHkv * pre_n[b] + h * n;
-      local += pc.id(s0 + n - 1) - pc.id(s0) + 1;
-    }
+  for (int i = 0; i < sper; ++i) {
+    const int s = wseg0 + 32 * i + lane;
+    SegItems g;
+    if (s < nseg) local += seg_at(s, g);
   }
   int total_items;
   run = cta_exclusive_scan<kThreads>(local, warp_sums, &total_items);
@@ -258,26 +269,15 @@ __device__ void plan_dynamic_body(
     if (tid == 0) pool[0] = pool[1] = pool[2] = 0;
     return;
   }
+  run = __shfl_sync(0xffffffffu, run, 0);   // items before this warp's segments
 
-  // 4. segment offsets and items.  The items of the 32 segments a warp holds
-  //    at step i are written by the whole warp as one flat range (lane j
-  //    takes every 32nd), so a long segment is not left to one thread.
+  // 4. segment offsets and items.  The items of the warp's 32 segments of a
+  //    group are one flat range written by the whole warp (lane j takes
+  //    every 32nd), so a long segment is not left to one thread.
   for (int i = 0; i < sper; ++i) {
-    const int s = sb + i;
-    SegItems g{0, 0, 0, 0, run, 0};
-    int cnt = 0;
-    if (s < se) {
-      g.b = s >> 3;
-      g.h = s & 7;
-      g.n = pre_n[g.b + 1] - pre_n[g.b];
-      g.s0 = kHkv * pre_n[g.b] + g.h * g.n;
-      seg_ptr[s] = run;
-      if (g.n > 0) {
-        g.p0 = pc.id(g.s0);
-        cnt = pc.id(g.s0 + g.n - 1) - g.p0 + 1;
-      }
-      run += cnt;
-    }
+    const int s = wseg0 + 32 * i + lane;
+    SegItems g{0, 0, 0, 0, 0, 0};
+    const int cnt = s < nseg ? seg_at(s, g) : 0;
     int incl = cnt;   // inclusive scan of the counts over the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -285,6 +285,8 @@ __device__ void plan_dynamic_body(
       if (lane >= o) incl += y;
     }
     const int excl = incl - cnt;
+    g.first = run + excl;
+    if (s < nseg) seg_ptr[s] = g.first;
     const int wtotal = __shfl_sync(0xffffffffu, incl, 31);
     for (int base = 0; base < wtotal; base += 32) {
       const int v = base + lane;
@@ -303,6 +305,7 @@ __device__ void plan_dynamic_body(
       const int j = v - __shfl_sync(0xffffffffu, excl, src);
       if (v < wtotal) w.write(pc, j, items, cta_s, home_s);
     }
+    run += wtotal;
   }
   if (tid == 0) seg_ptr[nseg] = total_items;
   //    bounds that start at or past the last tile hold no item

@@ -89,6 +89,7 @@ extern "C" int hpc_decode_step(const void* q, const void* k, const void* v,
   HPC_CHECK_ARG(seq_lens && plan && plan->items && plan->cta_ptr && plan->seg_ptr &&
                 plan->home_end && plan->pool && plan->seg_done);
   HPC_CHECK_ARG(max_blocks >= 1 && plan->num_ctas >= 1 && plan->capacity >= 0);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
   if (batch > HPC_MAX_BATCH || plan->num_ctas > HPC_MAX_PLAN_CTAS) return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(batch) * max_blocks * hpc::kHkv >= (int64_t{1} << 30))
     return HPC_ERR_UNSUPPORTED;
