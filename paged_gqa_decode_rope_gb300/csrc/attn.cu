@@ -54,9 +54,11 @@ struct AttnTraits {
   static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
   static constexpr int kStageBytes = 2 * kPageBytes;          // K page + V page
-  static constexpr int kStages = kFp8 ? 10 : 6;
+  static constexpr int kStages = kFp8 ? 9 : 6;
   static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
-  static constexpr int kGroups = 2;                           // groups take alternate tiles
+  // groups take tiles in turn; FP8 tiles carry a longer per-tile chain (the
+  // conversions) at half the bytes, so they need a third group in flight
+  static constexpr int kGroups = kFp8 ? 3 : 2;
   static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
   static constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
@@ -722,10 +724,13 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         constexpr int kMergeChunk = 1024;
         static_assert(kMergeChunk * kGroup <= T::kConsumerWarps * kGroup * T::kOStride,
                       "the lse staging area must fit in the merge slices");
-        static_assert(32 * T::kConsumerWarps * 4 == kGroup * kD, "one float4 of output per thread");
+        static_assert(32 * T::kConsumerWarps * 4 >= kGroup * kD, "one float4 of output per thread");
         float* lse_s = sm_o;
         const int i0 = seg_ptr[seg];
-        const int e = threadIdx.x * 4;
+        // one float4 of output per thread; threads past the 1024 outputs
+        // only stage lse values and meet at the barriers
+        const bool has_out = threadIdx.x * 4 < kGroup * kD;
+        const int e = has_out ? threadIdx.x * 4 : 0;
         const int hh = e >> 7;
         float M = -INFINITY, W = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -737,7 +742,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           if (!(synced = cons_sync())) break;
           float Mn = M;
           for (int k = 0; k < m; ++k) Mn = fmaxf(Mn, lse_s[k * kGroup + hh]);
-          if (Mn != -INFINITY) {
+          if (has_out && Mn != -INFINITY) {
             const float sc = __expf(M - Mn);   // 0 while M is still -inf
             acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
             W *= sc;
@@ -761,7 +766,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         uint2 packed;
         packed.x = pack_bf16(acc.x * inv, acc.y * inv);
         packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
+        if (has_out)
+          *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
       }
     }
     if (!cons_sync()) break;
