@@ -229,6 +229,27 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(x, ws, device):
+    """The largest of x over the ranks of the job (x itself on one rank)."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed, rank):
+    """Every rank draws its own batch of the workload (weak scaling)."""
+    return seed + rank
+
+
+def whole_job_tbps(ws, bytes_per_rank_step, steps, elapsed_ms):
+    """Bytes of all ranks' batches over the slowest rank's time, in TB/s."""
+    return ws * bytes_per_rank_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ reference ------
 
 def run_reference(args):
@@ -272,7 +293,7 @@ def run_ours(args):
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
 
-    wl = Workload(args.workload, seed=args.seed + rank)
+    wl = Workload(args.workload, seed=rank_seed(args.seed, rank))
     cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
     step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
     stream = torch.cuda.current_stream()
@@ -322,13 +343,9 @@ def run_ours(args):
     if sampler:
         sampler.stop()
         clocks = sampler.summary(wall0, wall1)
-    # max over ranks
-    if ws > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, ws, "cuda")
     ms_per_step = elapsed_ms / args.steps
-    value = ws * algo_bytes * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tbps(ws, algo_bytes, args.steps, elapsed_ms)
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the four calls, D2H of the output
@@ -356,12 +373,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = ws * algo_bytes / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, "cuda")
+    e2e_value = whole_job_tbps(ws, algo_bytes, 1, e2e_ms)
 
     # dynamic vs static equal split on the same kernels (attention + merge)
     sched = None

@@ -338,6 +338,20 @@ int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
  * num_ctas * (1 + pool_chunks) + 8 * batch. */
 int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas, int32_t pool_chunks);
 
+/* Self-test of the bounded pipeline wait (no counterpart on the pages).
+ * Every wait of the attention pipeline gives up after a time limit (1 s),
+ * sets HPC_STATUS_WAIT_TIMEOUT and winds its CTA down, so a stuck pipeline
+ * becomes a status word instead of a hung GPU.  This call runs that same wait
+ * on an mbarrier phase that can never complete, with the given limit: on
+ * return of the stream work, *status has HPC_STATUS_WAIT_TIMEOUT set and
+ * *waited_ns (if not NULL) holds how long the wait lasted (>= limit_ns).
+ * Nothing faults; the context stays usable.
+ *   limit_ns   1e3 .. 1e9 (HPC_ERR_INVALID_ARG otherwise)
+ *   status     (device) int32, bits or-ed in
+ *   waited_ns  (device) uint64 [1] or NULL */
+int hpc_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, uint64_t* waited_ns,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -65,6 +65,7 @@ SIGNATURES = {
         _c_p, _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
     "hpc_decode_num_ctas": (ctypes.c_int, [_c_i32, ctypes.POINTER(_c_i32)]),
     "hpc_plan_capacity": (_c_i32, [_c_i32, _c_i32, _c_i32]),
+    "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }
 
 _lib = None

@@ -67,11 +67,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs.  Returns false (after recording the timeout) if it did not.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, HPC_STATUS_WAIT_TIMEOUT);
       return false;
     }

@@ -87,3 +87,7 @@ def test_host_argument_checks(lib):
     assert lib.hpc_decode_attn(*a) == HPC_ERR_UNSUPPORTED
     assert lib.hpc_merge(NULL, fake, ctypes.byref(plan), 4, fake, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_merge(fake, fake, ctypes.byref(plan), 0, fake, NULL) == 0
+    # the wait self-test: limit outside 1 us .. 1 s, or no status word
+    assert lib.hpc_selftest_wait_timeout(10, fake, NULL, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_selftest_wait_timeout(2 * 10 ** 9, fake, NULL, NULL) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_selftest_wait_timeout(10 ** 6, NULL, NULL, NULL) == HPC_ERR_INVALID_ARG

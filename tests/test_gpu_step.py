@@ -40,3 +40,38 @@ def test_decode_step_end_to_end(name, two_launch):
         q_out, want = od.decode_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], [L - 1], qw, kw, sub,
                                      row[None, :], [L], [slot], wl.kv_dtype, scale, heads=heads)
         gu.compare(got[b], want[0], *tol, label="%s seq %d" % (name, b))
+
+
+@pytest.mark.parametrize("two_launch", [True, False])
+def test_decode_step_in_cuda_graph(two_launch):
+    """The step is capturable: graph replays give the eager step's output bit
+    for bit (the step is deterministic), and replays of a captured plan reset
+    their own counters."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("mixed", seed=1)
+    cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+
+    def run():
+        return step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
+                    wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens,
+                    two_launch=two_launch)
+
+    eager = run().clone()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        run()                                    # warm on the capture stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            out = run()
+    step.out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert torch.equal(out, eager)
