@@ -479,21 +479,62 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     }
   }
 
-  for (uint32_t n = 0;; ++n) {
-    // next item from the producer
+  // An item descriptor from the producer's ring (slot n % R), handed back as
+  // soon as it is read; false after an abort.
+  struct Desc {
+    int i;
+    Item it;
+  };
+  auto fetch_desc = [&](uint32_t n, Desc& d) -> bool {
     const int rslot = static_cast<int>(n % R);
     bool ok = !*abort_flag && mbar_wait(smem_u32(&item_full[rslot]), (n / R) & 1, status);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
       if (lane == 0) *abort_flag = 1;
-      break;
+      return false;
     }
     const volatile int* slot = ring + rslot * T::kRingInts;
-    const int i = slot[0];
-    const Item it{slot[1], slot[2], slot[3], slot[4], slot[5], slot[5] >= 0};
+    d.i = slot[0];
+    d.it = Item{slot[1], slot[2], slot[3], slot[4], slot[5], slot[5] >= 0};
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
-    if (i < 0) break;
+    return true;
+  };
+  // The item's q words (this lane's share of the B operand Q^T of the 8 query
+  // heads of its KV head, head = r) and, with the merge fused in, its
+  // segment's first item and item count.  Issued one item ahead, so the
+  // loads are in flight during the previous item's epilogue.
+  auto load_item = [&](const Desc& d, uint32_t (&qw)[8][2], int& first, int& count) {
+    first = 0;
+    count = 0;
+    if (d.i < 0 || !d.it.ok) return;
+    const uint16_t* qrow = q + (static_cast<int64_t>(d.it.seq) * kHq + d.it.h * kGroup + r) * kD;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      if constexpr (kFp8) {
+        const uint2 x = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
+        qw[ks][0] = x.x;
+        qw[ks][1] = x.y;
+      } else {
+        qw[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
+        qw[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c);
+      }
+    }
+    if (fuse) {
+      const int seg = d.it.seq * kHkv + d.it.h;
+      first = seg_ptr[seg];
+      count = seg_ptr[seg + 1] - first;
+    }
+  };
+
+  Desc cur{-1, Item{-1, -1, 0, 0, 0, false}};
+  uint32_t qw[8][2];
+  int seg_first = 0, seg_items = 0;
+  bool have = fetch_desc(0, cur);
+  if (have) load_item(cur, qw, seg_first, seg_items);
+  for (uint32_t n = 0; have && cur.i >= 0; ++n) {
+    const int i = cur.i;
+    const Item it = cur.it;
 
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2c, 2c+1
     float o[8][4];
@@ -503,16 +544,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     if (it.ok) {
       // B operand Q^T for the 8 query heads of this KV head (head = r)
       uint32_t bq[8][2];
-      const uint16_t* qrow = q + (static_cast<int64_t>(it.seq) * kHq + it.h * kGroup + r) * kD;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         if constexpr (kFp8) {
-          const uint2 x = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
-          bq[ks][0] = pack_f16(bf16_lo(x.x), bf16_hi(x.x));
-          bq[ks][1] = pack_f16(bf16_lo(x.y), bf16_hi(x.y));
+          bq[ks][0] = pack_f16(bf16_lo(qw[ks][0]), bf16_hi(qw[ks][0]));
+          bq[ks][1] = pack_f16(bf16_lo(qw[ks][1]), bf16_hi(qw[ks][1]));
         } else {
-          bq[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
-          bq[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c);
+          bq[ks][0] = qw[ks][0];
+          bq[ks][1] = qw[ks][1];
         }
       }
 
@@ -628,6 +667,15 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     }
     if (dead) break;
 
+    // the next item's descriptor, q words and segment bounds: their loads
+    // overlap this item's epilogue
+    Desc nxt{-1, Item{-1, -1, 0, 0, 0, false}};
+    uint32_t qw_next[8][2];
+    int next_first = 0, next_items = 0;
+    have = fetch_desc(n + 1, nxt);
+    if (!have) break;
+    load_item(nxt, qw_next, next_first, next_items);
+
     // ---- merge the warps' states and write the item's partial: every warp
     // stores its raw (m, l, O) in its own slice; after one barrier each
     // output element is combined over the warps in a fixed order (the result
@@ -662,7 +710,6 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     // with the merge fused in: a segment of one item is final here; a segment
     // of several items is merged by the CTA that finishes its last item
     const int seg = it.seq * kHkv + it.h;
-    const int seg_items = fuse && it.ok ? seg_ptr[seg + 1] - seg_ptr[seg] : 0;
     const bool direct = fuse && it.ok && seg_items == 1;
     {
       const int ct = threadIdx.x;   // consumer thread
@@ -704,9 +751,9 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       }
     }
     if (fuse && it.ok && !direct) {
-      __threadfence();             // this CTA's partial is visible device-wide...
-      if (!cons_sync()) break;     // ...for every writer, before the count
+      if (!cons_sync()) break;     // every thread's share of the partial is written
       if (threadIdx.x == 0) {
+        __threadfence();           // the CTA's partial is visible device-wide before the count
         const int done = atomicAdd(&seg_done[seg], 1);
         *merge_flag = done == seg_items - 1;
         if (done == seg_items - 1) {
@@ -726,7 +773,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
                       "the lse staging area must fit in the merge slices");
         static_assert(32 * T::kConsumerWarps * 4 >= kGroup * kD, "one float4 of output per thread");
         float* lse_s = sm_o;
-        const int i0 = seg_ptr[seg];
+        const int i0 = seg_first;
         // one float4 of output per thread; threads past the 1024 outputs
         // only stage lse values and meet at the barriers
         const bool has_out = threadIdx.x * 4 < kGroup * kD;
@@ -771,6 +818,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       }
     }
     if (!cons_sync()) break;
+    cur = nxt;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qw[ks][0] = qw_next[ks][0];
+      qw[ks][1] = qw_next[ks][1];
+    }
+    seg_first = next_first;
+    seg_items = next_items;
   }
   if (cta_clock != nullptr && threadIdx.x == 0) record_cta_clock(cta_clock, t_start);
 }
