@@ -109,9 +109,13 @@ typedef struct {
  *   seg_done [batch * 8]       per-segment count of finished items, used by
  *                              hpc_decode_attn_merge (zeroed by the planner,
  *                              left at zero by every run)
- * num_ctas is the grid of hpc_decode_attn; for the length-proportional plan
- * use hpc_decode_num_ctas().  A length-proportional plan with J pool chunks
- * needs capacity >= num_ctas * (1 + J) + 8 * batch (hpc_plan_capacity).
+ * num_ctas is the number of work queues ("CTA ranges") the plan deals to.
+ * hpc_decode_attn runs each queue on one group of 4 consumer warps fed by its
+ * own producer warp; a CTA hosts 2 queues (BF16) or 3 (FP8), so the grid is
+ * ceil(num_ctas / 2) or ceil(num_ctas / 3) CTAs.  For the length-proportional
+ * plan use hpc_decode_num_ctas() (SMs x queues per CTA).  A
+ * length-proportional plan with J pool chunks needs
+ * capacity >= num_ctas * (1 + J) + 8 * batch (hpc_plan_capacity).
  * items must be 16-byte aligned. */
 typedef struct {
   hpc_work_item* items;
@@ -227,7 +231,7 @@ int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_b
  *                the tile is skipped)
  *   seq_lens     (device) int32 [batch]
  *   plan         (host) plan written by hpc_decode_plan / _static for the same
- *                seq_lens; its num_ctas is the grid.  A plan may be run any
+ *                seq_lens; its num_ctas queues set the grid.  A plan may be run any
  *                number of times, but launches that share one plan must not
  *                overlap on the GPU (they share its pool counters).
  *   partial_o    (device) float32 [plan->capacity, 8, 128], written per item
@@ -258,9 +262,11 @@ int hpc_decode_attn_merge(const void* q, const void* kv_cache, int32_t kv_dtype,
 
 /* Diagnostic variant of hpc_decode_attn: the same kernel, which also writes
  * for every CTA c of the grid cta_clock[3c] = start and cta_clock[3c+1] = end
- * (the GPU's global timer, ns) and cta_clock[3c+2] = the SM it ran on.  Used to
- * measure SM occupancy and tail idle time of a schedule.
- *   cta_clock  (device) uint64 [plan->num_ctas * 3], written.
+ * (the GPU's global timer, ns; the end is when the last of the CTA's queues
+ * is done) and cta_clock[3c+2] = the SM it ran on.  Used to measure SM
+ * occupancy and tail idle time of a schedule.
+ *   cta_clock  (device) uint64 [plan->num_ctas * 3] (the grid's rows are
+ *              written; the grid has at most plan->num_ctas CTAs).
  * Errors: as hpc_decode_attn, and HPC_ERR_INVALID_ARG if cta_clock is null. */
 int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int32_t kv_dtype,
                              const float* kv_scale, int32_t num_blocks,
@@ -288,11 +294,12 @@ int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* 
  *   Arguments as in hpc_decode_attn, plus
  *   out  (device) bf16 [batch, 64, 128], written as by hpc_merge.
  * Limits and behaviour:
- *   - plan->capacity must be <= HPC_NOALLOC_MAX_ITEMS (2048 work items, an
- *     8.5 MB array that every GPU loading the library holds until exit);
+ *   - plan->capacity must be <= HPC_NOALLOC_MAX_ITEMS (4096 work items, a
+ *     16.9 MB array that every GPU loading the library holds until exit);
  *     a larger plan returns HPC_ERR_UNSUPPORTED and launches nothing.  A
- *     length-proportional plan on 152 CTAs with the default 4 pool chunks
- *     fits batches up to 161 sequences.
+ *     length-proportional plan with the default 4 pool chunks on a 152-SM
+ *     GPU fits batches up to 322 sequences (BF16, 304 queues) or 227 (FP8,
+ *     456 queues).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call before any
  *     stream capture.
@@ -301,7 +308,7 @@ int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* 
  *     needs clearing.  Calls that overlap on the GPU (other streams, other
  *     threads) race on the array: serialise them.
  * Errors: as hpc_decode_attn and hpc_merge, plus the capacity limit above. */
-#define HPC_NOALLOC_MAX_ITEMS 2048
+#define HPC_NOALLOC_MAX_ITEMS 4096
 int hpc_decode_attn_merge_noalloc(const void* q, const void* kv_cache, int32_t kv_dtype,
                                   const float* kv_scale, int32_t num_blocks,
                                   const int32_t* block_table, int32_t max_blocks,
@@ -330,8 +337,9 @@ int hpc_decode_step(const void* q, const void* k, const void* v, const int32_t* 
                     float* partial_o, float* partial_lse, void* q_out, void* out, float sm_scale,
                     int32_t* status, cudaStream_t stream);
 
-/* Persistent grid of hpc_decode_attn on the current device (SM count times
- * resident CTAs per SM) for the given KV dtype: the num_ctas to plan for. */
+/* Work queues of the persistent hpc_decode_attn grid on the current device
+ * for the given KV dtype: SM count x queues per CTA (2 for BF16, 3 for FP8),
+ * one CTA per SM.  The num_ctas to plan for. */
 int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
 
 /* Items a length-proportional plan may need:

@@ -13,7 +13,7 @@ HPC_OK = 0
 HPC_ERR_INVALID_ARG = -1
 HPC_ERR_UNSUPPORTED = -2
 HPC_ERR_CUDA = -3
-NOALLOC_MAX_ITEMS = 2048
+NOALLOC_MAX_ITEMS = 4096
 
 STATUS_BITS = {
     1: "BAD_BLOCK", 2: "BAD_SLOT", 4: "BAD_SEQ_LEN", 8: "BAD_POSITION",

@@ -54,34 +54,34 @@ struct AttnTraits {
   static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
   static constexpr int kStageBytes = 2 * kPageBytes;          // K page + V page
-  static constexpr int kStages = kFp8 ? 9 : 6;
-  static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
-  // groups take tiles in turn; FP8 tiles carry a longer per-tile chain (the
-  // conversions) at half the bytes, so they need a third group in flight
+  // A CTA hosts kGroups independent work queues.  A queue has its own producer
+  // warp, stage ring, item ring and 4 consumer warps, and runs whole work
+  // items, so one queue's epilogue and merge overlap the other queues'
+  // streaming.  FP8 tiles carry a longer per-tile chain (the conversions) at
+  // half the bytes, so FP8 keeps three queues in flight.
   static constexpr int kGroups = kFp8 ? 3 : 2;
+  static constexpr int kGroupStages = 3;                      // stage ring of one queue
+  static constexpr int kStages = kGroups * kGroupStages;
+  static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
   static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
-  static constexpr int kThreads = 32 * (kConsumerWarps + 1);  // + the producer warp
+  static constexpr int kGroupThreads = 32 * kWarpsPerGroup;
+  static constexpr int kThreads = 32 * (kConsumerWarps + kGroups);   // + a producer warp per queue
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
   static constexpr int kOffO = kStages * kStageBytes;                 // [warps][8][kOStride]
   static constexpr int kOffM = kOffO + kConsumerWarps * kGroup * kOStride * 4;
   static constexpr int kOffL = kOffM + kConsumerWarps * kGroup * 4;
   static constexpr int kOffBar = kOffL + kConsumerWarps * kGroup * 4;
-  static constexpr int kItemRing = 4;                         // items queued ahead
-  // barriers: full[S], empty[S], item_full[R], item_empty[R], consumer barrier
-  static constexpr int kNumBars = 2 * kStages + 2 * kItemRing + 1;
-  static constexpr int kOffOk = kOffBar + kNumBars * 8;
+  static constexpr int kItemRing = 2;                         // items queued ahead, per queue
+  // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier
+  static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1;
+  static constexpr int kOffOk = kOffBar + kGroups * kGroupBars * 8;
   static constexpr int kOffRing = kOffOk + kStages * 4;
   static constexpr int kRingInts = 8;                         // idx, seq, h, t0, t1, len
-  static constexpr int kOffAbort = kOffRing + kItemRing * kRingInts * 4;
-  static constexpr int kSmemUsed = kOffAbort + 16;
+  // flags: the CTA's abort flag, then one merge flag per queue
+  static constexpr int kOffFlags = kOffRing + kGroups * kItemRing * kRingInts * 4;
+  static constexpr int kSmemUsed = kOffFlags + 4 * (1 + kGroups);
   static constexpr int kSmemBytes = kSmemUsed + 1024;         // slack for 1024-byte alignment
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
-  // A consumer waits on full[s] by the parity of its use (g / kStages) & 1,
-  // which names the right phase only if the same warp saw the stage's previous
-  // phase complete.  That holds when every use of a stage belongs to one group,
-  // i.e. kStages % kGroups == 0; otherwise a warp can pass its wait while the
-  // stage's previous copy (another group's tile) is still in flight.
-  static_assert(kStages % kGroups == 0, "each stage must always serve the same group");
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
 };
 
@@ -166,11 +166,13 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     const float* __restrict__ kv_scale, const int32_t* __restrict__ block_table, int32_t max_blocks,
     int32_t num_blocks, const int32_t* __restrict__ seq_lens, int32_t batch,
     const hpc_work_item* items, const int32_t* cta_ptr, const int32_t* home_end, int32_t* pool,
-    int32_t capacity, float* __restrict__ partial_o, float* __restrict__ partial_lse,
+    int32_t capacity, int32_t num_queues, float* __restrict__ partial_o,
+    float* __restrict__ partial_lse,
     float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
     const int32_t* seg_ptr, int32_t* seg_done, uint16_t* __restrict__ out) {
   using T = AttnTraits<kFp8>;
-  constexpr int S = T::kStages;
+  constexpr int G = T::kGroups;
+  constexpr int SG = T::kGroupStages;
   constexpr int R = T::kItemRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -178,30 +180,39 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   float* sm_o = reinterpret_cast<float*>(smem + T::kOffO);
   float* sm_m = reinterpret_cast<float*>(smem + T::kOffM);
   float* sm_l = reinterpret_cast<float*>(smem + T::kOffL);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
-  uint64_t* empty = full + S;
-  uint64_t* item_full = empty + S;
-  uint64_t* item_empty = item_full + R;
-  uint64_t* cons_bar = item_empty + R;
-  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + T::kOffOk);
-  volatile int* ring = reinterpret_cast<volatile int*>(smem + T::kOffRing);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kOffAbort);
-  volatile int* merge_flag = abort_flag + 1;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kOffFlags);
   const bool fuse = out != nullptr;   // merge the partials in this kernel
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // warps 0 .. 4G-1 consume (queue k: warps 4k .. 4k+3); warp 4G + k produces for queue k
+  const bool is_producer = warp >= T::kConsumerWarps;
+  const int grp = is_producer ? warp - T::kConsumerWarps : warp / T::kWarpsPerGroup;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kOffBar) + grp * T::kGroupBars;
+  uint64_t* empty = full + SG;
+  uint64_t* item_full = empty + SG;
+  uint64_t* item_empty = item_full + R;
+  uint64_t* cons_bar = item_empty + R;
+  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + T::kOffOk) + grp * SG;
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + T::kOffRing) + grp * R * T::kRingInts;
+  volatile int* merge_flag = abort_flag + 1 + grp;
+  const uint32_t stage_base = smem_u32(smem) + grp * SG * T::kStageBytes;   // this queue's stages
+
   const unsigned long long t_start = cta_clock != nullptr ? globaltimer_ns() : 0ull;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), T::kWarpsPerGroup);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
+    for (int k = 0; k < G; ++k) {
+      uint64_t* b = bars + k * T::kGroupBars;
+      for (int st = 0; st < SG; ++st) {
+        mbar_init(smem_u32(&b[st]), 1);                           // full
+        mbar_init(smem_u32(&b[SG + st]), T::kWarpsPerGroup);      // empty
+      }
+      for (int r = 0; r < R; ++r) {
+        mbar_init(smem_u32(&b[2 * SG + r]), 1);                   // item_full
+        mbar_init(smem_u32(&b[2 * SG + R + r]), T::kWarpsPerGroup);   // item_empty
+      }
+      mbar_init(smem_u32(&b[2 * SG + 2 * R]), T::kGroupThreads);  // the queue's consumer barrier
     }
-    for (int r = 0; r < R; ++r) {
-      mbar_init(smem_u32(&item_full[r]), 1);
-      mbar_init(smem_u32(&item_empty[r]), T::kConsumerWarps);
-    }
-    mbar_init(smem_u32(cons_bar), 32 * T::kConsumerWarps);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -210,29 +221,40 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   // from here on the plan, q and the cache are read
   pdl_wait();
 
-  // The pool counters are pool[0] (next claim) and pool[1] (CTAs done
-  // claiming); the last CTA to finish claiming resets both, so the same plan
-  // can be run again.
+  // The pool counters are pool[0] (next claim) and pool[1] (queues done
+  // claiming); the last queue to finish claiming resets both, so the same
+  // plan can be run again.  Every queue of the grid takes part in the pool.
+  const int queues_in_grid = static_cast<int>(gridDim.x) * G;
   auto finish_claims = [&]() {
-    if (atomicAdd(&pool[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    if (atomicAdd(&pool[1], 1) == queues_in_grid - 1) {
       pool[0] = 0;
       pool[1] = 0;
     }
   };
 
-  const int home_begin = cta_ptr[blockIdx.x];
-  const int home_stop = home_end[blockIdx.x];
+  // every thread checks the ranges of all the CTA's queues, so that the CTA
+  // leaves as a whole on a bad plan; queues past num_queues have no home part
   const int pool_len = pool[2];
-  const bool bad_range = home_begin < 0 || home_stop < home_begin || home_stop > capacity ||
-                         pool_len < 0 || pool_len > capacity;
+  bool bad_range = pool_len < 0 || pool_len > capacity;
+#pragma unroll
+  for (int k = 0; k < G; ++k) {
+    const int vq = static_cast<int>(blockIdx.x) * G + k;
+    if (vq < num_queues) {
+      const int b0 = cta_ptr[vq], b1 = home_end[vq];
+      bad_range = bad_range || b0 < 0 || b1 < b0 || b1 > capacity;
+    }
+  }
   if (bad_range) {
     if (threadIdx.x == 0) {
       atomicOr(status, HPC_STATUS_BAD_PLAN);
-      finish_claims();
+      for (int k = 0; k < G; ++k) finish_claims();
       if (cta_clock != nullptr) record_cta_clock(cta_clock, t_start);
     }
     return;
   }
+  const int vq = static_cast<int>(blockIdx.x) * G + grp;   // this warp's queue
+  const int home_begin = vq < num_queues ? cta_ptr[vq] : 0;
+  const int home_stop = vq < num_queues ? home_end[vq] : 0;
 
   __syncthreads();
 
@@ -242,11 +264,10 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   // block ids of the next 32 tiles are fetched while the current 32 are
   // issued (across item boundaries), and a pool claim is made when an item
   // starts and resolved during its last chunk.
-  if (warp == T::kConsumerWarps) {
+  if (is_producer) {
     const uint64_t policy = l2_evict_first_policy();
-    const uint32_t stage0 = smem_u32(smem);
     const int4* items4 = reinterpret_cast<const int4*>(items);
-    uint32_t g = 0;          // tiles issued so far by this CTA
+    uint32_t g = 0;          // tiles issued so far into this queue's ring
     uint32_t n_pushed = 0;   // items handed to the consumers so far
     bool claiming = true;    // the pool is not known to be empty yet
     bool alive = true;
@@ -349,8 +370,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     auto issue = [&](int bid, int h, bool data) -> bool {
       int tok = 1;
       if (lane == 0) {
-        const int s = static_cast<int>(g % S);
-        const uint32_t use = g / S;
+        const int s = static_cast<int>(g % SG);
+        const uint32_t use = g / SG;
         if (*abort_flag) {
           tok = 0;
         } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
@@ -362,7 +383,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           if (data && bid >= 0 && bid < num_blocks) {
             stage_ok[s] = 1;
             mbar_arrive_expect_tx(fb, T::kStageBytes);
-            const uint32_t dst = stage0 + s * T::kStageBytes;
+            const uint32_t dst = stage_base + s * T::kStageBytes;
             const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
             const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
             if constexpr (kFp8) {
@@ -396,10 +417,6 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
       } else {
         start_claim();
-        // start the item on a slot of group 0 (padding slots carry no data),
-        // so tile t of the item always goes to group (t - t0) % kGroups,
-        // whichever CTA runs it: the output does not depend on run order
-        while (alive && g % T::kGroups != 0) alive = issue(-1, 0, false);
       }
       Next nxt{-1, make_int4(-1, -1, 0, 0), -1};
       Item nit{-1, -1, 0, 0, 0, false};
@@ -434,22 +451,21 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     // After a fault, copies may still be landing in stages nobody will wait
     // on: wait for the last one issued into every stage before exiting.
     if (lane == 0 && *abort_flag) {
-      for (uint32_t s = 0; s < static_cast<uint32_t>(S) && s < g; ++s) {
-        const uint32_t last = s + S * ((g - 1 - s) / S);
-        mbar_wait(smem_u32(&full[s]), (last / S) & 1, status);
+      for (uint32_t s = 0; s < static_cast<uint32_t>(SG) && s < g; ++s) {
+        const uint32_t last = s + SG * ((g - 1 - s) / SG);
+        mbar_wait(smem_u32(&full[s]), (last / SG) & 1, status);
       }
     }
     return;
   }
 
   // ------------------------------------------------------------ consumers
-  const uint32_t grp = warp / T::kWarpsPerGroup;   // this warp's tiles: g % kGroups == grp
   const int wq = warp % T::kWarpsPerGroup;         // token quarter of each tile
+  const int gt = threadIdx.x - grp * T::kGroupThreads;   // thread index within the queue
   const int r = lane >> 2, c = lane & 3;
   const float k_scale = kFp8 ? kv_scale[0] : 1.f;
   const float v_scale = kFp8 ? kv_scale[1] : 1.f;
   const float scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
-  const uint32_t stage0 = smem_u32(smem);
   const int sw = lane & 7;                                        // swizzle of this lane's row
   const int row = 16 * wq + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row (token)
   const int hi = lane >> 4;                                        // second 16-byte chunk
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   uint32_t bar_phase = 0;
   bool dead = false;
 
-  // all consumer threads meet; bounded, so a stuck peer ends in a timeout
+  // the queue's consumer threads meet; bounded, so a stuck peer ends in a timeout
   auto cons_sync = [&]() -> bool {
     mbar_arrive(smem_u32(cons_bar));
     bool ok = !*abort_flag && mbar_wait(smem_u32(cons_bar), bar_phase & 1, status);
@@ -555,24 +571,10 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         }
       }
 
-      // the producer's padding slots: wait for them and hand them back
-      for (; g % T::kGroups != 0; ++g) {
-        if (dead || g % T::kGroups != grp) continue;
-        const int s = static_cast<int>(g % S);
-        bool tok = !*abort_flag && mbar_wait(smem_u32(&full[s]), (g / S) & 1, status);
-        tok = __all_sync(0xffffffffu, tok);
-        if (!tok) {
-          if (lane == 0) *abort_flag = 1;
-          dead = true;
-          continue;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-      }
       for (int t = it.t0; t < it.t1; ++t, ++g) {
-        if (dead || g % T::kGroups != grp) continue;
-        const int s = static_cast<int>(g % S);
-        const uint32_t use = g / S;
+        if (dead) continue;
+        const int s = static_cast<int>(g % SG);
+        const uint32_t use = g / SG;
         bool tok = !*abort_flag && mbar_wait(smem_u32(&full[s]), use & 1, status);
         tok = __all_sync(0xffffffffu, tok);
         if (!tok) {
@@ -582,7 +584,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         }
         const int nvalid = it.len - t * kPage - 16 * wq;   // valid tokens of my 16
         if (stage_ok[s] && nvalid > 0) {
-          const uint32_t kb = stage0 + s * T::kStageBytes;
+          const uint32_t kb = stage_base + s * T::kStageBytes;
           const uint32_t vb = kb + T::kPageBytes;
 
           // S^T = K Q^T  (rows: my 16 tokens, cols: 8 heads); two chains
@@ -708,23 +710,23 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     }
     if (!cons_sync()) break;
     // with the merge fused in: a segment of one item is final here; a segment
-    // of several items is merged by the CTA that finishes its last item
+    // of several items is merged by the queue that finishes its last item
     const int seg = it.seq * kHkv + it.h;
     const bool direct = fuse && it.ok && seg_items == 1;
+    const int w0 = grp * T::kWarpsPerGroup;   // the queue's first consumer warp
     {
-      const int ct = threadIdx.x;   // consumer thread
       float* dst = partial_o + static_cast<int64_t>(i) * kGroup * kD;
 #pragma unroll
-      for (int e = ct * 4; e < kGroup * kD; e += 32 * T::kConsumerWarps * 4) {
+      for (int e = gt * 4; e < kGroup * kD; e += T::kGroupThreads * 4) {
         const int hh = e >> 7;      // head of these 4 outputs
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < T::kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kGroup + hh]);
+        for (int w = w0; w < w0 + T::kWarpsPerGroup; ++w) M = fmaxf(M, sm_m[w * kGroup + hh]);
         const float Ms = M == -INFINITY ? 0.f : M;
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < T::kConsumerWarps; ++w) {
+        for (int w = w0; w < w0 + T::kWarpsPerGroup; ++w) {
           const float wt = exp2_ftz(sm_m[w * kGroup + hh] - Ms);
           L += wt * sm_l[w * kGroup + hh];
           const float4 x =
@@ -752,8 +754,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     }
     if (fuse && it.ok && !direct) {
       if (!cons_sync()) break;     // every thread's share of the partial is written
-      if (threadIdx.x == 0) {
-        __threadfence();           // the CTA's partial is visible device-wide before the count
+      if (gt == 0) {
+        __threadfence();           // the partial is visible device-wide before the count
         const int done = atomicAdd(&seg_done[seg], 1);
         *merge_flag = done == seg_items - 1;
         if (done == seg_items - 1) {
@@ -764,57 +766,68 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       if (!cons_sync()) break;
       if (*merge_flag) {
         // the last item of the segment: merge its partials.  The lse values
-        // are staged in shared memory (the merge slices are free now) by one
-        // parallel load, so the per-thread loop is a single pass of
+        // are staged in shared memory (the queue's merge slices are free now)
+        // by one parallel load, so the per-thread loop is a single pass of
         // independent float4 loads through L2; segments of more than
         // kMergeChunk items are taken chunk by chunk with an online rescale.
-        constexpr int kMergeChunk = 1024;
-        static_assert(kMergeChunk * kGroup <= T::kConsumerWarps * kGroup * T::kOStride,
-                      "the lse staging area must fit in the merge slices");
-        static_assert(32 * T::kConsumerWarps * 4 >= kGroup * kD, "one float4 of output per thread");
-        float* lse_s = sm_o;
+        constexpr int kMergeChunk = 512;
+        constexpr int kOuts = kGroup * kD / (4 * T::kGroupThreads);   // float4 outputs per thread
+        static_assert(kMergeChunk * kGroup <= T::kWarpsPerGroup * kGroup * T::kOStride,
+                      "the lse staging area must fit in the queue's merge slices");
+        static_assert(kOuts * 4 * T::kGroupThreads == kGroup * kD, "outputs split evenly");
+        float* lse_s = sm_o + w0 * kGroup * T::kOStride;
         const int i0 = seg_first;
-        // one float4 of output per thread; threads past the 1024 outputs
-        // only stage lse values and meet at the barriers
-        const bool has_out = threadIdx.x * 4 < kGroup * kD;
-        const int e = has_out ? threadIdx.x * 4 : 0;
-        const int hh = e >> 7;
-        float M = -INFINITY, W = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M[kOuts], W[kOuts];
+        float4 acc[kOuts];
+#pragma unroll
+        for (int u = 0; u < kOuts; ++u) {
+          M[u] = -INFINITY;
+          W[u] = 0.f;
+          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         bool synced = true;
         for (int base = 0; base < seg_items && synced; base += kMergeChunk) {
           const int m = min(kMergeChunk, seg_items - base);
-          for (int x = threadIdx.x; x < m * kGroup; x += 32 * T::kConsumerWarps)
+          for (int x = gt; x < m * kGroup; x += T::kGroupThreads)
             lse_s[x] = __ldcg(partial_lse + static_cast<int64_t>(i0 + base) * kGroup + x);
           if (!(synced = cons_sync())) break;
-          float Mn = M;
-          for (int k = 0; k < m; ++k) Mn = fmaxf(Mn, lse_s[k * kGroup + hh]);
-          if (has_out && Mn != -INFINITY) {
-            const float sc = __expf(M - Mn);   // 0 while M is still -inf
-            acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-            W *= sc;
-            const float* po = partial_o + static_cast<int64_t>(i0 + base) * kGroup * kD + e;
+#pragma unroll
+          for (int u = 0; u < kOuts; ++u) {
+            const int e = (gt + u * T::kGroupThreads) * 4;
+            const int hh = e >> 7;
+            float Mn = M[u];
+            for (int k = 0; k < m; ++k) Mn = fmaxf(Mn, lse_s[k * kGroup + hh]);
+            if (Mn != -INFINITY) {
+              const float sc = __expf(M[u] - Mn);   // 0 while M is still -inf
+              acc[u].x *= sc; acc[u].y *= sc; acc[u].z *= sc; acc[u].w *= sc;
+              W[u] *= sc;
+              const float* po = partial_o + static_cast<int64_t>(i0 + base) * kGroup * kD + e;
 #pragma unroll 8
-            for (int k = 0; k < m; ++k) {
-              const float w = __expf(lse_s[k * kGroup + hh] - Mn);
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * kGroup * kD));
-              acc.x += w * x.x;
-              acc.y += w * x.y;
-              acc.z += w * x.z;
-              acc.w += w * x.w;
-              W += w;
+              for (int k = 0; k < m; ++k) {
+                const float w = __expf(lse_s[k * kGroup + hh] - Mn);
+                const float4 x =
+                    __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * kGroup * kD));
+                acc[u].x += w * x.x;
+                acc[u].y += w * x.y;
+                acc[u].z += w * x.z;
+                acc[u].w += w * x.w;
+                W[u] += w;
+              }
+              M[u] = Mn;
             }
-            M = Mn;
           }
           synced = cons_sync();   // before the staging area is overwritten
         }
         if (!synced) break;
-        const float inv = W > 0.f ? 1.f / W : 0.f;
-        uint2 packed;
-        packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-        packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-        if (has_out)
+#pragma unroll
+        for (int u = 0; u < kOuts; ++u) {
+          const int e = (gt + u * T::kGroupThreads) * 4;
+          const float inv = W[u] > 0.f ? 1.f / W[u] : 0.f;
+          uint2 packed;
+          packed.x = pack_bf16(acc[u].x * inv, acc[u].y * inv);
+          packed.y = pack_bf16(acc[u].z * inv, acc[u].w * inv);
           *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
+        }
       }
     }
     if (!cons_sync()) break;
@@ -827,7 +840,10 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     seg_first = next_first;
     seg_items = next_items;
   }
-  if (cta_clock != nullptr && threadIdx.x == 0) record_cta_clock(cta_clock, t_start);
+  if (cta_clock != nullptr) {
+    named_bar_sync(1, 32 * T::kConsumerWarps);   // every queue of the CTA is done
+    if (threadIdx.x == 0) record_cta_clock(cta_clock, t_start);
+  }
 }
 
 // ------------------------------------------------------------ host side
@@ -885,7 +901,7 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan->num_ctas);
+  cfg.gridDim = dim3((plan->num_ctas + T::kGroups - 1) / T::kGroups);   // kGroups queues per CTA
   cfg.blockDim = dim3(T::kThreads);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = stream;
@@ -898,7 +914,7 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
       &cfg, decode_attn_kernel<kFp8>, map, static_cast<const uint16_t*>(q), kv_scale, block_table,
       max_blocks, num_blocks, seq_lens, batch, static_cast<const hpc_work_item*>(plan->items),
       static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
-      plan->pool, plan->capacity, partial_o, partial_lse, sm_scale, status, cta_clock,
+      plan->pool, plan->capacity, plan->num_ctas, partial_o, partial_lse, sm_scale, status, cta_clock,
       static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out);
   return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
@@ -978,6 +994,9 @@ extern "C" int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas) {
   if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
-  *num_ctas = sms;   // one resident CTA per SM (the stage ring takes ~200 KB)
+  // one resident CTA per SM (the stage rings take ~200 KB), each running
+  // 2 (BF16) or 3 (FP8) work queues
+  *num_ctas = sms * (kv_dtype == HPC_KV_BF16 ? hpc::AttnTraits<false>::kGroups
+                                             : hpc::AttnTraits<true>::kGroups);
   return HPC_OK;
 }
