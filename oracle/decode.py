@@ -190,6 +190,35 @@ def decode_attention(q, cache, block_row, length, kv_dtype, k_scale=1.0, v_scale
     return out
 
 
+def decode_attention_mt(q, cache, block_row, length, kv_dtype, k_scale=1.0, v_scale=1.0,
+                        heads=None, scale=1.0 / math.sqrt(D)):
+    """Multi-token decode attention of one sequence: q [q_len,64,128] ->
+    out [q_len,64,128] (float64).
+
+    The sequence holds ``length`` tokens, the last q_len of them new in this
+    step (a multi-token-prediction layer decodes its draft tokens together).
+    New token t sits at position p_t = length - q_len + t and sees the keys at
+    positions 0..p_t: the whole history and the new tokens up to itself.  A
+    token that sees no key (length < q_len) gets zeros.  q_len = 1 is
+    ``decode_attention``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    qn = q.shape[0]
+    out = np.full((qn, HQ, D), np.nan)
+    heads = range(HQ) if heads is None else heads
+    by_kv = {}
+    for j in heads:
+        by_kv.setdefault(j // GROUP, []).append(j)
+    for h, js in by_kv.items():
+        if length > 0:
+            K, V = gather_kv(cache, block_row, length, h, kv_dtype, k_scale, v_scale)
+        for t in range(qn):
+            seen = int(length) - qn + 1 + t          # keys visible to new token t
+            for j in js:
+                out[t, j] = attention_head(q[t, j], K[:seen], V[:seen], scale) if seen > 0 else 0.0
+    return out
+
+
 def brute_force_attention(q, K, V, scale):
     """Pure-Python triple loop version of ``attention_head`` for tiny inputs."""
     L, d = len(K), len(q)
@@ -227,4 +256,32 @@ def decode_step(q, k, v, positions, q_w, k_w, cache, block_table, seq_lens,
     for b in seqs:
         out[b] = decode_attention(q_out[b], cache, block_table[b], int(seq_lens[b]),
                                   kv_dtype, ks, vs, heads=heads)
+    return q_out, out
+
+
+def decode_step_mt(q, k, v, positions, q_w, k_w, cache, block_table, seq_lens, slot_mapping,
+                   kv_dtype, kv_scale=(1.0, 1.0), heads=None, seqs=None):
+    """The multi-token step: q [B,q_len,64,128], k and v [B,q_len,8,128],
+    positions and slot_mapping [B,q_len].
+
+    1. the prologue of every new token (RoPE at its own position, RMSNorm,
+       BF16 q, k and v written into its cache slot), tokens in order;
+    2. ``decode_attention_mt`` of the BF16 q over the cache.
+
+    Returns (q_out [B,q_len,64,128], out [B,q_len,64,128]); rows of sequences
+    not in ``seqs`` are NaN.
+    """
+    B, qn = len(seq_lens), q.shape[1]
+    seqs = range(B) if seqs is None else seqs
+    q_out = np.full((B, qn, HQ, D), np.nan)
+    out = np.full((B, qn, HQ, D), np.nan)
+    ks, vs = float(kv_scale[0]), float(kv_scale[1])
+    for b in seqs:
+        for t in range(qn):
+            qo, ko, vo = prologue_token(q[b, t], k[b, t], v[b, t], positions[b][t], q_w, k_w)
+            write_kv(cache, slot_mapping[b][t], ko, vo, kv_dtype, ks, vs)
+            q_out[b, t] = nx.bf16_round(qo)
+    for b in seqs:
+        out[b] = decode_attention_mt(q_out[b], cache, block_table[b], int(seq_lens[b]),
+                                     kv_dtype, ks, vs, heads=heads)
     return q_out, out

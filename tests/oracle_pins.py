@@ -136,6 +136,60 @@ def check_attention_sdpa(decode_attention_fn, rng, kv_dtype=0):
         assert np.allclose(out, ref, rtol=1e-11, atol=1e-12), (b, np.max(np.abs(out - ref)))
 
 
+def check_attention_mt_sdpa(mt_fn, rng):
+    """Multi-token decode over a paged cache equals torch SDPA (float64,
+    enable_gqa) with an explicit boolean mask: query t of q_len, at position
+    L - q_len + t, may attend to key s iff s <= L - q_len + t.  A query that
+    sees no key (L < q_len) must give zeros."""
+    from oracle import decode as od
+    cases = [(2, 2), (2, 65), (3, 64), (3, 130), (4, 4), (4, 129), (2, 1), (4, 2)]
+    n_pages = [-(-L // 64) for _, L in cases]
+    nb = sum(n_pages) + 2
+    perm = rng.permutation(nb)
+    Kc = rng.standard_normal((nb, 8, 64, D))
+    Vc = rng.standard_normal((nb, 8, 64, D))
+    cache = np.stack([od.encode_kv(Kc, 0), od.encode_kv(Vc, 0)], axis=1)
+    o = 0
+    for (qn, L), n in zip(cases, n_pages):
+        bt = perm[o:o + n]
+        o += n
+        q = rng.standard_normal((qn, 64, D))
+        out = mt_fn(q, cache, bt, L, 0)
+        K = np.concatenate([od.decode_kv(cache[pg, 0], 0) for pg in bt], axis=1)[:, :L]
+        V = np.concatenate([od.decode_kv(cache[pg, 1], 0) for pg in bt], axis=1)[:, :L]
+        mask = np.arange(L)[None, :] <= (L - qn + np.arange(qn))[:, None]      # [q_len, L]
+        for t in range(qn):
+            if not mask[t].any():
+                assert np.all(out[t] == 0.0), (qn, L, t)
+                continue
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q[t])[None, :, None, :], torch.from_numpy(K)[None],
+                torch.from_numpy(V)[None], attn_mask=torch.from_numpy(mask[t:t + 1]),
+                enable_gqa=True)[0, :, 0, :].numpy()
+            assert np.allclose(out[t], ref, rtol=1e-11, atol=1e-12), (qn, L, t)
+
+
+def check_attention_mt_causal(mt_fn, single_fn, rng):
+    """Changing the value of the last new token changes only the last query's
+    output; with q_len = 1 the multi-token form is the single-token one."""
+    from oracle import decode as od
+    L, qn = 200, 3
+    Kc = rng.standard_normal((4, 8, 64, D))
+    Vc = rng.standard_normal((4, 8, 64, D))
+    cache = np.stack([od.encode_kv(Kc, 0), od.encode_kv(Vc, 0)], axis=1)
+    bt = np.array([2, 0, 3, 1])
+    q = rng.standard_normal((qn, 64, D))
+    a = mt_fn(q, cache, bt, L, 0)
+    c2 = cache.copy()
+    last = L - 1
+    c2[bt[last // 64], 1, :, last % 64] = od.encode_kv(rng.standard_normal((8, D)) * 5, 0)
+    b = mt_fn(q, c2, bt, L, 0)
+    assert np.array_equal(a[:qn - 1], b[:qn - 1])
+    assert np.abs(a[qn - 1] - b[qn - 1]).max() > 1e-3
+    one = mt_fn(q[:1], cache, bt, L, 0)[0]
+    assert np.array_equal(one, single_fn(q[0], cache, bt, L, 0))
+
+
 def check_split_merge(partial_fn, merge_fn, rng):
     """Splitting the keys at arbitrary cut points and merging the partials
     equals the unsplit result; lse equals scipy's logsumexp."""

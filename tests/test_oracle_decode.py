@@ -65,6 +65,14 @@ def test_attention_matches_sdpa_gqa(rng):
     pins.check_attention_sdpa(od.decode_attention, rng)
 
 
+def test_multi_token_attention_matches_masked_sdpa(rng):
+    pins.check_attention_mt_sdpa(od.decode_attention_mt, rng)
+
+
+def test_multi_token_attention_is_causal(rng):
+    pins.check_attention_mt_causal(od.decode_attention_mt, od.decode_attention, rng)
+
+
 def test_split_merge_equals_unsplit(rng):
     pins.check_split_merge(od.partial_attention, od.merge_partials, rng)
 
@@ -162,3 +170,45 @@ def test_decode_step_tiny_matches_composition(rng):
     for s in slots:
         mask[s // 64, s % 64] = False
     assert np.array_equal(cache.transpose(0, 3, 1, 2, 4)[mask], c0.transpose(0, 3, 1, 2, 4)[mask])
+
+
+def test_multi_token_step_writes_every_new_token_and_is_the_single_step_at_one(rng):
+    """The multi-token step writes each new token into its own slot at its own
+    position, and with q_len = 1 it is the single-token step."""
+    lengths = [3, 66, 130]
+    qn = 3
+    n = [-(-L // 64) for L in lengths]
+    nb = sum(n) + 1
+    bt = np.zeros((3, max(n)), np.int64)
+    perm = rng.permutation(nb)
+    o = 0
+    for b in range(3):
+        bt[b, :n[b]] = perm[o:o + n[b]]
+        o += n[b]
+    cache = od.encode_kv(rng.standard_normal((nb, 2, 8, 64, 128)), 0)
+    q = rng.standard_normal((3, qn, 64, 128))
+    k = rng.standard_normal((3, qn, 8, 128))
+    v = rng.standard_normal((3, qn, 8, 128))
+    qw = nx.bf16_round(1 + 0.1 * rng.standard_normal(128))
+    kw = nx.bf16_round(1 + 0.1 * rng.standard_normal(128))
+    pos = [[L - qn + t for t in range(qn)] for L in lengths]
+    slots = [[bt[b, p // 64] * 64 + p % 64 for p in pos[b]] for b in range(3)]
+    c1 = cache.copy()
+    q_out, out = od.decode_step_mt(q, k, v, pos, qw, kw, c1, bt, lengths, slots, 0)
+    for b in range(3):
+        for t in range(qn):
+            qo, ko, vo = od.prologue_token(q[b, t], k[b, t], v[b, t], pos[b][t], qw, kw)
+            assert np.array_equal(q_out[b, t], nx.bf16_round(qo))
+            blk, off = divmod(slots[b][t], 64)
+            assert np.array_equal(c1[blk, 0, :, off], od.encode_kv(ko, 0))
+            assert np.array_equal(c1[blk, 1, :, off], od.encode_kv(vo, 0))
+    # q_len = 1: the last new token alone, after the others were written
+    c2 = c1.copy()
+    last = [[p[-1]] for p in pos]
+    lslots = [[s[-1]] for s in slots]
+    q1, o1 = od.decode_step_mt(q[:, -1:], k[:, -1:], v[:, -1:], last, qw, kw, c2, bt, lengths, lslots, 0)
+    c3 = c1.copy()
+    q2, o2 = od.decode_step(q[:, -1], k[:, -1], v[:, -1], [p[0] for p in last], qw, kw, c3, bt,
+                            lengths, [s[0] for s in lslots], 0)
+    assert np.array_equal(o1[:, 0], o2) and np.array_equal(q1[:, 0], q2)
+    assert np.allclose(out[:, -1], o2, rtol=0, atol=1e-12)

@@ -179,3 +179,31 @@ def test_plan_mutants_fail():
     a = op.plan_dynamic(lens, 6, 1)[0]
     b = plan_floor_quota(lens, 6, 1)
     assert [tuple(i) for i in a] != [tuple(i) for i in b]
+
+
+def _mt_mutant(kind):
+    """A copy of the multi-token attention with one plausible mistake."""
+    def fn(q, cache, block_row, length, kv_dtype, k_scale=1.0, v_scale=1.0):
+        q = np.asarray(q, dtype=np.float64)
+        qn = q.shape[0]
+        out = np.zeros((qn, od.HQ, od.D))
+        for h in range(od.HKV):
+            K, V = od.gather_kv(cache, block_row, length, h, kv_dtype, k_scale, v_scale)
+            for t in range(qn):
+                if kind == "no_mask":
+                    seen = length
+                elif kind == "self_hidden":
+                    seen = length - qn + t
+                else:                                   # "reversed": new tokens in the wrong order
+                    seen = length - t
+                for j in range(h * 8, h * 8 + 8):
+                    if seen > 0:
+                        out[t, j] = od.attention_head(q[t, j], K[:seen], V[:seen])
+        return out
+    return fn
+
+
+@pytest.mark.parametrize("kind", ["no_mask", "self_hidden", "reversed"])
+def test_multi_token_mutants_fail_masked_sdpa(kind):
+    with pytest.raises(AssertionError):
+        pins.check_attention_mt_sdpa(_mt_mutant(kind), np.random.default_rng(3))
