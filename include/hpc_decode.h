@@ -57,6 +57,7 @@ extern "C" {
 #define HPC_PAGE_TOKENS 64
 #define HPC_MAX_BATCH 8192          /* planner limit on the batch size */
 #define HPC_MAX_PLAN_CTAS 16384     /* length-proportional planner limit on num_ctas */
+#define HPC_MAX_Q_LEN 4             /* new tokens per sequence in multi-token decode */
 #define HPC_MAX_NUM_BLOCKS 2097151  /* cache blocks addressable by the TMA map */
 
 typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
@@ -345,6 +346,42 @@ int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
 /* Items a length-proportional plan may need:
  * num_ctas * (1 + pool_chunks) + 8 * batch. */
 int32_t hpc_plan_capacity(int32_t batch, int32_t num_ctas, int32_t pool_chunks);
+
+/* Multi-token decode: q_len = 2 .. HPC_MAX_Q_LEN new tokens per sequence,
+ * decoded together (the draft tokens of a multi-token-prediction layer).
+ * seq_lens counts every token of a sequence, the q_len new ones included;
+ * new token j of sequence b sits at position seq_lens[b] - q_len + j and
+ * attends to the keys at positions 0 .. seq_lens[b] - q_len + j (its
+ * history and the new tokens up to itself).  A token that sees no key gets
+ * zeros.  The prologue needs no variant: hpc_rope_norm_kvwrite treats its
+ * batch as independent tokens, so call it with batch * q_len tokens, their
+ * own positions and slots, in [batch][q_len] order.
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", intro of "Two new HPC backends in the vLLM ecosystem" (the served
+ * model's multi-token-prediction layer); the attention is that of
+ * hpc_decode_attn with the causal order among the new tokens.
+ * Arguments as hpc_decode_attn / hpc_decode_attn_merge / hpc_merge, except:
+ *   q            (device) bf16 [batch, q_len, 64, 128]
+ *   q_len        1 .. HPC_MAX_Q_LEN (1 is hpc_decode_attn)
+ *   partial_o    (device) float32 [plan->capacity, q_len, 8, 128]
+ *   partial_lse  (device) float32 [plan->capacity, q_len, 8]
+ *   out          (device) bf16 [batch, q_len, 64, 128]
+ * The plan is the same as for single-token decode (tiles per sequence).
+ * Errors: as the single-token calls, and HPC_ERR_INVALID_ARG for q_len out of
+ * range. */
+int hpc_decode_attn_mt(const void* q, const void* kv_cache, int32_t kv_dtype,
+                       const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
+                       int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                       const hpc_plan* plan, float* partial_o, float* partial_lse,
+                       float sm_scale, int32_t* status, cudaStream_t stream);
+int hpc_decode_attn_merge_mt(const void* q, const void* kv_cache, int32_t kv_dtype,
+                             const float* kv_scale, int32_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t batch, int32_t q_len,
+                             const hpc_plan* plan, float* partial_o, float* partial_lse,
+                             void* out, float sm_scale, int32_t* status, cudaStream_t stream);
+int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                 int32_t batch, int32_t q_len, void* out, cudaStream_t stream);
 
 /* Self-test of the bounded pipeline wait (no counterpart on the pages).
  * Every wait of the attention pipeline gives up after a time limit (1 s),

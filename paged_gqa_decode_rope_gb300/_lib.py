@@ -14,6 +14,7 @@ HPC_ERR_INVALID_ARG = -1
 HPC_ERR_UNSUPPORTED = -2
 HPC_ERR_CUDA = -3
 NOALLOC_MAX_ITEMS = 4096
+MAX_Q_LEN = 4
 
 STATUS_BITS = {
     1: "BAD_BLOCK", 2: "BAD_SLOT", 4: "BAD_SEQ_LEN", 8: "BAD_POSITION",
@@ -65,6 +66,13 @@ SIGNATURES = {
         _c_p, _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
     "hpc_decode_num_ctas": (ctypes.c_int, [_c_i32, ctypes.POINTER(_c_i32)]),
     "hpc_plan_capacity": (_c_i32, [_c_i32, _c_i32, _c_i32]),
+    "hpc_decode_attn_mt": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_i32, ctypes.POINTER(Plan),
+        _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_decode_attn_merge_mt": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_i32, ctypes.POINTER(Plan),
+        _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_merge_mt": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(Plan), _c_i32, _c_i32, _c_p, _c_p]),
     "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }
 

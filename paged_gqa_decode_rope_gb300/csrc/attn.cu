@@ -1,954 +1,32 @@
-// Split-KV paged GQA decode attention (q_len = 1), sm_103a.
-//
-// Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
-// Hopper": intro of "Two new HPC backends in the vLLM ecosystem" (64 query
-// heads, 8 KV heads, head_dim 128) and "Why does dynamic scheduling matter
-// for attention?" (split-KV over 64-token tiles dealt to compute units in
-// proportion to length; BF16 and FP8).  Page "[vllm] Introducing the HPC-Ops
-// attention backend", introduction (FP8 E4M3 models).
-//
-// Design (GB300-first; the pages give no kernel structure):
-//  * Persistent grid, one CTA per SM.  CTA c runs the work items
-//    cta_ptr[c] .. cta_ptr[c+1]-1 of the plan.  The path is bound by HBM: each
-//    64-token K page and V page of a KV head is read exactly once and serves
-//    all 8 query heads of its group.
-//  * One producer warp streams pages with TMA (cp.async.bulk.tensor, 128-byte
-//    swizzle, L2 evict-first) into a ring of stages guarded by mbarriers; a
-//    stage is one tile = the K page + the V page of one (block, kv_head).
-//    Block ids are fetched 32 at a time by the whole warp, so the issue loop
-//    never waits on a global load per tile.
-//  * Two groups of four consumer warps take alternate tiles, so two tiles are
-//    in flight through the math at once; inside a group the four warps split
-//    the tile's 64 tokens, 16 each.  Every warp keeps its own
-//    online-softmax state (running max m, sum l, output O) for the current
-//    item; at the end of an item the states are merged in shared memory, in a
-//    fixed warp order, and written as one partial (O, lse).
-//  * Tensor cores at q_len = 1 without padding: S^T[16 tok x 8 heads] =
-//    K[16 x 128] . Q^T[128 x 8] (m16n8k16, tokens on M, heads on N), then
-//    O^T[128 x 8] += V^T[128 x 16 tok] . P^T[16 x 8] (d on M, heads on N).
-//    The softmax runs on the S^T accumulator fragment; movmatrix transposes
-//    P^T into the B-operand layout, so P never touches shared memory.
-//  * FP8 E4M3 pages are converted to f16 in registers after ldmatrix
-//    (exact), q is taken to f16 once per item; the k scale folds into the
-//    softmax scale and the v scale into the output.  For FP8 the dot products
-//    run over a fixed permutation of d (and the V rows over a permutation of
-//    d inside each 16-row tile) that makes each ldmatrix word feed the MMA
-//    directly; q uses the same permutation and the epilogue undoes it.
-//  * Tokens past the sequence length get p = 0 and their V entries are
-//    zeroed in registers (the cache may hold NaN there: 0 * NaN is NaN).
-//  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
-//    HPC_STATUS_WAIT_TIMEOUT and winds down, waiting for its own copies.
-#include <mutex>
-
-#include <cudaTypedefs.h>
-
-#include "common.cuh"
-#include "internal.h"
-
-namespace hpc {
-namespace {
-
-template <bool kFp8>
-struct AttnTraits {
-  static constexpr int kElem = kFp8 ? 1 : 2;
-  static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
-  static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
-  static constexpr int kStageBytes = 2 * kPageBytes;          // K page + V page
-  // A CTA hosts kGroups independent work queues.  A queue has its own producer
-  // warp, stage ring, item ring and 4 consumer warps, and runs whole work
-  // items, so one queue's epilogue and merge overlap the other queues'
-  // streaming.  FP8 tiles carry a longer per-tile chain (the conversions) at
-  // half the bytes, so FP8 keeps three queues in flight.
-  static constexpr int kGroups = kFp8 ? 3 : 2;
-  static constexpr int kGroupStages = 3;                      // stage ring of one queue
-  static constexpr int kStages = kGroups * kGroupStages;
-  static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
-  static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
-  static constexpr int kGroupThreads = 32 * kWarpsPerGroup;
-  static constexpr int kThreads = 32 * (kConsumerWarps + kGroups);   // + a producer warp per queue
-  static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
-  static constexpr int kOffO = kStages * kStageBytes;                 // [warps][8][kOStride]
-  static constexpr int kOffM = kOffO + kConsumerWarps * kGroup * kOStride * 4;
-  static constexpr int kOffL = kOffM + kConsumerWarps * kGroup * 4;
-  static constexpr int kOffBar = kOffL + kConsumerWarps * kGroup * 4;
-  static constexpr int kItemRing = 2;                         // items queued ahead, per queue
-  // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier
-  static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1;
-  static constexpr int kOffOk = kOffBar + kGroups * kGroupBars * 8;
-  static constexpr int kOffRing = kOffOk + kStages * 4;
-  static constexpr int kRingInts = 8;                         // idx, seq, h, t0, t1, len
-  // flags: the CTA's abort flag, then one merge flag per queue
-  static constexpr int kOffFlags = kOffRing + kGroups * kItemRing * kRingInts * 4;
-  static constexpr int kSmemUsed = kOffFlags + 4 * (1 + kGroups);
-  static constexpr int kSmemBytes = kSmemUsed + 1024;         // slack for 1024-byte alignment
-  static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
-  static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
-};
-
-struct Item {
-  int seq, h, t0, t1, len;
-  bool ok;
-};
-
-// The item (w = {seq, kv_head, tile_begin, tile_end}) checked against the
-// batch, with `len` the length of its sequence (-1 if the sequence id is bad).
-__device__ __forceinline__ Item make_item(int4 w, int len, int batch, int max_blocks) {
-  Item it{w.x, w.y, w.z, w.w, 0, false};
-  if (it.seq >= 0 && it.seq < batch && it.h >= 0 && it.h < kHkv && len >= 0 &&
-      len <= max_blocks * kPage) {
-    const int n = (len + kPage - 1) / kPage;
-    if (it.t0 >= 0 && it.t0 < it.t1 && it.t1 <= n) {
-      it.ok = true;
-      it.len = len;
-    }
-  }
-  return it;
-}
-
-// Diagnostic record of one CTA: [start ns, end ns, SM id] (globaltimer).
-__device__ __forceinline__ void record_cta_clock(unsigned long long* cta_clock,
-                                                 unsigned long long t_start) {
-  uint32_t smid;
-  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-  cta_clock[3 * blockIdx.x + 0] = t_start;
-  cta_clock[3 * blockIdx.x + 1] = globaltimer_ns();
-  cta_clock[3 * blockIdx.x + 2] = smid;
-}
-
-// O^T += V^T P^T for one warp's 16 tokens (rows: d, cols: 8 heads).  With
-// kMask, V entries of tokens past the length are zeroed first (mask01 covers
-// the fragment's tokens 2c, 2c+1; mask23 tokens 2c+8, 2c+9).
-template <bool kFp8, bool kMask>
-__device__ __forceinline__ void pv_tile(uint32_t vb, int row, int vtok_bf16, int vsel_bf16, int hi,
-                                        int sw, uint32_t pb0, uint32_t pb1, uint32_t mask01,
-                                        uint32_t mask23, float (&o)[8][4]) {
-  if constexpr (kFp8) {
-#pragma unroll
-    for (int mp = 0; mp < 4; ++mp) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_t(vb + row * 128 + ((((2 * mp + hi) & 7) ^ sw) << 4), r0, r1, r2, r3);
-      // r0: tokens 2c, 2c+1 at d 2r, 2r+1 (bytes t0d0, t0d1, t1d0, t1d1); the
-      // byte shuffle pairs the two tokens of one d for each f16x2
-      const uint32_t x = prmt(r0, 0, 0x3120), y = prmt(r1, 0, 0x3120);
-      const uint32_t z = prmt(r2, 0, 0x3120), w = prmt(r3, 0, 0x3120);
-      uint32_t a[8] = {e4m3x2_to_f16x2(x & 0xffff), e4m3x2_to_f16x2(x >> 16),
-                       e4m3x2_to_f16x2(y & 0xffff), e4m3x2_to_f16x2(y >> 16),
-                       e4m3x2_to_f16x2(z & 0xffff), e4m3x2_to_f16x2(z >> 16),
-                       e4m3x2_to_f16x2(w & 0xffff), e4m3x2_to_f16x2(w >> 16)};
-      if constexpr (kMask) {
-        a[0] &= mask01; a[1] &= mask01; a[2] &= mask23; a[3] &= mask23;
-        a[4] &= mask01; a[5] &= mask01; a[6] &= mask23; a[7] &= mask23;
-      }
-      mma_f16(o[2 * mp], a[0], a[1], a[2], a[3], pb0, pb1);
-      mma_f16(o[2 * mp + 1], a[4], a[5], a[6], a[7], pb0, pb1);
-    }
-  } else {
-#pragma unroll
-    for (int mi = 0; mi < 8; ++mi) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(vb + (mi >> 2) * (64 * 128) + vtok_bf16 * 128 + ((((2 * mi + vsel_bf16) & 7) ^ sw) << 4),
-                a0, a1, a2, a3);
-      if constexpr (kMask) {
-        a0 &= mask01; a1 &= mask01; a2 &= mask23; a3 &= mask23;
-      }
-      mma_bf16(o[mi], a0, a1, a2, a3, pb0, pb1);
-    }
-  }
-}
-
-template <bool kFp8>
-__global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_kernel(
-    // q, the plan arrays and the cache may be written by the kernel this one
-    // is a programmatic dependent of: they are read with plain (coherent)
-    // loads, never as restrict/read-only data, so that no load of them can be
-    // hoisted above the grid-dependency wait
-    const __grid_constant__ CUtensorMap kv_map, const uint16_t* q,
-    const float* __restrict__ kv_scale, const int32_t* __restrict__ block_table, int32_t max_blocks,
-    int32_t num_blocks, const int32_t* __restrict__ seq_lens, int32_t batch,
-    const hpc_work_item* items, const int32_t* cta_ptr, const int32_t* home_end, int32_t* pool,
-    int32_t capacity, int32_t num_queues, float* __restrict__ partial_o,
-    float* __restrict__ partial_lse,
-    float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
-    const int32_t* seg_ptr, int32_t* seg_done, uint16_t* __restrict__ out) {
-  using T = AttnTraits<kFp8>;
-  constexpr int G = T::kGroups;
-  constexpr int SG = T::kGroupStages;
-  constexpr int R = T::kItemRing;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  float* sm_o = reinterpret_cast<float*>(smem + T::kOffO);
-  float* sm_m = reinterpret_cast<float*>(smem + T::kOffM);
-  float* sm_l = reinterpret_cast<float*>(smem + T::kOffL);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + T::kOffFlags);
-  const bool fuse = out != nullptr;   // merge the partials in this kernel
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  // warps 0 .. 4G-1 consume (queue k: warps 4k .. 4k+3); warp 4G + k produces for queue k
-  const bool is_producer = warp >= T::kConsumerWarps;
-  const int grp = is_producer ? warp - T::kConsumerWarps : warp / T::kWarpsPerGroup;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + T::kOffBar) + grp * T::kGroupBars;
-  uint64_t* empty = full + SG;
-  uint64_t* item_full = empty + SG;
-  uint64_t* item_empty = item_full + R;
-  uint64_t* cons_bar = item_empty + R;
-  volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + T::kOffOk) + grp * SG;
-  volatile int* ring = reinterpret_cast<volatile int*>(smem + T::kOffRing) + grp * R * T::kRingInts;
-  volatile int* merge_flag = abort_flag + 1 + grp;
-  const uint32_t stage_base = smem_u32(smem) + grp * SG * T::kStageBytes;   // this queue's stages
-
-  const unsigned long long t_start = cta_clock != nullptr ? globaltimer_ns() : 0ull;
-  if (threadIdx.x == 0) {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::kOffBar);
-    for (int k = 0; k < G; ++k) {
-      uint64_t* b = bars + k * T::kGroupBars;
-      for (int st = 0; st < SG; ++st) {
-        mbar_init(smem_u32(&b[st]), 1);                           // full
-        mbar_init(smem_u32(&b[SG + st]), T::kWarpsPerGroup);      // empty
-      }
-      for (int r = 0; r < R; ++r) {
-        mbar_init(smem_u32(&b[2 * SG + r]), 1);                   // item_full
-        mbar_init(smem_u32(&b[2 * SG + R + r]), T::kWarpsPerGroup);   // item_empty
-      }
-      mbar_init(smem_u32(&b[2 * SG + 2 * R]), T::kGroupThreads);  // the queue's consumer barrier
-    }
-    *abort_flag = 0;
-    mbar_fence_init();
-  }
-  if (warp == T::kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
-  // everything above is independent of the previous kernel on the stream;
-  // from here on the plan, q and the cache are read
-  pdl_wait();
-
-  // The pool counters are pool[0] (next claim) and pool[1] (queues done
-  // claiming); the last queue to finish claiming resets both, so the same
-  // plan can be run again.  Every queue of the grid takes part in the pool.
-  const int queues_in_grid = static_cast<int>(gridDim.x) * G;
-  auto finish_claims = [&]() {
-    if (atomicAdd(&pool[1], 1) == queues_in_grid - 1) {
-      pool[0] = 0;
-      pool[1] = 0;
-    }
-  };
-
-  // every thread checks the ranges of all the CTA's queues, so that the CTA
-  // leaves as a whole on a bad plan; queues past num_queues have no home part
-  const int pool_len = pool[2];
-  bool bad_range = pool_len < 0 || pool_len > capacity;
-#pragma unroll
-  for (int k = 0; k < G; ++k) {
-    const int vq = static_cast<int>(blockIdx.x) * G + k;
-    if (vq < num_queues) {
-      const int b0 = cta_ptr[vq], b1 = home_end[vq];
-      bad_range = bad_range || b0 < 0 || b1 < b0 || b1 > capacity;
-    }
-  }
-  if (bad_range) {
-    if (threadIdx.x == 0) {
-      atomicOr(status, HPC_STATUS_BAD_PLAN);
-      for (int k = 0; k < G; ++k) finish_claims();
-      if (cta_clock != nullptr) record_cta_clock(cta_clock, t_start);
-    }
-    return;
-  }
-  const int vq = static_cast<int>(blockIdx.x) * G + grp;   // this warp's queue
-  const int home_begin = vq < num_queues ? cta_ptr[vq] : 0;
-  const int home_stop = vq < num_queues ? home_end[vq] : 0;
-
-  __syncthreads();
-
-  // ------------------------------------------------------------ producer
-  // The producer does not wait on a global load in its issue loop: the home
-  // items' descriptors and lengths arrive 32 at a time (one per lane), the
-  // block ids of the next 32 tiles are fetched while the current 32 are
-  // issued (across item boundaries), and a pool claim is made when an item
-  // starts and resolved during its last chunk.
-  if (is_producer) {
-    const uint64_t policy = l2_evict_first_policy();
-    const int4* items4 = reinterpret_cast<const int4*>(items);
-    uint32_t g = 0;          // tiles issued so far into this queue's ring
-    uint32_t n_pushed = 0;   // items handed to the consumers so far
-    bool claiming = true;    // the pool is not known to be empty yet
-    bool alive = true;
-    int ticket = -1;         // lane 0: an unresolved pool claim (its counter value)
-
-    // home items, 32 at a time: lane j holds item hb_next - hb_cnt + j
-    int hb_next = home_begin, hb_cnt = 0, hb_pos = 0;
-    int4 hw = make_int4(-1, -1, 0, 0);
-    int hlen = -1;
-    auto load_home_batch = [&]() {
-      hb_cnt = min(32, home_stop - hb_next);
-      hb_pos = 0;
-      hw = make_int4(-1, -1, 0, 0);
-      hlen = -1;
-      if (lane < hb_cnt) {
-        hw = items4[hb_next + lane];
-        hlen = (hw.x >= 0 && hw.x < batch) ? __ldg(seq_lens + hw.x) : -1;
-      }
-      hb_next += hb_cnt;
-    };
-    // start a pool claim (lane 0) once the home part is used up
-    auto start_claim = [&]() {
-      if (lane == 0 && claiming && ticket < 0 && hb_pos == hb_cnt && hb_next == home_stop)
-        ticket = atomicAdd(&pool[0], 1);
-    };
-    // next item: {index, descriptor, length}; index -1 when nothing is left
-    struct Next {
-      int idx;
-      int4 w;
-      int len;
-    };
-    auto next_item = [&]() -> Next {
-      while (true) {
-        if (hb_pos == hb_cnt && hb_next < home_stop) load_home_batch();
-        if (hb_pos < hb_cnt) {
-          Next n;
-          n.idx = hb_next - hb_cnt + hb_pos;
-          n.w.x = __shfl_sync(0xffffffffu, hw.x, hb_pos);
-          n.w.y = __shfl_sync(0xffffffffu, hw.y, hb_pos);
-          n.w.z = __shfl_sync(0xffffffffu, hw.z, hb_pos);
-          n.w.w = __shfl_sync(0xffffffffu, hw.w, hb_pos);
-          n.len = __shfl_sync(0xffffffffu, hlen, hb_pos);
-          ++hb_pos;
-          return n;
-        }
-        if (!claiming) return Next{-1, make_int4(-1, -1, 0, 0), -1};
-        start_claim();
-        const int k = __shfl_sync(0xffffffffu, ticket, 0);
-        if (lane == 0) ticket = -1;
-        if (k < pool_len) {
-          const int idx = pool[3 + k];
-          if (idx < 0 || idx >= capacity) {
-            if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
-            continue;
-          }
-          Next n;
-          n.idx = idx;
-          n.w = items4[idx];
-          n.len = (n.w.x >= 0 && n.w.x < batch) ? __ldg(seq_lens + n.w.x) : -1;
-          return n;
-        }
-        claiming = false;
-        if (lane == 0) finish_claims();
-        return Next{-1, make_int4(-1, -1, 0, 0), -1};
-      }
-    };
-    // block ids of tiles tb .. tb+31 of an item (lane j: tile tb + j)
-    auto fetch_bids = [&](const Item& it, int tb) -> int {
-      const int t = tb + lane;
-      return (it.ok && t < it.t1) ? __ldg(block_table + static_cast<int64_t>(it.seq) * max_blocks + t)
-                                  : 0;
-    };
-    // hand an item's descriptor (or the end mark) to the consumers
-    auto push_item = [&](int idx, const Item& it) -> bool {
-      int ok = 1;
-      if (lane == 0) {
-        const int r = static_cast<int>(n_pushed % R);
-        const uint32_t use = n_pushed / R;
-        if (*abort_flag) {
-          ok = 0;
-        } else if (use > 0 && !mbar_wait(smem_u32(&item_empty[r]), (use - 1) & 1, status)) {
-          *abort_flag = 1;
-          ok = 0;
-        }
-        if (ok) {
-          volatile int* slot = ring + r * T::kRingInts;
-          slot[0] = idx;
-          slot[1] = it.seq;
-          slot[2] = it.h;
-          slot[3] = it.t0;
-          slot[4] = it.t1;
-          slot[5] = it.ok ? it.len : -1;
-          mbar_arrive(smem_u32(&item_full[r]));
-        }
-      }
-      ++n_pushed;
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
-    };
-    // one stage: a tile (data, block id bid), or a slot without data
-    auto issue = [&](int bid, int h, bool data) -> bool {
-      int tok = 1;
-      if (lane == 0) {
-        const int s = static_cast<int>(g % SG);
-        const uint32_t use = g / SG;
-        if (*abort_flag) {
-          tok = 0;
-        } else if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, status)) {
-          *abort_flag = 1;
-          tok = 0;
-        }
-        if (tok) {
-          const uint32_t fb = smem_u32(&full[s]);
-          if (data && bid >= 0 && bid < num_blocks) {
-            stage_ok[s] = 1;
-            mbar_arrive_expect_tx(fb, T::kStageBytes);
-            const uint32_t dst = stage_base + s * T::kStageBytes;
-            const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
-            const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
-            if constexpr (kFp8) {
-              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-              tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
-            } else {
-              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-              tma_load_2d(dst + T::kBoxBytes, &kv_map, 64, yk, fb, policy);
-              tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
-              tma_load_2d(dst + T::kPageBytes + T::kBoxBytes, &kv_map, 64, yv, fb, policy);
-            }
-          } else {
-            if (data) atomicOr(status, HPC_STATUS_BAD_BLOCK);
-            stage_ok[s] = 0;
-            mbar_arrive(fb);
-          }
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, tok, 0)) return false;
-      ++g;
-      return true;
-    };
-
-    Next cur = next_item();
-    Item it = make_item(cur.w, cur.len, batch, max_blocks);
-    int cur_bids = fetch_bids(it, it.t0);
-    while (alive) {
-      if (!push_item(cur.idx, it)) break;
-      if (cur.idx < 0) break;
-      if (!it.ok) {
-        if (lane == 0) atomicOr(status, HPC_STATUS_BAD_PLAN);
-      } else {
-        start_claim();
-      }
-      Next nxt{-1, make_int4(-1, -1, 0, 0), -1};
-      Item nit{-1, -1, 0, 0, 0, false};
-      int nxt_bids = 0;
-      bool have_next = false;
-      for (int tb = it.t0; it.ok && tb < it.t1 && alive; tb += 32) {
-        const int nt = min(32, it.t1 - tb);
-        int pre = 0;
-        if (tb + 32 < it.t1) {
-          pre = fetch_bids(it, tb + 32);              // the next chunk of this item
-        } else {
-          nxt = next_item();                          // the next item and its first chunk
-          nit = make_item(nxt.w, nxt.len, batch, max_blocks);
-          nxt_bids = fetch_bids(nit, nit.t0);
-          have_next = true;
-        }
-        for (int j = 0; j < nt && alive; ++j)
-          alive = issue(__shfl_sync(0xffffffffu, cur_bids, j), it.h, true);
-        cur_bids = pre;
-      }
-      if (!alive) break;
-      if (!have_next) {
-        nxt = next_item();
-        nit = make_item(nxt.w, nxt.len, batch, max_blocks);
-        nxt_bids = fetch_bids(nit, nit.t0);
-      }
-      cur = nxt;
-      it = nit;
-      cur_bids = nxt_bids;
-    }
-    if (claiming && lane == 0) finish_claims();   // stopped early by a fault
-    // After a fault, copies may still be landing in stages nobody will wait
-    // on: wait for the last one issued into every stage before exiting.
-    if (lane == 0 && *abort_flag) {
-      for (uint32_t s = 0; s < static_cast<uint32_t>(SG) && s < g; ++s) {
-        const uint32_t last = s + SG * ((g - 1 - s) / SG);
-        mbar_wait(smem_u32(&full[s]), (last / SG) & 1, status);
-      }
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  const int wq = warp % T::kWarpsPerGroup;         // token quarter of each tile
-  const int gt = threadIdx.x - grp * T::kGroupThreads;   // thread index within the queue
-  const int r = lane >> 2, c = lane & 3;
-  const float k_scale = kFp8 ? kv_scale[0] : 1.f;
-  const float v_scale = kFp8 ? kv_scale[1] : 1.f;
-  const float scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
-  const int sw = lane & 7;                                        // swizzle of this lane's row
-  const int row = 16 * wq + (lane & 7) + ((lane >> 3) & 1) * 8;   // ldmatrix row (token)
-  const int hi = lane >> 4;                                        // second 16-byte chunk
-  const int vtok_bf16 = 16 * wq + (lane & 7) + hi * 8;             // V^T .trans row (token)
-  const int vsel_bf16 = (lane >> 3) & 1;                           // V^T d half
-  uint32_t g = 0;
-  uint32_t bar_phase = 0;
-  bool dead = false;
-
-  // the queue's consumer threads meet; bounded, so a stuck peer ends in a timeout
-  auto cons_sync = [&]() -> bool {
-    mbar_arrive(smem_u32(cons_bar));
-    bool ok = !*abort_flag && mbar_wait(smem_u32(cons_bar), bar_phase & 1, status);
-    ++bar_phase;
-    ok = __all_sync(0xffffffffu, ok);   // the same answer for the whole warp
-    if (!ok && lane == 0) *abort_flag = 1;
-    return ok;
-  };
-
-  // with the merge fused in, the rows of empty sequences (no items) are
-  // zeroed here, the segments spread over the CTAs of the grid
-  if (fuse) {
-    for (int sg = blockIdx.x; sg < batch * kHkv; sg += gridDim.x) {
-      if (seg_ptr[sg + 1] != seg_ptr[sg]) continue;
-      for (int e = threadIdx.x * 4; e < kGroup * kD; e += 32 * T::kConsumerWarps * 4)
-        *reinterpret_cast<uint2*>(out + static_cast<int64_t>(sg) * kGroup * kD + e) = make_uint2(0u, 0u);
-    }
-  }
-
-  // An item descriptor from the producer's ring (slot n % R), handed back as
-  // soon as it is read; false after an abort.
-  struct Desc {
-    int i;
-    Item it;
-  };
-  auto fetch_desc = [&](uint32_t n, Desc& d) -> bool {
-    const int rslot = static_cast<int>(n % R);
-    bool ok = !*abort_flag && mbar_wait(smem_u32(&item_full[rslot]), (n / R) & 1, status);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) {
-      if (lane == 0) *abort_flag = 1;
-      return false;
-    }
-    const volatile int* slot = ring + rslot * T::kRingInts;
-    d.i = slot[0];
-    d.it = Item{slot[1], slot[2], slot[3], slot[4], slot[5], slot[5] >= 0};
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
-    return true;
-  };
-  // The item's q words (this lane's share of the B operand Q^T of the 8 query
-  // heads of its KV head, head = r) and, with the merge fused in, its
-  // segment's first item and item count.  Issued one item ahead, so the
-  // loads are in flight during the previous item's epilogue.
-  auto load_item = [&](const Desc& d, uint32_t (&qw)[8][2], int& first, int& count) {
-    first = 0;
-    count = 0;
-    if (d.i < 0 || !d.it.ok) return;
-    const uint16_t* qrow = q + (static_cast<int64_t>(d.it.seq) * kHq + d.it.h * kGroup + r) * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      if constexpr (kFp8) {
-        const uint2 x = *reinterpret_cast<const uint2*>(qrow + 16 * ks + 4 * c);
-        qw[ks][0] = x.x;
-        qw[ks][1] = x.y;
-      } else {
-        qw[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * c);
-        qw[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * c);
-      }
-    }
-    if (fuse) {
-      const int seg = d.it.seq * kHkv + d.it.h;
-      first = seg_ptr[seg];
-      count = seg_ptr[seg + 1] - first;
-    }
-  };
-
-  Desc cur{-1, Item{-1, -1, 0, 0, 0, false}};
-  uint32_t qw[8][2];
-  int seg_first = 0, seg_items = 0;
-  bool have = fetch_desc(0, cur);
-  if (have) load_item(cur, qw, seg_first, seg_items);
-  for (uint32_t n = 0; have && cur.i >= 0; ++n) {
-    const int i = cur.i;
-    const Item it = cur.it;
-
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2c, 2c+1
-    float o[8][4];
-#pragma unroll
-    for (int mi = 0; mi < 8; ++mi) o[mi][0] = o[mi][1] = o[mi][2] = o[mi][3] = 0.f;
-
-    if (it.ok) {
-      // B operand Q^T for the 8 query heads of this KV head (head = r)
-      uint32_t bq[8][2];
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if constexpr (kFp8) {
-          bq[ks][0] = pack_f16(bf16_lo(qw[ks][0]), bf16_hi(qw[ks][0]));
-          bq[ks][1] = pack_f16(bf16_lo(qw[ks][1]), bf16_hi(qw[ks][1]));
-        } else {
-          bq[ks][0] = qw[ks][0];
-          bq[ks][1] = qw[ks][1];
-        }
-      }
-
-      for (int t = it.t0; t < it.t1; ++t, ++g) {
-        if (dead) continue;
-        const int s = static_cast<int>(g % SG);
-        const uint32_t use = g / SG;
-        bool tok = !*abort_flag && mbar_wait(smem_u32(&full[s]), use & 1, status);
-        tok = __all_sync(0xffffffffu, tok);
-        if (!tok) {
-          if (lane == 0) *abort_flag = 1;
-          dead = true;
-          continue;
-        }
-        const int nvalid = it.len - t * kPage - 16 * wq;   // valid tokens of my 16
-        if (stage_ok[s] && nvalid > 0) {
-          const uint32_t kb = stage_base + s * T::kStageBytes;
-          const uint32_t vb = kb + T::kPageBytes;
-
-          // S^T = K Q^T  (rows: my 16 tokens, cols: 8 heads); two chains
-          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (kFp8) {
-#pragma unroll
-            for (int kp = 0; kp < 4; ++kp) {
-              uint32_t r0, r1, r2, r3;
-              ldsm_x4(kb + row * 128 + ((((2 * kp + hi) & 7) ^ sw) << 4), r0, r1, r2, r3);
-              mma_f16(sa, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
-                      e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), bq[2 * kp][0],
-                      bq[2 * kp][1]);
-              mma_f16(sb, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
-                      e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16), bq[2 * kp + 1][0],
-                      bq[2 * kp + 1][1]);
-            }
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(kb + (ks >> 2) * T::kBoxBytes + row * 128 + ((((2 * ks + hi) & 7) ^ sw) << 4),
-                      a0, a1, a2, a3);
-              if (ks & 1) mma_bf16(sb, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
-              else        mma_bf16(sa, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
-            }
-          }
-          // fragment: x0 = S[tok r][head 2c], x1 = [r][2c+1], x2 = [r+8][2c], x3 = [r+8][2c+1]
-          float x0 = (sa[0] + sb[0]) * scale_log2, x1 = (sa[1] + sb[1]) * scale_log2;
-          float x2 = (sa[2] + sb[2]) * scale_log2, x3 = (sa[3] + sb[3]) * scale_log2;
-          uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-          if (nvalid < 16) {
-            if (r >= nvalid) x0 = x1 = -INFINITY;
-            if (r + 8 >= nvalid) x2 = x3 = -INFINITY;
-            mask01 = (2 * c < nvalid ? 0x0000ffffu : 0u) | (2 * c + 1 < nvalid ? 0xffff0000u : 0u);
-            mask23 = (2 * c + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * c + 9 < nvalid ? 0xffff0000u : 0u);
-          }
-          float mt0 = fmaxf(x0, x2), mt1 = fmaxf(x1, x3);
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, off));
-            mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, off));
-          }
-          const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);
-          const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-          const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-          const float al0 = exp2_ftz(m0 - ms0), al1 = exp2_ftz(m1 - ms1);
-          const float p0 = exp2_ftz(x0 - ms0), p1 = exp2_ftz(x1 - ms1);
-          const float p2 = exp2_ftz(x2 - ms0), p3 = exp2_ftz(x3 - ms1);
-          l0 = l0 * al0 + (p0 + p2);
-          l1 = l1 * al1 + (p1 + p3);
-          m0 = mn0;
-          m1 = mn1;
-          // the running max rarely moves after the first tiles: skip the
-          // (exact, multiply-by-one) rescale when no lane needs it
-          if (!__all_sync(0xffffffffu, al0 == 1.f && al1 == 1.f)) {
-#pragma unroll
-            for (int mi = 0; mi < 8; ++mi) {
-              o[mi][0] *= al0;
-              o[mi][1] *= al1;
-              o[mi][2] *= al0;
-              o[mi][3] *= al1;
-            }
-          }
-          // P^T fragment -> B operand (k = token, n = head) by an 8x8 transpose
-          uint32_t pb0, pb1;
-          if constexpr (kFp8) {
-            pb0 = movmatrix_t(pack_f16(p0, p1));
-            pb1 = movmatrix_t(pack_f16(p2, p3));
-          } else {
-            pb0 = movmatrix_t(pack_bf16(p0, p1));
-            pb1 = movmatrix_t(pack_bf16(p2, p3));
-          }
-
-          if (nvalid < 16)
-            pv_tile<kFp8, true>(vb, row, vtok_bf16, vsel_bf16, hi, sw, pb0, pb1, mask01, mask23, o);
-          else
-            pv_tile<kFp8, false>(vb, row, vtok_bf16, vsel_bf16, hi, sw, pb0, pb1, mask01, mask23, o);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-      }
-    }
-    if (dead) break;
-
-    // the next item's descriptor, q words and segment bounds: their loads
-    // overlap this item's epilogue
-    Desc nxt{-1, Item{-1, -1, 0, 0, 0, false}};
-    uint32_t qw_next[8][2];
-    int next_first = 0, next_items = 0;
-    have = fetch_desc(n + 1, nxt);
-    if (!have) break;
-    load_item(nxt, qw_next, next_first, next_items);
-
-    // ---- merge the warps' states and write the item's partial: every warp
-    // stores its raw (m, l, O) in its own slice; after one barrier each
-    // output element is combined over the warps in a fixed order (the result
-    // is bit-reproducible) with the log-sum-exp weights of its head
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 4);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 8);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 4);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 8);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
-    if (lane < 4) {
-      sm_m[warp * kGroup + 2 * c] = m0;
-      sm_m[warp * kGroup + 2 * c + 1] = m1;
-      sm_l[warp * kGroup + 2 * c] = l0;
-      sm_l[warp * kGroup + 2 * c + 1] = l1;
-    }
-    {
-      float* o_h0 = sm_o + (warp * kGroup + 2 * c) * T::kOStride;
-      float* o_h1 = o_h0 + T::kOStride;
-#pragma unroll
-      for (int mi = 0; mi < 8; ++mi) {
-        // rows of the O^T fragment: d_a for o[mi][0..1], d_b for o[mi][2..3]
-        const int d_a = kFp8 ? 16 * mi + 2 * r : 16 * mi + r;
-        const int d_b = kFp8 ? d_a + 1 : d_a + 8;
-        o_h0[d_a] = o[mi][0];
-        o_h1[d_a] = o[mi][1];
-        o_h0[d_b] = o[mi][2];
-        o_h1[d_b] = o[mi][3];
-      }
-    }
-    if (!cons_sync()) break;
-    // with the merge fused in: a segment of one item is final here; a segment
-    // of several items is merged by the queue that finishes its last item
-    const int seg = it.seq * kHkv + it.h;
-    const bool direct = fuse && it.ok && seg_items == 1;
-    const int w0 = grp * T::kWarpsPerGroup;   // the queue's first consumer warp
-    {
-      float* dst = partial_o + static_cast<int64_t>(i) * kGroup * kD;
-#pragma unroll
-      for (int e = gt * 4; e < kGroup * kD; e += T::kGroupThreads * 4) {
-        const int hh = e >> 7;      // head of these 4 outputs
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = w0; w < w0 + T::kWarpsPerGroup; ++w) M = fmaxf(M, sm_m[w * kGroup + hh]);
-        const float Ms = M == -INFINITY ? 0.f : M;
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = w0; w < w0 + T::kWarpsPerGroup; ++w) {
-          const float wt = exp2_ftz(sm_m[w * kGroup + hh] - Ms);
-          L += wt * sm_l[w * kGroup + hh];
-          const float4 x =
-              *reinterpret_cast<const float4*>(sm_o + (w * kGroup + hh) * T::kOStride + (e & 127));
-          acc.x += wt * x.x;
-          acc.y += wt * x.y;
-          acc.z += wt * x.z;
-          acc.w += wt * x.w;
-        }
-        const float inv = L > 0.f ? v_scale / L : 0.f;
-        if (direct) {
-          uint2 packed;
-          packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-          packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-          // segment s holds rows s*8 .. s*8+7 of the [batch*64, 128] output
-          *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
-        } else {
-          *reinterpret_cast<float4*>(dst + e) =
-              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-          if ((e & 127) == 0)
-            partial_lse[static_cast<int64_t>(i) * kGroup + hh] =
-                L > 0.f ? (Ms + log2f(L)) * 0.6931471805599453f : -INFINITY;
-        }
-      }
-    }
-    if (fuse && it.ok && !direct) {
-      if (!cons_sync()) break;     // every thread's share of the partial is written
-      if (gt == 0) {
-        __threadfence();           // the partial is visible device-wide before the count
-        const int done = atomicAdd(&seg_done[seg], 1);
-        *merge_flag = done == seg_items - 1;
-        if (done == seg_items - 1) {
-          seg_done[seg] = 0;       // reset for the next run of this plan
-          __threadfence();
-        }
-      }
-      if (!cons_sync()) break;
-      if (*merge_flag) {
-        // the last item of the segment: merge its partials.  The lse values
-        // are staged in shared memory (the queue's merge slices are free now)
-        // by one parallel load, so the per-thread loop is a single pass of
-        // independent float4 loads through L2; segments of more than
-        // kMergeChunk items are taken chunk by chunk with an online rescale.
-        constexpr int kMergeChunk = 512;
-        constexpr int kOuts = kGroup * kD / (4 * T::kGroupThreads);   // float4 outputs per thread
-        static_assert(kMergeChunk * kGroup <= T::kWarpsPerGroup * kGroup * T::kOStride,
-                      "the lse staging area must fit in the queue's merge slices");
-        static_assert(kOuts * 4 * T::kGroupThreads == kGroup * kD, "outputs split evenly");
-        float* lse_s = sm_o + w0 * kGroup * T::kOStride;
-        const int i0 = seg_first;
-        float M[kOuts], W[kOuts];
-        float4 acc[kOuts];
-#pragma unroll
-        for (int u = 0; u < kOuts; ++u) {
-          M[u] = -INFINITY;
-          W[u] = 0.f;
-          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        bool synced = true;
-        for (int base = 0; base < seg_items && synced; base += kMergeChunk) {
-          const int m = min(kMergeChunk, seg_items - base);
-          for (int x = gt; x < m * kGroup; x += T::kGroupThreads)
-            lse_s[x] = __ldcg(partial_lse + static_cast<int64_t>(i0 + base) * kGroup + x);
-          if (!(synced = cons_sync())) break;
-#pragma unroll
-          for (int u = 0; u < kOuts; ++u) {
-            const int e = (gt + u * T::kGroupThreads) * 4;
-            const int hh = e >> 7;
-            float Mn = M[u];
-            for (int k = 0; k < m; ++k) Mn = fmaxf(Mn, lse_s[k * kGroup + hh]);
-            if (Mn != -INFINITY) {
-              const float sc = __expf(M[u] - Mn);   // 0 while M is still -inf
-              acc[u].x *= sc; acc[u].y *= sc; acc[u].z *= sc; acc[u].w *= sc;
-              W[u] *= sc;
-              const float* po = partial_o + static_cast<int64_t>(i0 + base) * kGroup * kD + e;
-#pragma unroll 8
-              for (int k = 0; k < m; ++k) {
-                const float w = __expf(lse_s[k * kGroup + hh] - Mn);
-                const float4 x =
-                    __ldcg(reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * kGroup * kD));
-                acc[u].x += w * x.x;
-                acc[u].y += w * x.y;
-                acc[u].z += w * x.z;
-                acc[u].w += w * x.w;
-                W[u] += w;
-              }
-              M[u] = Mn;
-            }
-          }
-          synced = cons_sync();   // before the staging area is overwritten
-        }
-        if (!synced) break;
-#pragma unroll
-        for (int u = 0; u < kOuts; ++u) {
-          const int e = (gt + u * T::kGroupThreads) * 4;
-          const float inv = W[u] > 0.f ? 1.f / W[u] : 0.f;
-          uint2 packed;
-          packed.x = pack_bf16(acc[u].x * inv, acc[u].y * inv);
-          packed.y = pack_bf16(acc[u].z * inv, acc[u].w * inv);
-          *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(seg) * kGroup) * kD + e) = packed;
-        }
-      }
-    }
-    if (!cons_sync()) break;
-    cur = nxt;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qw[ks][0] = qw_next[ks][0];
-      qw[ks][1] = qw_next[ks][1];
-    }
-    seg_first = next_first;
-    seg_items = next_items;
-  }
-  if (cta_clock != nullptr) {
-    named_bar_sync(1, 32 * T::kConsumerWarps);   // every queue of the CTA is done
-    if (threadIdx.x == 0) record_cta_clock(cta_clock, t_start);
-  }
-}
-
-// ------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-template <bool kFp8>
-cudaError_t ensure_smem_attr() {
-  // once per device: the dynamic shared memory opt-in is a per-device setting
-  static std::mutex mu;
-  static bool done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           AttnTraits<kFp8>::kSmemBytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
-  return e;
-}
-
-template <bool kFp8>
-int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int32_t num_blocks,
-                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
-                int32_t batch, const hpc_plan* plan, float* partial_o, float* partial_lse,
-                float sm_scale, int32_t* status, unsigned long long* cta_clock, uint16_t* out,
-                bool pdl, cudaStream_t stream) {
-  using T = AttnTraits<kFp8>;
-  auto encode = tensor_map_encoder();
-  if (encode == nullptr) return HPC_ERR_CUDA;
-  if (ensure_smem_attr<kFp8>() != cudaSuccess) return HPC_ERR_CUDA;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
-                              static_cast<cuuint64_t>(num_blocks) * 2 * kHkv * kPage};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * T::kElem};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / T::kElem), static_cast<cuuint32_t>(kPage)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult cr = encode(&map,
-                             kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                             2, const_cast<void*>(kv_cache), dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((plan->num_ctas + T::kGroups - 1) / T::kGroups);   // kGroups queues per CTA
-  cfg.blockDim = dim3(T::kThreads);
-  cfg.dynamicSmemBytes = T::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, decode_attn_kernel<kFp8>, map, static_cast<const uint16_t*>(q), kv_scale, block_table,
-      max_blocks, num_blocks, seq_lens, batch, static_cast<const hpc_work_item*>(plan->items),
-      static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
-      plan->pool, plan->capacity, plan->num_ctas, partial_o, partial_lse, sm_scale, status, cta_clock,
-      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out);
-  return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
-}
-
-}  // namespace
-}  // namespace hpc
+// Single-token decode attention entry points (q_len = 1) and the attention
+// launcher shared with the step and the no-allocation entry point.  The
+// kernel itself is in attn_kernel.cuh; multi-token decode is in attn_mt.cu.
+#include "attn_kernel.cuh"
 
 int hpc::launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
                             const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
                             int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
-                            const hpc_plan* plan, float* partial_o, float* partial_lse,
-                            float sm_scale, int32_t* status, unsigned long long* cta_clock,
-                            void* out, bool pdl, cudaStream_t stream) {
-  HPC_CHECK_ARG(q && kv_cache && block_table && seq_lens && plan && partial_o && partial_lse &&
-                status && plan->items && plan->cta_ptr && plan->home_end && plan->pool);
-  HPC_CHECK_ARG(num_blocks > 0 && max_blocks >= 1 && batch >= 0 && plan->num_ctas >= 1 &&
-                plan->capacity >= 0);
-  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
-  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
-  if (out != nullptr) HPC_CHECK_ARG(plan->seg_ptr && plan->seg_done);
-  if (num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
-  if (plan->num_ctas > 0x7fffffff - 1) return HPC_ERR_UNSUPPORTED;
+                            int32_t q_len, const hpc_plan* plan, float* partial_o,
+                            float* partial_lse, float sm_scale, int32_t* status,
+                            unsigned long long* cta_clock, void* out, bool pdl,
+                            cudaStream_t stream) {
+  const int rc = hpc::check_attn_args(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                      max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                      status, out);
+  if (rc != HPC_OK) return rc;
+  HPC_CHECK_ARG(q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
+  if (q_len > 1)
+    return hpc::launch_decode_attn_multi(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                         max_blocks, seq_lens, batch, q_len, plan, partial_o,
+                                         partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
+  auto* o = static_cast<uint16_t*>(out);
   if (kv_dtype == HPC_KV_BF16)
-    return hpc::launch_attn<false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                   seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
-                                   cta_clock, static_cast<uint16_t*>(out), pdl, stream);
-  if (kv_dtype == HPC_KV_FP8_E4M3) {
-    HPC_CHECK_ARG(kv_scale != nullptr);
-    return hpc::launch_attn<true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                  seq_lens, batch, plan, partial_o, partial_lse, sm_scale, status,
-                                  cta_clock, static_cast<uint16_t*>(out), pdl, stream);
-  }
-  return HPC_ERR_UNSUPPORTED;
+    return hpc::launch_attn<false, 1>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                      seq_lens, batch, 1, plan, partial_o, partial_lse, sm_scale,
+                                      status, cta_clock, o, pdl, stream);
+  return hpc::launch_attn<true, 1>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                   seq_lens, batch, 1, plan, partial_o, partial_lse, sm_scale,
+                                   status, cta_clock, o, pdl, stream);
 }
 
 extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
@@ -958,7 +36,7 @@ extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_d
                                float* partial_o, float* partial_lse, float sm_scale,
                                int32_t* status, cudaStream_t stream) {
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
                                  sm_scale, status, nullptr, nullptr, false, stream);
 }
 
@@ -971,7 +49,7 @@ extern "C" int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int
                                         unsigned long long* cta_clock, cudaStream_t stream) {
   HPC_CHECK_ARG(cta_clock != nullptr);
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
                                  sm_scale, status, cta_clock, nullptr, false, stream);
 }
 
@@ -983,7 +61,7 @@ extern "C" int hpc_decode_attn_merge(const void* q, const void* kv_cache, int32_
                                      float sm_scale, int32_t* status, cudaStream_t stream) {
   HPC_CHECK_ARG(out != nullptr);
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
                                  sm_scale, status, nullptr, out, false, stream);
 }
 

@@ -7,10 +7,12 @@
 // combination is the exact one: with lse_k = log sum exp(s) over split k,
 // out = sum_k exp(lse_k - M) O_k / sum_k exp(lse_k - M), M = max_k lse_k.
 //
-// One CTA per (sequence, kv_head) segment, 256 threads: warp r handles query
-// head 8h + r and each lane 4 consecutive elements, so every partial row is
-// one coalesced 512-byte read.  Items are combined in item order (that is,
-// tile order), which makes the output bit-reproducible.
+// One CTA per (sequence, kv_head) segment and new token, 256 threads: warp r
+// handles query head 8h + r and each lane 4 consecutive elements, so every
+// partial row is one coalesced 512-byte read.  Items are combined in item
+// order (that is, tile order), which makes the output bit-reproducible.  With
+// q_len new tokens per sequence the partial of item i for token j is row
+// (i*q_len + j)*8 + r, and the output row is (b*q_len + j)*64 + 8h + r.
 #include "common.cuh"
 
 namespace hpc {
@@ -19,30 +21,33 @@ namespace {
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ partial_o,
                                                     const float* __restrict__ partial_lse,
                                                     const int32_t* __restrict__ seg_ptr,
-                                                    int32_t capacity,
+                                                    int32_t capacity, int32_t q_len,
                                                     uint16_t* __restrict__ out) {
   const int s = blockIdx.x;            // segment = seq * 8 + kv_head
+  const int j = blockIdx.y;            // new token
   const int r = threadIdx.x >> 5;      // query head within the group
   const int d = (threadIdx.x & 31) * 4;
+  // partial row of item i, output row of this CTA
+  auto prow = [&](int i) { return (static_cast<int64_t>(i) * q_len + j) * kGroup + r; };
+  const int64_t orow = (static_cast<int64_t>(s / kHkv) * q_len + j) * kHq + (s % kHkv) * kGroup + r;
   int i0 = seg_ptr[s], i1 = seg_ptr[s + 1];
   if (i0 < 0 || i1 < i0 || i1 > capacity) i1 = i0;   // a corrupt plan merges to zeros
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i1 - i0 == 1) {
-    acc = *reinterpret_cast<const float4*>(partial_o + (static_cast<int64_t>(i0) * kGroup + r) * kD + d);
+    acc = *reinterpret_cast<const float4*>(partial_o + prow(i0) * kD + d);
   } else if (i1 > i0) {
     // both loops are unrolled so that several partials are in flight at once
     // (a long sequence's segment holds tens of items)
     float M = -INFINITY;
 #pragma unroll 8
-    for (int i = i0; i < i1; ++i) M = fmaxf(M, partial_lse[static_cast<int64_t>(i) * kGroup + r]);
+    for (int i = i0; i < i1; ++i) M = fmaxf(M, partial_lse[prow(i)]);
     if (M != -INFINITY) {
       float wsum = 0.f;
 #pragma unroll 8
       for (int i = i0; i < i1; ++i) {
-        const float w = expf(partial_lse[static_cast<int64_t>(i) * kGroup + r] - M);
-        const float4 o =
-            *reinterpret_cast<const float4*>(partial_o + (static_cast<int64_t>(i) * kGroup + r) * kD + d);
+        const float w = expf(partial_lse[prow(i)] - M);
+        const float4 o = *reinterpret_cast<const float4*>(partial_o + prow(i) * kD + d);
         acc.x += w * o.x;
         acc.y += w * o.y;
         acc.z += w * o.z;
@@ -59,22 +64,24 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   uint2 packed;
   packed.x = pack_bf16(acc.x, acc.y);
   packed.y = pack_bf16(acc.z, acc.w);
-  // segment s = b*8 + h holds query heads 8h .. 8h+7 of sequence b, i.e. rows
-  // s*8 .. s*8+7 of the [batch*64, 128] output
-  *reinterpret_cast<uint2*>(out + (static_cast<int64_t>(s) * kGroup + r) * kD + d) = packed;
+  *reinterpret_cast<uint2*>(out + orow * kD + d) = packed;
 }
 
 }  // namespace
 }  // namespace hpc
 
-extern "C" int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
-                         int32_t batch, void* out, cudaStream_t stream) {
+extern "C" int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                            int32_t batch, int32_t q_len, void* out, cudaStream_t stream) {
   HPC_CHECK_ARG(partial_o && partial_lse && plan && plan->seg_ptr && out);
-  HPC_CHECK_ARG(batch >= 0);
+  HPC_CHECK_ARG(batch >= 0 && q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
   if (batch == 0) return HPC_OK;
   if (static_cast<int64_t>(batch) * hpc::kHkv > 0x7fffffff) return HPC_ERR_UNSUPPORTED;
-  hpc::merge_kernel<<<batch * hpc::kHkv, 256, 0, stream>>>(partial_o, partial_lse, plan->seg_ptr,
-                                                          plan->capacity,
-                                                          static_cast<uint16_t*>(out));
+  hpc::merge_kernel<<<dim3(batch * hpc::kHkv, q_len), 256, 0, stream>>>(
+      partial_o, partial_lse, plan->seg_ptr, plan->capacity, q_len, static_cast<uint16_t*>(out));
   return HPC_LAUNCH_STATUS();
+}
+
+extern "C" int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                         int32_t batch, void* out, cudaStream_t stream) {
+  return hpc_merge_mt(partial_o, partial_lse, plan, batch, 1, out, stream);
 }

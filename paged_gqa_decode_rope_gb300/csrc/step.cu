@@ -121,6 +121,6 @@ extern "C" int hpc_decode_step(const void* q, const void* k, const void* v,
   }
   if (cudaPeekAtLastError() != cudaSuccess) return HPC_ERR_CUDA;
   return hpc::launch_decode_attn(q_out, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
                                  sm_scale, status, nullptr, out, true, stream);
 }

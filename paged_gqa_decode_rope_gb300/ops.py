@@ -360,3 +360,112 @@ class DecodeStep:
                           slot_mapping, kv_scale, self.q_out, self.status)
         self.plan_step(seq_lens)
         return self.attend(self.q_out, kv_cache, kv_scale, block_table, seq_lens)
+
+
+# ------------------------------------------------------------ multi-token decode
+
+def _check_attn_mt(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                   partial_lse, status):
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, q_len, 64, 128]")
+    B, qn = q.shape[0], q.shape[1]
+    if not 1 <= qn <= _lib.MAX_Q_LEN:
+        raise ValueError("q_len must be 1 .. %d" % _lib.MAX_Q_LEN)
+    _want(q, "q", _BF16, (B, qn, HQ, D))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    if kv_cache.dim() != 5 or tuple(kv_cache.shape[1:]) != (2, HKV, PAGE, D):
+        raise ValueError("kv_cache must be [num_blocks, 2, 8, 64, 128]")
+    if kv_dtype == KV_FP8:
+        _want(kv_scale, "kv_scale", (torch.float32,), (2,))
+    _want(block_table, "block_table", (torch.int32,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if plan.batch != B:
+        raise ValueError("plan was made for batch %d, not %d" % (plan.batch, B))
+    _want(partial_o, "partial_o", (torch.float32,))
+    _want(partial_lse, "partial_lse", (torch.float32,))
+    if (partial_o.numel() < plan.capacity * qn * HKV * D or
+            partial_lse.numel() < plan.capacity * qn * HKV):
+        raise ValueError("partial buffers are smaller than capacity x q_len rows")
+    _want(status, "status", (torch.int32,), (1,))
+    return B, qn
+
+
+def decode_attn_mt(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                   partial_lse, status, sm_scale=None):
+    """Multi-token decode attention (q [B, q_len, 64, 128]): partials per item and new token."""
+    B, qn = _check_attn_mt(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan,
+                           partial_o, partial_lse, status)
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    check("hpc_decode_attn_mt", _lib.lib().hpc_decode_attn_mt(
+        _p(q), _p(kv_cache), kv_dtype, _p(kv_scale if kv_dtype == KV_FP8 else None),
+        kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(seq_lens), B, qn,
+        ctypes.byref(plan.c), _p(partial_o), _p(partial_lse), scale, _p(status), _stream()))
+
+
+def decode_attn_merge_mt(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                         partial_lse, out, status, sm_scale=None):
+    """Multi-token decode attention with the merge fused in: writes out [B, q_len, 64, 128]."""
+    B, qn = _check_attn_mt(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan,
+                           partial_o, partial_lse, status)
+    _want(out, "out", _BF16, (B, qn, HQ, D))
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    check("hpc_decode_attn_merge_mt", _lib.lib().hpc_decode_attn_merge_mt(
+        _p(q), _p(kv_cache), kv_dtype, _p(kv_scale if kv_dtype == KV_FP8 else None),
+        kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(seq_lens), B, qn,
+        ctypes.byref(plan.c), _p(partial_o), _p(partial_lse), _p(out), scale, _p(status),
+        _stream()))
+
+
+def merge_mt(partial_o, partial_lse, plan, out):
+    """Log-sum-exp merge of multi-token partials into out [B, q_len, 64, 128]."""
+    B, qn = plan.batch, out.shape[1]
+    _want(partial_o, "partial_o", (torch.float32,))
+    _want(partial_lse, "partial_lse", (torch.float32,))
+    _want(out, "out", _BF16, (B, qn, HQ, D))
+    check("hpc_merge_mt", _lib.lib().hpc_merge_mt(
+        _p(partial_o), _p(partial_lse), ctypes.byref(plan.c), B, qn, _p(out), _stream()))
+
+
+class DecodeStepMT:
+    """Multi-token decode of q_len new tokens per sequence: the prologue of all
+    B * q_len tokens, the plan, and the attention (merge fused or separate),
+    with buffers allocated once for a batch size and q_len."""
+
+    def __init__(self, batch, q_len, kv_dtype, max_blocks, device="cuda", n_ctas=None,
+                 pool_chunks=POOL_CHUNKS, pool_min_tiles=POOL_MIN_TILES, fused=True, min_tiles=1):
+        self.batch, self.q_len, self.kv_dtype, self.max_blocks = batch, q_len, kv_dtype, max_blocks
+        self.fused, self.min_tiles = fused, min_tiles
+        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles)
+        cap = max(self.plan.capacity, 1)
+        self.partial_o = torch.empty((cap, q_len, HKV, D), dtype=torch.float32, device=device)
+        self.partial_lse = torch.empty((cap, q_len, HKV), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.q_out = torch.empty((batch, q_len, HQ, D), dtype=torch.bfloat16, device=device)
+        self.out = torch.empty((batch, q_len, HQ, D), dtype=torch.bfloat16, device=device)
+
+    def plan_step(self, seq_lens):
+        decode_plan(seq_lens, self.max_blocks, self.plan, self.status, self.min_tiles)
+
+    def attend(self, q, kv_cache, kv_scale, block_table, seq_lens):
+        if self.fused:
+            decode_attn_merge_mt(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens,
+                                 self.plan, self.partial_o, self.partial_lse, self.out, self.status)
+        else:
+            decode_attn_mt(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens, self.plan,
+                           self.partial_o, self.partial_lse, self.status)
+            merge_mt(self.partial_o, self.partial_lse, self.plan, self.out)
+        return self.out
+
+    def __call__(self, q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, slot_mapping,
+                 kv_scale, block_table, seq_lens):
+        """q [B,q_len,64,128], k and v [B,q_len,8,128], positions and
+        slot_mapping [B,q_len]; seq_lens counts the new tokens."""
+        B, qn = self.batch, self.q_len
+        rope_norm_kvwrite(q.reshape(B * qn, HQ, D), k.reshape(B * qn, HKV, D),
+                          v.reshape(B * qn, HKV, D), positions.reshape(B * qn), cos_sin, q_norm_w,
+                          k_norm_w, kv_cache, self.kv_dtype, slot_mapping.reshape(B * qn), kv_scale,
+                          self.q_out.view(B * qn, HQ, D), self.status)
+        self.plan_step(seq_lens)
+        return self.attend(self.q_out, kv_cache, kv_scale, block_table, seq_lens)
