@@ -48,6 +48,7 @@ def _parse():
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-static", action="store_true", help="skip the static-schedule comparison")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-multi-token", action="store_true", help="skip the multi-token decode timings")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
@@ -380,6 +381,7 @@ def run_ours(args):
     sched = None
     if rank == 0 and not args.no_static:
         sched = schedule_comparison(ops, wl, stream)
+    mt = multi_token_times(ops, wl, stream) if rank == 0 and not args.no_multi_token else None
 
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -423,6 +425,7 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "schedules": sched,
+        "multi_token": mt,
     }
     print(json.dumps(line))
 
@@ -436,6 +439,40 @@ def _describe(wl):
             parts.append("%dx%d" % (int((L == x).sum()), x))
         return " + ".join(parts) + " tokens, 64q/8kv, d128, %s KV, 64-token pages" % kv
     return "%d seqs, %d tokens, 64q/8kv, d128, %s KV, 64-token pages" % (wl.batch, wl.tokens, kv)
+
+
+def multi_token_times(ops, wl, stream, reps=200):
+    """Multi-token decode on the same batch: the attention with the merge fused
+    in for q_len = 2 and 4 new tokens per sequence (the cache and lengths of
+    the workload, random BF16 q), CUDA events over ``reps`` launches.  Bytes
+    are the KV bytes plus q_len times the Q + O bytes; flops 4 * 64 * 128 per
+    query token and key."""
+    import torch
+    out = {}
+    peak_gbs, _ = _load_peaks()
+    for qn in (2, 4):
+        g = torch.Generator(device="cuda").manual_seed(qn)
+        q = torch.randn((wl.batch, qn, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+        step = ops.DecodeStepMT(wl.batch, qn, wl.kv_dtype, wl.max_blocks)
+        step.plan_step(wl.seq_lens)
+        for _ in range(5):
+            step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if int(step.status.item()) != 0:
+            raise RuntimeError("device status %d in the multi-token run" % int(step.status.item()))
+        us = a.elapsed_time(b) / reps * 1e3
+        nbytes = wl.kv_bytes() + qn * wl.qo_bytes()
+        flops = 4.0 * 64 * 128 * qn * wl.tokens
+        out["q_len=%d" % qn] = {"attn_us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
+                                "frac": round(nbytes / us / 1e3 / peak_gbs, 4),
+                                "TFLOP/s": round(flops / us / 1e6, 2)}
+    return out
 
 
 def schedule_comparison(ops, wl, stream):
