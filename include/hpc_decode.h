@@ -62,6 +62,23 @@ extern "C" {
 
 typedef enum { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
 
+/* Type of the attention query q: BF16, or E4M3 codes of q / q_scale (the
+ * prologue quantises it; only with an FP8-E4M3 cache, whose products with it
+ * run as E4M3 x E4M3 tensor-core products). */
+typedef enum { HPC_Q_BF16 = 0, HPC_Q_FP8_E4M3 = 1 } hpc_q_dtype;
+
+/* Type of the attention output, chosen by the caller. */
+typedef enum { HPC_OUT_BF16 = 0, HPC_OUT_FP16 = 1, HPC_OUT_FP32 = 2 } hpc_out_dtype;
+
+/* Options of the _ex attention calls; NULL means the single-token BF16 form
+ * ({1, HPC_Q_BF16, 1.0f, HPC_OUT_BF16}). */
+typedef struct {
+  int32_t q_len;      /* new tokens per sequence, 1 .. HPC_MAX_Q_LEN */
+  int32_t q_dtype;    /* hpc_q_dtype */
+  float q_scale;      /* dequantisation scale of an E4M3 q (q = code * q_scale) */
+  int32_t out_dtype;  /* hpc_out_dtype */
+} hpc_attn_options;
+
 enum {
   HPC_OK = 0,
   HPC_ERR_INVALID_ARG = -1,
@@ -382,6 +399,46 @@ int hpc_decode_attn_merge_mt(const void* q, const void* kv_cache, int32_t kv_dty
                              void* out, float sm_scale, int32_t* status, cudaStream_t stream);
 int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
                  int32_t batch, int32_t q_len, void* out, cudaStream_t stream);
+
+/* The general forms of the prologue, the attention and the merge.
+ * hpc_rope_norm_kvwrite_ex is hpc_rope_norm_kvwrite with the q output type
+ * chosen: q_dtype = HPC_Q_FP8_E4M3 stores q_out as uint8 E4M3 codes of
+ * q / q_scale ([batch, 64, 128], RNE, saturating at +-448) instead of BF16.
+ * hpc_decode_attn_ex / hpc_decode_attn_merge_ex / hpc_merge_ex are the
+ * attention calls with the options above: q is BF16 [batch, q_len, 64, 128]
+ * or (HPC_Q_FP8_E4M3, FP8 cache only) uint8 codes of the same shape; out is
+ * [batch, q_len, 64, 128] of the chosen out_dtype and 16-byte aligned;
+ * partials are float32 [plan->capacity, q_len, 8, 128] and
+ * [plan->capacity, q_len, 8].  The scores of an E4M3 q are
+ * (q_code . k_code) * q_scale * k_scale * sm_scale, the code products
+ * accumulated in fp32.
+ * Source: page "[vllm] Introducing the HPC-Ops attention backend" (the
+ * output dtype as a parameter of the caller; FP8 E4M3 models); page "vLLM and
+ * Tencent Hunyuan upstream two HPC backends for NVIDIA Hopper" (FP8 attention).
+ * Errors: as the plain calls; HPC_ERR_UNSUPPORTED for an E4M3 q with a BF16
+ * cache or an unknown dtype; HPC_ERR_INVALID_ARG for q_len out of range or a
+ * non-positive q_scale. */
+int hpc_rope_norm_kvwrite_ex(const void* q, const void* k, const void* v,
+                             const int32_t* positions, const float* cos_sin, int32_t max_pos,
+                             const void* q_norm_w, const void* k_norm_w, float eps,
+                             void* kv_cache, int32_t kv_dtype, int32_t num_blocks,
+                             const int64_t* slot_mapping, const float* kv_scale,
+                             int32_t q_dtype, float q_scale, void* q_out, int32_t batch,
+                             int32_t* status, cudaStream_t stream);
+int hpc_decode_attn_ex(const void* q, const void* kv_cache, int32_t kv_dtype,
+                       const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
+                       int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                       const hpc_attn_options* opts, const hpc_plan* plan, float* partial_o,
+                       float* partial_lse, float sm_scale, int32_t* status, cudaStream_t stream);
+int hpc_decode_attn_merge_ex(const void* q, const void* kv_cache, int32_t kv_dtype,
+                             const float* kv_scale, int32_t num_blocks,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t batch,
+                             const hpc_attn_options* opts, const hpc_plan* plan,
+                             float* partial_o, float* partial_lse, void* out, float sm_scale,
+                             int32_t* status, cudaStream_t stream);
+int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                 int32_t batch, const hpc_attn_options* opts, void* out, cudaStream_t stream);
 
 /* Self-test of the bounded pipeline wait (no counterpart on the pages).
  * Every wait of the attention pipeline gives up after a time limit (1 s),

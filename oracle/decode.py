@@ -260,16 +260,20 @@ def decode_step(q, k, v, positions, q_w, k_w, cache, block_table, seq_lens,
 
 
 def decode_step_mt(q, k, v, positions, q_w, k_w, cache, block_table, seq_lens, slot_mapping,
-                   kv_dtype, kv_scale=(1.0, 1.0), heads=None, seqs=None):
+                   kv_dtype, kv_scale=(1.0, 1.0), heads=None, seqs=None, q_scale=None):
     """The multi-token step: q [B,q_len,64,128], k and v [B,q_len,8,128],
     positions and slot_mapping [B,q_len].
 
     1. the prologue of every new token (RoPE at its own position, RMSNorm,
-       BF16 q, k and v written into its cache slot), tokens in order;
-    2. ``decode_attention_mt`` of the BF16 q over the cache.
+       q stored, k and v written into its cache slot), tokens in order; q is
+       stored as BF16, or with ``q_scale`` as the E4M3 code of q / q_scale
+       (the same encoder as the FP8 cache: RNE, saturating);
+    2. ``decode_attention_mt`` of the stored q (dequantised: code * q_scale)
+       over the cache.
 
-    Returns (q_out [B,q_len,64,128], out [B,q_len,64,128]); rows of sequences
-    not in ``seqs`` are NaN.
+    Returns (q_out [B,q_len,64,128], out [B,q_len,64,128]); q_out holds the
+    values the attention used (BF16 values, or dequantised E4M3 codes); rows
+    of sequences not in ``seqs`` are NaN.
     """
     B, qn = len(seq_lens), q.shape[1]
     seqs = range(B) if seqs is None else seqs
@@ -280,7 +284,10 @@ def decode_step_mt(q, k, v, positions, q_w, k_w, cache, block_table, seq_lens, s
         for t in range(qn):
             qo, ko, vo = prologue_token(q[b, t], k[b, t], v[b, t], positions[b][t], q_w, k_w)
             write_kv(cache, slot_mapping[b][t], ko, vo, kv_dtype, ks, vs)
-            q_out[b, t] = nx.bf16_round(qo)
+            if q_scale is None:
+                q_out[b, t] = nx.bf16_round(qo)
+            else:
+                q_out[b, t] = decode_kv(encode_kv(qo, KV_FP8, q_scale), KV_FP8, q_scale)
     for b in seqs:
         out[b] = decode_attention_mt(q_out[b], cache, block_table[b], int(seq_lens[b]),
                                      kv_dtype, ks, vs, heads=heads)

@@ -15,6 +15,8 @@ HPC_ERR_UNSUPPORTED = -2
 HPC_ERR_CUDA = -3
 NOALLOC_MAX_ITEMS = 4096
 MAX_Q_LEN = 4
+Q_BF16, Q_FP8 = 0, 1
+OUT_BF16, OUT_FP16, OUT_FP32 = 0, 1, 2
 
 STATUS_BITS = {
     1: "BAD_BLOCK", 2: "BAD_SLOT", 4: "BAD_SEQ_LEN", 8: "BAD_POSITION",
@@ -36,6 +38,12 @@ class Plan(ctypes.Structure):
 
 class PlanParams(ctypes.Structure):
     _fields_ = [("min_tiles", _c_i32), ("pool_chunks", _c_i32), ("pool_min_tiles", _c_i32)]
+
+
+class AttnOptions(ctypes.Structure):
+    """hpc_attn_options: new tokens per sequence, q type and scale, output type."""
+    _fields_ = [("q_len", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
+                ("q_scale", ctypes.c_float), ("out_dtype", ctypes.c_int32)]
 
 
 # name -> (restype, argtypes); the order follows include/hpc_decode.h
@@ -73,6 +81,17 @@ SIGNATURES = {
         _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_i32, ctypes.POINTER(Plan),
         _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
     "hpc_merge_mt": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(Plan), _c_i32, _c_i32, _c_p, _c_p]),
+    "hpc_rope_norm_kvwrite_ex": (ctypes.c_int, [
+        _c_p, _c_p, _c_p, _c_p, _c_p, _c_i32, _c_p, _c_p, ctypes.c_float,
+        _c_p, _c_i32, _c_i32, _c_p, _c_p, _c_i32, ctypes.c_float, _c_p, _c_i32, _c_p, _c_p]),
+    "hpc_decode_attn_ex": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(AttnOptions),
+        ctypes.POINTER(Plan), _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_decode_attn_merge_ex": (ctypes.c_int, [
+        _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(AttnOptions),
+        ctypes.POINTER(Plan), _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
+    "hpc_merge_ex": (ctypes.c_int, [_c_p, _c_p, ctypes.POINTER(Plan), _c_i32,
+                                    ctypes.POINTER(AttnOptions), _c_p, _c_p]),
     "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }
 

@@ -6,27 +6,27 @@
 int hpc::launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
                             const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
                             int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
-                            int32_t q_len, const hpc_plan* plan, float* partial_o,
+                            const hpc_attn_options& opts, const hpc_plan* plan, float* partial_o,
                             float* partial_lse, float sm_scale, int32_t* status,
                             unsigned long long* cta_clock, void* out, bool pdl,
                             cudaStream_t stream) {
-  const int rc = hpc::check_attn_args(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                      max_blocks, seq_lens, batch, plan, partial_o, partial_lse,
-                                      status, out);
+  int rc = hpc::check_attn_args(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                max_blocks, seq_lens, batch, plan, partial_o, partial_lse, status,
+                                out);
   if (rc != HPC_OK) return rc;
-  HPC_CHECK_ARG(q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
-  if (q_len > 1)
-    return hpc::launch_decode_attn_multi(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                         max_blocks, seq_lens, batch, q_len, plan, partial_o,
-                                         partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
-  auto* o = static_cast<uint16_t*>(out);
-  if (kv_dtype == HPC_KV_BF16)
-    return hpc::launch_attn<false, 1>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                      seq_lens, batch, 1, plan, partial_o, partial_lse, sm_scale,
-                                      status, cta_clock, o, pdl, stream);
-  return hpc::launch_attn<true, 1>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
-                                   seq_lens, batch, 1, plan, partial_o, partial_lse, sm_scale,
-                                   status, cta_clock, o, pdl, stream);
+  rc = hpc::check_attn_options(opts, kv_dtype, out);
+  if (rc != HPC_OK) return rc;
+  if (opts.q_len == 1)
+    return hpc::launch_attn_layout<1>(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                      max_blocks, seq_lens, batch, opts, plan, partial_o,
+                                      partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
+  if (opts.q_len == 2)
+    return hpc::launch_decode_attn_q2(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                      max_blocks, seq_lens, batch, opts, plan, partial_o,
+                                      partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
+  return hpc::launch_decode_attn_q4(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                    max_blocks, seq_lens, batch, opts, plan, partial_o, partial_lse,
+                                    sm_scale, status, cta_clock, out, pdl, stream);
 }
 
 extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype,
@@ -36,7 +36,8 @@ extern "C" int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_d
                                float* partial_o, float* partial_lse, float sm_scale,
                                int32_t* status, cudaStream_t stream) {
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, hpc::default_attn_options(), plan,
+                                 partial_o, partial_lse,
                                  sm_scale, status, nullptr, nullptr, false, stream);
 }
 
@@ -49,7 +50,8 @@ extern "C" int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int
                                         unsigned long long* cta_clock, cudaStream_t stream) {
   HPC_CHECK_ARG(cta_clock != nullptr);
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, hpc::default_attn_options(), plan,
+                                 partial_o, partial_lse,
                                  sm_scale, status, cta_clock, nullptr, false, stream);
 }
 
@@ -61,7 +63,8 @@ extern "C" int hpc_decode_attn_merge(const void* q, const void* kv_cache, int32_
                                      float sm_scale, int32_t* status, cudaStream_t stream) {
   HPC_CHECK_ARG(out != nullptr);
   return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, hpc::default_attn_options(), plan,
+                                 partial_o, partial_lse,
                                  sm_scale, status, nullptr, out, false, stream);
 }
 
@@ -77,4 +80,31 @@ extern "C" int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas) {
   *num_ctas = sms * (kv_dtype == HPC_KV_BF16 ? hpc::AttnTraits<false>::kGroups
                                              : hpc::AttnTraits<true>::kGroups);
   return HPC_OK;
+}
+
+extern "C" int hpc_decode_attn_ex(const void* q, const void* kv_cache, int32_t kv_dtype,
+                                  const float* kv_scale, int32_t num_blocks,
+                                  const int32_t* block_table, int32_t max_blocks,
+                                  const int32_t* seq_lens, int32_t batch,
+                                  const hpc_attn_options* opts, const hpc_plan* plan,
+                                  float* partial_o, float* partial_lse, float sm_scale,
+                                  int32_t* status, cudaStream_t stream) {
+  const hpc_attn_options o = opts != nullptr ? *opts : hpc::default_attn_options();
+  return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                 max_blocks, seq_lens, batch, o, plan, partial_o, partial_lse,
+                                 sm_scale, status, nullptr, nullptr, false, stream);
+}
+
+extern "C" int hpc_decode_attn_merge_ex(const void* q, const void* kv_cache, int32_t kv_dtype,
+                                        const float* kv_scale, int32_t num_blocks,
+                                        const int32_t* block_table, int32_t max_blocks,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        const hpc_attn_options* opts, const hpc_plan* plan,
+                                        float* partial_o, float* partial_lse, void* out,
+                                        float sm_scale, int32_t* status, cudaStream_t stream) {
+  HPC_CHECK_ARG(out != nullptr);
+  const hpc_attn_options o = opts != nullptr ? *opts : hpc::default_attn_options();
+  return hpc::launch_decode_attn(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
+                                 max_blocks, seq_lens, batch, o, plan, partial_o, partial_lse,
+                                 sm_scale, status, nullptr, out, false, stream);
 }

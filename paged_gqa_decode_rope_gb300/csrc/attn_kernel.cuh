@@ -163,24 +163,40 @@ __device__ __forceinline__ void pv_tile(uint32_t vb, int row, int vtok_bf16, int
   }
 }
 
+// Four consecutive output elements (index a multiple of 4) in the caller's
+// output type.
+__device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, float b, float c,
+                                           float d, int32_t out_dtype) {
+  if (out_dtype == HPC_OUT_FP32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + idx) = make_float4(a, b, c, d);
+  } else {
+    uint2 p;
+    p.x = out_dtype == HPC_OUT_FP16 ? pack_f16(a, b) : pack_bf16(a, b);
+    p.y = out_dtype == HPC_OUT_FP16 ? pack_f16(c, d) : pack_bf16(c, d);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + idx) = p;
+  }
+}
+
 // kQ: query layout, 1 (decode), 2 or 4 new tokens per sequence (q_len = 3
-// runs the 4-token layout with the fourth query's warp idle).
-template <bool kFp8, int kQ>
+// runs the 4-token layout with the fourth query's warp idle).  kQ8: q is E4M3
+// codes (FP8 cache only) and QK^T runs as E4M3 x E4M3 products.
+template <bool kFp8, int kQ, bool kQ8>
 __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_kernel(
     // q, the plan arrays and the cache may be written by the kernel this one
     // is a programmatic dependent of: they are read with plain (coherent)
     // loads, never as restrict/read-only data, so that no load of them can be
     // hoisted above the grid-dependency wait
-    const __grid_constant__ CUtensorMap kv_map, const uint16_t* q,
+    const __grid_constant__ CUtensorMap kv_map, const void* q, float q_scale,
     const float* __restrict__ kv_scale, const int32_t* __restrict__ block_table, int32_t max_blocks,
     int32_t num_blocks, const int32_t* __restrict__ seq_lens, int32_t batch, int32_t q_len,
     const hpc_work_item* items, const int32_t* cta_ptr, const int32_t* home_end, int32_t* pool,
     int32_t capacity, int32_t num_queues, float* __restrict__ partial_o,
     float* __restrict__ partial_lse,
     float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
-    const int32_t* seg_ptr, int32_t* seg_done, uint16_t* __restrict__ out) {
+    const int32_t* seg_ptr, int32_t* seg_done, void* __restrict__ out, int32_t out_dtype) {
   using T = AttnTraits<kFp8>;
   static_assert(kQ == 1 || kQ == 2 || kQ == 4, "query layouts of 1, 2 or 4 tokens");
+  static_assert(kFp8 || !kQ8, "an E4M3 q needs an E4M3 cache");
   constexpr int kWq = T::kWarpsPerGroup / kQ;   // warps per query
   constexpr int kMB = kQ;                       // 16-token blocks per warp and tile
   constexpr int G = T::kGroups;
@@ -479,7 +495,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   const int r = lane >> 2, c = lane & 3;
   const float k_scale = kFp8 ? kv_scale[0] : 1.f;
   const float v_scale = kFp8 ? kv_scale[1] : 1.f;
-  const float scale_log2 = sm_scale * k_scale * 1.4426950408889634f;
+  const float scale_log2 = sm_scale * k_scale * (kQ8 ? q_scale : 1.f) * 1.4426950408889634f;
   const int sw = lane & 7;                                        // swizzle of this lane's row
   const int row = tok0 + (lane & 7) + ((lane >> 3) & 1) * 8;      // ldmatrix row (token), block 0
   const int hi = lane >> 4;                                        // second 16-byte chunk
@@ -507,8 +523,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       const int sb = sg / kHkv, sh = sg % kHkv;
       for (int ej = threadIdx.x * 4; ej < q_len * kGroup * kD; ej += 32 * T::kConsumerWarps * 4) {
         const int j = ej / (kGroup * kD), e = ej - j * kGroup * kD;
-        *reinterpret_cast<uint2*>(out + ((static_cast<int64_t>(sb) * q_len + j) * kHq + sh * kGroup) * kD +
-                                  e) = make_uint2(0u, 0u);
+        store_out4(out, ((static_cast<int64_t>(sb) * q_len + j) * kHq + sh * kGroup) * kD + e, 0.f, 0.f,
+                   0.f, 0.f, out_dtype);
       }
     }
   }
@@ -548,8 +564,18 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       count = seg_ptr[seg + 1] - first;
     }
     if (qj >= q_len) return;   // a warp of the 4-token layout without a query
-    const uint16_t* qrow =
-        q + ((static_cast<int64_t>(d.it.seq) * q_len + qj) * kHq + d.it.h * kGroup + r) * kD;
+    const int64_t qr = (static_cast<int64_t>(d.it.seq) * q_len + qj) * kHq + d.it.h * kGroup + r;
+    if constexpr (kQ8) {
+      // B operand of m16n8k32 for k-step kp: codes 32kp + 4c .. +3 and 32kp + 16 + 4c .. +3
+      const uint8_t* qrow8 = static_cast<const uint8_t*>(q) + qr * kD;
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        qw[kp][0] = *reinterpret_cast<const uint32_t*>(qrow8 + 32 * kp + 4 * c);
+        qw[kp][1] = *reinterpret_cast<const uint32_t*>(qrow8 + 32 * kp + 16 + 4 * c);
+      }
+      return;
+    }
+    const uint16_t* qrow = static_cast<const uint16_t*>(q) + qr * kD;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       if constexpr (kFp8) {
@@ -582,7 +608,10 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       uint32_t bq[8][2];
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        if constexpr (kFp8) {
+        if constexpr (kQ8) {
+          bq[ks][0] = qw[ks][0];   // E4M3 codes as they are (entries 4..7 unused)
+          bq[ks][1] = qw[ks][1];
+        } else if constexpr (kFp8) {
           bq[ks][0] = pack_f16(bf16_lo(qw[ks][0]), bf16_hi(qw[ks][0]));
           bq[ks][1] = pack_f16(bf16_lo(qw[ks][1]), bf16_hi(qw[ks][1]));
         } else {
@@ -616,7 +645,17 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           for (int mb = 0; mb < kMB; ++mb) {
             const int rowb = row + 16 * mb;
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (kFp8) {
+            if constexpr (kQ8) {
+              // the ldmatrix words of a 16-token x 32-byte slab are the m16n8k32
+              // A fragments of the codes themselves: no conversion
+#pragma unroll
+              for (int kp = 0; kp < 4; ++kp) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4(kb + rowb * 128 + ((((2 * kp + hi) & 7) ^ sw) << 4), r0, r1, r2, r3);
+                if (kp & 1) mma_e4m3(sb, r0, r1, r2, r3, bq[kp][0], bq[kp][1]);
+                else        mma_e4m3(sa, r0, r1, r2, r3, bq[kp][0], bq[kp][1]);
+              }
+            } else if constexpr (kFp8) {
 #pragma unroll
               for (int kp = 0; kp < 4; ++kp) {
                 uint32_t r0, r1, r2, r3;
@@ -796,11 +835,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         }
         const float inv = L > 0.f ? v_scale / L : 0.f;
         if (direct) {
-          uint2 packed;
-          packed.x = pack_bf16(acc.x * inv, acc.y * inv);
-          packed.y = pack_bf16(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(out + ((static_cast<int64_t>(it.seq) * q_len + j) * kHq +
-                                           it.h * kGroup) * kD + e) = packed;
+          store_out4(out, ((static_cast<int64_t>(it.seq) * q_len + j) * kHq + it.h * kGroup) * kD + e,
+                     acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, out_dtype);
         } else {
           *reinterpret_cast<float4*>(dst + e) =
               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -889,11 +925,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           if (j >= q_len) continue;
           const int e = ej - j * kGroup * kD;
           const float inv = W[u] > 0.f ? 1.f / W[u] : 0.f;
-          uint2 packed;
-          packed.x = pack_bf16(acc[u].x * inv, acc[u].y * inv);
-          packed.y = pack_bf16(acc[u].z * inv, acc[u].w * inv);
-          *reinterpret_cast<uint2*>(out + ((static_cast<int64_t>(it.seq) * q_len + j) * kHq +
-                                           it.h * kGroup) * kD + e) = packed;
+          store_out4(out, ((static_cast<int64_t>(it.seq) * q_len + j) * kHq + it.h * kGroup) * kD + e,
+                     acc[u].x * inv, acc[u].y * inv, acc[u].z * inv, acc[u].w * inv, out_dtype);
         }
       }
     }
@@ -929,7 +962,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-template <bool kFp8, int kQ>
+template <bool kFp8, int kQ, bool kQ8>
 cudaError_t ensure_smem_attr() {
   // once per device: the dynamic shared memory opt-in is a per-device setting
   static std::mutex mu;
@@ -939,22 +972,22 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ, kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            AttnTraits<kFp8>::kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <bool kFp8, int kQ>
+template <bool kFp8, int kQ, bool kQ8>
 int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int32_t num_blocks,
                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
-                int32_t batch, int32_t q_len, const hpc_plan* plan, float* partial_o, float* partial_lse,
-                float sm_scale, int32_t* status, unsigned long long* cta_clock, uint16_t* out,
-                bool pdl, cudaStream_t stream) {
+                int32_t batch, const hpc_attn_options& opts, const hpc_plan* plan,
+                float* partial_o, float* partial_lse, float sm_scale, int32_t* status,
+                unsigned long long* cta_clock, void* out, bool pdl, cudaStream_t stream) {
   using T = AttnTraits<kFp8>;
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
-  if (ensure_smem_attr<kFp8, kQ>() != cudaSuccess) return HPC_ERR_CUDA;
+  if (ensure_smem_attr<kFp8, kQ, kQ8>() != cudaSuccess) return HPC_ERR_CUDA;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
                               static_cast<cuuint64_t>(num_blocks) * 2 * kHkv * kPage};
@@ -978,12 +1011,35 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, decode_attn_kernel<kFp8, kQ>, map, static_cast<const uint16_t*>(q), kv_scale, block_table,
-      max_blocks, num_blocks, seq_lens, batch, q_len, static_cast<const hpc_work_item*>(plan->items),
+      &cfg, decode_attn_kernel<kFp8, kQ, kQ8>, map, q, opts.q_scale, kv_scale, block_table,
+      max_blocks, num_blocks, seq_lens, batch, opts.q_len,
+      static_cast<const hpc_work_item*>(plan->items),
       static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
       plan->pool, plan->capacity, plan->num_ctas, partial_o, partial_lse, sm_scale, status, cta_clock,
-      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out);
+      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out, opts.out_dtype);
   return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+// The kernel instances of one query layout: BF16 cache, E4M3 cache with a
+// BF16 q, E4M3 cache with an E4M3 q.
+template <int kQ>
+int launch_attn_layout(const void* q, const void* kv_cache, int32_t kv_dtype, const float* kv_scale,
+                       int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,
+                       const int32_t* seq_lens, int32_t batch, const hpc_attn_options& opts,
+                       const hpc_plan* plan, float* partial_o, float* partial_lse, float sm_scale,
+                       int32_t* status, unsigned long long* cta_clock, void* out, bool pdl,
+                       cudaStream_t stream) {
+  if (kv_dtype == HPC_KV_BF16)
+    return launch_attn<false, kQ, false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                         seq_lens, batch, opts, plan, partial_o, partial_lse,
+                                         sm_scale, status, cta_clock, out, pdl, stream);
+  if (opts.q_dtype == HPC_Q_FP8_E4M3)
+    return launch_attn<true, kQ, true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                       seq_lens, batch, opts, plan, partial_o, partial_lse,
+                                       sm_scale, status, cta_clock, out, pdl, stream);
+  return launch_attn<true, kQ, false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
+                                      seq_lens, batch, opts, plan, partial_o, partial_lse, sm_scale,
+                                      status, cta_clock, out, pdl, stream);
 }
 
 // The checks every attention entry point makes before launching.
@@ -1003,6 +1059,21 @@ inline int check_attn_args(const void* q, const void* kv_cache, int32_t kv_dtype
   else if (kv_dtype != HPC_KV_BF16) return HPC_ERR_UNSUPPORTED;
   if (num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks) * kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
+  return HPC_OK;
+}
+
+// The checks of the attention options.
+inline int check_attn_options(const hpc_attn_options& o, int32_t kv_dtype, const void* out) {
+  HPC_CHECK_ARG(o.q_len >= 1 && o.q_len <= HPC_MAX_Q_LEN);
+  if (o.q_dtype != HPC_Q_BF16 && o.q_dtype != HPC_Q_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+  if (o.q_dtype == HPC_Q_FP8_E4M3) {
+    if (kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+    HPC_CHECK_ARG(o.q_scale > 0.0f && o.q_scale < 3.0e38f);
+  }
+  if (o.out_dtype != HPC_OUT_BF16 && o.out_dtype != HPC_OUT_FP16 && o.out_dtype != HPC_OUT_FP32)
+    return HPC_ERR_UNSUPPORTED;
+  if (out != nullptr)
+    HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(out) & (o.out_dtype == HPC_OUT_FP32 ? 15 : 7)) == 0);
   return HPC_OK;
 }
 

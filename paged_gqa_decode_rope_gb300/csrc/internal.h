@@ -5,26 +5,37 @@
 
 namespace hpc {
 
-// hpc_decode_attn / _merge / _profiled and their multi-token forms in one:
-// checks the arguments and launches the attention kernel for q_len new
-// tokens per sequence (1 .. HPC_MAX_Q_LEN).  out != nullptr fuses the merge;
-// cta_clock != nullptr records per-CTA clocks; pdl launches the kernel as a
-// programmatic dependent of the previous kernel on the stream.
+// hpc_decode_attn / _merge / _profiled / _ex in one: checks the arguments and
+// the options and launches the attention kernel.  out != nullptr fuses the
+// merge; cta_clock != nullptr records per-CTA clocks; pdl launches the kernel
+// as a programmatic dependent of the previous kernel on the stream.
 int launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, const float* kv_scale,
                        int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,
-                       const int32_t* seq_lens, int32_t batch, int32_t q_len, const hpc_plan* plan,
-                       float* partial_o, float* partial_lse, float sm_scale, int32_t* status,
-                       unsigned long long* cta_clock, void* out, bool pdl, cudaStream_t stream);
+                       const int32_t* seq_lens, int32_t batch, const hpc_attn_options& opts,
+                       const hpc_plan* plan, float* partial_o, float* partial_lse, float sm_scale,
+                       int32_t* status, unsigned long long* cta_clock, void* out, bool pdl,
+                       cudaStream_t stream);
 
-// The multi-token launches (q_len 2 .. HPC_MAX_Q_LEN), arguments already
-// checked; in their own translation unit so that the kernel instances
+// The launches of the 2- and 4-token query layouts (arguments already
+// checked), each in its own translation unit so that the kernel instances
 // compile in parallel.
-int launch_decode_attn_multi(const void* q, const void* kv_cache, int32_t kv_dtype,
-                             const float* kv_scale, int32_t num_blocks, const int32_t* block_table,
-                             int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
-                             int32_t q_len, const hpc_plan* plan, float* partial_o,
-                             float* partial_lse, float sm_scale, int32_t* status,
-                             unsigned long long* cta_clock, void* out, bool pdl,
-                             cudaStream_t stream);
+#define HPC_LAYOUT_LAUNCH_ARGS                                                                    \
+  const void *q, const void *kv_cache, int32_t kv_dtype, const float *kv_scale,                   \
+      int32_t num_blocks, const int32_t *block_table, int32_t max_blocks,                         \
+      const int32_t *seq_lens, int32_t batch, const hpc_attn_options &opts, const hpc_plan *plan, \
+      float *partial_o, float *partial_lse, float sm_scale, int32_t *status,                      \
+      unsigned long long *cta_clock, void *out, bool pdl, cudaStream_t stream
+int launch_decode_attn_q2(HPC_LAYOUT_LAUNCH_ARGS);
+int launch_decode_attn_q4(HPC_LAYOUT_LAUNCH_ARGS);
+
+// The single-token BF16 options: {1, HPC_Q_BF16, 1.0f, HPC_OUT_BF16}.
+inline hpc_attn_options default_attn_options() {
+  hpc_attn_options o;
+  o.q_len = 1;
+  o.q_dtype = HPC_Q_BF16;
+  o.q_scale = 1.0f;
+  o.out_dtype = HPC_OUT_BF16;
+  return o;
+}
 
 }  // namespace hpc

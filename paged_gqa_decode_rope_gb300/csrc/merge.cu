@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
                                                     const float* __restrict__ partial_lse,
                                                     const int32_t* __restrict__ seg_ptr,
                                                     int32_t capacity, int32_t q_len,
-                                                    uint16_t* __restrict__ out) {
+                                                    void* __restrict__ out, int32_t out_dtype) {
   const int s = blockIdx.x;            // segment = seq * 8 + kv_head
   const int j = blockIdx.y;            // new token
   const int r = threadIdx.x >> 5;      // query head within the group
@@ -61,27 +61,51 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
       acc.w *= inv;
     }
   }
-  uint2 packed;
-  packed.x = pack_bf16(acc.x, acc.y);
-  packed.y = pack_bf16(acc.z, acc.w);
-  *reinterpret_cast<uint2*>(out + orow * kD + d) = packed;
+  if (out_dtype == HPC_OUT_FP32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + orow * kD + d) = acc;
+  } else {
+    uint2 packed;
+    packed.x = out_dtype == HPC_OUT_FP16 ? pack_f16(acc.x, acc.y) : pack_bf16(acc.x, acc.y);
+    packed.y = out_dtype == HPC_OUT_FP16 ? pack_f16(acc.z, acc.w) : pack_bf16(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + orow * kD + d) = packed;
+  }
 }
 
 }  // namespace
 }  // namespace hpc
 
-extern "C" int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
-                            int32_t batch, int32_t q_len, void* out, cudaStream_t stream) {
+extern "C" int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                            int32_t batch, const hpc_attn_options* opts, void* out,
+                            cudaStream_t stream) {
   HPC_CHECK_ARG(partial_o && partial_lse && plan && plan->seg_ptr && out);
-  HPC_CHECK_ARG(batch >= 0 && q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
+  hpc_attn_options o;
+  o.q_len = 1;
+  o.q_dtype = HPC_Q_BF16;
+  o.q_scale = 1.0f;
+  o.out_dtype = HPC_OUT_BF16;
+  if (opts != nullptr) o = *opts;
+  HPC_CHECK_ARG(batch >= 0 && o.q_len >= 1 && o.q_len <= HPC_MAX_Q_LEN);
+  if (o.out_dtype != HPC_OUT_BF16 && o.out_dtype != HPC_OUT_FP16 && o.out_dtype != HPC_OUT_FP32)
+    return HPC_ERR_UNSUPPORTED;
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(out) & (o.out_dtype == HPC_OUT_FP32 ? 15 : 7)) == 0);
   if (batch == 0) return HPC_OK;
   if (static_cast<int64_t>(batch) * hpc::kHkv > 0x7fffffff) return HPC_ERR_UNSUPPORTED;
-  hpc::merge_kernel<<<dim3(batch * hpc::kHkv, q_len), 256, 0, stream>>>(
-      partial_o, partial_lse, plan->seg_ptr, plan->capacity, q_len, static_cast<uint16_t*>(out));
+  hpc::merge_kernel<<<dim3(batch * hpc::kHkv, o.q_len), 256, 0, stream>>>(
+      partial_o, partial_lse, plan->seg_ptr, plan->capacity, o.q_len, out, o.out_dtype);
   return HPC_LAUNCH_STATUS();
+}
+
+extern "C" int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                            int32_t batch, int32_t q_len, void* out, cudaStream_t stream) {
+  hpc_attn_options o;
+  o.q_len = q_len;
+  o.q_dtype = HPC_Q_BF16;
+  o.q_scale = 1.0f;
+  o.out_dtype = HPC_OUT_BF16;
+  return hpc_merge_ex(partial_o, partial_lse, plan, batch, &o, out, stream);
 }
 
 extern "C" int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
                          int32_t batch, void* out, cudaStream_t stream) {
-  return hpc_merge_mt(partial_o, partial_lse, plan, batch, 1, out, stream);
+  return hpc_merge_ex(partial_o, partial_lse, plan, batch, nullptr, out, stream);
 }

@@ -34,15 +34,16 @@ __global__ void rope_table_kernel(double theta, int32_t max_pos, float* __restri
   }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kQ8>
 __global__ void __launch_bounds__(256) prologue_kernel(
     const uint16_t* q, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
     const int32_t* __restrict__ positions, const float* __restrict__ cos_sin, int32_t max_pos,
     const uint16_t* __restrict__ q_w, const uint16_t* __restrict__ k_w, float eps,
     uint8_t* __restrict__ kv_cache, int32_t num_blocks, const int64_t* __restrict__ slot_mapping,
-    const float* __restrict__ kv_scale, uint16_t* q_out, int32_t* __restrict__ status) {
-  prologue_heads<kFp8>(blockIdx.y, blockIdx.x, q, k, v, positions, cos_sin, max_pos, q_w, k_w, eps,
-                       kv_cache, num_blocks, slot_mapping, kv_scale, q_out, status);
+    const float* __restrict__ kv_scale, void* q_out, float q_scale,
+    int32_t* __restrict__ status) {
+  prologue_heads<kFp8, kQ8>(blockIdx.y, blockIdx.x, q, k, v, positions, cos_sin, max_pos, q_w, k_w, eps,
+                       kv_cache, num_blocks, slot_mapping, kv_scale, q_out, q_scale, status);
 }
 
 }  // namespace
@@ -59,18 +60,21 @@ extern "C" int hpc_rope_cos_sin_cache(double theta, int32_t max_pos, float* cos_
   return HPC_LAUNCH_STATUS();
 }
 
-extern "C" int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
-                                     const int32_t* positions, const float* cos_sin,
-                                     int32_t max_pos, const void* q_norm_w, const void* k_norm_w,
-                                     float eps, void* kv_cache, int32_t kv_dtype,
-                                     int32_t num_blocks, const int64_t* slot_mapping,
-                                     const float* kv_scale, void* q_out, int32_t batch,
-                                     int32_t* status, cudaStream_t stream) {
+extern "C" int hpc_rope_norm_kvwrite_ex(const void* q, const void* k, const void* v,
+                                        const int32_t* positions, const float* cos_sin,
+                                        int32_t max_pos, const void* q_norm_w,
+                                        const void* k_norm_w, float eps, void* kv_cache,
+                                        int32_t kv_dtype, int32_t num_blocks,
+                                        const int64_t* slot_mapping, const float* kv_scale,
+                                        int32_t q_dtype, float q_scale, void* q_out,
+                                        int32_t batch, int32_t* status, cudaStream_t stream) {
   HPC_CHECK_ARG(q && k && v && positions && cos_sin && q_norm_w && k_norm_w && kv_cache &&
                 slot_mapping && q_out && status);
   HPC_CHECK_ARG(batch >= 0 && max_pos > 0 && num_blocks > 0 && eps >= 0.0f);
   if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
   if (kv_dtype == HPC_KV_FP8_E4M3) HPC_CHECK_ARG(kv_scale != nullptr);
+  if (q_dtype != HPC_Q_BF16 && q_dtype != HPC_Q_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+  if (q_dtype == HPC_Q_FP8_E4M3) HPC_CHECK_ARG(q_scale > 0.0f && q_scale < 3.0e38f);
   if (batch > 65535) return HPC_ERR_UNSUPPORTED;
   if (batch == 0) return HPC_OK;
   const dim3 grid(hpc::kGroup + 1, batch);
@@ -80,15 +84,29 @@ extern "C" int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v
   auto* qw = static_cast<const uint16_t*>(q_norm_w);
   auto* kw = static_cast<const uint16_t*>(k_norm_w);
   auto* cache = static_cast<uint8_t*>(kv_cache);
-  auto* qo = static_cast<uint16_t*>(q_out);
+  auto launch = [&](auto kernel) {
+    kernel<<<grid, 256, 0, stream>>>(qp, kp, vp, positions, cos_sin, max_pos, qw, kw, eps, cache,
+                                     num_blocks, slot_mapping, kv_scale, q_out, q_scale, status);
+  };
+  const bool q8 = q_dtype == HPC_Q_FP8_E4M3;
   if (kv_dtype == HPC_KV_BF16) {
-    hpc::prologue_kernel<false><<<grid, 256, 0, stream>>>(qp, kp, vp, positions, cos_sin, max_pos,
-                                                           qw, kw, eps, cache, num_blocks,
-                                                           slot_mapping, kv_scale, qo, status);
+    if (q8) launch(hpc::prologue_kernel<false, true>);
+    else launch(hpc::prologue_kernel<false, false>);
   } else {
-    hpc::prologue_kernel<true><<<grid, 256, 0, stream>>>(qp, kp, vp, positions, cos_sin, max_pos,
-                                                          qw, kw, eps, cache, num_blocks,
-                                                          slot_mapping, kv_scale, qo, status);
+    if (q8) launch(hpc::prologue_kernel<true, true>);
+    else launch(hpc::prologue_kernel<true, false>);
   }
   return HPC_LAUNCH_STATUS();
+}
+
+extern "C" int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
+                                     const int32_t* positions, const float* cos_sin,
+                                     int32_t max_pos, const void* q_norm_w, const void* k_norm_w,
+                                     float eps, void* kv_cache, int32_t kv_dtype,
+                                     int32_t num_blocks, const int64_t* slot_mapping,
+                                     const float* kv_scale, void* q_out, int32_t batch,
+                                     int32_t* status, cudaStream_t stream) {
+  return hpc_rope_norm_kvwrite_ex(q, k, v, positions, cos_sin, max_pos, q_norm_w, k_norm_w, eps,
+                                  kv_cache, kv_dtype, num_blocks, slot_mapping, kv_scale,
+                                  HPC_Q_BF16, 1.0f, q_out, batch, status, stream);
 }

@@ -1,6 +1,7 @@
-// Device code of the fused decode prologue (RoPE -> per-head RMSNorm -> BF16 q
-// output and K/V write into the paged cache), shared by the standalone
-// prologue kernel and the fused prologue + planner kernel.
+// Device code of the fused decode prologue (RoPE -> per-head RMSNorm -> q
+// output, BF16 or E4M3 codes of q / q_scale, and K/V write into the paged
+// cache), shared by the standalone prologue kernel and the fused prologue +
+// planner kernel.
 //
 // Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
 // Hopper", section "Why does dynamic scheduling matter for attention?" (RoPE
@@ -18,14 +19,15 @@
 namespace hpc {
 namespace {
 
-template <bool kFp8>
+// kQ8: q is stored as E4M3 codes of q / q_scale (RNE, saturating) instead of BF16.
+template <bool kFp8, bool kQ8>
 __device__ __forceinline__ void prologue_heads(
     int b, int xblk, const uint16_t* q, const uint16_t* __restrict__ k,
     const uint16_t* __restrict__ v, const int32_t* __restrict__ positions,
     const float* __restrict__ cos_sin, int32_t max_pos, const uint16_t* __restrict__ q_w,
     const uint16_t* __restrict__ k_w, float eps, uint8_t* __restrict__ kv_cache,
     int32_t num_blocks, const int64_t* __restrict__ slot_mapping,
-    const float* __restrict__ kv_scale, uint16_t* q_out, int32_t* __restrict__ status) {
+    const float* __restrict__ kv_scale, void* q_out, float q_scale, int32_t* __restrict__ status) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool is_kv = xblk == kGroup;   // the 9th block of a sequence
@@ -70,9 +72,16 @@ __device__ __forceinline__ void prologue_heads(
   const float y2 = r2 * inv * bf16_lo(wb), y3 = r3 * inv * bf16_hi(wb);
 
   if (!is_kv) {
-    uint16_t* dst = q_out + (static_cast<int64_t>(b) * kHq + xblk * kGroup + warp) * kD;
-    *reinterpret_cast<uint32_t*>(dst + d0) = pack_bf16(y0, y1);
-    *reinterpret_cast<uint32_t*>(dst + kD / 2 + d0) = pack_bf16(y2, y3);
+    const int64_t row = static_cast<int64_t>(b) * kHq + xblk * kGroup + warp;
+    if constexpr (kQ8) {
+      uint8_t* dst = static_cast<uint8_t*>(q_out) + row * kD;
+      *reinterpret_cast<uint16_t*>(dst + d0) = f32x2_to_e4m3x2(y0 / q_scale, y1 / q_scale);
+      *reinterpret_cast<uint16_t*>(dst + kD / 2 + d0) = f32x2_to_e4m3x2(y2 / q_scale, y3 / q_scale);
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(q_out) + row * kD;
+      *reinterpret_cast<uint32_t*>(dst + d0) = pack_bf16(y0, y1);
+      *reinterpret_cast<uint32_t*>(dst + kD / 2 + d0) = pack_bf16(y2, y3);
+    }
     return;
   }
 

@@ -42,9 +42,9 @@ __global__ void __launch_bounds__(kStepThreads) prologue_plan_kernel(
                                     seg_done, capacity, num_ctas, status, step_smem);
   } else {
     const int blk = blockIdx.x - 1;
-    prologue_heads<kFp8>(blk / (kGroup + 1), blk % (kGroup + 1), q, k, v, positions, cos_sin,
-                         max_pos, q_w, k_w, eps, kv_cache, num_blocks, slot_mapping, kv_scale,
-                         q_out, status);
+    prologue_heads<kFp8, false>(blk / (kGroup + 1), blk % (kGroup + 1), q, k, v, positions, cos_sin,
+                                max_pos, q_w, k_w, eps, kv_cache, num_blocks, slot_mapping,
+                                kv_scale, q_out, 1.0f, status);
   }
 }
 
@@ -121,6 +121,7 @@ extern "C" int hpc_decode_step(const void* q, const void* k, const void* v,
   }
   if (cudaPeekAtLastError() != cudaSuccess) return HPC_ERR_CUDA;
   return hpc::launch_decode_attn(q_out, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
-                                 max_blocks, seq_lens, batch, 1, plan, partial_o, partial_lse,
+                                 max_blocks, seq_lens, batch, hpc::default_attn_options(), plan,
+                                 partial_o, partial_lse,
                                  sm_scale, status, nullptr, out, true, stream);
 }

@@ -469,3 +469,134 @@ class DecodeStepMT:
                           self.q_out.view(B * qn, HQ, D), self.status)
         self.plan_step(seq_lens)
         return self.attend(self.q_out, kv_cache, kv_scale, block_table, seq_lens)
+
+
+
+# ------------------------------------------------------------ general (_ex) forms
+
+Q_BF16, Q_FP8 = _lib.Q_BF16, _lib.Q_FP8
+OUT_BF16, OUT_FP16, OUT_FP32 = _lib.OUT_BF16, _lib.OUT_FP16, _lib.OUT_FP32
+_OUT_TORCH = {OUT_BF16: torch.bfloat16, OUT_FP16: torch.float16, OUT_FP32: torch.float32}
+
+
+def rope_norm_kvwrite_ex(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, kv_dtype,
+                         slot_mapping, kv_scale, q_out, status, q_dtype=Q_BF16, q_scale=1.0, eps=EPS):
+    """The prologue with the q output type chosen: q_out is BF16 [T,64,128], or
+    uint8 E4M3 codes of q / q_scale [T,64,128] with q_dtype = Q_FP8."""
+    T = q.shape[0]
+    _want(q, "q", _BF16, (T, HQ, D))
+    _want(k, "k", _BF16, (T, HKV, D))
+    _want(v, "v", _BF16, (T, HKV, D))
+    _want(positions, "positions", (torch.int32,), (T,))
+    _want(cos_sin, "cos_sin", (torch.float32,))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    _want(slot_mapping, "slot_mapping", (torch.int64,), (T,))
+    if kv_dtype == KV_FP8:
+        _want(kv_scale, "kv_scale", (torch.float32,), (2,))
+    _want(q_out, "q_out", (torch.uint8,) if q_dtype == Q_FP8 else _BF16, (T, HQ, D))
+    _want(status, "status", (torch.int32,), (1,))
+    check("hpc_rope_norm_kvwrite_ex", _lib.lib().hpc_rope_norm_kvwrite_ex(
+        _p(q), _p(k), _p(v), _p(positions), _p(cos_sin), cos_sin.shape[0], _p(q_norm_w),
+        _p(k_norm_w), float(eps), _p(kv_cache), kv_dtype, kv_cache.shape[0], _p(slot_mapping),
+        _p(kv_scale if kv_dtype == KV_FP8 else None), int(q_dtype), float(q_scale), _p(q_out), T,
+        _p(status), _stream()))
+
+
+def _opts(q_len, q_dtype, q_scale, out_dtype):
+    return _lib.AttnOptions(int(q_len), int(q_dtype), float(q_scale), int(out_dtype))
+
+
+def decode_attn_ex(q, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, plan, partial_o,
+                   partial_lse, status, q_dtype=Q_BF16, q_scale=1.0, out=None, out_dtype=OUT_BF16,
+                   sm_scale=None):
+    """The attention with options: q [B, q_len, 64, 128] (BF16, or uint8 E4M3
+    codes with q_dtype = Q_FP8); with ``out`` given the merge is fused in and
+    out [B, q_len, 64, 128] of ``out_dtype`` is written, else partials."""
+    B, qn = q.shape[0], q.shape[1]
+    if q.dim() != 4 or not 1 <= qn <= _lib.MAX_Q_LEN:
+        raise ValueError("q must be [batch, q_len <= %d, 64, 128]" % _lib.MAX_Q_LEN)
+    _want(q, "q", (torch.uint8,) if q_dtype == Q_FP8 else _BF16, (B, qn, HQ, D))
+    _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+    _want(block_table, "block_table", (torch.int32,))
+    _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+    if plan.batch != B:
+        raise ValueError("plan was made for batch %d, not %d" % (plan.batch, B))
+    if (partial_o.numel() < plan.capacity * qn * HKV * D or
+            partial_lse.numel() < plan.capacity * qn * HKV):
+        raise ValueError("partial buffers are smaller than capacity x q_len rows")
+    _want(status, "status", (torch.int32,), (1,))
+    o = _opts(qn, q_dtype, q_scale, out_dtype)
+    scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+    ks = _p(kv_scale if kv_dtype == KV_FP8 else None)
+    if out is None:
+        check("hpc_decode_attn_ex", _lib.lib().hpc_decode_attn_ex(
+            _p(q), _p(kv_cache), kv_dtype, ks, kv_cache.shape[0], _p(block_table),
+            block_table.shape[1], _p(seq_lens), B, ctypes.byref(o), ctypes.byref(plan.c),
+            _p(partial_o), _p(partial_lse), scale, _p(status), _stream()))
+    else:
+        _want(out, "out", (_OUT_TORCH[out_dtype],), (B, qn, HQ, D))
+        check("hpc_decode_attn_merge_ex", _lib.lib().hpc_decode_attn_merge_ex(
+            _p(q), _p(kv_cache), kv_dtype, ks, kv_cache.shape[0], _p(block_table),
+            block_table.shape[1], _p(seq_lens), B, ctypes.byref(o), ctypes.byref(plan.c),
+            _p(partial_o), _p(partial_lse), _p(out), scale, _p(status), _stream()))
+
+
+def merge_ex(partial_o, partial_lse, plan, out, out_dtype=OUT_BF16):
+    B, qn = plan.batch, out.shape[1]
+    _want(out, "out", (_OUT_TORCH[out_dtype],), (B, qn, HQ, D))
+    o = _opts(qn, Q_BF16, 1.0, out_dtype)
+    check("hpc_merge_ex", _lib.lib().hpc_merge_ex(
+        _p(partial_o), _p(partial_lse), ctypes.byref(plan.c), B, ctypes.byref(o), _p(out),
+        _stream()))
+
+
+class DecodeStepEx:
+    """The step in its general form: q_len new tokens per sequence, q stored as
+    BF16 or E4M3 (q_dtype, q_scale; E4M3 needs an FP8 cache), output of
+    out_dtype; prologue of the B * q_len tokens, plan, attention (merge fused
+    or separate)."""
+
+    def __init__(self, batch, kv_dtype, max_blocks, q_len=1, q_dtype=Q_BF16, q_scale=1.0,
+                 out_dtype=OUT_BF16, device="cuda", n_ctas=None, pool_chunks=POOL_CHUNKS,
+                 pool_min_tiles=POOL_MIN_TILES, fused=True, min_tiles=1):
+        self.batch, self.kv_dtype, self.max_blocks = batch, kv_dtype, max_blocks
+        self.q_len, self.q_dtype, self.q_scale, self.out_dtype = q_len, q_dtype, q_scale, out_dtype
+        self.fused, self.min_tiles = fused, min_tiles
+        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles)
+        cap = max(self.plan.capacity, 1)
+        self.partial_o = torch.empty((cap, q_len, HKV, D), dtype=torch.float32, device=device)
+        self.partial_lse = torch.empty((cap, q_len, HKV), dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.q_out = torch.empty((batch, q_len, HQ, D),
+                                 dtype=torch.uint8 if q_dtype == Q_FP8 else torch.bfloat16,
+                                 device=device)
+        self.out = torch.empty((batch, q_len, HQ, D), dtype=_OUT_TORCH[out_dtype], device=device)
+
+    def plan_step(self, seq_lens):
+        decode_plan(seq_lens, self.max_blocks, self.plan, self.status, self.min_tiles)
+
+    def attend(self, q, kv_cache, kv_scale, block_table, seq_lens):
+        if self.fused:
+            decode_attn_ex(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens, self.plan,
+                           self.partial_o, self.partial_lse, self.status, self.q_dtype,
+                           self.q_scale, self.out, self.out_dtype)
+        else:
+            decode_attn_ex(q, kv_cache, self.kv_dtype, kv_scale, block_table, seq_lens, self.plan,
+                           self.partial_o, self.partial_lse, self.status, self.q_dtype,
+                           self.q_scale)
+            merge_ex(self.partial_o, self.partial_lse, self.plan, self.out, self.out_dtype)
+        return self.out
+
+    def __call__(self, q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, slot_mapping,
+                 kv_scale, block_table, seq_lens):
+        """q [B,q_len,64,128], k and v [B,q_len,8,128], positions and
+        slot_mapping [B,q_len]; seq_lens counts the new tokens."""
+        B, qn = self.batch, self.q_len
+        rope_norm_kvwrite_ex(q.reshape(B * qn, HQ, D), k.reshape(B * qn, HKV, D),
+                             v.reshape(B * qn, HKV, D), positions.reshape(B * qn), cos_sin,
+                             q_norm_w, k_norm_w, kv_cache, self.kv_dtype,
+                             slot_mapping.reshape(B * qn), kv_scale,
+                             self.q_out.view(B * qn, HQ, D), self.status, self.q_dtype,
+                             self.q_scale)
+        self.plan_step(seq_lens)
+        return self.attend(self.q_out, kv_cache, kv_scale, block_table, seq_lens)

@@ -1,0 +1,149 @@
+"""E4M3 query (q quantised to E4M3 codes, its products with the E4M3 cache
+on the tensor cores) and the caller-chosen output type, against the float64
+oracle on the same dequantised values."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as od
+from oracle import numerics as nx
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+LENGTHS = [1, 2, 63, 64, 65, 300, 4097, 9000]
+
+
+def _q_codes(B, qn, seed):
+    """E4M3 codes of a N(0,1) q with a per-tensor scale max|q|/448 (host)."""
+    rng = np.random.default_rng(seed)
+    qf = rng.standard_normal((B, qn, 64, 128))
+    scale = float(np.abs(qf).max() / 448.0)
+    codes = od.encode_kv(qf, od.KV_FP8, scale).astype(np.uint8)
+    return codes, scale
+
+
+def _oracle_mt(wl, qvals, b, heads=None):
+    L = int(wl.lengths[b])
+    sub, row = gu.seq_view(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
+    sc = wl.kv_scale.cpu().numpy().astype(np.float64)
+    return od.decode_attention_mt(qvals[b], sub, row, L, wl.kv_dtype, sc[0], sc[1], heads=heads)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("q_len", [1, 2, 4])
+def test_fp8_query_attention_matches_oracle(q_len, fused):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=80 + q_len, lengths=LENGTHS, kv_dtype=od.KV_FP8,
+                  include_new_token=True)
+    codes, qs = _q_codes(wl.batch, q_len, 3 + q_len)
+    q = torch.as_tensor(codes, device="cuda")
+    qvals = od.decode_kv(codes, od.KV_FP8, qs)
+    step = ops.DecodeStepEx(wl.batch, od.KV_FP8, wl.max_blocks, q_len=q_len, q_dtype=ops.Q_FP8,
+                            q_scale=qs, fused=fused)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got))
+    for b in range(wl.batch):
+        gu.compare(got[b], _oracle_mt(wl, qvals, b), gu.TOL_FP8_MAX, None,
+                   label="q_len %d seq %d (L=%d)" % (q_len, b, wl.lengths[b]))
+
+
+def test_fp8_query_full_mixed():
+    """The E4M3 q on the full mixed FP8 batch, sampled rows."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("mixed_fp8", seed=4, include_new_token=True)
+    codes, qs = _q_codes(wl.batch, 1, 17)
+    q = torch.as_tensor(codes, device="cuda")
+    qvals = od.decode_kv(codes, od.KV_FP8, qs)
+    step = ops.DecodeStepEx(wl.batch, od.KV_FP8, wl.max_blocks, q_dtype=ops.Q_FP8, q_scale=qs)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    got = gu.bf16_host(out)
+    for b in (0, 5, 31):
+        heads = list(range(0, 64, 9)) if wl.lengths[b] > 65536 else None
+        gu.compare(got[b], _oracle_mt(wl, qvals, b, heads), gu.TOL_FP8_MAX, None, label="seq %d" % b)
+
+
+@pytest.mark.parametrize("kv", [0, 1])
+def test_output_types(kv):
+    """FP32, FP16 and BF16 outputs of one run: the FP32 output matches the
+    oracle, and the FP16 / BF16 outputs are the FP32 values rounded to nearest
+    (fused and standalone merges alike)."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=90 + kv, lengths=[5, 64, 700, 5000], kv_dtype=kv,
+                  include_new_token=True)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    q = torch.randn((wl.batch, 2, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+    outs = {}
+    for fused in (True, False):
+        for od_ in (ops.OUT_FP32, ops.OUT_FP16, ops.OUT_BF16):
+            step = ops.DecodeStepEx(wl.batch, kv, wl.max_blocks, q_len=2, out_dtype=od_, fused=fused)
+            step.plan_step(wl.seq_lens)
+            outs[(fused, od_)] = step.attend(q, wl.cache, wl.kv_scale, wl.block_table,
+                                             wl.seq_lens).clone()
+            torch.cuda.synchronize()
+            assert int(step.status.item()) == 0
+    for fused in (True, False):
+        f32 = outs[(fused, ops.OUT_FP32)]
+        assert outs[(fused, ops.OUT_FP32)].dtype == torch.float32
+        assert torch.equal(outs[(fused, ops.OUT_FP16)], f32.to(torch.float16))
+        assert torch.equal(outs[(fused, ops.OUT_BF16)], f32.to(torch.bfloat16))
+    qv = gu.bf16_host(q)
+    got = outs[(True, ops.OUT_FP32)].cpu().numpy().astype(np.float64)
+    tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if kv == 0 else (gu.TOL_FP8_MAX, None)
+    for b in range(wl.batch):
+        gu.compare(got[b], _oracle_mt(wl, qv, b), *tol, label="fp32 out seq %d" % b)
+
+
+def test_fp8_query_step_end_to_end():
+    """Prologue storing E4M3 q codes (within one code of the oracle's), plan
+    and attention against the oracle on the cache and q codes the GPU wrote."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    qn = 2
+    wl = Workload("custom", seed=95, lengths=[2, 64, 65, 1000], kv_dtype=od.KV_FP8)
+    B = wl.batch
+    g = torch.Generator(device="cuda").manual_seed(13)
+    q = torch.randn((B, qn, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+    k = torch.randn((B, qn, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, qn, 8, 128), generator=g, device="cuda").to(torch.bfloat16)
+    pos = np.array([[L - qn + t for t in range(qn)] for L in wl.lengths], dtype=np.int32)
+    slots = np.array([[wl.block_table_np[b][p // 64] * 64 + p % 64 for p in pos[b]]
+                      for b in range(B)], dtype=np.int64)
+    cos_sin = ops.rope_cos_sin_cache(int(wl.lengths.max()) + 1)
+    qs = 0.02
+    step = ops.DecodeStepEx(B, od.KV_FP8, wl.max_blocks, q_len=qn, q_dtype=ops.Q_FP8, q_scale=qs)
+    out = step(q, k, v, torch.as_tensor(pos, device="cuda"), cos_sin, wl.q_norm_w, wl.k_norm_w,
+               wl.cache, torch.as_tensor(slots, device="cuda"), wl.kv_scale, wl.block_table,
+               wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    got = gu.bf16_host(out)
+    codes = step.q_out.cpu().numpy()
+    qh, kh, vh = gu.bf16_host(q), gu.bf16_host(k), gu.bf16_host(v)
+    qw, kw = gu.bf16_host(wl.q_norm_w), gu.bf16_host(wl.k_norm_w)
+    for b in range(B):
+        for t in range(qn):
+            qo, _, _ = od.prologue_token(qh[b, t], kh[b, t], vh[b, t], int(pos[b, t]), qw, kw)
+            mine = od.decode_kv(od.encode_kv(qo, od.KV_FP8, qs), od.KV_FP8, 1.0)
+            gpu = od.decode_kv(codes[b, t], od.KV_FP8, 1.0)
+            assert np.all(np.abs(gpu - mine) <= nx.e4m3_step(np.maximum(np.abs(gpu), np.abs(mine))))
+    qvals = od.decode_kv(codes, od.KV_FP8, qs)
+    for b in range(B):
+        gu.compare(got[b], _oracle_mt(wl, qvals, b), gu.TOL_FP8_MAX, None, label="step seq %d" % b)

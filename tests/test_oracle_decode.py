@@ -212,3 +212,37 @@ def test_multi_token_step_writes_every_new_token_and_is_the_single_step_at_one(r
                             lengths, [s[0] for s in lslots], 0)
     assert np.array_equal(o1[:, 0], o2) and np.array_equal(q1[:, 0], q2)
     assert np.allclose(out[:, -1], o2, rtol=0, atol=1e-12)
+
+
+
+def test_fp8_query_step_quantises_q_with_the_cache_encoder(rng):
+    """With an E4M3 q the step stores code(q / q_scale) and attends with
+    code * q_scale; a q_scale that makes q exact on the E4M3 grid gives the
+    BF16-q result of the same values."""
+    lengths = [70, 5]
+    qn = 2
+    bt = np.array([[0, 1], [2, 0]])
+    cache = od.encode_kv(rng.standard_normal((3, 2, 8, 64, 128)) * 0.5, od.KV_FP8, 0.01)
+    q = rng.standard_normal((2, qn, 64, 128))
+    k = rng.standard_normal((2, qn, 8, 128))
+    v = rng.standard_normal((2, qn, 8, 128))
+    w = np.ones(128)
+    pos = [[L - qn + t for t in range(qn)] for L in lengths]
+    slots = [[bt[b, p // 64] * 64 + p % 64 for p in pos[b]] for b in range(2)]
+    c1 = cache.copy()
+    qs = 0.004
+    q_used, out = od.decode_step_mt(q, k, v, pos, w, w, c1, bt, lengths, slots, od.KV_FP8,
+                                    (0.01, 0.01), q_scale=qs)
+    for b in range(2):
+        for t in range(qn):
+            qo, _, _ = od.prologue_token(q[b, t], k[b, t], v[b, t], pos[b][t], w, w)
+            codes = od.encode_kv(qo, od.KV_FP8, qs)
+            assert np.array_equal(q_used[b, t], od.decode_kv(codes, od.KV_FP8, qs))
+    # attention is decode_attention_mt of those values
+    for b in range(2):
+        want = od.decode_attention_mt(q_used[b], c1, bt[b], lengths[b], od.KV_FP8, 0.01, 0.01)
+        assert np.array_equal(out[b], want)
+    # a q already on the E4M3 grid (scaled by a power of two) is stored exactly
+    grid = od.decode_kv(od.encode_kv(rng.standard_normal((64, 128)), od.KV_FP8, 1.0), od.KV_FP8, 1.0)
+    back = od.decode_kv(od.encode_kv(grid * 0.25, od.KV_FP8, 0.25), od.KV_FP8, 0.25)
+    assert np.array_equal(back, grid * 0.25)
