@@ -444,16 +444,23 @@ def _describe(wl):
 def multi_token_times(ops, wl, stream, reps=200):
     """Multi-token decode on the same batch: the attention with the merge fused
     in for q_len = 2 and 4 new tokens per sequence (the cache and lengths of
-    the workload, random BF16 q), CUDA events over ``reps`` launches.  Bytes
+    the workload, random BF16 q), and on an FP8 cache also with an E4M3 q
+    (q_len 1, 2, 4; q quantised with scale max|q|/448 as input synthesis),
+    CUDA events over ``reps`` launches.  Bytes
     are the KV bytes plus q_len times the Q + O bytes; flops 4 * 64 * 128 per
     query token and key."""
     import torch
     out = {}
     peak_gbs, _ = _load_peaks()
-    for qn in (2, 4):
+    runs = [(qn, ops.Q_BF16) for qn in (2, 4)]
+    if wl.kv_dtype == 1:                       # an FP8 cache also takes an E4M3 q
+        runs += [(qn, ops.Q_FP8) for qn in (1, 2, 4)]
+    for qn, qd in runs:
         g = torch.Generator(device="cuda").manual_seed(qn)
-        q = torch.randn((wl.batch, qn, 64, 128), generator=g, device="cuda").to(torch.bfloat16)
-        step = ops.DecodeStepMT(wl.batch, qn, wl.kv_dtype, wl.max_blocks)
+        q = torch.randn((wl.batch, qn, 64, 128), generator=g, device="cuda")
+        qs = float(q.abs().max()) / 448.0
+        q = (q / qs).to(torch.float8_e4m3fn).view(torch.uint8) if qd == ops.Q_FP8 else q.to(torch.bfloat16)
+        step = ops.DecodeStepEx(wl.batch, wl.kv_dtype, wl.max_blocks, q_len=qn, q_dtype=qd, q_scale=qs)
         step.plan_step(wl.seq_lens)
         for _ in range(5):
             step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
@@ -469,7 +476,8 @@ def multi_token_times(ops, wl, stream, reps=200):
         us = a.elapsed_time(b) / reps * 1e3
         nbytes = wl.kv_bytes() + qn * wl.qo_bytes()
         flops = 4.0 * 64 * 128 * qn * wl.tokens
-        out["q_len=%d" % qn] = {"attn_us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
+        out["q_len=%d%s" % (qn, ", E4M3 q" if qd == ops.Q_FP8 else "")] = {
+                                "attn_us": round(us, 2), "GB/s": round(nbytes / us / 1e3, 1),
                                 "frac": round(nbytes / us / 1e3 / peak_gbs, 4),
                                 "TFLOP/s": round(flops / us / 1e6, 2)}
     return out
