@@ -192,6 +192,8 @@ int hpc_rope_cos_sin_cache(double theta, int32_t max_pos, float* cos_sin, cudaSt
  *   q_out         (device) bf16 [batch, 64, 128]; may alias q
  *   status        (device) int32; BAD_POSITION skips the sequence entirely,
  *                 BAD_SLOT skips its cache write
+ * The batch is a list of independent tokens: for multi-token decode and
+ * prefill pass every new token with its own position and slot.
  * Errors: HPC_ERR_INVALID_ARG for a null required pointer, batch < 0,
  * max_pos <= 0 or num_blocks <= 0; HPC_ERR_UNSUPPORTED for an unknown dtype. */
 int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
@@ -439,6 +441,45 @@ int hpc_decode_attn_merge_ex(const void* q, const void* kv_cache, int32_t kv_dty
                              int32_t* status, cudaStream_t stream);
 int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
                  int32_t batch, const hpc_attn_options* opts, void* out, cudaStream_t stream);
+
+/* Prefill and mixed prefill + decode batches through the same paged cache.
+ * Sequence b has q_len_b = query_start[b+1] - query_start[b] >= 0 new tokens
+ * (a prompt chunk, a whole prompt, or one decode token), packed in
+ * [query_start[b], query_start[b+1]) of q and out, and seq_lens[b] >= q_len_b
+ * tokens in all, the new ones included.  New token i of sequence b sits at
+ * position seq_lens[b] - q_len_b + i and attends to the keys at positions
+ * 0 .. seq_lens[b] - q_len_b + i: its history and the new tokens up to
+ * itself.  Write the new tokens' K and V first (hpc_rope_norm_kvwrite on the
+ * packed tokens with their own positions and slots).  Decode sequences may
+ * also go through hpc_decode_attn_* (split-KV, better for long histories);
+ * both read the same cache.  BF16 caches only so far.
+ * hpc_prefill_plan: unit_ptr[b] = first work unit of sequence b (8 kv heads
+ * x ceil(q_len_b / 16) token blocks), unit_ptr[batch] = all units; zeroes
+ * counters.  hpc_prefill_attn deals the units to a persistent grid through
+ * counters[0] and leaves both counters at zero (the plan can run again;
+ * launches that share one plan must not overlap).
+ * Source: page "[vllm] Introducing the HPC-Ops attention backend" (prefill,
+ * decode and mixed batches); page "vLLM and Tencent Hunyuan upstream two HPC
+ * backends for NVIDIA Hopper", intro of "Two new HPC backends in the vLLM
+ * ecosystem" (heads, head_dim, paged cache).
+ *   query_start  (device) int32 [batch + 1], nondecreasing
+ *   unit_ptr     (device) int32 [batch + 1];  counters (device) int32 [2]
+ *   q            (device) bf16 [query_start[batch], 64, 128]
+ *   out          (device) [query_start[batch], 64, 128] of out_dtype, written
+ *                for every new token of a valid sequence
+ *   status       BAD_SEQ_LEN for q_len_b < 0, q_len_b > seq_lens[b] or
+ *                seq_lens[b] > max_blocks * 64 (the sequence is skipped);
+ *                BAD_BLOCK for a block id out of range (the tile is skipped)
+ * Errors: HPC_ERR_INVALID_ARG for null pointers or bad sizes;
+ * HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or num_blocks >
+ * HPC_MAX_NUM_BLOCKS. */
+int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32_t* unit_ptr,
+                     int32_t* counters, int32_t* status, cudaStream_t stream);
+int hpc_prefill_attn(const void* q, const int32_t* query_start, const void* kv_cache,
+                     int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
+                     const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                     int32_t batch, const int32_t* unit_ptr, int32_t* counters, void* out,
+                     int32_t out_dtype, float sm_scale, int32_t* status, cudaStream_t stream);
 
 /* Self-test of the bounded pipeline wait (no counterpart on the pages).
  * Every wait of the attention pipeline gives up after a time limit (1 s),

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(
     uint8_t* __restrict__ kv_cache, int32_t num_blocks, const int64_t* __restrict__ slot_mapping,
     const float* __restrict__ kv_scale, void* q_out, float q_scale,
     int32_t* __restrict__ status) {
-  prologue_heads<kFp8, kQ8>(blockIdx.y, blockIdx.x, q, k, v, positions, cos_sin, max_pos, q_w, k_w, eps,
+  prologue_heads<kFp8, kQ8>(blockIdx.x, blockIdx.y, q, k, v, positions, cos_sin, max_pos, q_w, k_w, eps,
                        kv_cache, num_blocks, slot_mapping, kv_scale, q_out, q_scale, status);
 }
 
@@ -75,9 +75,8 @@ extern "C" int hpc_rope_norm_kvwrite_ex(const void* q, const void* k, const void
   if (kv_dtype == HPC_KV_FP8_E4M3) HPC_CHECK_ARG(kv_scale != nullptr);
   if (q_dtype != HPC_Q_BF16 && q_dtype != HPC_Q_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
   if (q_dtype == HPC_Q_FP8_E4M3) HPC_CHECK_ARG(q_scale > 0.0f && q_scale < 3.0e38f);
-  if (batch > 65535) return HPC_ERR_UNSUPPORTED;
   if (batch == 0) return HPC_OK;
-  const dim3 grid(hpc::kGroup + 1, batch);
+  const dim3 grid(batch, hpc::kGroup + 1);   // tokens on x: any token count of a prefill
   auto* qp = static_cast<const uint16_t*>(q);
   auto* kp = static_cast<const uint16_t*>(k);
   auto* vp = static_cast<const uint16_t*>(v);

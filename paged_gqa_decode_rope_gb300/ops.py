@@ -600,3 +600,45 @@ class DecodeStepEx:
                              self.q_scale)
         self.plan_step(seq_lens)
         return self.attend(self.q_out, kv_cache, kv_scale, block_table, seq_lens)
+
+
+
+# ------------------------------------------------------------ prefill / mixed batches
+
+class PrefillAttention:
+    """Attention of packed new tokens (prompt chunks, prompts or decode
+    tokens) over the paged cache: sequence b owns rows query_start[b] ..
+    query_start[b+1]-1 of q and out and sees its history plus its new tokens
+    up to each one.  The unit plan and counters are allocated once."""
+
+    def __init__(self, batch, device="cuda", out_dtype=OUT_BF16):
+        self.batch, self.out_dtype = batch, out_dtype
+        self.unit_ptr = torch.zeros(batch + 1, dtype=torch.int32, device=device)
+        self.counters = torch.zeros(2, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def plan(self, query_start):
+        _want(query_start, "query_start", (torch.int32,), (self.batch + 1,))
+        check("hpc_prefill_plan", _lib.lib().hpc_prefill_plan(
+            _p(query_start), self.batch, _p(self.unit_ptr), _p(self.counters), _p(self.status),
+            _stream()))
+
+    def __call__(self, q, query_start, kv_cache, kv_dtype, kv_scale, block_table, seq_lens, out,
+                 sm_scale=None):
+        B = self.batch
+        T = q.shape[0]
+        _want(q, "q", _BF16, (T, HQ, D))
+        _want(query_start, "query_start", (torch.int32,), (B + 1,))
+        _want(kv_cache, "kv_cache", _cache_dtypes(kv_dtype))
+        _want(block_table, "block_table", (torch.int32,))
+        if block_table.dim() != 2 or block_table.shape[0] != B:
+            raise ValueError("block_table must be [batch, max_blocks]")
+        _want(seq_lens, "seq_lens", (torch.int32,), (B,))
+        _want(out, "out", (_OUT_TORCH[self.out_dtype],), (T, HQ, D))
+        scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+        check("hpc_prefill_attn", _lib.lib().hpc_prefill_attn(
+            _p(q), _p(query_start), _p(kv_cache), kv_dtype,
+            _p(kv_scale if kv_dtype == KV_FP8 else None), kv_cache.shape[0], _p(block_table),
+            block_table.shape[1], _p(seq_lens), B, _p(self.unit_ptr), _p(self.counters), _p(out),
+            int(self.out_dtype), scale, _p(self.status), _stream()))
+        return out

@@ -169,6 +169,35 @@ def check_attention_mt_sdpa(mt_fn, rng):
             assert np.allclose(out[t], ref, rtol=1e-11, atol=1e-12), (qn, L, t)
 
 
+def check_attention_prefill_sdpa(mt_fn, rng):
+    """Prompt-sized blocks of new tokens (a whole prompt, L = q_len, and a
+    chunk after a history) equal torch SDPA with the causal mask of their
+    positions; for a whole prompt that is SDPA's own is_causal."""
+    from oracle import decode as od
+    for qn, L in ((70, 70), (45, 200)):
+        n_pages = -(-L // 64)
+        Kc = rng.standard_normal((n_pages + 1, 8, 64, D))
+        Vc = rng.standard_normal((n_pages + 1, 8, 64, D))
+        cache = np.stack([od.encode_kv(Kc, 0), od.encode_kv(Vc, 0)], axis=1)
+        bt = rng.permutation(n_pages + 1)[:n_pages]
+        q = rng.standard_normal((qn, 64, D)) * 0.5
+        out = mt_fn(q, cache, bt, L, 0)
+        K = np.concatenate([od.decode_kv(cache[pg, 0], 0) for pg in bt], axis=1)[:, :L]
+        V = np.concatenate([od.decode_kv(cache[pg, 1], 0) for pg in bt], axis=1)[:, :L]
+        qt = torch.from_numpy(q.transpose(1, 0, 2))[None]            # [1, 64, q_len, 128]
+        if qn == L:
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, torch.from_numpy(K)[None], torch.from_numpy(V)[None], is_causal=True,
+                enable_gqa=True)
+        else:
+            mask = np.arange(L)[None, :] <= (L - qn + np.arange(qn))[:, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+                attn_mask=torch.from_numpy(mask), enable_gqa=True)
+        ref = ref[0].numpy().transpose(1, 0, 2)                        # [q_len, 64, 128]
+        assert np.allclose(out, ref, rtol=1e-11, atol=1e-12), (qn, L)
+
+
 def check_attention_mt_causal(mt_fn, single_fn, rng):
     """Changing the value of the last new token changes only the last query's
     output; with q_len = 1 the multi-token form is the single-token one."""

@@ -1,0 +1,130 @@
+"""Prefill and mixed prefill + decode batches through the same paged cache,
+against the float64 oracle (each new token sees its history and the new
+tokens up to itself).  The cache holds every token of every sequence (the new
+ones included) and NaN elsewhere, so any read past a sequence's length shows
+up as a non-finite output."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import decode as od
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _batch(lengths, q_lens, seed):
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=seed, lengths=lengths, kv_dtype=0, include_new_token=True)
+    qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    q = torch.randn((int(qs[-1]), 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+    return wl, q, torch.as_tensor(qs, device="cuda"), qs
+
+
+def _check(wl, q, qs, out, seqs=None, heads=None, tol=(gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN)):
+    got = out.float().cpu().numpy().astype(np.float64)
+    qh = gu.bf16_host(q)
+    for b in (range(wl.batch) if seqs is None else seqs):
+        a, e = int(qs[b]), int(qs[b + 1])
+        if e == a:
+            continue
+        L = int(wl.lengths[b])
+        sub, row = gu.seq_view(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
+        want = od.decode_attention_mt(qh[a:e], sub, row, L, wl.kv_dtype, heads=heads)
+        gu.compare(got[a:e], want, *tol, label="seq %d (L=%d, q_len=%d)" % (b, L, e - a))
+
+
+def test_prefill_prompts_and_chunks():
+    """Whole prompts (q_len = L, tile and block edges) and chunks after a
+    history, one launch; a second launch of the same plan gives the same bits."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [1, 16, 17, 64, 65, 130, 300, 1000, 2200]
+    q_lens = [1, 16, 17, 64, 65, 130, 37, 200, 33]
+    wl, q, qst, qs = _batch(lengths, q_lens, 5)
+    pf = ops.PrefillAttention(wl.batch)
+    pf.plan(qst)
+    out = torch.empty_like(q)
+    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    again = pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, torch.empty_like(q))
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) == 0
+    assert int(pf.counters.abs().sum().item()) == 0
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    assert torch.isfinite(out.float()).all()
+    _check(wl, q, qs, out)
+
+
+def test_mixed_batch_prefill_and_decode_kernels_on_one_cache():
+    """A mixed batch: decode sequences (one new token, long histories) through
+    the split-KV decode path, prompt chunks through the prefill kernel; both
+    over the one cache, both against the oracle; the prefill kernel run on the
+    decode sequences too gives the decode path's result."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    lengths = [20000, 4096, 513, 700, 90, 3000]
+    q_lens = [1, 1, 1, 120, 90, 64]
+    wl, q, qst, qs = _batch(lengths, q_lens, 8)
+    out = torch.empty_like(q)
+    pf = ops.PrefillAttention(wl.batch)
+    pf.plan(qst)
+    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) == 0
+    _check(wl, q, qs, out, seqs=[1, 2, 3, 4, 5])
+    _check(wl, q, qs, out, seqs=[0], heads=list(range(0, 64, 9)))
+    # the decode sequences through the decode path (split-KV), same cache
+    dec = [0, 1, 2]
+    sub = Workload("custom", seed=8, lengths=[lengths[i] for i in dec], kv_dtype=0,
+                   include_new_token=True)
+    step = ops.DecodeStep(len(dec), 0, wl.max_blocks)
+    bt = wl.block_table[dec].contiguous()
+    sl = wl.seq_lens[dec].contiguous()
+    qd = torch.stack([q[int(qs[b])] for b in dec])
+    step.plan_step(sl)
+    od_out = step.attend(qd, wl.cache, wl.kv_scale, bt, sl)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    d = (od_out.float() - torch.stack([out[int(qs[b])] for b in dec]).float()).abs()
+    assert float(d.max()) <= 4e-3 and float(d.mean()) <= 2e-4
+
+
+def test_prefill_output_types_and_empty_sequences():
+    """FP32 output matches the oracle; FP16 output is it rounded; sequences
+    without new tokens take no unit and write nothing."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [100, 50, 600, 70]
+    q_lens = [20, 0, 48, 0]
+    wl, q, qst, qs = _batch(lengths, q_lens, 11)
+    outs = {}
+    for od_ in (ops.OUT_FP32, ops.OUT_FP16):
+        pf = ops.PrefillAttention(wl.batch, out_dtype=od_)
+        pf.plan(qst)
+        o = torch.full((q.shape[0], 64, 128), float("nan"), device="cuda",
+                       dtype=torch.float32 if od_ == ops.OUT_FP32 else torch.float16)
+        outs[od_] = pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, o)
+        torch.cuda.synchronize()
+        assert int(pf.status.item()) == 0
+        assert int(pf.unit_ptr[-1].item()) == 8 * (2 + 3)
+    assert torch.equal(outs[ops.OUT_FP16], outs[ops.OUT_FP32].to(torch.float16))
+    _check(wl, q, qs, outs[ops.OUT_FP32])
+
+
+def test_prefill_bad_lengths_set_status_and_skip():
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [64, 100]
+    q_lens = [80, 10]                         # sequence 0 has more new tokens than tokens
+    wl, q, qst, qs = _batch(lengths, q_lens, 13)
+    pf = ops.PrefillAttention(wl.batch)
+    pf.plan(qst)
+    out = torch.zeros_like(q)
+    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) & 4          # HPC_STATUS_BAD_SEQ_LEN
+    assert not out[:80].float().abs().any()   # skipped
+    _check(wl, q, qs, out, seqs=[1])

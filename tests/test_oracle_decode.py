@@ -69,6 +69,10 @@ def test_multi_token_attention_matches_masked_sdpa(rng):
     pins.check_attention_mt_sdpa(od.decode_attention_mt, rng)
 
 
+def test_prefill_blocks_match_causal_sdpa(rng):
+    pins.check_attention_prefill_sdpa(od.decode_attention_mt, rng)
+
+
 def test_multi_token_attention_is_causal(rng):
     pins.check_attention_mt_causal(od.decode_attention_mt, od.decode_attention, rng)
 
