@@ -382,6 +382,7 @@ def run_ours(args):
     if rank == 0 and not args.no_static:
         sched = schedule_comparison(ops, wl, stream)
     mt = multi_token_times(ops, wl, stream) if rank == 0 and not args.no_multi_token else None
+    pre = prefill_times(ops, stream) if rank == 0 and not args.no_multi_token else None
 
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -426,6 +427,7 @@ def run_ours(args):
         "clocks": clocks,
         "schedules": sched,
         "multi_token": mt,
+        "prefill": pre,
     }
     print(json.dumps(line))
 
@@ -439,6 +441,58 @@ def _describe(wl):
             parts.append("%dx%d" % (int((L == x).sum()), x))
         return " + ".join(parts) + " tokens, 64q/8kv, d128, %s KV, 64-token pages" % kv
     return "%d seqs, %d tokens, 64q/8kv, d128, %s KV, 64-token pages" % (wl.batch, wl.tokens, kv)
+
+
+def prefill_times(ops, stream, reps=10):
+    """Prefill attention (BF16 cache): 4 whole prompts of 4096 tokens, and 8
+    chunks of 512 new tokens after 7680-token histories; CUDA events over
+    ``reps`` launches.  Flops 4 * 64 * 128 per query token and visible key
+    (the causal triangle counted exactly)."""
+    import torch
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    res = {}
+    peaks = _load_peak_tflops()
+    for name, lengths, q_lens in (("4 prompts x 4096", [4096] * 4, [4096] * 4),
+                                  ("8 chunks of 512 after 7680", [8192] * 8, [512] * 8)):
+        wl = Workload("custom", seed=21, lengths=lengths, kv_dtype=0, include_new_token=True)
+        qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+        g = torch.Generator(device="cuda").manual_seed(1)
+        q = torch.randn((int(qs[-1]), 64, 128), generator=g, device="cuda").to(torch.bfloat16)
+        qst = torch.as_tensor(qs, device="cuda")
+        out = torch.empty_like(q)
+        pf = ops.PrefillAttention(wl.batch)
+        pf.plan(qst)
+        for _ in range(2):
+            pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if int(pf.status.item()) != 0:
+            raise RuntimeError("device status %d in the prefill run" % int(pf.status.item()))
+        us = a.elapsed_time(b) / reps * 1e3
+        keys = sum(sum(L - n + i + 1 for i in range(n)) for L, n in zip(lengths, q_lens))
+        flops = 4.0 * 64 * 128 * keys
+        tf = flops / us / 1e6
+        res[name] = {"us": round(us, 1), "TFLOP/s": round(tf, 1),
+                     "frac_of_bf16_peak": round(tf / peaks, 4) if peaks else None}
+    return res
+
+
+def _load_peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("bf16_tflops", "bf16_tflops_burst"):
+            if k in d:
+                return float(d[k])
+    except (OSError, ValueError):
+        pass
+    return None
 
 
 def multi_token_times(ops, wl, stream, reps=200):
