@@ -464,15 +464,15 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  * ecosystem" (heads, head_dim, paged cache).
  *   query_start  (device) int32 [batch + 1], nondecreasing
  *   unit_ptr     (device) int32 [batch + 1];  counters (device) int32 [2]
- *   q            (device) bf16 [query_start[batch], 64, 128]
- *   out          (device) [query_start[batch], 64, 128] of out_dtype, written
- *                for every new token of a valid sequence
+ *   q            (device) bf16 [query_start[batch], 64, 128], 16-byte aligned
+ *   out          (device) [query_start[batch], 64, 128] of out_dtype, 16-byte
+ *                aligned, written for every new token of a valid sequence
  *   status       BAD_SEQ_LEN for q_len_b < 0, q_len_b > seq_lens[b] or
  *                seq_lens[b] > max_blocks * 64 (the sequence is skipped);
  *                BAD_BLOCK for a block id out of range (the tile is skipped)
- * Errors: HPC_ERR_INVALID_ARG for null pointers or bad sizes;
- * HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or num_blocks >
- * HPC_MAX_NUM_BLOCKS. */
+ * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes or misaligned q,
+ * out or kv_cache; HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or
+ * num_blocks > HPC_MAX_NUM_BLOCKS. */
 int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32_t* unit_ptr,
                      int32_t* counters, int32_t* status, cudaStream_t stream);
 int hpc_prefill_attn(const void* q, const int32_t* query_start, const void* kv_cache,

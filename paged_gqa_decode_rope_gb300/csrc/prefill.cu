@@ -28,6 +28,7 @@
 //  * Every wait is bounded (kWaitLimitNs), as in the decode kernel.
 #include "attn_kernel.cuh"
 #include "plan_body.cuh"
+#include "prefill_tc.cuh"
 
 namespace hpc {
 namespace {
@@ -414,18 +415,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(
   }
 }
 
-cudaError_t prefill_smem_optin() {
+template <typename Kernel>
+cudaError_t smem_optin_once(Kernel kernel, int bytes, bool (&done)[64]) {
   static std::mutex mu;
-  static bool done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kPfSmemBytes);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
+}
+
+cudaError_t prefill_smem_optin() {
+  static bool done[64] = {};
+  return smem_optin_once(prefill_attn_kernel, kPfSmemBytes, done);
+}
+
+cudaError_t prefill_tc_smem_optin() {
+  static bool done[64] = {};
+  return smem_optin_once(prefill_tc_kernel, tc::kSmemBytes, done);
 }
 
 }  // namespace
@@ -453,7 +463,7 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
   HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
   if (out_dtype != HPC_OUT_BF16 && out_dtype != HPC_OUT_FP16 && out_dtype != HPC_OUT_FP32)
     return HPC_ERR_UNSUPPORTED;
-  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(out) & (out_dtype == HPC_OUT_FP32 ? 7 : 3)) == 0);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0);
   (void)kv_scale;
   if (kv_dtype != HPC_KV_BF16) return HPC_ERR_UNSUPPORTED;   // an E4M3 cache: not yet
   if (batch > HPC_MAX_BATCH || num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
@@ -461,7 +471,6 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
   if (batch == 0) return HPC_OK;
   auto encode = hpc::tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
-  if (hpc::prefill_smem_optin() != cudaSuccess) return HPC_ERR_CUDA;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hpc::kD),
                               static_cast<cuuint64_t>(num_blocks) * 2 * hpc::kHkv * hpc::kPage};
@@ -477,7 +486,8 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
-  hpc::prefill_attn_kernel<<<sms, hpc::kPfThreads, hpc::kPfSmemBytes, stream>>>(
+  if (hpc::prefill_tc_smem_optin() != cudaSuccess) return HPC_ERR_CUDA;
+  hpc::prefill_tc_kernel<<<sms, hpc::tc::kThreads, hpc::tc::kSmemBytes, stream>>>(
       map, static_cast<const uint16_t*>(q), query_start, seq_lens, batch, block_table, max_blocks,
       num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
   return HPC_LAUNCH_STATUS();
