@@ -454,7 +454,7 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  * also go through hpc_decode_attn_* (split-KV, better for long histories);
  * both read the same cache.  BF16 caches only so far.
  * hpc_prefill_plan: unit_ptr[b] = first work unit of sequence b (8 kv heads
- * x ceil(q_len_b / 16) token blocks), unit_ptr[batch] = all units; zeroes
+ * x ceil(q_len_b / 32) token blocks), unit_ptr[batch] = all units; zeroes
  * counters.  hpc_prefill_attn deals the units to a persistent grid through
  * counters[0] and leaves both counters at zero (the plan can run again;
  * launches that share one plan must not overlap).
@@ -470,8 +470,9 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  *   status       BAD_SEQ_LEN for q_len_b < 0, q_len_b > seq_lens[b] or
  *                seq_lens[b] > max_blocks * 64 (the sequence is skipped);
  *                BAD_BLOCK for a block id out of range (the tile is skipped)
- * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes or misaligned q,
- * out or kv_cache; HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or
+ * sm_scale must be positive (the softmax takes row maxima of unscaled scores).
+ * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes, sm_scale <= 0 or
+ * misaligned q, out or kv_cache; HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or
  * num_blocks > HPC_MAX_NUM_BLOCKS. */
 int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32_t* unit_ptr,
                      int32_t* counters, int32_t* status, cudaStream_t stream);

@@ -1,24 +1,30 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05): the work
-// unit of prefill.cu (sequence, kv_head, 16 new tokens) as one 128-row tile,
-// row r = 8 * token + query head of the group.
+// Prefill attention on the 5th-generation tensor cores (tcgen05).
 //
-// Source: as prefill.cu (prefill, decode and mixed batches over the paged
-// cache; 64 query heads, 8 KV heads, head_dim 128).
+// Source: page "[vllm] Introducing the HPC-Ops attention backend" (the
+// backend serves prefill, decode and mixed batches); page "vLLM and Tencent
+// Hunyuan upstream two HPC backends for NVIDIA Hopper", intro of "Two new HPC
+// backends in the vLLM ecosystem" (64 query heads, 8 KV heads, head_dim 128,
+// paged KV in 64-token blocks).  Each new token attends to its history and
+// the new tokens up to itself.
 //
-// Per unit and 64-key tile (warp roles):
-//  * producer warp: claims units, hands them on through a ring, and streams
-//    the visible K and V pages by TMA into a 3-stage ring (128-byte swizzle);
-//  * MMA warp (one elected lane issues): S = Q K^T into one of two TMEM
-//    buffers (M 128, N 64 keys, K 128 as 8 K-major steps), then, once the
-//    softmax has written P, O += P V (A = P K-major, B = V MN-major, two
-//    N = 64 halves of d), O resident in TMEM for the whole unit;
-//  * softmax warpgroup (4 warps, thread = row): loads its S row from TMEM,
-//    masks by position, keeps the running maximum until it grows by more
-//    than 2^8 (only then rescales its O row in TMEM), writes P as BF16 into
-//    shared memory, zeroes V rows past the sequence length, and at the end
-//    divides its O row by the row sum and stores it.
-// Every mbarrier wait is bounded; on a timeout the CTA winds down, and the
-// TMEM it holds is freed before it exits.
+// A work unit is (sequence, kv_head, 32 new tokens): two 128-row tiles
+// ("lanes"), row r = 8 * token + query head of the group, tokens 0..15 in
+// lane 0 and 16..31 in lane 1.  Both lanes read the same K/V pages, which one
+// producer warp streams by TMA into a ring of stages (64-row x 128-byte
+// boxes, 128-byte swizzle).  Per 64-key tile and lane:
+//  * S = Q K^T (M 128, N 64, K 128: eight K-major steps, both operands in
+//    shared memory) into one of the lane's two TMEM score buffers;
+//  * its softmax warpgroup (thread = row) loads the row of S, masks it by
+//    position, keeps the running maximum until it grows by more than 2^8
+//    (only then rescaling the row of O in TMEM), and writes P as BF16 pairs
+//    back over the scores;
+//  * O += P V (M 128, N 128 = d, K 64: four steps, A = P read from TMEM, B =
+//    V MN-major in shared memory), O resident in TMEM for the whole unit.
+// One warp issues every MMA; the two lanes' softmax runs overlap the other
+// lane's products.  V rows past the sequence length (or of a tile whose
+// block id is bad) are zeroed before any P V reads them: the cache may hold
+// NaN there.  Every mbarrier wait is bounded; on a timeout the CTA winds
+// down, lets its copies and products finish, and frees its TMEM.
 #pragma once
 
 #include "common.cuh"
@@ -27,40 +33,44 @@ namespace hpc {
 namespace {
 namespace tc {
 
-constexpr int kThreads = 192;          // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr int kWarpProd = 4;
-constexpr int kWarpMma = 5;
-constexpr int kStages = 3;
+constexpr int kThreads = 320;      // warps 0-3 softmax of lane 0, 4-7 of lane 1, 8 producer, 9 MMA
+constexpr int kWarpProd = 8;
+constexpr int kWarpMma = 9;
+constexpr int kStages = 4;
 constexpr int kBox = 64 * 128;                      // one 64-row x 128-byte TMA box
-constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (128 d)
+constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (d = 128)
 constexpr int kStageBytes = 2 * kPage;              // K page + V page
-constexpr int kOffQ = kStages * kStageBytes;        // Q: 2 halves of d x 128 rows x 128 B
+constexpr int kOffQ = kStages * kStageBytes;        // per lane: 2 halves of d x 128 rows x 128 B
 constexpr int kQBytes = 2 * 128 * 128;
-constexpr int kOffP = kOffQ + kQBytes;              // P: 2 buffers x 128 rows x 64 keys (BF16)
-constexpr int kPBytes = 128 * 128;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-// mbarriers (index of the first of each kind)
-constexpr int kBarFull = 0;        // [3] stage landed (TMA)
-constexpr int kBarEmpty = 3;       // [3] stage consumed (the tile's P V done)
-constexpr int kBarSFull = 6;       // [2] S buffer written (tcgen05.commit)
-constexpr int kBarSFree = 8;       // [2] S buffer read (128 softmax threads)
-constexpr int kBarPFull = 10;      // [2] P buffer written (128 softmax threads)
-constexpr int kBarPFree = 12;      // [2] P buffer read (the P V done)
-constexpr int kBarODone = 14;      // every P V done, in order
-constexpr int kBarOFinal = 15;     // a unit's last P V done
-constexpr int kBarOFree = 16;      // a unit's O read out (128 softmax threads)
-constexpr int kBarQReady = 17;     // a unit's Q written (128 softmax threads)
-constexpr int kBarUnitFull = 18;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 20;  // [2] unit descriptor read (MMA warp + 4 softmax warps)
-constexpr int kBarDrain = 22;      // every tcgen05 op of the MMA warp done (at exit)
-constexpr int kNumBars = 23;
+constexpr int kOffBar = kOffQ + 2 * kQBytes;
+// mbarriers (index of the first of each kind; [l] per lane, [l][i] per lane and buffer)
+constexpr int kBarFull = 0;        // [4] stage landed (TMA)
+constexpr int kBarEmpty = 4;       // [4] stage consumed (the tile's P V products done)
+constexpr int kBarSFull = 8;       // [2][2] scores written
+constexpr int kBarPFull = 12;      // [2][2] P written over the scores (128 softmax threads)
+constexpr int kBarODone = 16;      // [2] each P V of the lane done, in order
+constexpr int kBarOFinal = 18;     // [2] the lane's last P V of a unit done
+constexpr int kBarOFree = 20;      // [2] the lane's O read out (128 softmax threads)
+constexpr int kBarQReady = 22;     // [2] the lane's Q written (128 softmax threads)
+constexpr int kBarUnitFull = 24;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 26;  // [2] unit descriptor read (MMA warp + 8 softmax warps)
+constexpr int kBarDrain = 28;      // every product of the MMA warp done (at exit)
+constexpr int kNumBars = 29;
+constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
-constexpr int kOffOk = kOffRing + 2 * 4 * 4;
+constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;
 constexpr int kOffMisc = kOffOk + kStages * 4;      // [0] abort flag, [1] TMEM address
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;                 // S0 0..63, S1 64..127, O 128..255
-constexpr int kTokens = 16;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;    // + slack for the 1024-byte alignment
+constexpr uint32_t kTmemCols = 512;                 // lane l: S 256l + {0, 64}, O 256l + 128
+constexpr int kLaneTokens = 16;
+constexpr int kUnitTokens = 32;
 constexpr float kRescaleLog2 = 8.0f;                // rescale O only when the max grows by > 2^8
+
+// tiles of a lane of a unit: 0 without new tokens, else those its last token sees
+__device__ __forceinline__ int lane_tiles(int qlen, int L, int first_token) {
+  const int cnt = min(kLaneTokens, qlen - first_token);
+  return cnt > 0 ? (L - qlen + first_token + cnt - 1) / hpc::kPage + 1 : 0;
+}
 
 }  // namespace tc
 
@@ -106,18 +116,18 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(tc::kBarFull + s), 1);
       mbar_init(bar(tc::kBarEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(bar(tc::kBarSFull + i), 1);
-      mbar_init(bar(tc::kBarSFree + i), 128);
       mbar_init(bar(tc::kBarPFull + i), 128);
-      mbar_init(bar(tc::kBarPFree + i), 1);
-      mbar_init(bar(tc::kBarUnitFull + i), 1);
-      mbar_init(bar(tc::kBarUnitEmpty + i), 5);
     }
-    mbar_init(bar(tc::kBarODone), 1);
-    mbar_init(bar(tc::kBarOFinal), 1);
-    mbar_init(bar(tc::kBarOFree), 128);
-    mbar_init(bar(tc::kBarQReady), 128);
+    for (int l = 0; l < 2; ++l) {
+      mbar_init(bar(tc::kBarODone + l), 1);
+      mbar_init(bar(tc::kBarOFinal + l), 1);
+      mbar_init(bar(tc::kBarOFree + l), 128);
+      mbar_init(bar(tc::kBarQReady + l), 128);
+      mbar_init(bar(tc::kBarUnitFull + l), 1);
+      mbar_init(bar(tc::kBarUnitEmpty + l), 9);
+    }
     mbar_init(bar(tc::kBarDrain), 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -137,17 +147,35 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     if (!ok && lane == 0) *abort_flag = 1;
     return ok;
   };
+  // the next unit descriptor (slot u & 1), handed back once read
+  struct Unit {
+    int b, h, pair, nt[2];
+  };
+  auto read_unit = [&](uint32_t u, Unit& d) -> bool {
+    const int r = static_cast<int>(u & 1);
+    if (!wait_all(tc::kBarUnitFull + r, (u >> 1) & 1)) return false;
+    const volatile int* slot = ring + r * tc::kRingInts;
+    d.b = slot[0];
+    d.h = slot[1];
+    d.pair = slot[2];
+    d.nt[0] = slot[3];
+    d.nt[1] = slot[4];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(tc::kBarUnitEmpty + r));
+    return true;
+  };
 
   if (warp == tc::kWarpProd) {
     // ---------------------------------------------------------- producer
-    const uint64_t policy = l2_evict_first_policy();
-    uint32_t g = 0, n_pushed = 0;   // tiles issued, units handed on
+    // every pair of new tokens of a sequence reads the KV head's pages again
+    const uint64_t policy = l2_evict_last_policy();
+    uint32_t g = 0, n_pushed = 0;   // stream tiles issued, units handed on
     bool alive = true;
     while (alive) {
       int u = 0;
       if (lane == 0) u = atomicAdd(&counters[0], 1);
       u = __shfl_sync(0xffffffffu, u, 0);
-      int b = -1, h = 0, qb = 0, ntiles = 0;
+      int b = -1, h = 0, pair = 0, nt0 = 0, nt1 = 0;
       if (u < total_units) {
         int lo = 0, hi = batch;   // the last b with unit_ptr[b] <= u (32-ary search)
         while (hi - lo > 1) {
@@ -161,17 +189,18 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         b = lo;
         const int j = u - unit_ptr[b];
         const int qs = query_start[b], qlen = query_start[b + 1] - qs, L = seq_lens[b];
-        const int nqb = (qlen + tc::kTokens - 1) / tc::kTokens;
+        const int npair = (qlen + tc::kUnitTokens - 1) / tc::kUnitTokens;
         h = j % kHkv;
-        qb = nqb - 1 - j / kHkv;   // the blocks with the most keys first
-        if (qlen < 1 || L < qlen || L > max_blocks * kPage || qb < 0) {
+        pair = npair - 1 - j / kHkv;   // the pairs with the most keys first
+        if (qlen < 1 || L < qlen || L > max_blocks * kPage || pair < 0) {
           if (lane == 0) atomicOr(status, HPC_STATUS_BAD_SEQ_LEN);
-          ntiles = -1;
+          nt0 = nt1 = -1;
         } else {
-          const int last = min(tc::kTokens, qlen - qb * tc::kTokens) - 1;
-          ntiles = (L - qlen + qb * tc::kTokens + last) / kPage + 1;
+          nt0 = tc::lane_tiles(qlen, L, pair * tc::kUnitTokens);
+          nt1 = tc::lane_tiles(qlen, L, pair * tc::kUnitTokens + tc::kLaneTokens);
         }
       }
+      const int ntiles = max(nt0, nt1);
       int ok = 1;
       if (lane == 0) {
         const int r = static_cast<int>(n_pushed & 1);
@@ -183,11 +212,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           ok = 0;
         }
         if (ok) {
-          volatile int* slot = ring + r * 4;
+          volatile int* slot = ring + r * tc::kRingInts;
           slot[0] = b;
           slot[1] = h;
-          slot[2] = qb;
-          slot[3] = ntiles;
+          slot[2] = pair;
+          slot[3] = nt0;
+          slot[4] = nt1;
           mbar_arrive(bar(tc::kBarUnitFull + r));
         }
       }
@@ -210,7 +240,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
             }
             if (tok) {
               // a bad block id loads block 0 in its place and marks the
-              // stage: the softmax masks its keys and zeroes its V rows
+              // stage: its keys are masked and its V rows zeroed
               const bool good = bid >= 0 && bid < num_blocks;
               if (!good) {
                 atomicOr(status, HPC_STATUS_BAD_BLOCK);
@@ -248,232 +278,263 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
   } else if (warp == tc::kWarpMma) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdescS = umma_idesc_bf16(128, 64, false);
-    constexpr uint32_t kIdescO = umma_idesc_bf16(128, 64, true);
-    uint32_t G = 0, U = 0, V = 0;   // tiles, unit descriptors read, units with tiles
+    constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, true);
+    uint32_t G = 0, U = 0;            // stream tiles, unit descriptors read
+    uint32_t Gl[2] = {0, 0};          // tiles of each lane
+    uint32_t Vl[2] = {0, 0};          // units with tiles, per lane
     bool dead = false;
-    // O (+)= P V of global tile gp; the unit's first overwrites O, its last
-    // also signals the readout
-    auto issue_pv = [&](uint32_t gp, bool first, bool last) {
-      if (dead || !wait_all(tc::kBarPFull + (gp & 1), (gp >> 1) & 1) ||
-          (first && V > 0 && !wait_all(tc::kBarOFree, (V - 1) & 1))) {
-        dead = true;
-        return;
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t pb = base + tc::kOffP + (gp & 1) * tc::kPBytes;
-        const uint32_t vb = base + (gp % tc::kStages) * tc::kStageBytes + tc::kPage;
+    Unit d;
+    // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
+    auto issue_pv = [&](int jj) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {        // 16 keys per step
-#pragma unroll
-          for (int dh = 0; dh < 2; ++dh)        // halves of d, N = 64 each
-            umma_bf16_ss(tmem + 128 + 64 * dh, umma_smem_desc(pb + 32 * ks, 1024, 1024),
-                         umma_smem_desc(vb + dh * tc::kBox + ks * 2048, 1024, 1024), kIdescO,
-                         !(first && ks == 0));
-        }
-        umma_commit(bar(tc::kBarPFree + (gp & 1)));
-        umma_commit(bar(tc::kBarEmpty + gp % tc::kStages));
-        umma_commit(bar(tc::kBarODone));
-        if (last) umma_commit(bar(tc::kBarOFinal));
-      }
-      __syncwarp();
-    };
-    while (!dead) {
-      const int r = static_cast<int>(U & 1);
-      if (!wait_all(tc::kBarUnitFull + r, (U >> 1) & 1)) break;
-      const int b = ring[r * 4 + 0], ntiles = ring[r * 4 + 3];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(tc::kBarUnitEmpty + r));
-      ++U;
-      if (b < 0) break;
-      if (ntiles <= 0) continue;
-      if (!wait_all(tc::kBarQReady, V & 1)) break;
-      const uint32_t n = static_cast<uint32_t>(ntiles);
-      for (uint32_t t = 0; t < n && !dead; ++t) {
-        const uint32_t g = G + t;
-        if (!wait_all(tc::kBarFull + g % tc::kStages, (g / tc::kStages) & 1) ||
-            (g >= 2 && !wait_all(tc::kBarSFree + (g & 1), ((g - 2) >> 1) & 1))) {
+      for (int l = 0; l < 2; ++l) {
+        if (dead) break;
+        if (jj >= d.nt[l]) continue;
+        const uint32_t gl = Gl[l] + jj;
+        if (!wait_all(tc::kBarPFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
+            (jj == 0 && Vl[l] > 0 && !wait_all(tc::kBarOFree + l, (Vl[l] - 1) & 1))) {
           dead = true;
           break;
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t qa = base + tc::kOffQ;
-          const uint32_t kb = base + (g % tc::kStages) * tc::kStageBytes;
+          const uint32_t vb = base + ((G + jj) % tc::kStages) * tc::kStageBytes + tc::kPage;
+          const uint32_t pcol = tmem + 256 * l + 64 * (gl & 1);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {       // 16 of d per step
-            const uint32_t off = (ks >> 2) * tc::kBox * 2 + (ks & 3) * 32;
-            const uint32_t koff = (ks >> 2) * tc::kBox + (ks & 3) * 32;
-            umma_bf16_ss(tmem + 64 * (g & 1), umma_smem_desc(qa + off, 1024, 1024),
-                         umma_smem_desc(kb + koff, 1024, 1024), kIdescS, ks > 0);
-          }
-          umma_commit(bar(tc::kBarSFull + (g & 1)));
+          for (int ks = 0; ks < 4; ++ks)   // 16 keys per step
+            umma_bf16_ts(tmem + 256 * l + 128, pcol + 8 * ks,
+                         umma_smem_desc(vb + ks * 2048, tc::kBox, 1024), kIdescO,
+                         !(jj == 0 && ks == 0));
+          umma_commit(bar(tc::kBarODone + l));
+          if (jj == d.nt[l] - 1) umma_commit(bar(tc::kBarOFinal + l));
         }
         __syncwarp();
-        if (t >= 1) issue_pv(g - 1, t == 1, false);
+      }
+      if (!dead && lane == 0) umma_commit(bar(tc::kBarEmpty + (G + jj) % tc::kStages));
+      __syncwarp();
+    };
+    while (!dead) {
+      if (!read_unit(U, d)) break;
+      ++U;
+      if (d.b < 0) break;
+      const int nt = max(d.nt[0], d.nt[1]);
+      if (nt <= 0) continue;
+      const int L = seq_lens[d.b];
+#pragma unroll
+      for (int l = 0; l < 2; ++l)
+        if (!dead && d.nt[l] > 0 && !wait_all(tc::kBarQReady + l, Vl[l] & 1)) dead = true;
+      for (int j = 0; j < nt && !dead; ++j) {
+        const uint32_t g = G + j;
+        const int s = static_cast<int>(g % tc::kStages);
+        if (!wait_all(tc::kBarFull + s, (g / tc::kStages) & 1)) {
+          dead = true;
+          break;
+        }
+        // V rows past the sequence length or of a bad tile -> zeros, before
+        // any P V of the tile reads them
+        const int keep = stage_ok[s] ? max(0, min(64, L - 64 * j)) : 0;
+        if (keep < 64) {
+          uint8_t* vst = smem + s * tc::kStageBytes + tc::kPage;
+          for (int z = lane; z < (64 - keep) * 16; z += 32) {
+            const int vr = keep + (z >> 4), box = (z >> 3) & 1, c8 = z & 7;
+            *reinterpret_cast<uint4*>(vst + box * tc::kBox + vr * 128 + (c8 << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t kb = base + s * tc::kStageBytes;
+#pragma unroll
+          for (int l = 0; l < 2; ++l) {
+            if (j >= d.nt[l]) continue;
+            const uint32_t gl = Gl[l] + j;
+            const uint32_t qa = base + tc::kOffQ + l * tc::kQBytes;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {   // 16 of d per step
+              const uint32_t off = (ks >> 2) * 2 * tc::kBox + (ks & 3) * 32;
+              const uint32_t koff = (ks >> 2) * tc::kBox + (ks & 3) * 32;
+              umma_bf16_ss(tmem + 256 * l + 64 * (gl & 1), umma_smem_desc(qa + off, 1024, 1024),
+                           umma_smem_desc(kb + koff, 1024, 1024), kIdescS, ks > 0);
+            }
+            umma_commit(bar(tc::kBarSFull + 2 * l + (gl & 1)));
+          }
+        }
+        __syncwarp();
+        if (j >= 1) issue_pv(j - 1);
       }
       if (dead) break;
-      issue_pv(G + n - 1, n == 1, true);
-      G += n;
-      ++V;
+      issue_pv(nt - 1);
+      if (dead) break;
+      G += nt;
+#pragma unroll
+      for (int l = 0; l < 2; ++l) {
+        if (d.nt[l] > 0) {
+          Gl[l] += d.nt[l];
+          ++Vl[l];
+        }
+      }
     }
-    // every tcgen05 op issued here has completed before TMEM is freed
+    // every product issued here has completed before TMEM is freed
     if (lane == 0) {
       umma_commit(bar(tc::kBarDrain));
       mbar_wait(bar(tc::kBarDrain), 0, status);
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------------- softmax warpgroup
-    const int row = threadIdx.x;                       // 0 .. 127: 8 * token + head
+    // ---------------------------------------------------------- softmax warpgroups
+    const int l = warp >> 2;                           // lane (tile) of the unit
+    const int row = threadIdx.x & 127;                 // 8 * token + head
     const int tok = row >> 3, hl = row & 7;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * l;
+    uint8_t* qtile = smem + tc::kOffQ + l * tc::kQBytes;
     const float scale_log2 = sm_scale * 1.4426950408889634f;
-    uint32_t G = 0, U = 0, V = 0;
+    uint32_t G = 0, U = 0, Gl = 0, Vl = 0;
     bool dead = false;
+    Unit d;
     while (!dead) {
-      const int r = static_cast<int>(U & 1);
-      if (!wait_all(tc::kBarUnitFull + r, (U >> 1) & 1)) break;
-      const int b = ring[r * 4 + 0], h = ring[r * 4 + 1], qb = ring[r * 4 + 2],
-                ntiles = ring[r * 4 + 3];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(tc::kBarUnitEmpty + r));
+      if (!read_unit(U, d)) break;
       ++U;
-      if (b < 0) break;
-      if (ntiles <= 0) continue;
-      const int qs = query_start[b], qlen = query_start[b + 1] - qs, L = seq_lens[b];
-      const int i = qb * tc::kTokens + tok;
+      if (d.b < 0) break;
+      const int nt = max(d.nt[0], d.nt[1]);
+      if (nt <= 0) continue;
+      const int ntl = l ? d.nt[1] : d.nt[0];
+      if (ntl <= 0) {
+        G += nt;
+        continue;
+      }
+      const int qs = query_start[d.b], qlen = query_start[d.b + 1] - qs, L = seq_lens[d.b];
+      const int i = d.pair * tc::kUnitTokens + l * tc::kLaneTokens + tok;
       const bool valid = i < qlen;
       const int pos = L - qlen + i;
-      const int head = h * kGroup + hl;
-      // this row of Q into the swizzled tile (zeros past the chunk); the
-      // previous unit's S products, the last readers of the tile, are done
+      const int head = d.h * kGroup + hl;
+      // this row of Q into the lane's swizzled tile (zeros past the chunk);
+      // the lane's previous products, the last readers of the tile, are done
       {
         const uint4* src =
             reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(qs + i) * kHq + head) * kD);
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-          const int half = ch >> 3, c8 = ch & 7;
-          *reinterpret_cast<uint4*>(smem + tc::kOffQ + half * 2 * tc::kBox + row * 128 +
-                                    ((c8 ^ (row & 7)) << 4)) = v;
+        for (int hd = 0; hd < 2; ++hd) {   // halves of d
+          uint4 v[8];
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) v[c8] = make_uint4(0u, 0u, 0u, 0u);
+          if (valid) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) v[c8] = src[8 * hd + c8];
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(qtile + hd * 2 * tc::kBox + row * 128 +
+                                      ((c8 ^ (row & 7)) << 4)) = v[c8];
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(tc::kBarQReady));
-      float m_used = -INFINITY, l = 0.f;
-      const uint32_t n = static_cast<uint32_t>(ntiles);
-      for (uint32_t t = 0; t < n; ++t) {
-        const uint32_t g = G + t;
+      mbar_arrive(bar(tc::kBarQReady + l));
+      float m_used = -INFINITY, lsum = 0.f;
+      for (int j = 0; j < ntl; ++j) {
+        const uint32_t g = G + j, gl = Gl + j;
         const int s = static_cast<int>(g % tc::kStages);
-        if (!wait_all(tc::kBarSFull + (g & 1), (g >> 1) & 1) ||
+        if (!wait_all(tc::kBarSFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
             !wait_all(tc::kBarFull + s, (g / tc::kStages) & 1)) {
           dead = true;
           break;
         }
         tc_fence_after();
         uint32_t sr[64];
-        tmem_ld64(tmem + lane_addr + 64 * (g & 1), sr);
+        tmem_ld64(trow + 64 * (gl & 1), sr);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(tc::kBarSFree + (g & 1)));
         const bool tile_ok = stage_ok[s] != 0;
-        const int key0 = static_cast<int>(t) * kPage;
-        float mx = -INFINITY;
+        const int key0 = j * kPage;
+        // keys of this tile the row sees: 0 .. lim (none for lim < 0); only
+        // the tiles on a row's diagonal (or a bad tile) need the mask
+        const int lim = (valid && tile_ok) ? min(63, pos - key0) : -1;
         float x[64];
+        if (__all_sync(0xffffffffu, lim == 63)) {
 #pragma unroll
-        for (int jk = 0; jk < 64; ++jk) {
-          x[jk] = (valid && tile_ok && key0 + jk <= pos) ? __uint_as_float(sr[jk]) * scale_log2
-                                                          : -INFINITY;
-          mx = fmaxf(mx, x[jk]);
+          for (int jk = 0; jk < 64; ++jk) x[jk] = __uint_as_float(sr[jk]);
+        } else {
+#pragma unroll
+          for (int jk = 0; jk < 64; ++jk) x[jk] = jk <= lim ? __uint_as_float(sr[jk]) : -INFINITY;
         }
+        // the row maximum of the raw scores in 8 independent chains; the
+        // scale is positive, so it commutes with the maximum
+        float m8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) m8[c] = x[c];
+#pragma unroll
+        for (int jk = 8; jk < 64; ++jk) m8[jk & 7] = fmaxf(m8[jk & 7], x[jk]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale_log2;
         // the running maximum moves only when it grows by more than 2^8
         // (weights stay <= 2^8); the row's O is then rescaled in TMEM
         const bool grow = mx > m_used + tc::kRescaleLog2;
         const float alpha = grow ? exp2_ftz(m_used - mx) : 1.f;   // 0 while m_used = -inf
         if (grow) {
-          l *= alpha;
+          lsum *= alpha;
           m_used = mx;
         }
-        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // the previous tile's P V must be in O before it is rescaled
-          if (!wait_all(tc::kBarODone, (g - 1) & 1)) {
+          if (!wait_all(tc::kBarODone + l, (gl - 1) & 1)) {
             dead = true;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t ov[64];
-            tmem_ld64(tmem + lane_addr + 128 + 64 * half, ov);
+          for (int qc = 0; qc < 4; ++qc) {
+            uint32_t ov[32];
+            tmem_ld32(trow + 128 + 32 * qc, ov);
             tmem_wait_ld();
 #pragma unroll
-            for (int jk = 0; jk < 64; ++jk) ov[jk] = __float_as_uint(__uint_as_float(ov[jk]) * alpha);
-            tmem_st64(tmem + lane_addr + 128 + 64 * half, ov);
+            for (int jk = 0; jk < 32; ++jk) ov[jk] = __float_as_uint(__uint_as_float(ov[jk]) * alpha);
+            tmem_st32(trow + 128 + 32 * qc, ov);
           }
-          tmem_wait_st();
         }
-        const float ms = m_used == -INFINITY ? 0.f : m_used;
-        float ps = 0.f;
+        // p = 2^(s * scale - m) as one FMA and one exponential, packed as
+        // BF16 pairs over the scores; the row sum in 4 independent chains
+        const float nms = m_used == -INFINITY ? 0.f : -m_used;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int jk = 0; jk < 32; ++jk) {
-          const float p0 = exp2_ftz(x[2 * jk] - ms), p1 = exp2_ftz(x[2 * jk + 1] - ms);
-          ps += p0 + p1;
+          const float p0 = exp2_ftz(fmaf(x[2 * jk], scale_log2, nms));
+          const float p1 = exp2_ftz(fmaf(x[2 * jk + 1], scale_log2, nms));
+          ps[jk & 3] += p0 + p1;
           pk[jk] = pack_bf16(p0, p1);
         }
-        l += ps;
-        // P row into its buffer once the P V two tiles back has read it
-        if (g >= 2 && !wait_all(tc::kBarPFree + (g & 1), ((g - 2) >> 1) & 1)) {
-          dead = true;
-          break;
-        }
-        uint8_t* prow = smem + tc::kOffP + (g & 1) * tc::kPBytes + row * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-        // V rows past the sequence length (the cache may hold NaN there) or
-        // of a bad tile become zeros: 0 * NaN would poison O
-        const int keep = tile_ok ? max(0, min(64, L - key0)) : 0;
-        if (keep < 64) {
-          uint8_t* vst = smem + s * tc::kStageBytes + tc::kPage;
-          const int nz = (64 - keep) * 16;   // 16-byte chunks: rows x 2 boxes x 8
-          for (int z = row; z < nz; z += 128) {
-            const int vr = keep + (z >> 4), box = (z >> 3) & 1, c8 = z & 7;
-            *reinterpret_cast<uint4*>(vst + box * tc::kBox + vr * 128 + (c8 << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        fence_proxy_async_smem();
+        lsum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tmem_st32(trow + 64 * (gl & 1), pk);
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(tc::kBarPFull + (g & 1)));
+        mbar_arrive(bar(tc::kBarPFull + 2 * l + (gl & 1)));
       }
       if (dead) break;
-      // the row of O once the unit's last P V is done: divide by the row sum, store
-      if (!wait_all(tc::kBarOFinal, V & 1)) break;
+      // the row of O once the lane's last P V is done: divide by the row sum, store
+      if (!wait_all(tc::kBarOFinal + l, Vl & 1)) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
       const int64_t orow = (static_cast<int64_t>(qs + i) * kHq + head) * kD;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t ov[64];
-        tmem_ld64(tmem + lane_addr + 128 + 64 * half, ov);
+      for (int qc = 0; qc < 4; ++qc) {
+        uint32_t ov[32];
+        tmem_ld32(trow + 128 + 32 * qc, ov);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
-          for (int jk = 0; jk < 64; jk += 8) {
+          for (int jk = 0; jk < 32; jk += 8) {
             float v8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(ov[jk + e]) * inv;
-            store_out8(out, orow + 64 * half + jk, v8, out_dtype);
+            store_out8(out, orow + 32 * qc + jk, v8, out_dtype);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(tc::kBarOFree));
-      G += n;
-      ++V;
+      mbar_arrive(bar(tc::kBarOFree + l));
+      G += nt;
+      Gl += ntl;
+      ++Vl;
     }
   }
   // every warp is done with TMEM: free it
