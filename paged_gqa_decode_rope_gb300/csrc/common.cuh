@@ -261,6 +261,69 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
                : "memory");
 }
 
+// The chains below are executed by a whole converged warp: the descriptors
+// stay warp-uniform and one elected thread issues every product of the chain
+// back to back (issued one by one from a single diverged thread, each product
+// costs the issuing thread far more than the tensor core's time for it).
+
+// Q K^T over d = 128 as one chain of eight K-major steps (16 of d each):
+// a_desc / b_desc describe the first 16 columns of two 128-byte-swizzled
+// halves; a step moves 32 bytes along a row, the second half starts
+// kAHalf / kBHalf bytes further.  The first step overwrites D.
+template <uint32_t kAHalf, uint32_t kBHalf>
+__device__ __forceinline__ void umma_bf16_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                  uint32_t idesc) {
+  constexpr uint32_t ah = kAHalf >> 4, bh = kBHalf >> 4;
+  asm volatile(
+      "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 pf, %4, %4;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(0u),
+        "n"(ah), "n"(bh), "n"(ah + 2), "n"(bh + 2), "n"(ah + 4), "n"(bh + 4), "n"(ah + 6), "n"(bh + 6)
+      : "memory");
+}
+
+// O (+)= P V over 64 keys as one chain of four steps (16 keys each): P from
+// TMEM (8 columns per step), V MN-major (2048 bytes = 16 rows per step).
+__device__ __forceinline__ void umma_bf16_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+      "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// tcgen05.commit by one elected thread of a converged warp.
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+               "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+               ::"r"(bar) : "memory");
+}
+
 // Arrive once on an mbarrier when every earlier tcgen05 op of this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -351,6 +414,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Per-warpgroup register budget (every warp of the warpgroup executes it):
+// dec hands registers back to the CTA's pool, inc waits until the pool has
+// them, so the launch must hold at least the sum of the raised budgets.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 
 // Named barrier among `nthreads` threads (a multiple of 32), id >= 1.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

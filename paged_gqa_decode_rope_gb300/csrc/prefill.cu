@@ -63,6 +63,12 @@ cudaError_t prefill_tc_smem_optin() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  // the warpgroups' raised register budgets must fit what a CTA is launched
+  // with, or the raise would wait for registers that never come
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs * tc::kThreads < tc::kRegsNeeded) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            tc::kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;

@@ -33,9 +33,14 @@ namespace hpc {
 namespace {
 namespace tc {
 
-constexpr int kThreads = 320;      // warps 0-3 softmax of lane 0, 4-7 of lane 1, 8 producer, 9 MMA
+// warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: producer, 9: MMA, 10-11 idle
+// (the third warpgroup only lends its registers to the softmax warpgroups)
+constexpr int kThreads = 384;
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
+constexpr int kRegsNeeded = 256 * kRegsSoftmax + 128 * kRegsOther;   // per CTA
 constexpr int kStages = 4;
 constexpr int kBox = 64 * 128;                      // one 64-row x 128-byte TMA box
 constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (d = 128)
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
 
   if (warp == tc::kWarpProd) {
     // ---------------------------------------------------------- producer
+    regs_dec<tc::kRegsOther>();
     // every pair of new tokens of a sequence reads the KV head's pages again
     const uint64_t policy = l2_evict_last_policy();
     uint32_t g = 0, n_pushed = 0;   // stream tiles issued, units handed on
@@ -277,41 +283,43 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     }
   } else if (warp == tc::kWarpMma) {
     // ---------------------------------------------------------- MMA issuer
+    // The whole warp runs the loop (descriptors warp-uniform); one elected
+    // thread issues each chain of products and each commit.
+    regs_dec<tc::kRegsOther>();
     constexpr uint32_t kIdescS = umma_idesc_bf16(128, 64, false);
     constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, true);
-    uint32_t G = 0, U = 0;            // stream tiles, unit descriptors read
-    uint32_t Gl[2] = {0, 0};          // tiles of each lane
-    uint32_t Vl[2] = {0, 0};          // units with tiles, per lane
+    // descriptors of the first step of each operand; a step adds a constant
+    const uint64_t desc_q = umma_smem_desc(base + tc::kOffQ, 1024, 1024);
+    const uint64_t desc_k = umma_smem_desc(base, 1024, 1024);
+    const uint64_t desc_v = umma_smem_desc(base + tc::kPage, tc::kBox, 1024);
+    constexpr uint64_t kStageStep = tc::kStageBytes >> 4;
+    constexpr uint64_t kQStep = tc::kQBytes >> 4;
+    uint32_t G = 0, U = 0;          // stream tiles, unit descriptors read
+    uint32_t Gl0 = 0, Gl1 = 0;      // tiles of each lane
+    uint32_t Vl0 = 0, Vl1 = 0;      // units with tiles, per lane
     bool dead = false;
     Unit d;
     // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
     auto issue_pv = [&](int jj) {
+      const uint32_t st = (G + jj) % tc::kStages;
 #pragma unroll
       for (int l = 0; l < 2; ++l) {
-        if (dead) break;
-        if (jj >= d.nt[l]) continue;
-        const uint32_t gl = Gl[l] + jj;
+        const int ntl = l ? d.nt[1] : d.nt[0];
+        if (dead || jj >= ntl) continue;
+        const uint32_t gl = (l ? Gl1 : Gl0) + jj;
+        const uint32_t vl = l ? Vl1 : Vl0;
         if (!wait_all(tc::kBarPFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
-            (jj == 0 && Vl[l] > 0 && !wait_all(tc::kBarOFree + l, (Vl[l] - 1) & 1))) {
+            (jj == 0 && vl > 0 && !wait_all(tc::kBarOFree + l, (vl - 1) & 1))) {
           dead = true;
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t vb = base + ((G + jj) % tc::kStages) * tc::kStageBytes + tc::kPage;
-          const uint32_t pcol = tmem + 256 * l + 64 * (gl & 1);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)   // 16 keys per step
-            umma_bf16_ts(tmem + 256 * l + 128, pcol + 8 * ks,
-                         umma_smem_desc(vb + ks * 2048, tc::kBox, 1024), kIdescO,
-                         !(jj == 0 && ks == 0));
-          umma_commit(bar(tc::kBarODone + l));
-          if (jj == d.nt[l] - 1) umma_commit(bar(tc::kBarOFinal + l));
-        }
-        __syncwarp();
+        umma_bf16_ts_k64(tmem + 256 * l + 128, tmem + 256 * l + 64 * (gl & 1),
+                         desc_v + st * kStageStep, kIdescO, jj != 0);
+        umma_commit_elect(bar(tc::kBarODone + l));
+        if (jj == ntl - 1) umma_commit_elect(bar(tc::kBarOFinal + l));
       }
-      if (!dead && lane == 0) umma_commit(bar(tc::kBarEmpty + (G + jj) % tc::kStages));
-      __syncwarp();
+      if (!dead) umma_commit_elect(bar(tc::kBarEmpty + st));
     };
     while (!dead) {
       if (!read_unit(U, d)) break;
@@ -320,70 +328,62 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       const int nt = max(d.nt[0], d.nt[1]);
       if (nt <= 0) continue;
       const int L = seq_lens[d.b];
-#pragma unroll
-      for (int l = 0; l < 2; ++l)
-        if (!dead && d.nt[l] > 0 && !wait_all(tc::kBarQReady + l, Vl[l] & 1)) dead = true;
+      if ((d.nt[0] > 0 && !wait_all(tc::kBarQReady + 0, Vl0 & 1)) ||
+          (d.nt[1] > 0 && !wait_all(tc::kBarQReady + 1, Vl1 & 1)))
+        break;
       for (int j = 0; j < nt && !dead; ++j) {
         const uint32_t g = G + j;
-        const int s = static_cast<int>(g % tc::kStages);
-        if (!wait_all(tc::kBarFull + s, (g / tc::kStages) & 1)) {
+        const uint32_t st = g % tc::kStages;
+        if (!wait_all(tc::kBarFull + st, (g / tc::kStages) & 1)) {
           dead = true;
           break;
         }
         // V rows past the sequence length or of a bad tile -> zeros, before
-        // any P V of the tile reads them
-        const int keep = stage_ok[s] ? max(0, min(64, L - 64 * j)) : 0;
+        // any P V of the tile reads them (the last tile of a sequence only)
+        const int keep = stage_ok[st] ? max(0, min(64, L - 64 * j)) : 0;
         if (keep < 64) {
-          uint8_t* vst = smem + s * tc::kStageBytes + tc::kPage;
-          for (int z = lane; z < (64 - keep) * 16; z += 32) {
-            const int vr = keep + (z >> 4), box = (z >> 3) & 1, c8 = z & 7;
-            *reinterpret_cast<uint4*>(vst + box * tc::kBox + vr * 128 + (c8 << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
+          uint4* vst = reinterpret_cast<uint4*>(smem + st * tc::kStageBytes + tc::kPage);
+          for (int z = keep * 8 + lane; z < 64 * 8; z += 32) {   // rows keep..63, both boxes
+            vst[z] = make_uint4(0u, 0u, 0u, 0u);
+            vst[tc::kBox / 16 + z] = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
         }
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kb = base + s * tc::kStageBytes;
-#pragma unroll
-          for (int l = 0; l < 2; ++l) {
-            if (j >= d.nt[l]) continue;
-            const uint32_t gl = Gl[l] + j;
-            const uint32_t qa = base + tc::kOffQ + l * tc::kQBytes;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {   // 16 of d per step
-              const uint32_t off = (ks >> 2) * 2 * tc::kBox + (ks & 3) * 32;
-              const uint32_t koff = (ks >> 2) * tc::kBox + (ks & 3) * 32;
-              umma_bf16_ss(tmem + 256 * l + 64 * (gl & 1), umma_smem_desc(qa + off, 1024, 1024),
-                           umma_smem_desc(kb + koff, 1024, 1024), kIdescS, ks > 0);
-            }
-            umma_commit(bar(tc::kBarSFull + 2 * l + (gl & 1)));
-          }
+        if (j < d.nt[0]) {
+          umma_bf16_ss_k128<2 * tc::kBox, tc::kBox>(tmem + 64 * ((Gl0 + j) & 1), desc_q,
+                                                    desc_k + st * kStageStep, kIdescS);
+          umma_commit_elect(bar(tc::kBarSFull + ((Gl0 + j) & 1)));
         }
-        __syncwarp();
+        if (j < d.nt[1]) {
+          umma_bf16_ss_k128<2 * tc::kBox, tc::kBox>(tmem + 256 + 64 * ((Gl1 + j) & 1),
+                                                    desc_q + kQStep, desc_k + st * kStageStep,
+                                                    kIdescS);
+          umma_commit_elect(bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)));
+        }
         if (j >= 1) issue_pv(j - 1);
       }
       if (dead) break;
       issue_pv(nt - 1);
       if (dead) break;
       G += nt;
-#pragma unroll
-      for (int l = 0; l < 2; ++l) {
-        if (d.nt[l] > 0) {
-          Gl[l] += d.nt[l];
-          ++Vl[l];
-        }
+      if (d.nt[0] > 0) {
+        Gl0 += d.nt[0];
+        ++Vl0;
+      }
+      if (d.nt[1] > 0) {
+        Gl1 += d.nt[1];
+        ++Vl1;
       }
     }
     // every product issued here has completed before TMEM is freed
-    if (lane == 0) {
-      umma_commit(bar(tc::kBarDrain));
-      mbar_wait(bar(tc::kBarDrain), 0, status);
-    }
+    umma_commit_elect(bar(tc::kBarDrain));
+    mbar_wait(bar(tc::kBarDrain), 0, status);
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ---------------------------------------------------------- softmax warpgroups
+    regs_inc<tc::kRegsSoftmax>();
     const int l = warp >> 2;                           // lane (tile) of the unit
     const int row = threadIdx.x & 127;                 // 8 * token + head
     const int tok = row >> 3, hl = row & 7;
@@ -536,6 +536,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       Gl += ntl;
       ++Vl;
     }
+  } else {
+    regs_dec<tc::kRegsOther>();   // the idle warps of the third warpgroup
   }
   // every warp is done with TMEM: free it
   tc_fence_before();
