@@ -50,17 +50,17 @@ constexpr int kQBytes = 2 * 128 * 128;
 constexpr int kOffBar = kOffQ + 2 * kQBytes;
 // mbarriers (index of the first of each kind; [l] per lane, [l][i] per lane and buffer)
 constexpr int kBarFull = 0;        // [4] stage landed (TMA)
-constexpr int kBarEmpty = 4;       // [4] stage consumed (the tile's P V products done)
+constexpr int kBarEmpty = 4;       // [4] stage consumed (both lanes' P V of the tile done)
 constexpr int kBarSFull = 8;       // [2][2] scores written
-constexpr int kBarPFull = 12;      // [2][2] P written over the scores (128 softmax threads)
-constexpr int kBarODone = 16;      // [2] each P V of the lane done, in order
-constexpr int kBarOFinal = 18;     // [2] the lane's last P V of a unit done
-constexpr int kBarOFree = 20;      // [2] the lane's O read out (128 softmax threads)
-constexpr int kBarQReady = 22;     // [2] the lane's Q written (128 softmax threads)
-constexpr int kBarUnitFull = 24;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 26;  // [2] unit descriptor read (MMA warp + 8 softmax warps)
-constexpr int kBarDrain = 28;      // every product of the MMA warp done (at exit)
-constexpr int kNumBars = 29;
+constexpr int kBarPFull = 12;      // [2] P of both lanes written (256 arrivals; a lane
+                                   //     without the tile arrives for it twice)
+constexpr int kBarOFinal = 14;     // [2] the lane's last P V of a unit done
+constexpr int kBarOFree = 16;      // [2] the lane's O read out (128 softmax threads)
+constexpr int kBarQReady = 18;     // [2] the lane's Q written (128 softmax threads)
+constexpr int kBarUnitFull = 20;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 22;  // [2] unit descriptor read (MMA warp + 8 softmax warps)
+constexpr int kBarDrain = 24;      // every product of the MMA warp done (at exit)
+constexpr int kNumBars = 25;
 constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
 constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;
@@ -121,12 +121,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(tc::kBarFull + s), 1);
       mbar_init(bar(tc::kBarEmpty + s), 1);
     }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(tc::kBarSFull + i), 1);
-      mbar_init(bar(tc::kBarPFull + i), 128);
-    }
+    for (int i = 0; i < 4; ++i) mbar_init(bar(tc::kBarSFull + i), 1);
     for (int l = 0; l < 2; ++l) {
-      mbar_init(bar(tc::kBarODone + l), 1);
+      mbar_init(bar(tc::kBarPFull + l), 256);
       mbar_init(bar(tc::kBarOFinal + l), 1);
       mbar_init(bar(tc::kBarOFree + l), 128);
       mbar_init(bar(tc::kBarQReady + l), 128);
@@ -145,8 +142,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
   const uint32_t tmem = *tmem_slot;
   const int total_units = unit_ptr[batch];
 
-  // a bounded wait by the whole warp; false (and the abort flag set) on a timeout
+  // a bounded wait by the whole warp; false (and the abort flag set) on a
+  // timeout.  Fast path: the phase is already complete for every lane.
   auto wait_all = [&](int b, uint32_t parity) -> bool {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar(b), parity))) return true;
     bool ok = !*abort_flag && mbar_wait(bar(b), parity, status);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && lane == 0) *abort_flag = 1;
@@ -301,25 +300,27 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     Unit d;
     // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
     auto issue_pv = [&](int jj) {
-      const uint32_t st = (G + jj) % tc::kStages;
+      const uint32_t g = G + jj, st = g % tc::kStages;
+      if (dead || !wait_all(tc::kBarPFull + (g & 1), (g >> 1) & 1)) {
+        dead = true;
+        return;
+      }
 #pragma unroll
       for (int l = 0; l < 2; ++l) {
         const int ntl = l ? d.nt[1] : d.nt[0];
-        if (dead || jj >= ntl) continue;
+        if (jj >= ntl) continue;
         const uint32_t gl = (l ? Gl1 : Gl0) + jj;
         const uint32_t vl = l ? Vl1 : Vl0;
-        if (!wait_all(tc::kBarPFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
-            (jj == 0 && vl > 0 && !wait_all(tc::kBarOFree + l, (vl - 1) & 1))) {
+        if (jj == 0 && vl > 0 && !wait_all(tc::kBarOFree + l, (vl - 1) & 1)) {
           dead = true;
-          break;
+          return;
         }
         tc_fence_after();
         umma_bf16_ts_k64(tmem + 256 * l + 128, tmem + 256 * l + 64 * (gl & 1),
                          desc_v + st * kStageStep, kIdescO, jj != 0);
-        umma_commit_elect(bar(tc::kBarODone + l));
         if (jj == ntl - 1) umma_commit_elect(bar(tc::kBarOFinal + l));
       }
-      if (!dead) umma_commit_elect(bar(tc::kBarEmpty + st));
+      umma_commit_elect(bar(tc::kBarEmpty + st));
     };
     while (!dead) {
       if (!read_unit(U, d)) break;
@@ -475,8 +476,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           m_used = mx;
         }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // the previous tile's P V must be in O before it is rescaled
-          if (!wait_all(tc::kBarODone + l, (gl - 1) & 1)) {
+          // the previous tile's P V must be in O before it is rescaled: its
+          // stage is emptied once both lanes' P V of it are done
+          if (!wait_all(tc::kBarEmpty + (g - 1) % tc::kStages, ((g - 1) / tc::kStages) & 1)) {
             dead = true;
             break;
           }
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         tmem_st32(trow + 64 * (gl & 1), pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar(tc::kBarPFull + 2 * l + (gl & 1)));
+        mbar_arrive_cnt(bar(tc::kBarPFull + (g & 1)), j < (l ? d.nt[0] : d.nt[1]) ? 1u : 2u);
       }
       if (dead) break;
       // the row of O once the lane's last P V is done: divide by the row sum, store
