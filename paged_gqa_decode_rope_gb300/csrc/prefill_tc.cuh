@@ -97,6 +97,77 @@ __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (
   }
 }
 
+// S = Q K^T of both lanes for one tile (executed by the whole converged MMA
+// warp; one elected thread issues): lane l, if present (en_l), gets eight
+// K-major steps (16 of d each) into d_l and a commit on bar_l.  Q halves of d
+// are 16 KB apart, K halves 8 KB; a step moves 32 bytes along a row.
+__device__ __forceinline__ void umma_qk_pair(uint32_t d0, uint32_t d1, uint64_t q0, uint64_t q1,
+                                             uint64_t k, uint32_t idesc, bool en0, bool en1,
+                                             uint32_t bar0, uint32_t bar1) {
+#define HPC_QK_STEP(D, Q, QO, KO, P)                                   \
+  "add.s64 a, " Q ", " QO ";\n\tadd.s64 b, %4, " KO ";\n\t"         \
+  "@" P " tcgen05.mma.cta_group::1.kind::f16 [" D "], a, b, %5, pt;\n\t"
+#define HPC_QK_CHAIN(D, Q, P)                                                        \
+  "@" P " tcgen05.mma.cta_group::1.kind::f16 [" D "], " Q ", %4, %5, pf;\n\t"     \
+  HPC_QK_STEP(D, Q, "2", "2", P) HPC_QK_STEP(D, Q, "4", "4", P)                      \
+  HPC_QK_STEP(D, Q, "6", "6", P) HPC_QK_STEP(D, Q, "1024", "512", P)                 \
+  HPC_QK_STEP(D, Q, "1026", "514", P) HPC_QK_STEP(D, Q, "1028", "516", P)            \
+  HPC_QK_STEP(D, Q, "1030", "518", P)
+  asm volatile(
+      "{\n\t.reg .pred e, e0, e1, pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 e0, %6, 0, e;\n\tsetp.ne.and.b32 e1, %7, 0, e;\n\t"
+      "setp.ne.b32 pf, %6, %6;\n\tsetp.eq.b32 pt, %6, %6;\n\t"
+      HPC_QK_CHAIN("%0", "%2", "e0")
+      "@e0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      HPC_QK_CHAIN("%1", "%3", "e1")
+      "@e1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
+      ::"r"(d0), "r"(d1), "l"(q0), "l"(q1), "l"(k), "r"(idesc), "r"(en0 ? 1u : 0u),
+        "r"(en1 ? 1u : 0u), "r"(bar0), "r"(bar1)
+      : "memory");
+#undef HPC_QK_CHAIN
+#undef HPC_QK_STEP
+}
+
+// O_l (+)= P_l V of both lanes for one tile (whole converged warp, one
+// elected thread issues): lane l, if present, gets four steps of 16 keys (P
+// from TMEM, 8 columns a step; V MN-major, 2048 bytes a step) into its O at
+// tmem + 256 l + 128, then a commit on fin_l if it was the lane's last tile;
+// the stage's empty barrier is committed after both.
+__device__ __forceinline__ void umma_pv_pair(uint32_t tmem, uint32_t p0, uint32_t p1, uint64_t v,
+                                             uint32_t idesc, bool acc, bool en0, bool en1,
+                                             bool last0, bool last1, uint32_t fin0, uint32_t fin1,
+                                             uint32_t empty) {
+#define HPC_PV_STEP(D, P, PO, VO, E)                                     \
+  "add.u32 a, " P ", " PO ";\n\tadd.s64 b, %3, " VO ";\n\t"         \
+  "@" E " tcgen05.mma.cta_group::1.kind::f16 [" D "], [a], b, %4, pt;\n\t"
+#define HPC_PV_CHAIN(D, P, E)                                                         \
+  "@" E " tcgen05.mma.cta_group::1.kind::f16 [" D "], [" P "], %3, %4, pa;\n\t"    \
+  HPC_PV_STEP(D, P, "8", "128", E) HPC_PV_STEP(D, P, "16", "256", E)                  \
+  HPC_PV_STEP(D, P, "24", "384", E)
+  const uint32_t o0 = tmem + 128, o1 = tmem + 384;
+  const uint32_t flags = (acc ? 1u : 0u) | (en0 ? 2u : 0u) | (en1 ? 4u : 0u) | (last0 ? 8u : 0u) |
+                         (last1 ? 16u : 0u);
+  asm volatile(
+      "{\n\t.reg .pred e, e0, e1, f0, f1, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a, t;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "and.b32 t, %5, 2;\n\tsetp.ne.and.b32 e0, t, 0, e;\n\t"
+      "and.b32 t, %5, 4;\n\tsetp.ne.and.b32 e1, t, 0, e;\n\t"
+      "and.b32 t, %5, 8;\n\tsetp.ne.and.b32 f0, t, 0, e0;\n\t"
+      "and.b32 t, %5, 16;\n\tsetp.ne.and.b32 f1, t, 0, e1;\n\t"
+      "and.b32 t, %5, 1;\n\tsetp.ne.b32 pa, t, 0;\n\tsetp.eq.b32 pt, t, t;\n\t"
+      HPC_PV_CHAIN("%0", "%1", "e0")
+      "@f0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+      HPC_PV_CHAIN("%2", "%7", "e1")
+      "@f1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
+      ::"r"(o0), "r"(p0), "r"(o1), "l"(v), "r"(idesc), "r"(flags), "r"(fin0), "r"(p1), "r"(fin1),
+        "r"(empty)
+      : "memory");
+#undef HPC_PV_CHAIN
+#undef HPC_PV_STEP
+}
+
 __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap kv_map, const uint16_t* __restrict__ q,
     const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
@@ -232,10 +303,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         const int t = tb + lane;
         const int bids = t < ntiles ? block_table[static_cast<int64_t>(b) * max_blocks + t] : 0;
         for (int jj = 0; jj < min(32, ntiles - tb) && alive; ++jj) {
-          int bid = __shfl_sync(0xffffffffu, bids, jj);
+          const int bid = __shfl_sync(0xffffffffu, bids, jj);
+          const bool good = bid >= 0 && bid < num_blocks;
+          const int s = static_cast<int>(g % tc::kStages);
           int tok = 1;
           if (lane == 0) {
-            const int s = static_cast<int>(g % tc::kStages);
             const uint32_t use = g / tc::kStages;
             if (*abort_flag) {
               tok = 0;
@@ -243,15 +315,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
               *abort_flag = 1;
               tok = 0;
             }
-            if (tok) {
-              // a bad block id loads block 0 in its place and marks the
-              // stage: its keys are masked and its V rows zeroed
-              const bool good = bid >= 0 && bid < num_blocks;
-              if (!good) {
-                atomicOr(status, HPC_STATUS_BAD_BLOCK);
-                bid = 0;
-              }
-              stage_ok[s] = good ? 1 : 0;
+            if (tok && good) {
+              stage_ok[s] = 1;
               const uint32_t fb = bar(tc::kBarFull + s);
               mbar_arrive_expect_tx(fb, tc::kStageBytes);
               const uint32_t dst = base + s * tc::kStageBytes;
@@ -261,6 +326,20 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
               tma_load_2d(dst + tc::kBox, &kv_map, 64, yk, fb, policy);
               tma_load_2d(dst + tc::kPage, &kv_map, 0, yv, fb, policy);
               tma_load_2d(dst + tc::kPage + tc::kBox, &kv_map, 64, yv, fb, policy);
+            }
+          }
+          tok = __shfl_sync(0xffffffffu, tok, 0);
+          if (tok && !good) {
+            // a bad block id: no copy; the stage's V becomes zeros and the
+            // stage is marked, so the softmax masks its keys (status set)
+            uint4* vst = reinterpret_cast<uint4*>(smem + s * tc::kStageBytes + tc::kPage);
+            for (int z = lane; z < tc::kPage / 16; z += 32) vst[z] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              atomicOr(status, HPC_STATUS_BAD_BLOCK);
+              stage_ok[s] = 0;
+              mbar_arrive(bar(tc::kBarFull + s));
             }
           }
           alive = __shfl_sync(0xffffffffu, tok, 0) != 0;
@@ -301,26 +380,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
     auto issue_pv = [&](int jj) {
       const uint32_t g = G + jj, st = g % tc::kStages;
-      if (dead || !wait_all(tc::kBarPFull + (g & 1), (g >> 1) & 1)) {
+      if (dead || !wait_all(tc::kBarPFull + (g & 1), (g >> 1) & 1) ||
+          (jj == 0 && ((d.nt[0] > 0 && Vl0 > 0 && !wait_all(tc::kBarOFree + 0, (Vl0 - 1) & 1)) ||
+                       (d.nt[1] > 0 && Vl1 > 0 && !wait_all(tc::kBarOFree + 1, (Vl1 - 1) & 1))))) {
         dead = true;
         return;
       }
-#pragma unroll
-      for (int l = 0; l < 2; ++l) {
-        const int ntl = l ? d.nt[1] : d.nt[0];
-        if (jj >= ntl) continue;
-        const uint32_t gl = (l ? Gl1 : Gl0) + jj;
-        const uint32_t vl = l ? Vl1 : Vl0;
-        if (jj == 0 && vl > 0 && !wait_all(tc::kBarOFree + l, (vl - 1) & 1)) {
-          dead = true;
-          return;
-        }
-        tc_fence_after();
-        umma_bf16_ts_k64(tmem + 256 * l + 128, tmem + 256 * l + 64 * (gl & 1),
-                         desc_v + st * kStageStep, kIdescO, jj != 0);
-        if (jj == ntl - 1) umma_commit_elect(bar(tc::kBarOFinal + l));
-      }
-      umma_commit_elect(bar(tc::kBarEmpty + st));
+      tc_fence_after();
+      umma_pv_pair(tmem, tmem + 64 * ((Gl0 + jj) & 1), tmem + 256 + 64 * ((Gl1 + jj) & 1),
+                   desc_v + st * kStageStep, kIdescO, jj != 0, jj < d.nt[0], jj < d.nt[1],
+                   jj == d.nt[0] - 1, jj == d.nt[1] - 1, bar(tc::kBarOFinal), bar(tc::kBarOFinal + 1),
+                   bar(tc::kBarEmpty + st));
     };
     while (!dead) {
       if (!read_unit(U, d)) break;
@@ -339,9 +409,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           dead = true;
           break;
         }
-        // V rows past the sequence length or of a bad tile -> zeros, before
-        // any P V of the tile reads them (the last tile of a sequence only)
-        const int keep = stage_ok[st] ? max(0, min(64, L - 64 * j)) : 0;
+        // V rows past the sequence length (the cache may hold NaN there) ->
+        // zeros before any P V of the tile reads them; only the page of the
+        // sequence's last key has such rows
+        const int keep = L - 64 * j;
         if (keep < 64) {
           uint4* vst = reinterpret_cast<uint4*>(smem + st * tc::kStageBytes + tc::kPage);
           for (int z = keep * 8 + lane; z < 64 * 8; z += 32) {   // rows keep..63, both boxes
@@ -352,17 +423,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           __syncwarp();
         }
         tc_fence_after();
-        if (j < d.nt[0]) {
-          umma_bf16_ss_k128<2 * tc::kBox, tc::kBox>(tmem + 64 * ((Gl0 + j) & 1), desc_q,
-                                                    desc_k + st * kStageStep, kIdescS);
-          umma_commit_elect(bar(tc::kBarSFull + ((Gl0 + j) & 1)));
-        }
-        if (j < d.nt[1]) {
-          umma_bf16_ss_k128<2 * tc::kBox, tc::kBox>(tmem + 256 + 64 * ((Gl1 + j) & 1),
-                                                    desc_q + kQStep, desc_k + st * kStageStep,
-                                                    kIdescS);
-          umma_commit_elect(bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)));
-        }
+        umma_qk_pair(tmem + 64 * ((Gl0 + j) & 1), tmem + 256 + 64 * ((Gl1 + j) & 1), desc_q,
+                     desc_q + kQStep, desc_k + st * kStageStep, kIdescS, j < d.nt[0], j < d.nt[1],
+                     bar(tc::kBarSFull + ((Gl0 + j) & 1)), bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)));
         if (j >= 1) issue_pv(j - 1);
       }
       if (dead) break;

@@ -128,3 +128,35 @@ def test_prefill_bad_lengths_set_status_and_skip():
     assert int(pf.status.item()) & 4          # HPC_STATUS_BAD_SEQ_LEN
     assert not out[:80].float().abs().any()   # skipped
     _check(wl, q, qs, out, seqs=[1])
+
+
+def test_prefill_bad_block_is_reported_and_skipped():
+    """A block id past the cache: the status says BAD_BLOCK, the page's keys
+    are left out of that sequence's attention, the other sequences are
+    untouched."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [300, 260, 100]
+    q_lens = [40, 70, 100]
+    wl, q, qst, qs = _batch(lengths, q_lens, 17)
+    wl.block_table[1, 2] = wl.num_blocks + 5           # page 2 (keys 128..191) of sequence 1
+    pf = ops.PrefillAttention(wl.batch)
+    pf.plan(qst)
+    out = torch.empty_like(q)
+    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) & 1                   # HPC_STATUS_BAD_BLOCK
+    _check(wl, q, qs, out, seqs=[0, 2])
+    L, n = lengths[1], q_lens[1]
+    sub, row = gu.seq_view(wl.cache, wl.block_table_np[1], L, 0)
+    qh = gu.bf16_host(q)[int(qs[1]):int(qs[2])]
+    keep = np.r_[0:128, 192:L]
+    want = np.zeros((n, 64, 128))
+    for h in range(8):
+        K, V = od.gather_kv(sub, row, L, h, 0, 1.0, 1.0)
+        for t in range(n):
+            vis = keep[keep <= L - n + t]
+            for j in range(8 * h, 8 * h + 8):
+                want[t, j] = od.attention_head(qh[t, j], K[vis], V[vis], 1.0 / np.sqrt(128))
+    gu.compare(out[int(qs[1]):int(qs[2])].float().cpu().numpy().astype(np.float64), want,
+               gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN, label="seq 1 without page 2")
