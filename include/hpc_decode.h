@@ -464,11 +464,12 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  * ecosystem" (heads, head_dim, paged cache).
  *   query_start  (device) int32 [batch + 1], nondecreasing
  *   unit_ptr     (device) int32 [batch + 1];  counters (device) int32 [2]
- *   q            (device) bf16 [query_start[batch], 64, 128], 16-byte aligned
- *   out          (device) [query_start[batch], 64, 128] of out_dtype, 16-byte
- *                aligned, written for every new token of a valid sequence
- *   status       BAD_SEQ_LEN for q_len_b < 0, q_len_b > seq_lens[b] or
- *                seq_lens[b] > max_blocks * 64 (the sequence is skipped);
+ *   q            (device) bf16 [num_tokens, 64, 128], 16-byte aligned
+ *   out          (device) [num_tokens, 64, 128] of out_dtype, 16-byte aligned,
+ *                written for every new token of a valid sequence
+ *   status       BAD_SEQ_LEN for q_len_b < 0, q_len_b > seq_lens[b],
+ *                seq_lens[b] > max_blocks * 64 or new tokens past num_tokens
+ *                (the sequence is skipped);
  *                BAD_BLOCK for a block id out of range (the tile is skipped)
  * sm_scale must be positive (the softmax takes row maxima of unscaled scores).
  * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes, sm_scale <= 0 or
@@ -476,7 +477,8 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  * num_blocks > HPC_MAX_NUM_BLOCKS. */
 int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32_t* unit_ptr,
                      int32_t* counters, int32_t* status, cudaStream_t stream);
-int hpc_prefill_attn(const void* q, const int32_t* query_start, const void* kv_cache,
+int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t* query_start,
+                     const void* kv_cache,
                      int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
                      const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
                      int32_t batch, const int32_t* unit_ptr, int32_t* counters, void* out,

@@ -94,7 +94,7 @@ SIGNATURES = {
                                     ctypes.POINTER(AttnOptions), _c_p, _c_p]),
     "hpc_prefill_plan": (ctypes.c_int, [_c_p, _c_i32, _c_p, _c_p, _c_p, _c_p]),
     "hpc_prefill_attn": (ctypes.c_int, [
-        _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p,
+        _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p,
         _c_i32, ctypes.c_float, _c_p, _c_p]),
     "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }

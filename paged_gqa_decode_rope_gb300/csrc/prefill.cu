@@ -88,7 +88,8 @@ extern "C" int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32
   return HPC_LAUNCH_STATUS();
 }
 
-extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const void* kv_cache,
+extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t* query_start,
+                                const void* kv_cache,
                                 int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
                                 const int32_t* block_table, int32_t max_blocks,
                                 const int32_t* seq_lens, int32_t batch, const int32_t* unit_ptr,
@@ -96,7 +97,7 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
                                 int32_t* status, cudaStream_t stream) {
   HPC_CHECK_ARG(q && query_start && kv_cache && block_table && seq_lens && unit_ptr && counters &&
                 out && status);
-  HPC_CHECK_ARG(batch >= 0 && num_blocks > 0 && max_blocks >= 1 && sm_scale > 0.f);
+  HPC_CHECK_ARG(batch >= 0 && num_tokens >= 0 && num_blocks > 0 && max_blocks >= 1 && sm_scale > 0.f);
   HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
   if (out_dtype != HPC_OUT_BF16 && out_dtype != HPC_OUT_FP16 && out_dtype != HPC_OUT_FP32)
     return HPC_ERR_UNSUPPORTED;
@@ -105,7 +106,7 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
   if (kv_dtype != HPC_KV_BF16) return HPC_ERR_UNSUPPORTED;   // an E4M3 cache: not yet
   if (batch > HPC_MAX_BATCH || num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
-  if (batch == 0) return HPC_OK;
+  if (batch == 0 || num_tokens == 0) return HPC_OK;
   auto encode = hpc::tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
   CUtensorMap map;
@@ -119,13 +120,27 @@ extern "C" int hpc_prefill_attn(const void* q, const int32_t* query_start, const
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
+  // q as [tokens][64 heads][128 d]: boxes of 16 tokens x 8 heads x 64 of d
+  CUtensorMap q_map;
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(hpc::kD), static_cast<cuuint64_t>(hpc::kHq),
+                               static_cast<cuuint64_t>(num_tokens)};
+  const cuuint64_t qstrides[2] = {static_cast<cuuint64_t>(hpc::kD) * 2,
+                                  static_cast<cuuint64_t>(hpc::kHq) * hpc::kD * 2};
+  const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(hpc::kGroup),
+                              static_cast<cuuint32_t>(hpc::tc::kLaneTokens)};
+  const cuuint32_t qestr[3] = {1, 1, 1};
+  const CUresult qr = encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims,
+                             qstrides, qbox, qestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (qr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
   if (hpc::prefill_tc_smem_optin() != cudaSuccess) return HPC_ERR_CUDA;
   hpc::prefill_tc_kernel<<<sms, hpc::tc::kThreads, hpc::tc::kSmemBytes, stream>>>(
-      map, static_cast<const uint16_t*>(q), query_start, seq_lens, batch, block_table, max_blocks,
+      map, q_map, num_tokens, query_start, seq_lens, batch, block_table, max_blocks,
       num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
   return HPC_LAUNCH_STATUS();
 }

@@ -13,7 +13,9 @@
 // producer warp streams by TMA into a ring of stages (64-row x 128-byte
 // boxes, 128-byte swizzle).  Per 64-key tile and lane:
 //  * S = Q K^T (M 128, N 64, K 128: eight K-major steps, both operands in
-//    shared memory) into one of the lane's two TMEM score buffers;
+//    shared memory) into one of the lane's two TMEM score buffers; the
+//    producer loads each lane's Q tile by TMA (a 3-D map over [tokens, heads,
+//    d]) as soon as the lane's last Q K^T of the previous unit is done;
 //  * its softmax warpgroup (thread = row) loads the row of S, masks it by
 //    position, keeps the running maximum until it grows by more than 2^8
 //    (only then rescaling the row of O in TMEM), and writes P as BF16 pairs
@@ -33,11 +35,12 @@ namespace hpc {
 namespace {
 namespace tc {
 
-// warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: producer, 9: MMA, 10-11 idle
-// (the third warpgroup only lends its registers to the softmax warpgroups)
+// warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: K/V producer, 9: MMA,
+// 10: Q loader, 11: idle (the third warpgroup lends registers to the softmax)
 constexpr int kThreads = 384;
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpQ = 10;
 constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsOther = 104;
 constexpr int kRegsNeeded = 256 * kRegsSoftmax + 128 * kRegsOther;   // per CTA
@@ -56,11 +59,12 @@ constexpr int kBarPFull = 12;      // [2] P of both lanes written (256 arrivals;
                                    //     without the tile arrives for it twice)
 constexpr int kBarOFinal = 14;     // [2] the lane's last P V of a unit done
 constexpr int kBarOFree = 16;      // [2] the lane's O read out (128 softmax threads)
-constexpr int kBarQReady = 18;     // [2] the lane's Q written (128 softmax threads)
-constexpr int kBarUnitFull = 20;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 22;  // [2] unit descriptor read (MMA warp + 8 softmax warps)
-constexpr int kBarDrain = 24;      // every product of the MMA warp done (at exit)
-constexpr int kNumBars = 25;
+constexpr int kBarQFull = 18;      // [2] the lane's Q tile landed (TMA)
+constexpr int kBarQFree = 20;      // [2] the lane's last Q K^T of a unit done
+constexpr int kBarUnitFull = 22;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 24;  // [2] unit descriptor read (MMA, Q loader, 8 softmax warps)
+constexpr int kBarDrain = 26;      // every product of the MMA warp done (at exit)
+constexpr int kNumBars = 27;
 constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
 constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;
@@ -99,11 +103,13 @@ __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (
 
 // S = Q K^T of both lanes for one tile (executed by the whole converged MMA
 // warp; one elected thread issues): lane l, if present (en_l), gets eight
-// K-major steps (16 of d each) into d_l and a commit on bar_l.  Q halves of d
+// K-major steps (16 of d each) into d_l and a commit on bar_l, and on
+// qfree_l too if it was the lane's last tile of the unit (its Q may go).  Q halves of d
 // are 16 KB apart, K halves 8 KB; a step moves 32 bytes along a row.
 __device__ __forceinline__ void umma_qk_pair(uint32_t d0, uint32_t d1, uint64_t q0, uint64_t q1,
                                              uint64_t k, uint32_t idesc, bool en0, bool en1,
-                                             uint32_t bar0, uint32_t bar1) {
+                                             uint32_t bar0, uint32_t bar1, bool last0, bool last1,
+                                             uint32_t qfree0, uint32_t qfree1) {
 #define HPC_QK_STEP(D, Q, QO, KO, P)                                   \
   "add.s64 a, " Q ", " QO ";\n\tadd.s64 b, %4, " KO ";\n\t"         \
   "@" P " tcgen05.mma.cta_group::1.kind::f16 [" D "], a, b, %5, pt;\n\t"
@@ -113,17 +119,23 @@ __device__ __forceinline__ void umma_qk_pair(uint32_t d0, uint32_t d1, uint64_t 
   HPC_QK_STEP(D, Q, "6", "6", P) HPC_QK_STEP(D, Q, "1024", "512", P)                 \
   HPC_QK_STEP(D, Q, "1026", "514", P) HPC_QK_STEP(D, Q, "1028", "516", P)            \
   HPC_QK_STEP(D, Q, "1030", "518", P)
+  const uint32_t flags = (en0 ? 1u : 0u) | (en1 ? 2u : 0u) | (last0 ? 4u : 0u) | (last1 ? 8u : 0u);
   asm volatile(
-      "{\n\t.reg .pred e, e0, e1, pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "{\n\t.reg .pred e, e0, e1, f0, f1, pf, pt;\n\t.reg .b64 a, b;\n\t.reg .b32 t;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.and.b32 e0, %6, 0, e;\n\tsetp.ne.and.b32 e1, %7, 0, e;\n\t"
-      "setp.ne.b32 pf, %6, %6;\n\tsetp.eq.b32 pt, %6, %6;\n\t"
+      "and.b32 t, %6, 1;\n\tsetp.ne.and.b32 e0, t, 0, e;\n\t"
+      "and.b32 t, %6, 2;\n\tsetp.ne.and.b32 e1, t, 0, e;\n\t"
+      "and.b32 t, %6, 4;\n\tsetp.ne.and.b32 f0, t, 0, e0;\n\t"
+      "and.b32 t, %6, 8;\n\tsetp.ne.and.b32 f1, t, 0, e1;\n\t"
+      "setp.ne.b32 pf, t, t;\n\tsetp.eq.b32 pt, t, t;\n\t"
       HPC_QK_CHAIN("%0", "%2", "e0")
-      "@e0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      "@e0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "@f0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
       HPC_QK_CHAIN("%1", "%3", "e1")
-      "@e1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
-      ::"r"(d0), "r"(d1), "l"(q0), "l"(q1), "l"(k), "r"(idesc), "r"(en0 ? 1u : 0u),
-        "r"(en1 ? 1u : 0u), "r"(bar0), "r"(bar1)
+      "@e1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      "@f1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}"
+      ::"r"(d0), "r"(d1), "l"(q0), "l"(q1), "l"(k), "r"(idesc), "r"(flags), "r"(bar0), "r"(bar1),
+        "r"(qfree0), "r"(qfree1)
       : "memory");
 #undef HPC_QK_CHAIN
 #undef HPC_QK_STEP
@@ -169,8 +181,8 @@ __device__ __forceinline__ void umma_pv_pair(uint32_t tmem, uint32_t p0, uint32_
 }
 
 __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
-    const __grid_constant__ CUtensorMap kv_map, const uint16_t* __restrict__ q,
-    const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
+    const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+    int32_t num_tokens, const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
     const int32_t* __restrict__ block_table, int32_t max_blocks, int32_t num_blocks,
     const int32_t* __restrict__ unit_ptr, int32_t* counters, void* __restrict__ out,
     int32_t out_dtype, float sm_scale, int32_t* __restrict__ status) {
@@ -197,16 +209,20 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(tc::kBarPFull + l), 256);
       mbar_init(bar(tc::kBarOFinal + l), 1);
       mbar_init(bar(tc::kBarOFree + l), 128);
-      mbar_init(bar(tc::kBarQReady + l), 128);
+      mbar_init(bar(tc::kBarQFull + l), 1);
+      mbar_init(bar(tc::kBarQFree + l), 1);
       mbar_init(bar(tc::kBarUnitFull + l), 1);
-      mbar_init(bar(tc::kBarUnitEmpty + l), 9);
+      mbar_init(bar(tc::kBarUnitEmpty + l), 10);
     }
     mbar_init(bar(tc::kBarDrain), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == tc::kWarpMma) tmem_alloc(smem_u32(tmem_slot), tc::kTmemCols);
-  if (warp == tc::kWarpProd && lane == 0) tma_prefetch_desc(&kv_map);
+  if (warp == tc::kWarpProd && lane == 0) {
+    tma_prefetch_desc(&kv_map);
+    tma_prefetch_desc(&q_map);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -268,7 +284,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         const int npair = (qlen + tc::kUnitTokens - 1) / tc::kUnitTokens;
         h = j % kHkv;
         pair = npair - 1 - j / kHkv;   // the pairs with the most keys first
-        if (qlen < 1 || L < qlen || L > max_blocks * kPage || pair < 0) {
+        if (qlen < 1 || L < qlen || L > max_blocks * kPage || pair < 0 || qs < 0 ||
+            qs + qlen > num_tokens) {
           if (lane == 0) atomicOr(status, HPC_STATUS_BAD_SEQ_LEN);
           nt0 = nt1 = -1;
         } else {
@@ -399,8 +416,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       const int nt = max(d.nt[0], d.nt[1]);
       if (nt <= 0) continue;
       const int L = seq_lens[d.b];
-      if ((d.nt[0] > 0 && !wait_all(tc::kBarQReady + 0, Vl0 & 1)) ||
-          (d.nt[1] > 0 && !wait_all(tc::kBarQReady + 1, Vl1 & 1)))
+      if ((d.nt[0] > 0 && !wait_all(tc::kBarQFull + 0, Vl0 & 1)) ||
+          (d.nt[1] > 0 && !wait_all(tc::kBarQFull + 1, Vl1 & 1)))
         break;
       for (int j = 0; j < nt && !dead; ++j) {
         const uint32_t g = G + j;
@@ -425,7 +442,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         tc_fence_after();
         umma_qk_pair(tmem + 64 * ((Gl0 + j) & 1), tmem + 256 + 64 * ((Gl1 + j) & 1), desc_q,
                      desc_q + kQStep, desc_k + st * kStageStep, kIdescS, j < d.nt[0], j < d.nt[1],
-                     bar(tc::kBarSFull + ((Gl0 + j) & 1)), bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)));
+                     bar(tc::kBarSFull + ((Gl0 + j) & 1)), bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)),
+                     j == d.nt[0] - 1, j == d.nt[1] - 1, bar(tc::kBarQFree), bar(tc::kBarQFree + 1));
         if (j >= 1) issue_pv(j - 1);
       }
       if (dead) break;
@@ -452,7 +470,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     const int row = threadIdx.x & 127;                 // 8 * token + head
     const int tok = row >> 3, hl = row & 7;
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * l;
-    uint8_t* qtile = smem + tc::kOffQ + l * tc::kQBytes;
     const float scale_log2 = sm_scale * 1.4426950408889634f;
     uint32_t G = 0, U = 0, Gl = 0, Vl = 0;
     bool dead = false;
@@ -473,28 +490,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       const bool valid = i < qlen;
       const int pos = L - qlen + i;
       const int head = d.h * kGroup + hl;
-      // this row of Q into the lane's swizzled tile (zeros past the chunk);
-      // the lane's previous products, the last readers of the tile, are done
-      {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(qs + i) * kHq + head) * kD);
-#pragma unroll
-        for (int hd = 0; hd < 2; ++hd) {   // halves of d
-          uint4 v[8];
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) v[c8] = make_uint4(0u, 0u, 0u, 0u);
-          if (valid) {
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) v[c8] = src[8 * hd + c8];
-          }
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8)
-            *reinterpret_cast<uint4*>(qtile + hd * 2 * tc::kBox + row * 128 +
-                                      ((c8 ^ (row & 7)) << 4)) = v[c8];
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(tc::kBarQReady + l));
       float m_used = -INFINITY, lsum = 0.f;
       for (int j = 0; j < ntl; ++j) {
         const uint32_t g = G + j, gl = Gl + j;
@@ -601,8 +596,49 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       Gl += ntl;
       ++Vl;
     }
+  } else if (warp == tc::kWarpQ) {
+    // ---------------------------------------------------------- Q loader
+    // Each lane's Q tile, [16 tokens][8 heads][64 of d] boxes (two halves of
+    // d), is loaded once the lane's last Q K^T of the previous unit is done.
+    regs_dec<tc::kRegsOther>();
+    const uint64_t policy = l2_evict_first_policy();   // Q is read once
+    uint32_t U = 0, vq0 = 0, vq1 = 0;
+    Unit d;
+    while (true) {
+      if (!read_unit(U, d)) break;
+      ++U;
+      if (d.b < 0) break;
+      if (max(d.nt[0], d.nt[1]) <= 0) continue;
+      const int tok0 = query_start[d.b] + d.pair * tc::kUnitTokens;
+      bool ok = true;
+#pragma unroll
+      for (int l = 0; l < 2; ++l) {
+        if ((l ? d.nt[1] : d.nt[0]) <= 0) continue;
+        uint32_t& vq = l ? vq1 : vq0;
+        if (vq > 0 && !wait_all(tc::kBarQFree + l, (vq - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const uint32_t qb = bar(tc::kBarQFull + l);
+          const uint32_t dst = base + tc::kOffQ + l * tc::kQBytes;
+          const int t = tok0 + l * tc::kLaneTokens;
+          mbar_arrive_expect_tx(qb, tc::kQBytes);
+          tma_load_3d(dst, &q_map, 0, d.h * kGroup, t, qb, policy);
+          tma_load_3d(dst + 2 * tc::kBox, &q_map, 64, d.h * kGroup, t, qb, policy);
+        }
+        ++vq;
+      }
+      if (!ok) break;
+    }
+    // copies still landing after an abort
+    if (lane == 0 && *abort_flag) {
+      if (vq0 > 0) mbar_wait(bar(tc::kBarQFull + 0), (vq0 - 1) & 1, status);
+      if (vq1 > 0) mbar_wait(bar(tc::kBarQFull + 1), (vq1 - 1) & 1, status);
+    }
+    __syncwarp();
   } else {
-    regs_dec<tc::kRegsOther>();   // the idle warps of the third warpgroup
+    regs_dec<tc::kRegsOther>();   // the idle warp of the third warpgroup
   }
   // every warp is done with TMEM: free it
   tc_fence_before();

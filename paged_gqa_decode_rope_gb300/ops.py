@@ -637,7 +637,7 @@ class PrefillAttention:
         _want(out, "out", (_OUT_TORCH[self.out_dtype],), (T, HQ, D))
         scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
         check("hpc_prefill_attn", _lib.lib().hpc_prefill_attn(
-            _p(q), _p(query_start), _p(kv_cache), kv_dtype,
+            _p(q), T, _p(query_start), _p(kv_cache), kv_dtype,
             _p(kv_scale if kv_dtype == KV_FP8 else None), kv_cache.shape[0], _p(block_table),
             block_table.shape[1], _p(seq_lens), B, _p(self.unit_ptr), _p(self.counters), _p(out),
             int(self.out_dtype), scale, _p(self.status), _stream()))
