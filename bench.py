@@ -35,7 +35,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attn µs/layer-step & KV-read TB/s vs HBM peak on mixed-length batches"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_traffic.json")
-ATTN_SRC = os.path.join(ROOT, "paged_gqa_decode_rope_gb300", "csrc", "attn.cu")
+# the sources of the attention kernel; the committed traffic record holds their hash
+ATTN_SRCS = [os.path.join(ROOT, "paged_gqa_decode_rope_gb300", "csrc", f)
+             for f in ("attn.cu", "attn_kernel.cuh", "common.cuh")]
 
 
 def _parse():
@@ -49,6 +51,9 @@ def _parse():
     p.add_argument("--no-static", action="store_true", help="skip the static-schedule comparison")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-multi-token", action="store_true", help="skip the multi-token decode timings")
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill timings")
+    p.add_argument("--prefill-only", action="store_true",
+                   help="run only the prefill timings and print them as one JSON line")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
@@ -209,16 +214,23 @@ def _load_peaks():
     return 6800.0, "fallback"
 
 
+def attn_src_sha256():
+    """One hash over the attention kernel's sources (in a fixed order)."""
+    h = hashlib.sha256()
+    for p in ATTN_SRCS:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic_record():
     """Per-launch DRAM bytes of the attention kernel from the committed ncu
-    summary, if it was taken on the current attn.cu; else None."""
+    summary, if it was taken on the current kernel sources; else None."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         rec = json.load(f)
-    with open(ATTN_SRC, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()
-    if rec.get("attn_cu_sha256") != h:
+    if rec.get("attn_src_sha256") != attn_src_sha256():
         return None
     return rec
 
@@ -382,7 +394,7 @@ def run_ours(args):
     if rank == 0 and not args.no_static:
         sched = schedule_comparison(ops, wl, stream)
     mt = multi_token_times(ops, wl, stream) if rank == 0 and not args.no_multi_token else None
-    pre = prefill_times(ops, stream) if rank == 0 and not args.no_multi_token else None
+    pre = prefill_times(ops, stream) if rank == 0 and not args.no_prefill else None
 
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -480,6 +492,17 @@ def prefill_times(ops, stream, reps=10):
         res[name] = {"us": round(us, 1), "TFLOP/s": round(tf, 1),
                      "frac_of_bf16_peak": round(tf / peaks, 4) if peaks else None}
     return res
+
+
+def run_prefill_only():
+    """The prefill timings alone (one GPU), as one JSON line."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_gqa_decode_rope_gb300 import ops
+    torch.cuda.set_device(0)
+    print(json.dumps({"prefill": prefill_times(ops, torch.cuda.current_stream())}))
 
 
 def _load_peak_tflops():
@@ -599,6 +622,9 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.prefill_only:
+        run_prefill_only()
         return
     run_ours(args)
 
