@@ -452,7 +452,11 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  * itself.  Write the new tokens' K and V first (hpc_rope_norm_kvwrite on the
  * packed tokens with their own positions and slots).  Decode sequences may
  * also go through hpc_decode_attn_* (split-KV, better for long histories);
- * both read the same cache.  BF16 caches only so far.
+ * both read the same cache.  With an E4M3 cache (kv_dtype HPC_KV_FP8_E4M3,
+ * kv_scale = [k_scale, v_scale] on the device, required) the result is the
+ * attention over the dequantised cache: the products run on F16 operands
+ * (every E4M3 value is an F16 value; q is rounded to F16, exact for |q| in
+ * [2^-14, 65504]).
  * hpc_prefill_plan: unit_ptr[b] = first work unit of sequence b (8 kv heads
  * x ceil(q_len_b / 32) token blocks), unit_ptr[batch] = all units; zeroes
  * counters.  hpc_prefill_attn deals the units to a persistent grid through
@@ -473,7 +477,8 @@ int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_pla
  *                BAD_BLOCK for a block id out of range (the tile is skipped)
  * sm_scale must be positive (the softmax takes row maxima of unscaled scores).
  * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes, sm_scale <= 0 or
- * misaligned q, out or kv_cache; HPC_ERR_UNSUPPORTED for an FP8 cache, batch > 8192 or
+ * misaligned q, out or kv_cache; HPC_ERR_INVALID_ARG for an E4M3 cache without kv_scale;
+ * HPC_ERR_UNSUPPORTED for another kv_dtype, batch > 8192 or
  * num_blocks > HPC_MAX_NUM_BLOCKS. */
 int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32_t* unit_ptr,
                      int32_t* counters, int32_t* status, cudaStream_t stream);

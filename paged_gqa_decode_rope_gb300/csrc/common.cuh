@@ -257,6 +257,12 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool b_mn) 
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// The same with F16 operands.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, bool b_mn) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // D[tmem] (+)= A[smem] B[smem]; issued by one thread.
 __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                              uint32_t idesc, bool accumulate) {

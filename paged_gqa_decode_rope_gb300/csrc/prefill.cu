@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kPfPlanThreads) prefill_plan_kernel(
   }
 }
 
+template <bool kFp8>
 cudaError_t prefill_tc_smem_optin() {
   static std::mutex mu;
   static bool done[64] = {};
@@ -66,10 +67,11 @@ cudaError_t prefill_tc_smem_optin() {
   // the warpgroups' raised register budgets must fit what a CTA is launched
   // with, or the raise would wait for registers that never come
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, prefill_tc_kernel);
+  e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<kFp8>);
   if (e != cudaSuccess) return e;
-  if (fa.numRegs * tc::kThreads < tc::kRegsNeeded) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (fa.numRegs * tc::Cfg<kFp8>::kThreads < tc::regs_needed<kFp8>())
+    return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(prefill_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            tc::kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
@@ -102,8 +104,9 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   if (out_dtype != HPC_OUT_BF16 && out_dtype != HPC_OUT_FP16 && out_dtype != HPC_OUT_FP32)
     return HPC_ERR_UNSUPPORTED;
   HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(q) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0);
-  (void)kv_scale;
-  if (kv_dtype != HPC_KV_BF16) return HPC_ERR_UNSUPPORTED;   // an E4M3 cache: not yet
+  if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+  const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+  HPC_CHECK_ARG(!fp8 || kv_scale != nullptr);
   if (batch > HPC_MAX_BATCH || num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
   if (batch == 0 || num_tokens == 0) return HPC_OK;
@@ -112,10 +115,12 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hpc::kD),
                               static_cast<cuuint64_t>(num_blocks) * 2 * hpc::kHkv * hpc::kPage};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hpc::kD) * 2};
-  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(hpc::kPage)};
+  // rows of 128 BF16 (two 64-element boxes per page) or 128 E4M3 codes (one box)
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hpc::kD) * (fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(hpc::kPage)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_cache),
+  const CUresult cr = encode(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             2, const_cast<void*>(kv_cache),
                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -138,9 +143,16 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
-  if (hpc::prefill_tc_smem_optin() != cudaSuccess) return HPC_ERR_CUDA;
-  hpc::prefill_tc_kernel<<<sms, hpc::tc::kThreads, hpc::tc::kSmemBytes, stream>>>(
-      map, q_map, num_tokens, query_start, seq_lens, batch, block_table, max_blocks,
-      num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
+  if (fp8) {
+    if (hpc::prefill_tc_smem_optin<true>() != cudaSuccess) return HPC_ERR_CUDA;
+    hpc::prefill_tc_kernel<true><<<sms, hpc::tc::Cfg<true>::kThreads, hpc::tc::kSmemBytes, stream>>>(
+        map, q_map, num_tokens, kv_scale, query_start, seq_lens, batch, block_table, max_blocks,
+        num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
+  } else {
+    if (hpc::prefill_tc_smem_optin<false>() != cudaSuccess) return HPC_ERR_CUDA;
+    hpc::prefill_tc_kernel<false><<<sms, hpc::tc::Cfg<false>::kThreads, hpc::tc::kSmemBytes, stream>>>(
+        map, q_map, num_tokens, kv_scale, query_start, seq_lens, batch, block_table, max_blocks,
+        num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
+  }
   return HPC_LAUNCH_STATUS();
 }

@@ -27,6 +27,13 @@
 // block id is bad) are zeroed before any P V reads them: the cache may hold
 // NaN there.  Every mbarrier wait is bounded; on a timeout the CTA winds
 // down, lets its copies and products finish, and frees its TMEM.
+//
+// E4M3 caches (kFp8): a converter warpgroup turns each landed page of codes
+// into F16 (every E4M3 value is an F16 value) in a second ring the MMA warp
+// reads, and turns each lane's BF16 Q tile into F16 in place (exact for
+// |q| in [2^-14, 65504]); both products then run on F16 operands.  The K
+// scale joins the softmax scale and the V scale the final division, so the
+// result is the attention over the dequantised cache.
 #pragma once
 
 #include "common.cuh"
@@ -36,39 +43,67 @@ namespace {
 namespace tc {
 
 // warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: K/V producer, 9: MMA,
-// 10: Q loader, 11: idle (the third warpgroup lends registers to the softmax)
-constexpr int kThreads = 384;
+// 10: Q loader, 11: idle, 12-15 (E4M3 caches): converter.  The third (and
+// fourth) warpgroup lend registers to the softmax warpgroups.
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpQ = 10;
-constexpr uint32_t kRegsSoftmax = 200;
-constexpr uint32_t kRegsOther = 104;
-constexpr int kRegsNeeded = 256 * kRegsSoftmax + 128 * kRegsOther;   // per CTA
-constexpr int kStages = 4;
+constexpr int kWarpConv0 = 12;
+constexpr int kPStages = 4;                         // producer ring (TMA)
 constexpr int kBox = 64 * 128;                      // one 64-row x 128-byte TMA box
 constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (d = 128)
-constexpr int kStageBytes = 2 * kPage;              // K page + V page
-constexpr int kOffQ = kStages * kStageBytes;        // per lane: 2 halves of d x 128 rows x 128 B
+constexpr int kTileBytes = 2 * kPage;               // K + V of one tile as the MMA reads them
+constexpr int kOffQ = 4 * kTileBytes;               // per lane: 2 halves of d x 128 rows x 128 B
 constexpr int kQBytes = 2 * 128 * 128;
 constexpr int kOffBar = kOffQ + 2 * kQBytes;
+
+template <bool kFp8>
+struct Cfg;
+template <>
+struct Cfg<false> {   // BF16 cache: the MMA reads the TMA ring itself
+  static constexpr int kThreads = 384;
+  static constexpr int kPStageBytes = 2 * kPage;    // K page + V page
+  static constexpr int kMStages = kPStages;         // tiles the MMA side holds
+  static constexpr int kOffM = 0;
+  static constexpr uint32_t kRegsSoftmax = 200, kRegsMid = 104, kRegsConv = 0;
+  static constexpr int kUnitReaders = 10;           // MMA, Q loader, 8 softmax warps
+};
+template <>
+struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a second ring
+  static constexpr int kThreads = 512;
+  static constexpr int kPStageBytes = 2 * 64 * 128; // K codes + V codes
+  static constexpr int kMStages = 2;
+  static constexpr int kOffM = kPStages * kPStageBytes;
+  static constexpr uint32_t kRegsSoftmax = 184, kRegsMid = 88, kRegsConv = 56;
+  static constexpr int kUnitReaders = 14;           // + the 4 converter warps
+};
+template <bool kFp8>
+constexpr int regs_needed() {   // per CTA, for the warpgroups' raised budgets
+  return 256 * Cfg<kFp8>::kRegsSoftmax + 128 * Cfg<kFp8>::kRegsMid + 128 * Cfg<kFp8>::kRegsConv;
+}
+
 // mbarriers (index of the first of each kind; [l] per lane, [l][i] per lane and buffer)
-constexpr int kBarFull = 0;        // [4] stage landed (TMA)
-constexpr int kBarEmpty = 4;       // [4] stage consumed (both lanes' P V of the tile done)
-constexpr int kBarSFull = 8;       // [2][2] scores written
-constexpr int kBarPFull = 12;      // [2] P of both lanes written (256 arrivals; a lane
+constexpr int kBarRawFull = 0;     // [4] producer stage landed (TMA)
+constexpr int kBarRawEmpty = 4;    // [4] producer stage consumed (BF16: the tile's P V products;
+                                   //     E4M3: the 128 converter threads)
+constexpr int kBarMFull = 8;       // [2] E4M3: F16 tile written (128 converter threads)
+constexpr int kBarMEmpty = 10;     // [2] E4M3: F16 tile consumed (both lanes' P V done)
+constexpr int kBarSFull = 12;      // [2][2] scores written
+constexpr int kBarPFull = 16;      // [2] P of both lanes written (256 arrivals; a lane
                                    //     without the tile arrives for it twice)
-constexpr int kBarOFinal = 14;     // [2] the lane's last P V of a unit done
-constexpr int kBarOFree = 16;      // [2] the lane's O read out (128 softmax threads)
-constexpr int kBarQFull = 18;      // [2] the lane's Q tile landed (TMA)
-constexpr int kBarQFree = 20;      // [2] the lane's last Q K^T of a unit done
-constexpr int kBarUnitFull = 22;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 24;  // [2] unit descriptor read (MMA, Q loader, 8 softmax warps)
-constexpr int kBarDrain = 26;      // every product of the MMA warp done (at exit)
-constexpr int kNumBars = 27;
+constexpr int kBarOFinal = 18;     // [2] the lane's last P V of a unit done
+constexpr int kBarOFree = 20;      // [2] the lane's O read out (128 softmax threads)
+constexpr int kBarQFull = 22;      // [2] the lane's Q tile landed (TMA)
+constexpr int kBarQReady = 24;     // [2] E4M3: the lane's Q tile turned into F16 (128 threads)
+constexpr int kBarQFree = 26;      // [2] the lane's last Q K^T of a unit done
+constexpr int kBarUnitFull = 28;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 30;  // [2] unit descriptor read (every warp that follows units)
+constexpr int kBarDrain = 32;      // every product of the MMA warp done (at exit)
+constexpr int kNumBars = 33;
 constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
-constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;
-constexpr int kOffMisc = kOffOk + kStages * 4;      // [0] abort flag, [1] TMEM address
+constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;   // [4] producer stages, [2] F16 tiles
+constexpr int kOffMisc = kOffOk + 8 * 4;            // [0] abort flag, [1] TMEM address
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;    // + slack for the 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;                 // lane l: S 256l + {0, 64}, O 256l + 128
 constexpr int kLaneTokens = 16;
@@ -180,9 +215,10 @@ __device__ __forceinline__ void umma_pv_pair(uint32_t tmem, uint32_t p0, uint32_
 #undef HPC_PV_STEP
 }
 
-__global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
+template <bool kFp8>
+__global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-    int32_t num_tokens, const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
+    int32_t num_tokens, const float* __restrict__ kv_scale, const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
     const int32_t* __restrict__ block_table, int32_t max_blocks, int32_t num_blocks,
     const int32_t* __restrict__ unit_ptr, int32_t* counters, void* __restrict__ out,
     int32_t out_dtype, float sm_scale, int32_t* __restrict__ status) {
@@ -192,7 +228,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tc::kOffBar);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   volatile int* ring = reinterpret_cast<volatile int*>(smem + tc::kOffRing);
+  using C = tc::Cfg<kFp8>;
+  // per producer stage and per tile the MMA side holds: 1 = a good block
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + tc::kOffOk);
+  volatile int* tile_ok_of = kFp8 ? stage_ok + tc::kPStages : stage_ok;
+  // the MMA side's ring: the TMA stages themselves, or the F16 tiles
+  constexpr int kBarTileFull = kFp8 ? tc::kBarMFull : tc::kBarRawFull;
+  constexpr int kBarTileEmpty = kFp8 ? tc::kBarMEmpty : tc::kBarRawEmpty;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc::kOffMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -200,9 +242,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
   const uint32_t base = smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < tc::kStages; ++s) {
-      mbar_init(bar(tc::kBarFull + s), 1);
-      mbar_init(bar(tc::kBarEmpty + s), 1);
+    for (int s = 0; s < tc::kPStages; ++s) {
+      mbar_init(bar(tc::kBarRawFull + s), 1);
+      mbar_init(bar(tc::kBarRawEmpty + s), kFp8 ? 128 : 1);
+    }
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(bar(tc::kBarMFull + c), 128);
+      mbar_init(bar(tc::kBarMEmpty + c), 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(bar(tc::kBarSFull + i), 1);
     for (int l = 0; l < 2; ++l) {
@@ -210,9 +256,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(tc::kBarOFinal + l), 1);
       mbar_init(bar(tc::kBarOFree + l), 128);
       mbar_init(bar(tc::kBarQFull + l), 1);
+      mbar_init(bar(tc::kBarQReady + l), 128);
       mbar_init(bar(tc::kBarQFree + l), 1);
       mbar_init(bar(tc::kBarUnitFull + l), 1);
-      mbar_init(bar(tc::kBarUnitEmpty + l), 10);
+      mbar_init(bar(tc::kBarUnitEmpty + l), C::kUnitReaders);
     }
     mbar_init(bar(tc::kBarDrain), 1);
     *abort_flag = 0;
@@ -258,7 +305,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
 
   if (warp == tc::kWarpProd) {
     // ---------------------------------------------------------- producer
-    regs_dec<tc::kRegsOther>();
+    regs_dec<C::kRegsMid>();
     // every pair of new tokens of a sequence reads the KV head's pages again
     const uint64_t policy = l2_evict_last_policy();
     uint32_t g = 0, n_pushed = 0;   // stream tiles issued, units handed on
@@ -322,41 +369,49 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         for (int jj = 0; jj < min(32, ntiles - tb) && alive; ++jj) {
           const int bid = __shfl_sync(0xffffffffu, bids, jj);
           const bool good = bid >= 0 && bid < num_blocks;
-          const int s = static_cast<int>(g % tc::kStages);
+          const int s = static_cast<int>(g % tc::kPStages);
           int tok = 1;
           if (lane == 0) {
-            const uint32_t use = g / tc::kStages;
+            const uint32_t use = g / tc::kPStages;
             if (*abort_flag) {
               tok = 0;
-            } else if (use > 0 && !mbar_wait(bar(tc::kBarEmpty + s), (use - 1) & 1, status)) {
+            } else if (use > 0 && !mbar_wait(bar(tc::kBarRawEmpty + s), (use - 1) & 1, status)) {
               *abort_flag = 1;
               tok = 0;
             }
             if (tok && good) {
               stage_ok[s] = 1;
-              const uint32_t fb = bar(tc::kBarFull + s);
-              mbar_arrive_expect_tx(fb, tc::kStageBytes);
-              const uint32_t dst = base + s * tc::kStageBytes;
+              const uint32_t fb = bar(tc::kBarRawFull + s);
+              mbar_arrive_expect_tx(fb, C::kPStageBytes);
+              const uint32_t dst = base + s * C::kPStageBytes;
               const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;
               const int yv = yk + kHkv * kPage;
-              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-              tma_load_2d(dst + tc::kBox, &kv_map, 64, yk, fb, policy);
-              tma_load_2d(dst + tc::kPage, &kv_map, 0, yv, fb, policy);
-              tma_load_2d(dst + tc::kPage + tc::kBox, &kv_map, 64, yv, fb, policy);
+              if constexpr (kFp8) {   // one 64-row x 128-code box per page
+                tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
+                tma_load_2d(dst + C::kPStageBytes / 2, &kv_map, 0, yv, fb, policy);
+              } else {                // two 64-row x 64-element boxes per page
+                tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
+                tma_load_2d(dst + tc::kBox, &kv_map, 64, yk, fb, policy);
+                tma_load_2d(dst + tc::kPage, &kv_map, 0, yv, fb, policy);
+                tma_load_2d(dst + tc::kPage + tc::kBox, &kv_map, 64, yv, fb, policy);
+              }
             }
           }
           tok = __shfl_sync(0xffffffffu, tok, 0);
           if (tok && !good) {
-            // a bad block id: no copy; the stage's V becomes zeros and the
-            // stage is marked, so the softmax masks its keys (status set)
-            uint4* vst = reinterpret_cast<uint4*>(smem + s * tc::kStageBytes + tc::kPage);
-            for (int z = lane; z < tc::kPage / 16; z += 32) vst[z] = make_uint4(0u, 0u, 0u, 0u);
-            fence_proxy_async_smem();
+            // a bad block id: no copy; the stage is marked (its keys are
+            // masked, its V rows zeroed: here for BF16, by the converter for
+            // E4M3) and the status set
+            if constexpr (!kFp8) {
+              uint4* vst = reinterpret_cast<uint4*>(smem + s * C::kPStageBytes + tc::kPage);
+              for (int z = lane; z < tc::kPage / 16; z += 32) vst[z] = make_uint4(0u, 0u, 0u, 0u);
+              fence_proxy_async_smem();
+            }
             __syncwarp();
             if (lane == 0) {
               atomicOr(status, HPC_STATUS_BAD_BLOCK);
               stage_ok[s] = 0;
-              mbar_arrive(bar(tc::kBarFull + s));
+              mbar_arrive(bar(tc::kBarRawFull + s));
             }
           }
           alive = __shfl_sync(0xffffffffu, tok, 0) != 0;
@@ -370,9 +425,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         counters[1] = 0;
       }
       if (*abort_flag) {   // copies still landing in stages nobody waits on
-        for (uint32_t s = 0; s < static_cast<uint32_t>(tc::kStages) && s < g; ++s) {
-          const uint32_t last = s + tc::kStages * ((g - 1 - s) / tc::kStages);
-          mbar_wait(bar(tc::kBarFull + s), (last / tc::kStages) & 1, status);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(tc::kPStages) && s < g; ++s) {
+          const uint32_t last = s + tc::kPStages * ((g - 1 - s) / tc::kPStages);
+          mbar_wait(bar(tc::kBarRawFull + s), (last / tc::kPStages) & 1, status);
         }
       }
     }
@@ -380,14 +435,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     // ---------------------------------------------------------- MMA issuer
     // The whole warp runs the loop (descriptors warp-uniform); one elected
     // thread issues each chain of products and each commit.
-    regs_dec<tc::kRegsOther>();
-    constexpr uint32_t kIdescS = umma_idesc_bf16(128, 64, false);
-    constexpr uint32_t kIdescO = umma_idesc_bf16(128, 128, true);
+    regs_dec<C::kRegsMid>();
+    constexpr uint32_t kIdescS = kFp8 ? umma_idesc_f16(128, 64, false) : umma_idesc_bf16(128, 64, false);
+    constexpr uint32_t kIdescO = kFp8 ? umma_idesc_f16(128, 128, true) : umma_idesc_bf16(128, 128, true);
     // descriptors of the first step of each operand; a step adds a constant
     const uint64_t desc_q = umma_smem_desc(base + tc::kOffQ, 1024, 1024);
-    const uint64_t desc_k = umma_smem_desc(base, 1024, 1024);
-    const uint64_t desc_v = umma_smem_desc(base + tc::kPage, tc::kBox, 1024);
-    constexpr uint64_t kStageStep = tc::kStageBytes >> 4;
+    const uint64_t desc_k = umma_smem_desc(base + C::kOffM, 1024, 1024);
+    const uint64_t desc_v = umma_smem_desc(base + C::kOffM + tc::kPage, tc::kBox, 1024);
+    constexpr uint64_t kStageStep = tc::kTileBytes >> 4;
     constexpr uint64_t kQStep = tc::kQBytes >> 4;
     uint32_t G = 0, U = 0;          // stream tiles, unit descriptors read
     uint32_t Gl0 = 0, Gl1 = 0;      // tiles of each lane
@@ -396,7 +451,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     Unit d;
     // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
     auto issue_pv = [&](int jj) {
-      const uint32_t g = G + jj, st = g % tc::kStages;
+      const uint32_t g = G + jj, st = g % C::kMStages;
       if (dead || !wait_all(tc::kBarPFull + (g & 1), (g >> 1) & 1) ||
           (jj == 0 && ((d.nt[0] > 0 && Vl0 > 0 && !wait_all(tc::kBarOFree + 0, (Vl0 - 1) & 1)) ||
                        (d.nt[1] > 0 && Vl1 > 0 && !wait_all(tc::kBarOFree + 1, (Vl1 - 1) & 1))))) {
@@ -407,7 +462,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       umma_pv_pair(tmem, tmem + 64 * ((Gl0 + jj) & 1), tmem + 256 + 64 * ((Gl1 + jj) & 1),
                    desc_v + st * kStageStep, kIdescO, jj != 0, jj < d.nt[0], jj < d.nt[1],
                    jj == d.nt[0] - 1, jj == d.nt[1] - 1, bar(tc::kBarOFinal), bar(tc::kBarOFinal + 1),
-                   bar(tc::kBarEmpty + st));
+                   bar(kBarTileEmpty + st));
     };
     while (!dead) {
       if (!read_unit(U, d)) break;
@@ -416,22 +471,23 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       const int nt = max(d.nt[0], d.nt[1]);
       if (nt <= 0) continue;
       const int L = seq_lens[d.b];
-      if ((d.nt[0] > 0 && !wait_all(tc::kBarQFull + 0, Vl0 & 1)) ||
-          (d.nt[1] > 0 && !wait_all(tc::kBarQFull + 1, Vl1 & 1)))
+      constexpr int kBarQ = kFp8 ? tc::kBarQReady : tc::kBarQFull;   // Q as the MMA reads it
+      if ((d.nt[0] > 0 && !wait_all(kBarQ + 0, Vl0 & 1)) ||
+          (d.nt[1] > 0 && !wait_all(kBarQ + 1, Vl1 & 1)))
         break;
       for (int j = 0; j < nt && !dead; ++j) {
         const uint32_t g = G + j;
-        const uint32_t st = g % tc::kStages;
-        if (!wait_all(tc::kBarFull + st, (g / tc::kStages) & 1)) {
+        const uint32_t st = g % C::kMStages;
+        if (!wait_all(kBarTileFull + st, (g / C::kMStages) & 1)) {
           dead = true;
           break;
         }
         // V rows past the sequence length (the cache may hold NaN there) ->
         // zeros before any P V of the tile reads them; only the page of the
-        // sequence's last key has such rows
+        // sequence's last key has such rows (the converter does it for E4M3)
         const int keep = L - 64 * j;
-        if (keep < 64) {
-          uint4* vst = reinterpret_cast<uint4*>(smem + st * tc::kStageBytes + tc::kPage);
+        if (!kFp8 && keep < 64) {
+          uint4* vst = reinterpret_cast<uint4*>(smem + st * tc::kTileBytes + tc::kPage);
           for (int z = keep * 8 + lane; z < 64 * 8; z += 32) {   // rows keep..63, both boxes
             vst[z] = make_uint4(0u, 0u, 0u, 0u);
             vst[tc::kBox / 16 + z] = make_uint4(0u, 0u, 0u, 0u);
@@ -465,12 +521,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     __syncwarp();
   } else if (warp < 8) {
     // ---------------------------------------------------------- softmax warpgroups
-    regs_inc<tc::kRegsSoftmax>();
+    regs_inc<C::kRegsSoftmax>();
     const int l = warp >> 2;                           // lane (tile) of the unit
     const int row = threadIdx.x & 127;                 // 8 * token + head
     const int tok = row >> 3, hl = row & 7;
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * l;
-    const float scale_log2 = sm_scale * 1.4426950408889634f;
+    // E4M3: scores of the codes times the K scale, outputs times the V scale
+    const float scale_log2 = sm_scale * 1.4426950408889634f * (kFp8 ? kv_scale[0] : 1.f);
+    const float v_scale = kFp8 ? kv_scale[1] : 1.f;
     uint32_t G = 0, U = 0, Gl = 0, Vl = 0;
     bool dead = false;
     Unit d;
@@ -493,9 +551,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       float m_used = -INFINITY, lsum = 0.f;
       for (int j = 0; j < ntl; ++j) {
         const uint32_t g = G + j, gl = Gl + j;
-        const int s = static_cast<int>(g % tc::kStages);
+        const int s = static_cast<int>(g % C::kMStages);
         if (!wait_all(tc::kBarSFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
-            !wait_all(tc::kBarFull + s, (g / tc::kStages) & 1)) {
+            !wait_all(kBarTileFull + s, (g / C::kMStages) & 1)) {
           dead = true;
           break;
         }
@@ -503,7 +561,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         uint32_t sr[64];
         tmem_ld64(trow + 64 * (gl & 1), sr);
         tmem_wait_ld();
-        const bool tile_ok = stage_ok[s] != 0;
+        const bool tile_ok = tile_ok_of[s] != 0;
         const int key0 = j * kPage;
         // keys of this tile the row sees: 0 .. lim (none for lim < 0); only
         // the tiles on a row's diagonal (or a bad tile) need the mask
@@ -536,7 +594,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
           // the previous tile's P V must be in O before it is rescaled: its
           // stage is emptied once both lanes' P V of it are done
-          if (!wait_all(tc::kBarEmpty + (g - 1) % tc::kStages, ((g - 1) / tc::kStages) & 1)) {
+          if (!wait_all(kBarTileEmpty + (g - 1) % C::kMStages, ((g - 1) / C::kMStages) & 1)) {
             dead = true;
             break;
           }
@@ -552,7 +610,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           }
         }
         // p = 2^(s * scale - m) as one FMA and one exponential, packed as
-        // BF16 pairs over the scores; the row sum in 4 independent chains
+        // BF16 (F16 for E4M3 caches) pairs over the scores; the row sum in 4
+        // independent chains
         const float nms = m_used == -INFINITY ? 0.f : -m_used;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
@@ -561,7 +620,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
           const float p0 = exp2_ftz(fmaf(x[2 * jk], scale_log2, nms));
           const float p1 = exp2_ftz(fmaf(x[2 * jk + 1], scale_log2, nms));
           ps[jk & 3] += p0 + p1;
-          pk[jk] = pack_bf16(p0, p1);
+          pk[jk] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
         }
         lsum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         tmem_st32(trow + 64 * (gl & 1), pk);
@@ -573,7 +632,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       // the row of O once the lane's last P V is done: divide by the row sum, store
       if (!wait_all(tc::kBarOFinal + l, Vl & 1)) break;
       tc_fence_after();
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float inv = lsum > 0.f ? v_scale / lsum : 0.f;
       const int64_t orow = (static_cast<int64_t>(qs + i) * kHq + head) * kD;
 #pragma unroll
       for (int qc = 0; qc < 4; ++qc) {
@@ -600,7 +659,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
     // ---------------------------------------------------------- Q loader
     // Each lane's Q tile, [16 tokens][8 heads][64 of d] boxes (two halves of
     // d), is loaded once the lane's last Q K^T of the previous unit is done.
-    regs_dec<tc::kRegsOther>();
+    regs_dec<C::kRegsMid>();
     const uint64_t policy = l2_evict_first_policy();   // Q is read once
     uint32_t U = 0, vq0 = 0, vq1 = 0;
     Unit d;
@@ -637,8 +696,107 @@ __global__ void __launch_bounds__(tc::kThreads, 1) prefill_tc_kernel(
       if (vq1 > 0) mbar_wait(bar(tc::kBarQFull + 1), (vq1 - 1) & 1, status);
     }
     __syncwarp();
+  } else if (kFp8 && warp >= tc::kWarpConv0) {
+    // ---------------------------------------------------------- converter (E4M3)
+    // Per unit: each lane's Q tile BF16 -> F16 in place (thread = row), then
+    // each tile's K and V codes -> F16 into the MMA side's ring, in the
+    // layout a BF16 stage has (two 64-column boxes per page, 128-byte
+    // swizzle); V rows past the sequence length, or of a bad block, -> 0.
+    regs_dec<C::kRegsConv>();
+    const int t = static_cast<int>(threadIdx.x) - 32 * tc::kWarpConv0;   // 0 .. 127
+    uint32_t G = 0, U = 0, vq0 = 0, vq1 = 0;
+    bool dead = false;
+    Unit d;
+    while (!dead) {
+      if (!read_unit(U, d)) break;
+      ++U;
+      if (d.b < 0) break;
+      const int nt = max(d.nt[0], d.nt[1]);
+      if (nt <= 0) continue;
+      const int L = seq_lens[d.b];
+#pragma unroll
+      for (int l = 0; l < 2; ++l) {
+        if (dead || (l ? d.nt[1] : d.nt[0]) <= 0) continue;
+        uint32_t& vq = l ? vq1 : vq0;
+        if (!wait_all(tc::kBarQFull + l, vq & 1)) {
+          dead = true;
+          break;
+        }
+        uint8_t* qrow = smem + tc::kOffQ + l * tc::kQBytes + t * 128;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {   // 8 BF16 -> 8 F16 per 16-byte chunk, in place
+          uint4* p = reinterpret_cast<uint4*>(qrow + (c >> 3) * 2 * tc::kBox + (c & 7) * 16);
+          uint4 w = *p;
+          w.x = pack_f16(bf16_lo(w.x), bf16_hi(w.x));
+          w.y = pack_f16(bf16_lo(w.y), bf16_hi(w.y));
+          w.z = pack_f16(bf16_lo(w.z), bf16_hi(w.z));
+          w.w = pack_f16(bf16_lo(w.w), bf16_hi(w.w));
+          *p = w;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(tc::kBarQReady + l));
+        ++vq;
+      }
+      for (int j = 0; j < nt && !dead; ++j) {
+        const uint32_t g = G + j;
+        const int s = static_cast<int>(g % tc::kPStages);
+        const int c = static_cast<int>(g % C::kMStages);
+        if (!wait_all(tc::kBarRawFull + s, (g / tc::kPStages) & 1) ||
+            (g >= static_cast<uint32_t>(C::kMStages) &&
+             !wait_all(tc::kBarMEmpty + c, ((g - C::kMStages) / C::kMStages) & 1))) {
+          dead = true;
+          break;
+        }
+        const bool ok = stage_ok[s] != 0;
+        const int keep = ok ? max(0, min(64, L - 64 * j)) : 0;
+        const uint8_t* raw = smem + s * C::kPStageBytes;
+        uint8_t* dst = smem + C::kOffM + c * tc::kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // source chunk: row r, 16 codes (d = 16 lc .. 16 lc + 15) at
+          // physical chunk sc; destination: half lc / 4 of d, logical
+          // chunks 2 (lc % 4) and the next, swizzled by the row
+          const int z = t + 128 * k, r = z >> 3, sc = z & 7, lc = sc ^ (r & 7);
+          const int hd = lc >> 2, dl = (lc & 3) * 2;
+          const int o0 = hd * tc::kBox + r * 128 + ((dl ^ (r & 7)) << 4);
+          const int o1 = hd * tc::kBox + r * 128 + (((dl + 1) ^ (r & 7)) << 4);
+          if (ok) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + sc * 16);
+            *reinterpret_cast<uint4*>(dst + o0) =
+                make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+            *reinterpret_cast<uint4*>(dst + o1) =
+                make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)),
+                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
+          }
+          uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+          if (r < keep) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + C::kPStageBytes / 2 + r * 128 + sc * 16);
+            v0 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+            v1 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)),
+                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
+          }
+          *reinterpret_cast<uint4*>(dst + tc::kPage + o0) = v0;
+          *reinterpret_cast<uint4*>(dst + tc::kPage + o1) = v1;
+        }
+        if (t == 0) tile_ok_of[c] = ok ? 1 : 0;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(tc::kBarMFull + c));
+        mbar_arrive(bar(tc::kBarRawEmpty + s));
+      }
+      G += nt;
+    }
   } else {
-    regs_dec<tc::kRegsOther>();   // the idle warp of the third warpgroup
+    regs_dec<C::kRegsMid>();   // the idle warp of the third warpgroup
   }
   // every warp is done with TMEM: free it
   tc_fence_before();

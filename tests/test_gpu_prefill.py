@@ -14,16 +14,21 @@ import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-def _batch(lengths, q_lens, seed):
+def _batch(lengths, q_lens, seed, kv_dtype=0):
     from paged_gqa_decode_rope_gb300.workloads import Workload
-    wl = Workload("custom", seed=seed, lengths=lengths, kv_dtype=0, include_new_token=True)
+    wl = Workload("custom", seed=seed, lengths=lengths, kv_dtype=kv_dtype, include_new_token=True)
     qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     g = torch.Generator(device="cuda").manual_seed(seed)
     q = torch.randn((int(qs[-1]), 64, 128), generator=g, device="cuda").to(torch.bfloat16)
     return wl, q, torch.as_tensor(qs, device="cuda"), qs
 
 
-def _check(wl, q, qs, out, seqs=None, heads=None, tol=(gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN)):
+def _check(wl, q, qs, out, seqs=None, heads=None, tol=None):
+    """Against the oracle over the cache as it is on the device (an E4M3
+    cache through the oracle's own decoder and the per-tensor scales)."""
+    if tol is None:
+        tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if wl.kv_dtype == 0 else (gu.TOL_FP8_MAX, None)
+    ks, vs = [float(x) for x in wl.kv_scale.cpu().numpy()] if wl.kv_dtype == 1 else (1.0, 1.0)
     got = out.float().cpu().numpy().astype(np.float64)
     qh = gu.bf16_host(q)
     for b in (range(wl.batch) if seqs is None else seqs):
@@ -32,7 +37,7 @@ def _check(wl, q, qs, out, seqs=None, heads=None, tol=(gu.TOL_BF16_MAX, gu.TOL_B
             continue
         L = int(wl.lengths[b])
         sub, row = gu.seq_view(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
-        want = od.decode_attention_mt(qh[a:e], sub, row, L, wl.kv_dtype, heads=heads)
+        want = od.decode_attention_mt(qh[a:e], sub, row, L, wl.kv_dtype, ks, vs, heads=heads)
         gu.compare(got[a:e], want, *tol, label="seq %d (L=%d, q_len=%d)" % (b, L, e - a))
 
 
@@ -130,33 +135,62 @@ def test_prefill_bad_lengths_set_status_and_skip():
     _check(wl, q, qs, out, seqs=[1])
 
 
-def test_prefill_bad_block_is_reported_and_skipped():
+@pytest.mark.parametrize("kv_dtype", [0, 1])
+def test_prefill_bad_block_is_reported_and_skipped(kv_dtype):
     """A block id past the cache: the status says BAD_BLOCK, the page's keys
     are left out of that sequence's attention, the other sequences are
-    untouched."""
+    untouched (BF16 and E4M3 caches)."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     lengths = [300, 260, 100]
     q_lens = [40, 70, 100]
-    wl, q, qst, qs = _batch(lengths, q_lens, 17)
+    wl, q, qst, qs = _batch(lengths, q_lens, 17, kv_dtype)
     wl.block_table[1, 2] = wl.num_blocks + 5           # page 2 (keys 128..191) of sequence 1
     pf = ops.PrefillAttention(wl.batch)
     pf.plan(qst)
     out = torch.empty_like(q)
-    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    pf(q, qst, wl.cache, kv_dtype, wl.kv_scale, wl.block_table, wl.seq_lens, out)
     torch.cuda.synchronize()
     assert int(pf.status.item()) & 1                   # HPC_STATUS_BAD_BLOCK
     _check(wl, q, qs, out, seqs=[0, 2])
     L, n = lengths[1], q_lens[1]
-    sub, row = gu.seq_view(wl.cache, wl.block_table_np[1], L, 0)
+    sub, row = gu.seq_view(wl.cache, wl.block_table_np[1], L, kv_dtype)
+    ks, vs = [float(x) for x in wl.kv_scale.cpu().numpy()] if kv_dtype == 1 else (1.0, 1.0)
     qh = gu.bf16_host(q)[int(qs[1]):int(qs[2])]
     keep = np.r_[0:128, 192:L]
     want = np.zeros((n, 64, 128))
     for h in range(8):
-        K, V = od.gather_kv(sub, row, L, h, 0, 1.0, 1.0)
+        K, V = od.gather_kv(sub, row, L, h, kv_dtype, ks, vs)
         for t in range(n):
             vis = keep[keep <= L - n + t]
             for j in range(8 * h, 8 * h + 8):
                 want[t, j] = od.attention_head(qh[t, j], K[vis], V[vis], 1.0 / np.sqrt(128))
+    tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if kv_dtype == 0 else (gu.TOL_FP8_MAX, None)
     gu.compare(out[int(qs[1]):int(qs[2])].float().cpu().numpy().astype(np.float64), want,
-               gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN, label="seq 1 without page 2")
+               *tol, label="seq 1 without page 2")
+
+
+def test_prefill_fp8_cache_prompts_and_chunks():
+    """An E4M3 cache: whole prompts and chunks after a history (tile and block
+    edges, a lane without tokens), against the oracle over the device's cache
+    codes and scales; FP16 and FP32 outputs are the same values."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [1, 16, 17, 64, 65, 130, 300, 1000, 2200]
+    q_lens = [1, 16, 17, 64, 65, 130, 37, 200, 33]
+    wl, q, qst, qs = _batch(lengths, q_lens, 23, kv_dtype=1)
+    outs = {}
+    for od_ in (ops.OUT_BF16, ops.OUT_FP32, ops.OUT_FP16):
+        pf = ops.PrefillAttention(wl.batch, out_dtype=od_)
+        pf.plan(qst)
+        o = torch.full((q.shape[0], 64, 128), float("nan"), device="cuda",
+                       dtype={ops.OUT_BF16: torch.bfloat16, ops.OUT_FP32: torch.float32,
+                              ops.OUT_FP16: torch.float16}[od_])
+        outs[od_] = pf(q, qst, wl.cache, 1, wl.kv_scale, wl.block_table, wl.seq_lens, o)
+        torch.cuda.synchronize()
+        assert int(pf.status.item()) == 0
+        assert int(pf.counters.abs().sum().item()) == 0
+    assert torch.equal(outs[ops.OUT_FP16], outs[ops.OUT_FP32].to(torch.float16))
+    assert torch.equal(outs[ops.OUT_BF16], outs[ops.OUT_FP32].to(torch.bfloat16))
+    _check(wl, q, qs, outs[ops.OUT_FP32])
+    _check(wl, q, qs, outs[ops.OUT_BF16])
