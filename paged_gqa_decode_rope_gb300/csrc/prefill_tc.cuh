@@ -49,34 +49,41 @@ constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpQ = 10;
 constexpr int kWarpConv0 = 12;
-constexpr int kPStages = 4;                         // producer ring (TMA)
 constexpr int kBox = 64 * 128;                      // one 64-row x 128-byte TMA box
 constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (d = 128)
 constexpr int kTileBytes = 2 * kPage;               // K + V of one tile as the MMA reads them
-constexpr int kOffQ = 4 * kTileBytes;               // per lane: 2 halves of d x 128 rows x 128 B
-constexpr int kQBytes = 2 * 128 * 128;
-constexpr int kOffBar = kOffQ + 2 * kQBytes;
+constexpr int kQBytes = 2 * 128 * 128;              // per lane: 2 halves of d x 128 rows x 128 B
+constexpr int kOffBar = 208 * 1024;                 // after the rings and Q of either layout
 
 template <bool kFp8>
 struct Cfg;
 template <>
 struct Cfg<false> {   // BF16 cache: the MMA reads the TMA ring itself
   static constexpr int kThreads = 384;
+  static constexpr int kPStages = 4;                // producer ring (TMA)
   static constexpr int kPStageBytes = 2 * kPage;    // K page + V page
   static constexpr int kMStages = kPStages;         // tiles the MMA side holds
   static constexpr int kOffM = 0;
+  static constexpr int kOffQ = kMStages * kTileBytes;
   static constexpr uint32_t kRegsSoftmax = 200, kRegsMid = 104, kRegsConv = 0;
   static constexpr int kUnitReaders = 10;           // MMA, Q loader, 8 softmax warps
 };
 template <>
 struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a second ring
   static constexpr int kThreads = 512;
+  static constexpr int kPStages = 3;
   static constexpr int kPStageBytes = 2 * 64 * 128; // K codes + V codes
-  static constexpr int kMStages = 2;
+  static constexpr int kMStages = 3;
   static constexpr int kOffM = kPStages * kPStageBytes;
+  static constexpr int kOffQ = kOffM + kMStages * kTileBytes;
   static constexpr uint32_t kRegsSoftmax = 184, kRegsMid = 88, kRegsConv = 56;
   static constexpr int kUnitReaders = 14;           // + the 4 converter warps
 };
+static_assert(Cfg<false>::kOffQ + 2 * kQBytes <= kOffBar, "BF16 layout overlaps the barriers");
+static_assert(Cfg<true>::kOffQ + 2 * kQBytes <= kOffBar, "E4M3 layout overlaps the barriers");
+static_assert(Cfg<false>::kPStages <= 4 && Cfg<true>::kPStages <= 4 && Cfg<true>::kMStages <= 4,
+              "barrier and flag arrays hold four stages");
+
 template <bool kFp8>
 constexpr int regs_needed() {   // per CTA, for the warpgroups' raised budgets
   return 256 * Cfg<kFp8>::kRegsSoftmax + 128 * Cfg<kFp8>::kRegsMid + 128 * Cfg<kFp8>::kRegsConv;
@@ -86,20 +93,20 @@ constexpr int regs_needed() {   // per CTA, for the warpgroups' raised budgets
 constexpr int kBarRawFull = 0;     // [4] producer stage landed (TMA)
 constexpr int kBarRawEmpty = 4;    // [4] producer stage consumed (BF16: the tile's P V products;
                                    //     E4M3: the 128 converter threads)
-constexpr int kBarMFull = 8;       // [2] E4M3: F16 tile written (128 converter threads)
-constexpr int kBarMEmpty = 10;     // [2] E4M3: F16 tile consumed (both lanes' P V done)
-constexpr int kBarSFull = 12;      // [2][2] scores written
-constexpr int kBarPFull = 16;      // [2] P of both lanes written (256 arrivals; a lane
+constexpr int kBarMFull = 8;       // [4] E4M3: F16 tile written (128 converter threads)
+constexpr int kBarMEmpty = 12;     // [4] E4M3: F16 tile consumed (both lanes' P V done)
+constexpr int kBarSFull = 16;      // [2][2] scores written
+constexpr int kBarPFull = 20;      // [2] P of both lanes written (256 arrivals; a lane
                                    //     without the tile arrives for it twice)
-constexpr int kBarOFinal = 18;     // [2] the lane's last P V of a unit done
-constexpr int kBarOFree = 20;      // [2] the lane's O read out (128 softmax threads)
-constexpr int kBarQFull = 22;      // [2] the lane's Q tile landed (TMA)
-constexpr int kBarQReady = 24;     // [2] E4M3: the lane's Q tile turned into F16 (128 threads)
-constexpr int kBarQFree = 26;      // [2] the lane's last Q K^T of a unit done
-constexpr int kBarUnitFull = 28;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 30;  // [2] unit descriptor read (every warp that follows units)
-constexpr int kBarDrain = 32;      // every product of the MMA warp done (at exit)
-constexpr int kNumBars = 33;
+constexpr int kBarOFinal = 22;     // [2] the lane's last P V of a unit done
+constexpr int kBarOFree = 24;      // [2] the lane's O read out (128 softmax threads)
+constexpr int kBarQFull = 26;      // [2] the lane's Q tile landed (TMA)
+constexpr int kBarQReady = 28;     // [2] E4M3: the lane's Q tile turned into F16 (128 threads)
+constexpr int kBarQFree = 30;      // [2] the lane's last Q K^T of a unit done
+constexpr int kBarUnitFull = 32;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 34;  // [2] unit descriptor read (every warp that follows units)
+constexpr int kBarDrain = 36;      // every product of the MMA warp done (at exit)
+constexpr int kNumBars = 37;
 constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
 constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;   // [4] producer stages, [2] F16 tiles
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   using C = tc::Cfg<kFp8>;
   // per producer stage and per tile the MMA side holds: 1 = a good block
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + tc::kOffOk);
-  volatile int* tile_ok_of = kFp8 ? stage_ok + tc::kPStages : stage_ok;
+  volatile int* tile_ok_of = kFp8 ? stage_ok + 4 : stage_ok;
   // the MMA side's ring: the TMA stages themselves, or the F16 tiles
   constexpr int kBarTileFull = kFp8 ? tc::kBarMFull : tc::kBarRawFull;
   constexpr int kBarTileEmpty = kFp8 ? tc::kBarMEmpty : tc::kBarRawEmpty;
@@ -242,11 +249,11 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   const uint32_t base = smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < tc::kPStages; ++s) {
+    for (int s = 0; s < C::kPStages; ++s) {
       mbar_init(bar(tc::kBarRawFull + s), 1);
       mbar_init(bar(tc::kBarRawEmpty + s), kFp8 ? 128 : 1);
     }
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < C::kMStages; ++c) {
       mbar_init(bar(tc::kBarMFull + c), 128);
       mbar_init(bar(tc::kBarMEmpty + c), 1);
     }
@@ -369,10 +376,10 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         for (int jj = 0; jj < min(32, ntiles - tb) && alive; ++jj) {
           const int bid = __shfl_sync(0xffffffffu, bids, jj);
           const bool good = bid >= 0 && bid < num_blocks;
-          const int s = static_cast<int>(g % tc::kPStages);
+          const int s = static_cast<int>(g % C::kPStages);
           int tok = 1;
           if (lane == 0) {
-            const uint32_t use = g / tc::kPStages;
+            const uint32_t use = g / C::kPStages;
             if (*abort_flag) {
               tok = 0;
             } else if (use > 0 && !mbar_wait(bar(tc::kBarRawEmpty + s), (use - 1) & 1, status)) {
@@ -425,9 +432,9 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         counters[1] = 0;
       }
       if (*abort_flag) {   // copies still landing in stages nobody waits on
-        for (uint32_t s = 0; s < static_cast<uint32_t>(tc::kPStages) && s < g; ++s) {
-          const uint32_t last = s + tc::kPStages * ((g - 1 - s) / tc::kPStages);
-          mbar_wait(bar(tc::kBarRawFull + s), (last / tc::kPStages) & 1, status);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(C::kPStages) && s < g; ++s) {
+          const uint32_t last = s + C::kPStages * ((g - 1 - s) / C::kPStages);
+          mbar_wait(bar(tc::kBarRawFull + s), (last / C::kPStages) & 1, status);
         }
       }
     }
@@ -439,7 +446,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
     constexpr uint32_t kIdescS = kFp8 ? umma_idesc_f16(128, 64, false) : umma_idesc_bf16(128, 64, false);
     constexpr uint32_t kIdescO = kFp8 ? umma_idesc_f16(128, 128, true) : umma_idesc_bf16(128, 128, true);
     // descriptors of the first step of each operand; a step adds a constant
-    const uint64_t desc_q = umma_smem_desc(base + tc::kOffQ, 1024, 1024);
+    const uint64_t desc_q = umma_smem_desc(base + C::kOffQ, 1024, 1024);
     const uint64_t desc_k = umma_smem_desc(base + C::kOffM, 1024, 1024);
     const uint64_t desc_v = umma_smem_desc(base + C::kOffM + tc::kPage, tc::kBox, 1024);
     constexpr uint64_t kStageStep = tc::kTileBytes >> 4;
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         }
         if (lane == 0) {
           const uint32_t qb = bar(tc::kBarQFull + l);
-          const uint32_t dst = base + tc::kOffQ + l * tc::kQBytes;
+          const uint32_t dst = base + C::kOffQ + l * tc::kQBytes;
           const int t = tok0 + l * tc::kLaneTokens;
           mbar_arrive_expect_tx(qb, tc::kQBytes);
           tma_load_3d(dst, &q_map, 0, d.h * kGroup, t, qb, policy);
@@ -722,7 +729,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
           dead = true;
           break;
         }
-        uint8_t* qrow = smem + tc::kOffQ + l * tc::kQBytes + t * 128;
+        uint8_t* qrow = smem + C::kOffQ + l * tc::kQBytes + t * 128;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {   // 8 BF16 -> 8 F16 per 16-byte chunk, in place
           uint4* p = reinterpret_cast<uint4*>(qrow + (c >> 3) * 2 * tc::kBox + (c & 7) * 16);
@@ -739,9 +746,9 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       }
       for (int j = 0; j < nt && !dead; ++j) {
         const uint32_t g = G + j;
-        const int s = static_cast<int>(g % tc::kPStages);
+        const int s = static_cast<int>(g % C::kPStages);
         const int c = static_cast<int>(g % C::kMStages);
-        if (!wait_all(tc::kBarRawFull + s, (g / tc::kPStages) & 1) ||
+        if (!wait_all(tc::kBarRawFull + s, (g / C::kPStages) & 1) ||
             (g >= static_cast<uint32_t>(C::kMStages) &&
              !wait_all(tc::kBarMEmpty + c, ((g - C::kMStages) / C::kMStages) & 1))) {
           dead = true;
