@@ -263,91 +263,10 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, bool b_mn) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] B[smem]; issued by one thread.
-__device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, bool accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-               : "memory");
-}
-
-// D[tmem] (+)= A[tmem] B[smem]: A (M rows on the TMEM lanes, two BF16 of K
-// per 32-bit column, the even one in the low half); issued by one thread.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, bool accumulate) {
-  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-               ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-               : "memory");
-}
-
-// The chains below are executed by a whole converged warp: the descriptors
-// stay warp-uniform and one elected thread issues every product of the chain
-// back to back (issued one by one from a single diverged thread, each product
-// costs the issuing thread far more than the tensor core's time for it).
-
-// Q K^T over d = 128 as one chain of eight K-major steps (16 of d each):
-// a_desc / b_desc describe the first 16 columns of two 128-byte-swizzled
-// halves; a step moves 32 bytes along a row, the second half starts
-// kAHalf / kBHalf bytes further.  The first step overwrites D.
-template <uint32_t kAHalf, uint32_t kBHalf>
-__device__ __forceinline__ void umma_bf16_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                  uint32_t idesc) {
-  constexpr uint32_t ah = kAHalf >> 4, bh = kBHalf >> 4;
-  asm volatile(
-      "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a, b;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 pf, %4, %4;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
-      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, %5;\n\tadd.s64 b, %2, %6;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, %7;\n\tadd.s64 b, %2, %8;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, %9;\n\tadd.s64 b, %2, %10;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-      "add.s64 a, %1, %11;\n\tadd.s64 b, %2, %12;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(0u),
-        "n"(ah), "n"(bh), "n"(ah + 2), "n"(bh + 2), "n"(ah + 4), "n"(bh + 4), "n"(ah + 6), "n"(bh + 6)
-      : "memory");
-}
-
-// O (+)= P V over 64 keys as one chain of four steps (16 keys each): P from
-// TMEM (8 columns per step), V MN-major (2048 bytes = 16 rows per step).
-__device__ __forceinline__ void umma_bf16_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
-      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-      "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
 // tcgen05.commit by one elected thread of a converged warp.
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-               ::"r"(bar) : "memory");
-}
-
-// Arrive once on an mbarrier when every earlier tcgen05 op of this thread is done.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(bar) : "memory");
 }
 
@@ -389,23 +308,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]),
         "=r"(r[63])
       : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,"
-      "%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,"
-      "%61,%62,%63,%64};"
-      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-        "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]),
-        "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]),
-        "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]),
-        "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]),
-        "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
       : "memory");
 }
 // 32 consecutive 32-bit columns of this thread's TMEM lane (warp-wide, 32x32b shape).
@@ -453,9 +355,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void red_add_shared(float* p, float v) {
-  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(p)), "f"(v) : "memory");
-}
 
 }  // namespace hpc
 

@@ -143,6 +143,12 @@ __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (
   }
 }
 
+// The two chains below are executed by the whole converged MMA warp: the
+// descriptors stay warp-uniform and one elected thread issues every product
+// of a chain back to back from one asm block (issued one by one from a single
+// diverged thread, each product costs the issuer far more than the tensor
+// core's time for it).
+
 // S = Q K^T of both lanes for one tile (executed by the whole converged MMA
 // warp; one elected thread issues): lane l, if present (en_l), gets eight
 // K-major steps (16 of d each) into d_l and a commit on bar_l, and on
