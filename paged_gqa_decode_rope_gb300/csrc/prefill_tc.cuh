@@ -125,6 +125,32 @@ __device__ __forceinline__ int lane_tiles(int qlen, int L, int first_token) {
 
 }  // namespace tc
 
+// Softmax arithmetic on two fp32 lanes at once (FMA2 / ADD2: one issue slot
+// for two elements) and the three-input maximum.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Eight consecutive output elements (index a multiple of 8) in the caller's type.
 __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (&v)[8],
                                            int32_t out_dtype) {
@@ -587,15 +613,17 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
 #pragma unroll
           for (int jk = 0; jk < 64; ++jk) x[jk] = jk <= lim ? __uint_as_float(sr[jk]) : -INFINITY;
         }
-        // the row maximum of the raw scores in 8 independent chains; the
-        // scale is positive, so it commutes with the maximum
+        // the row maximum of the raw scores, three-input maxima in 8
+        // independent chains; the scale is positive, so it commutes with the
+        // maximum
         float m8[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) m8[c] = x[c];
 #pragma unroll
-        for (int jk = 8; jk < 64; ++jk) m8[jk & 7] = fmaxf(m8[jk & 7], x[jk]);
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale_log2;
+        for (int jk = 8; jk < 64; jk += 2) m8[(jk >> 1) & 7] = max3f(m8[(jk >> 1) & 7], x[jk], x[jk + 1]);
+        const float mx =
+            max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+            scale_log2;
         // the running maximum moves only when it grows by more than 2^8
         // (weights stay <= 2^8); the row's O is then rescaled in TMEM
         const bool grow = mx > m_used + tc::kRescaleLog2;
@@ -626,16 +654,20 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         // BF16 (F16 for E4M3 caches) pairs over the scores; the row sum in 4
         // independent chains
         const float nms = m_used == -INFINITY ? 0.f : -m_used;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint64_t scale2 = f32x2(scale_log2, scale_log2), nms2 = f32x2(nms, nms);
+        uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // pairs of row sums
         uint32_t pk[32];
 #pragma unroll
         for (int jk = 0; jk < 32; ++jk) {
-          const float p0 = exp2_ftz(fmaf(x[2 * jk], scale_log2, nms));
-          const float p1 = exp2_ftz(fmaf(x[2 * jk + 1], scale_log2, nms));
-          ps[jk & 3] += p0 + p1;
+          float a0, a1;
+          f32x2_split(fma_f32x2(f32x2(x[2 * jk], x[2 * jk + 1]), scale2, nms2), a0, a1);
+          const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
+          ps2[jk & 3] = add_f32x2(ps2[jk & 3], f32x2(p0, p1));
           pk[jk] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
         }
-        lsum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        float s0, s1;
+        f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+        lsum += s0 + s1;
         tmem_st32(trow + 64 * (gl & 1), pk);
         tmem_wait_st();
         tc_fence_before();
