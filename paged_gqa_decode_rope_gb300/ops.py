@@ -642,3 +642,35 @@ class PrefillAttention:
             block_table.shape[1], _p(seq_lens), B, _p(self.unit_ptr), _p(self.counters), _p(out),
             int(self.out_dtype), scale, _p(self.status), _stream()))
         return out
+
+
+class HostInputs:
+    """A step's host-side inputs in one pinned buffer, mirrored by one device
+    buffer, so that they reach the device in a single copy.
+
+    ``specs`` maps a name to (shape, dtype); each tensor starts on a 256-byte
+    boundary of both buffers.  ``host[name]`` is the pinned view to fill,
+    ``dev[name]`` the device view to pass to the calls, and ``upload()``
+    issues the one host -> device copy on the current stream."""
+
+    def __init__(self, specs, device="cuda"):
+        self.offsets, total = {}, 0
+        for name, (shape, dtype) in specs.items():
+            nbytes = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            self.offsets[name] = (total, nbytes, tuple(shape), dtype)
+            total += (nbytes + 255) // 256 * 256
+        self.nbytes = total
+        self._host = torch.empty(total, dtype=torch.uint8)
+        if torch.device(device).type == "cuda":
+            self._host = self._host.pin_memory()
+        self._dev = torch.empty(total, dtype=torch.uint8, device=device)
+        self.host = {n: self._view(self._host, n) for n in self.offsets}
+        self.dev = {n: self._view(self._dev, n) for n in self.offsets}
+
+    def _view(self, buf, name):
+        off, nbytes, shape, dtype = self.offsets[name]
+        return buf[off:off + nbytes].view(dtype).view(shape)
+
+    def upload(self):
+        self._dev.copy_(self._host, non_blocking=True)
+        return self.dev
