@@ -13,7 +13,11 @@ Reading (the pages give no formula): flatten every (sequence, KV head) tile in
 (sequence, kv_head, tile) order; compute unit c is given the contiguous flat
 range [c*q, min((c+1)*q, T)) with q = max(min_tiles, ceil(T / C)); a work item
 is a piece of that range cut at (sequence, kv_head) boundaries.  Each unit then
-streams the same number of tiles, so work is proportional to length.
+streams the same number of tiles, so work is proportional to length.  When every
+sequence has the same number of tiles n and the B*8 segments are no more than
+the units, q is raised to n: each unit takes whole segments (the page notes
+that a static split suits uniform lengths; splitting equal segments further
+only adds partial results to merge).
 
 Runtime dealing of the tail (``pool_chunks`` = J > 0): units do not run at
 exactly the same speed, so the last P = floor(q / 8) tiles of every unit's
@@ -54,6 +58,8 @@ def plan_dynamic(seq_lens, num_ctas, min_tiles=1, pool_chunks=0, pool_min_tiles=
     n = [num_tiles(L) for L in seq_lens]
     T = HKV * sum(n)
     q = max(int(min_tiles), -(-T // num_ctas)) if T > 0 else max(int(min_tiles), 1)
+    if B > 0 and n[0] > 0 and all(x == n[0] for x in n) and B * HKV <= num_ctas:
+        q = max(q, n[0])
     P = q // 8 if pool_chunks > 0 else 0
     k = -(-P // pool_chunks) if P > 0 else 1
     if k < pool_min_tiles:                     # chunks too short to deal

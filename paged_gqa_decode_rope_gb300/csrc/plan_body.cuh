@@ -204,14 +204,20 @@ __device__ void plan_dynamic_body(
   const int b0 = min(batch, tid * per);
   const int b1 = min(batch, b0 + per);
 
-  // 1. tiles per sequence (staged in pre_n), then their exclusive prefix
+  // 1. tiles per sequence (staged in pre_n), then their exclusive prefix;
+  //    and whether every sequence has as many tiles as sequence 0
+  const int L0 = batch > 0 ? seq_lens[0] : 0;
+  const int n0 = (L0 > 0 && L0 <= max_blocks * kPage) ? (L0 + kPage - 1) / kPage : -1;
   int local = 0;
+  bool same = true;
   for (int b = b0; b < b1; ++b) {
     const int n = tiles_of(seq_lens, b, max_blocks, status);
     pre_n[b] = n;
     local += n;
+    same = same && n == n0;
   }
   for (int x = tid; x < batch * kHkv; x += kThreads) seg_done[x] = 0;
+  same = __syncthreads_and(same) != 0;
   int total_n;
   int run = cta_exclusive_scan<kThreads>(local, warp_sums, &total_n);
   for (int b = b0; b < b1; ++b) {
@@ -227,6 +233,9 @@ __device__ void plan_dynamic_body(
   Pieces pc;
   const uint32_t uC = static_cast<uint32_t>(C), uJ = static_cast<uint32_t>(pool_chunks);
   pc.q = max(min_tiles, static_cast<int>((static_cast<uint32_t>(T) + uC - 1u) / uC));
+  // equal lengths with no more segments than queues: one whole segment per
+  // queue (splitting them would only add partials and merges)
+  if (same && batch * kHkv <= C) pc.q = max(pc.q, n0);
   uint32_t P = pool_chunks > 0 ? static_cast<uint32_t>(pc.q) / 8u : 0u;
   pc.k = P > 0 ? static_cast<int>((P + uJ - 1u) / uJ) : 1;
   if (pc.k < pool_min_tiles) {                           // chunks too short to deal

@@ -57,6 +57,9 @@ def test_dynamic_plan_covers_and_balances(C, J, kmin):
             assert n <= C * (1 + J) + 8 * B, "capacity bound"
             T = 8 * sum(op.num_tiles(L) for L in lens)
             q = max(min_tiles, -(-T // C)) if T else min_tiles
+            ns = [op.num_tiles(L) for L in lens]
+            if ns and ns[0] > 0 and len(set(ns)) == 1 and 8 * B <= C:
+                q = max(q, ns[0])             # equal lengths: whole segments
             per_cta = [sum(items[i][3] - items[i][2] for i in range(cta_ptr[c], cta_ptr[c + 1]))
                        for c in range(C)]
             assert sum(per_cta) == T
@@ -98,3 +101,20 @@ def test_pool_min_chunk_hand_example():
     assert items == plain[0] and cta_ptr == plain[1] and pool == [] and home_end == cta_ptr[1:]
     # by hand: q = 44, so the plain plan cuts segment 3 ([33,44)) and 7 only at 44
     assert items[3] == (0, 3, 0, 11) and len(items) == 8
+
+
+def test_equal_lengths_get_whole_segments():
+    """Equal lengths with no more segments than units: every segment is one
+    item and unit c runs segment c (the proportional quota would have split
+    each of them); one tile more anywhere restores the proportional split."""
+    lens = [4096] * 32                                   # 256 segments of 64 tiles
+    items, cta_ptr, seg_ptr, home_end, pool = op.plan_dynamic(lens, 304)
+    assert len(items) == 256 and seg_ptr == list(range(257))
+    assert cta_ptr == list(range(257)) + [256] * 48
+    assert all(it[2] == 0 and it[3] == 64 for it in items)
+    op.check_coverage(lens, items, cta_ptr, seg_ptr, home_end, pool)
+    # more segments than units, or one unequal length: the plain quota (54)
+    items2, cta2, _, _, _ = op.plan_dynamic(lens, 200)
+    assert cta2[1] - cta2[0] >= 1 and any(it[3] - it[2] < 64 for it in items2)
+    items3, _, _, _, _ = op.plan_dynamic([4096] * 31 + [4097], 304)
+    assert any(it[3] - it[2] < 64 for it in items3)
