@@ -42,12 +42,13 @@ namespace hpc {
 namespace {
 namespace tc {
 
-// warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: K/V producer, 9: MMA,
-// 10: Q loader, 11: idle, 12-15 (E4M3 caches): converter.  The third (and
-// fourth) warpgroup lend registers to the softmax warpgroups.
+// warps 0-3: softmax of lane 0, 4-7: of lane 1, 8: K/V producer, 9: MMA of
+// lane 0, 10: Q loader, 11: MMA of lane 1, 12-15 (E4M3 caches): converter.
+// The third (and fourth) warpgroup lend registers to the softmax warpgroups.
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
 constexpr int kWarpQ = 10;
+constexpr int kWarpMma1 = 11;
 constexpr int kWarpConv0 = 12;
 constexpr int kBox = 64 * 128;                      // one 64-row x 128-byte TMA box
 constexpr int kPage = 2 * kBox;                     // BF16 page of one KV head (d = 128)
@@ -66,7 +67,7 @@ struct Cfg<false> {   // BF16 cache: the MMA reads the TMA ring itself
   static constexpr int kOffM = 0;
   static constexpr int kOffQ = kMStages * kTileBytes;
   static constexpr uint32_t kRegsSoftmax = 200, kRegsMid = 104, kRegsConv = 0;
-  static constexpr int kUnitReaders = 10;           // MMA, Q loader, 8 softmax warps
+  static constexpr int kUnitReaders = 11;           // 2 MMA, Q loader, 8 softmax warps
 };
 template <>
 struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a second ring
@@ -77,7 +78,7 @@ struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a secon
   static constexpr int kOffM = kPStages * kPStageBytes;
   static constexpr int kOffQ = kOffM + kMStages * kTileBytes;
   static constexpr uint32_t kRegsSoftmax = 184, kRegsMid = 88, kRegsConv = 56;
-  static constexpr int kUnitReaders = 14;           // + the 4 converter warps
+  static constexpr int kUnitReaders = 15;           // + the 4 converter warps
 };
 static_assert(Cfg<false>::kOffQ + 2 * kQBytes <= kOffBar, "BF16 layout overlaps the barriers");
 static_assert(Cfg<true>::kOffQ + 2 * kQBytes <= kOffBar, "E4M3 layout overlaps the barriers");
@@ -91,22 +92,21 @@ constexpr int regs_needed() {   // per CTA, for the warpgroups' raised budgets
 
 // mbarriers (index of the first of each kind; [l] per lane, [l][i] per lane and buffer)
 constexpr int kBarRawFull = 0;     // [4] producer stage landed (TMA)
-constexpr int kBarRawEmpty = 4;    // [4] producer stage consumed (BF16: the tile's P V products;
-                                   //     E4M3: the 128 converter threads)
+constexpr int kBarRawEmpty = 4;    // [4] E4M3: producer stage consumed (128 converter threads)
 constexpr int kBarMFull = 8;       // [4] E4M3: F16 tile written (128 converter threads)
-constexpr int kBarMEmpty = 12;     // [4] E4M3: F16 tile consumed (both lanes' P V done)
-constexpr int kBarSFull = 16;      // [2][2] scores written
-constexpr int kBarPFull = 20;      // [2] P of both lanes written (256 arrivals; a lane
-                                   //     without the tile arrives for it twice)
-constexpr int kBarOFinal = 22;     // [2] the lane's last P V of a unit done
-constexpr int kBarOFree = 24;      // [2] the lane's O read out (128 softmax threads)
-constexpr int kBarQFull = 26;      // [2] the lane's Q tile landed (TMA)
-constexpr int kBarQReady = 28;     // [2] E4M3: the lane's Q tile turned into F16 (128 threads)
-constexpr int kBarQFree = 30;      // [2] the lane's last Q K^T of a unit done
-constexpr int kBarUnitFull = 32;   // [2] unit descriptor handed on
-constexpr int kBarUnitEmpty = 34;  // [2] unit descriptor read (every warp that follows units)
-constexpr int kBarDrain = 36;      // every product of the MMA warp done (at exit)
-constexpr int kNumBars = 37;
+constexpr int kBarTEmpty = 12;     // [2][4] the lane's P V of the tile the MMA side holds done
+                                   //     (a lane without the tile commits for it at its unit end)
+constexpr int kBarSFull = 20;      // [2][2] scores written
+constexpr int kBarPFull = 24;      // [2][2] P written over the scores (128 softmax threads)
+constexpr int kBarOFinal = 28;     // [2] the lane's last P V of a unit done
+constexpr int kBarOFree = 30;      // [2] the lane's O read out (128 softmax threads)
+constexpr int kBarQFull = 32;      // [2] the lane's Q tile landed (TMA)
+constexpr int kBarQReady = 34;     // [2] E4M3: the lane's Q tile turned into F16 (128 threads)
+constexpr int kBarQFree = 36;      // [2] the lane's last Q K^T of a unit done
+constexpr int kBarUnitFull = 38;   // [2] unit descriptor handed on
+constexpr int kBarUnitEmpty = 40;  // [2] unit descriptor read (every warp that follows units)
+constexpr int kBarDrain = 42;      // [2] every product of the lane's MMA warp done (at exit)
+constexpr int kNumBars = 44;
 constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
 constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;   // [4] producer stages, [2] F16 tiles
@@ -169,88 +169,58 @@ __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (
   }
 }
 
-// The two chains below are executed by the whole converged MMA warp: the
-// descriptors stay warp-uniform and one elected thread issues every product
-// of a chain back to back from one asm block (issued one by one from a single
-// diverged thread, each product costs the issuer far more than the tensor
-// core's time for it).
+// The chains below are executed by a whole converged MMA warp (one per
+// lane): the descriptors stay warp-uniform and one elected thread issues
+// every product of a chain back to back from one asm block (issued one by one
+// from a single diverged thread, each product costs the issuer far more than
+// the tensor core's time for it).
 
-// S = Q K^T of both lanes for one tile (executed by the whole converged MMA
-// warp; one elected thread issues): lane l, if present (en_l), gets eight
-// K-major steps (16 of d each) into d_l and a commit on bar_l, and on
-// qfree_l too if it was the lane's last tile of the unit (its Q may go).  Q halves of d
-// are 16 KB apart, K halves 8 KB; a step moves 32 bytes along a row.
-__device__ __forceinline__ void umma_qk_pair(uint32_t d0, uint32_t d1, uint64_t q0, uint64_t q1,
-                                             uint64_t k, uint32_t idesc, bool en0, bool en1,
-                                             uint32_t bar0, uint32_t bar1, bool last0, bool last1,
-                                             uint32_t qfree0, uint32_t qfree1) {
-#define HPC_QK_STEP(D, Q, QO, KO, P)                                   \
-  "add.s64 a, " Q ", " QO ";\n\tadd.s64 b, %4, " KO ";\n\t"         \
-  "@" P " tcgen05.mma.cta_group::1.kind::f16 [" D "], a, b, %5, pt;\n\t"
-#define HPC_QK_CHAIN(D, Q, P)                                                        \
-  "@" P " tcgen05.mma.cta_group::1.kind::f16 [" D "], " Q ", %4, %5, pf;\n\t"     \
-  HPC_QK_STEP(D, Q, "2", "2", P) HPC_QK_STEP(D, Q, "4", "4", P)                      \
-  HPC_QK_STEP(D, Q, "6", "6", P) HPC_QK_STEP(D, Q, "1024", "512", P)                 \
-  HPC_QK_STEP(D, Q, "1026", "514", P) HPC_QK_STEP(D, Q, "1028", "516", P)            \
-  HPC_QK_STEP(D, Q, "1030", "518", P)
-  const uint32_t flags = (en0 ? 1u : 0u) | (en1 ? 2u : 0u) | (last0 ? 4u : 0u) | (last1 ? 8u : 0u);
+// S = Q K^T of one lane for one tile: eight K-major steps (16 of d each; Q
+// halves of d 16 KB apart, K halves 8 KB, a step 32 bytes along a row) into
+// d, a commit on s_full, and on q_free too if it was the lane's last tile of
+// the unit (its Q tile may then be replaced).
+__device__ __forceinline__ void umma_qk_lane(uint32_t d, uint64_t q, uint64_t k, uint32_t idesc,
+                                             uint32_t s_full, bool last, uint32_t q_free) {
+#define HPC_QK_STEP(QO, KO) \
+  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
   asm volatile(
-      "{\n\t.reg .pred e, e0, e1, f0, f1, pf, pt;\n\t.reg .b64 a, b;\n\t.reg .b32 t;\n\t"
+      "{\n\t.reg .pred e, f, pf, pt;\n\t.reg .b64 a, b;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "and.b32 t, %6, 1;\n\tsetp.ne.and.b32 e0, t, 0, e;\n\t"
-      "and.b32 t, %6, 2;\n\tsetp.ne.and.b32 e1, t, 0, e;\n\t"
-      "and.b32 t, %6, 4;\n\tsetp.ne.and.b32 f0, t, 0, e0;\n\t"
-      "and.b32 t, %6, 8;\n\tsetp.ne.and.b32 f1, t, 0, e1;\n\t"
-      "setp.ne.b32 pf, t, t;\n\tsetp.eq.b32 pt, t, t;\n\t"
-      HPC_QK_CHAIN("%0", "%2", "e0")
-      "@e0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
-      "@f0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
-      HPC_QK_CHAIN("%1", "%3", "e1")
-      "@e1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
-      "@f1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}"
-      ::"r"(d0), "r"(d1), "l"(q0), "l"(q1), "l"(k), "r"(idesc), "r"(flags), "r"(bar0), "r"(bar1),
-        "r"(qfree0), "r"(qfree1)
+      "setp.ne.and.b32 f, %5, 0, e;\n\t"
+      "setp.ne.b32 pf, %5, %5;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      HPC_QK_STEP("2", "2") HPC_QK_STEP("4", "4") HPC_QK_STEP("6", "6")
+      HPC_QK_STEP("1024", "512") HPC_QK_STEP("1026", "514") HPC_QK_STEP("1028", "516")
+      HPC_QK_STEP("1030", "518")
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+      ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free)
       : "memory");
-#undef HPC_QK_CHAIN
 #undef HPC_QK_STEP
 }
 
-// O_l (+)= P_l V of both lanes for one tile (whole converged warp, one
-// elected thread issues): lane l, if present, gets four steps of 16 keys (P
-// from TMEM, 8 columns a step; V MN-major, 2048 bytes a step) into its O at
-// tmem + 256 l + 128, then a commit on fin_l if it was the lane's last tile;
-// the stage's empty barrier is committed after both.
-__device__ __forceinline__ void umma_pv_pair(uint32_t tmem, uint32_t p0, uint32_t p1, uint64_t v,
-                                             uint32_t idesc, bool acc, bool en0, bool en1,
-                                             bool last0, bool last1, uint32_t fin0, uint32_t fin1,
-                                             uint32_t empty) {
-#define HPC_PV_STEP(D, P, PO, VO, E)                                     \
-  "add.u32 a, " P ", " PO ";\n\tadd.s64 b, %3, " VO ";\n\t"         \
-  "@" E " tcgen05.mma.cta_group::1.kind::f16 [" D "], [a], b, %4, pt;\n\t"
-#define HPC_PV_CHAIN(D, P, E)                                                         \
-  "@" E " tcgen05.mma.cta_group::1.kind::f16 [" D "], [" P "], %3, %4, pa;\n\t"    \
-  HPC_PV_STEP(D, P, "8", "128", E) HPC_PV_STEP(D, P, "16", "256", E)                  \
-  HPC_PV_STEP(D, P, "24", "384", E)
-  const uint32_t o0 = tmem + 128, o1 = tmem + 384;
-  const uint32_t flags = (acc ? 1u : 0u) | (en0 ? 2u : 0u) | (en1 ? 4u : 0u) | (last0 ? 8u : 0u) |
-                         (last1 ? 16u : 0u);
+// O += P V of one lane for one tile: four steps of 16 keys (P from TMEM, 8
+// columns a step; V MN-major, 2048 bytes a step; the first step overwrites O
+// unless `acc`), a commit on fin if it was the lane's last tile of the unit,
+// then a commit on the tile's empty barrier (which counts both lanes).
+__device__ __forceinline__ void umma_pv_lane(uint32_t o, uint32_t p, uint64_t v, uint32_t idesc,
+                                             bool acc, bool last, uint32_t fin, uint32_t empty) {
+#define HPC_PV_STEP(PO, VO) \
+  "add.u32 a, %1, " PO ";\n\tadd.s64 b, %2, " VO ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
+  const uint32_t flags = (acc ? 1u : 0u) | (last ? 2u : 0u);
   asm volatile(
-      "{\n\t.reg .pred e, e0, e1, f0, f1, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a, t;\n\t"
+      "{\n\t.reg .pred e, f, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a, t;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "and.b32 t, %5, 2;\n\tsetp.ne.and.b32 e0, t, 0, e;\n\t"
-      "and.b32 t, %5, 4;\n\tsetp.ne.and.b32 e1, t, 0, e;\n\t"
-      "and.b32 t, %5, 8;\n\tsetp.ne.and.b32 f0, t, 0, e0;\n\t"
-      "and.b32 t, %5, 16;\n\tsetp.ne.and.b32 f1, t, 0, e1;\n\t"
-      "and.b32 t, %5, 1;\n\tsetp.ne.b32 pa, t, 0;\n\tsetp.eq.b32 pt, t, t;\n\t"
-      HPC_PV_CHAIN("%0", "%1", "e0")
-      "@f0 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-      HPC_PV_CHAIN("%2", "%7", "e1")
-      "@f1 tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
-      ::"r"(o0), "r"(p0), "r"(o1), "l"(v), "r"(idesc), "r"(flags), "r"(fin0), "r"(p1), "r"(fin1),
-        "r"(empty)
+      "and.b32 t, %4, 1;\n\tsetp.ne.b32 pa, t, 0;\n\tsetp.eq.b32 pt, t, t;\n\t"
+      "and.b32 t, %4, 2;\n\tsetp.ne.and.b32 f, t, 0, e;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
+      HPC_PV_STEP("8", "128") HPC_PV_STEP("16", "256") HPC_PV_STEP("24", "384")
+      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+      ::"r"(o), "r"(p), "l"(v), "r"(idesc), "r"(flags), "r"(fin), "r"(empty)
       : "memory");
-#undef HPC_PV_CHAIN
 #undef HPC_PV_STEP
 }
 
@@ -273,7 +243,6 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   volatile int* tile_ok_of = kFp8 ? stage_ok + 4 : stage_ok;
   // the MMA side's ring: the TMA stages themselves, or the F16 tiles
   constexpr int kBarTileFull = kFp8 ? tc::kBarMFull : tc::kBarRawFull;
-  constexpr int kBarTileEmpty = kFp8 ? tc::kBarMEmpty : tc::kBarRawEmpty;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + tc::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + tc::kOffMisc + 4);
   const int warp = threadIdx.x >> 5;
@@ -283,15 +252,19 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kPStages; ++s) {
       mbar_init(bar(tc::kBarRawFull + s), 1);
-      mbar_init(bar(tc::kBarRawEmpty + s), kFp8 ? 128 : 1);
+      mbar_init(bar(tc::kBarRawEmpty + s), 128);
     }
     for (int c = 0; c < C::kMStages; ++c) {
       mbar_init(bar(tc::kBarMFull + c), 128);
-      mbar_init(bar(tc::kBarMEmpty + c), 1);
+      mbar_init(bar(tc::kBarTEmpty + c), 1);
+      mbar_init(bar(tc::kBarTEmpty + 4 + c), 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(bar(tc::kBarSFull + i), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(tc::kBarSFull + i), 1);
+      mbar_init(bar(tc::kBarPFull + i), 128);
+    }
     for (int l = 0; l < 2; ++l) {
-      mbar_init(bar(tc::kBarPFull + l), 256);
+      mbar_init(bar(tc::kBarDrain + l), 1);
       mbar_init(bar(tc::kBarOFinal + l), 1);
       mbar_init(bar(tc::kBarOFree + l), 128);
       mbar_init(bar(tc::kBarQFull + l), 1);
@@ -300,11 +273,10 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       mbar_init(bar(tc::kBarUnitFull + l), 1);
       mbar_init(bar(tc::kBarUnitEmpty + l), C::kUnitReaders);
     }
-    mbar_init(bar(tc::kBarDrain), 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == tc::kWarpMma) tmem_alloc(smem_u32(tmem_slot), tc::kTmemCols);
+  if (warp == tc::kWarpMma) tmem_alloc(smem_u32(tmem_slot), tc::kTmemCols);   // both lanes' columns
   if (warp == tc::kWarpProd && lane == 0) {
     tma_prefetch_desc(&kv_map);
     tma_prefetch_desc(&q_map);
@@ -414,9 +386,15 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
             const uint32_t use = g / C::kPStages;
             if (*abort_flag) {
               tok = 0;
-            } else if (use > 0 && !mbar_wait(bar(tc::kBarRawEmpty + s), (use - 1) & 1, status)) {
-              *abort_flag = 1;
-              tok = 0;
+            } else if (use > 0) {
+              const uint32_t par = (use - 1) & 1;
+              const bool freed = kFp8 ? mbar_wait(bar(tc::kBarRawEmpty + s), par, status)
+                                      : mbar_wait(bar(tc::kBarTEmpty + s), par, status) &&
+                                            mbar_wait(bar(tc::kBarTEmpty + 4 + s), par, status);
+              if (!freed) {
+                *abort_flag = 1;
+                tok = 0;
+              }
             }
             if (tok && good) {
               stage_ok[s] = 1;
@@ -470,38 +448,38 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         }
       }
     }
-  } else if (warp == tc::kWarpMma) {
-    // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs the loop (descriptors warp-uniform); one elected
-    // thread issues each chain of products and each commit.
+  } else if (warp == tc::kWarpMma || warp == tc::kWarpMma1) {
+    // ---------------------------------------------------------- MMA issuers
+    // One warp per lane: while one waits on its lane's barriers, the products
+    // the other has issued keep the tensor core busy.  The whole warp runs the
+    // loop (descriptors warp-uniform); one elected thread issues each chain
+    // and each commit.
     regs_dec<C::kRegsMid>();
+    const int l = warp == tc::kWarpMma ? 0 : 1;
     constexpr uint32_t kIdescS = kFp8 ? umma_idesc_f16(128, 64, false) : umma_idesc_bf16(128, 64, false);
     constexpr uint32_t kIdescO = kFp8 ? umma_idesc_f16(128, 128, true) : umma_idesc_bf16(128, 128, true);
     // descriptors of the first step of each operand; a step adds a constant
-    const uint64_t desc_q = umma_smem_desc(base + C::kOffQ, 1024, 1024);
+    const uint64_t desc_q = umma_smem_desc(base + C::kOffQ + l * tc::kQBytes, 1024, 1024);
     const uint64_t desc_k = umma_smem_desc(base + C::kOffM, 1024, 1024);
     const uint64_t desc_v = umma_smem_desc(base + C::kOffM + tc::kPage, tc::kBox, 1024);
     constexpr uint64_t kStageStep = tc::kTileBytes >> 4;
-    constexpr uint64_t kQStep = tc::kQBytes >> 4;
-    uint32_t G = 0, U = 0;          // stream tiles, unit descriptors read
-    uint32_t Gl0 = 0, Gl1 = 0;      // tiles of each lane
-    uint32_t Vl0 = 0, Vl1 = 0;      // units with tiles, per lane
+    const uint32_t tl = tmem + 256 * l;   // the lane's columns: S 0 / 64, O 128
+    constexpr int kBarQ = kFp8 ? tc::kBarQReady : tc::kBarQFull;   // Q as the MMA reads it
+    uint32_t G = 0, U = 0, Gl = 0, Vl = 0;   // stream tiles, units read, lane tiles, lane units
     bool dead = false;
     Unit d;
-    // O_l (+)= P_l V for tile jj of the unit, both lanes; then the stage is free
-    auto issue_pv = [&](int jj) {
-      const uint32_t g = G + jj, st = g % C::kMStages;
-      if (dead || !wait_all(tc::kBarPFull + (g & 1), (g >> 1) & 1) ||
-          (jj == 0 && ((d.nt[0] > 0 && Vl0 > 0 && !wait_all(tc::kBarOFree + 0, (Vl0 - 1) & 1)) ||
-                       (d.nt[1] > 0 && Vl1 > 0 && !wait_all(tc::kBarOFree + 1, (Vl1 - 1) & 1))))) {
+    // O += P V of the lane's tile jj of the unit (ntl tiles); then its share
+    // of the stage's release
+    auto issue_pv = [&](int jj, int ntl) {
+      const uint32_t g = G + jj, gl = Gl + jj, st = g % C::kMStages;
+      if (dead || !wait_all(tc::kBarPFull + 2 * l + (gl & 1), (gl >> 1) & 1) ||
+          (jj == 0 && Vl > 0 && !wait_all(tc::kBarOFree + l, (Vl - 1) & 1))) {
         dead = true;
         return;
       }
       tc_fence_after();
-      umma_pv_pair(tmem, tmem + 64 * ((Gl0 + jj) & 1), tmem + 256 + 64 * ((Gl1 + jj) & 1),
-                   desc_v + st * kStageStep, kIdescO, jj != 0, jj < d.nt[0], jj < d.nt[1],
-                   jj == d.nt[0] - 1, jj == d.nt[1] - 1, bar(tc::kBarOFinal), bar(tc::kBarOFinal + 1),
-                   bar(kBarTileEmpty + st));
+      umma_pv_lane(tl + 128, tl + 64 * (gl & 1), desc_v + st * kStageStep, kIdescO, jj != 0,
+                   jj == ntl - 1, bar(tc::kBarOFinal + l), bar(tc::kBarTEmpty + 4 * l + st));
     };
     while (!dead) {
       if (!read_unit(U, d)) break;
@@ -509,21 +487,21 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       if (d.b < 0) break;
       const int nt = max(d.nt[0], d.nt[1]);
       if (nt <= 0) continue;
+      const int ntl = l ? d.nt[1] : d.nt[0];
       const int L = seq_lens[d.b];
-      constexpr int kBarQ = kFp8 ? tc::kBarQReady : tc::kBarQFull;   // Q as the MMA reads it
-      if ((d.nt[0] > 0 && !wait_all(kBarQ + 0, Vl0 & 1)) ||
-          (d.nt[1] > 0 && !wait_all(kBarQ + 1, Vl1 & 1)))
-        break;
-      for (int j = 0; j < nt && !dead; ++j) {
-        const uint32_t g = G + j;
+      if (ntl > 0 && !wait_all(kBarQ + l, Vl & 1)) break;
+      for (int j = 0; j < ntl && !dead; ++j) {
+        const uint32_t g = G + j, gl = Gl + j;
         const uint32_t st = g % C::kMStages;
         if (!wait_all(kBarTileFull + st, (g / C::kMStages) & 1)) {
           dead = true;
           break;
         }
         // V rows past the sequence length (the cache may hold NaN there) ->
-        // zeros before any P V of the tile reads them; only the page of the
-        // sequence's last key has such rows (the converter does it for E4M3)
+        // zeros before this lane's P V of the tile reads them; only the page
+        // of the sequence's last key has such rows.  Both lanes' warps write
+        // the same zeros, each before its own P V (the converter does it for
+        // E4M3 caches).
         const int keep = L - 64 * j;
         if (!kFp8 && keep < 64) {
           uint4* vst = reinterpret_cast<uint4*>(smem + st * tc::kTileBytes + tc::kPage);
@@ -535,28 +513,35 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
           __syncwarp();
         }
         tc_fence_after();
-        umma_qk_pair(tmem + 64 * ((Gl0 + j) & 1), tmem + 256 + 64 * ((Gl1 + j) & 1), desc_q,
-                     desc_q + kQStep, desc_k + st * kStageStep, kIdescS, j < d.nt[0], j < d.nt[1],
-                     bar(tc::kBarSFull + ((Gl0 + j) & 1)), bar(tc::kBarSFull + 2 + ((Gl1 + j) & 1)),
-                     j == d.nt[0] - 1, j == d.nt[1] - 1, bar(tc::kBarQFree), bar(tc::kBarQFree + 1));
-        if (j >= 1) issue_pv(j - 1);
+        umma_qk_lane(tl + 64 * (gl & 1), desc_q, desc_k + st * kStageStep, kIdescS,
+                     bar(tc::kBarSFull + 2 * l + (gl & 1)), j == ntl - 1, bar(tc::kBarQFree + l));
+        if (j >= 1) issue_pv(j - 1, ntl);
       }
       if (dead) break;
-      issue_pv(nt - 1);
+      if (ntl > 0) issue_pv(ntl - 1, ntl);
+      if (dead) break;
+      // the release of the tiles this lane has none in: commits, so they
+      // arrive after the lane's earlier ones on the same barrier, each once
+      // its tile has landed (an earlier commit would complete a phase the
+      // producer has not waited for yet)
+      for (int j = max(ntl, 0); j < nt && !dead; ++j) {
+        const uint32_t g = G + j, st = g % C::kMStages;
+        if (!wait_all(kBarTileFull + st, (g / C::kMStages) & 1)) {
+          dead = true;
+          break;
+        }
+        umma_commit_elect(bar(tc::kBarTEmpty + 4 * l + st));
+      }
       if (dead) break;
       G += nt;
-      if (d.nt[0] > 0) {
-        Gl0 += d.nt[0];
-        ++Vl0;
-      }
-      if (d.nt[1] > 0) {
-        Gl1 += d.nt[1];
-        ++Vl1;
+      if (ntl > 0) {
+        Gl += ntl;
+        ++Vl;
       }
     }
     // every product issued here has completed before TMEM is freed
-    umma_commit_elect(bar(tc::kBarDrain));
-    mbar_wait(bar(tc::kBarDrain), 0, status);
+    umma_commit_elect(bar(tc::kBarDrain + l));
+    mbar_wait(bar(tc::kBarDrain + l), 0, status);
     __syncwarp();
   } else if (warp < 8) {
     // ---------------------------------------------------------- softmax warpgroups
@@ -633,9 +618,10 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
           m_used = mx;
         }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // the previous tile's P V must be in O before it is rescaled: its
-          // stage is emptied once both lanes' P V of it are done
-          if (!wait_all(kBarTileEmpty + (g - 1) % C::kMStages, ((g - 1) / C::kMStages) & 1)) {
+          // the previous tile's P V must be in O before it is rescaled: the
+          // lane's tile-empty barrier of that tile completes with it
+          if (!wait_all(tc::kBarTEmpty + 4 * l + (g - 1) % C::kMStages,
+                        ((g - 1) / C::kMStages) & 1)) {
             dead = true;
             break;
           }
@@ -671,7 +657,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         tmem_st32(trow + 64 * (gl & 1), pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive_cnt(bar(tc::kBarPFull + (g & 1)), j < (l ? d.nt[0] : d.nt[1]) ? 1u : 2u);
+        mbar_arrive(bar(tc::kBarPFull + 2 * l + (gl & 1)));
       }
       if (dead) break;
       // the row of O once the lane's last P V is done: divide by the row sum, store
@@ -788,7 +774,8 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         const int c = static_cast<int>(g % C::kMStages);
         if (!wait_all(tc::kBarRawFull + s, (g / C::kPStages) & 1) ||
             (g >= static_cast<uint32_t>(C::kMStages) &&
-             !wait_all(tc::kBarMEmpty + c, ((g - C::kMStages) / C::kMStages) & 1))) {
+             (!wait_all(tc::kBarTEmpty + c, ((g - C::kMStages) / C::kMStages) & 1) ||
+              !wait_all(tc::kBarTEmpty + 4 + c, ((g - C::kMStages) / C::kMStages) & 1)))) {
           dead = true;
           break;
         }
