@@ -77,7 +77,7 @@ struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a secon
   static constexpr int kMStages = 3;
   static constexpr int kOffM = kPStages * kPStageBytes;
   static constexpr int kOffQ = kOffM + kMStages * kTileBytes;
-  static constexpr uint32_t kRegsSoftmax = 184, kRegsMid = 88, kRegsConv = 56;
+  static constexpr uint32_t kRegsSoftmax = 192, kRegsMid = 72, kRegsConv = 56;
   static constexpr int kUnitReaders = 15;           // + the 4 converter warps
 };
 static_assert(Cfg<false>::kOffQ + 2 * kQBytes <= kOffBar, "BF16 layout overlaps the barriers");
