@@ -146,12 +146,14 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   if (fp8) {
     if (hpc::prefill_tc_smem_optin<true>() != cudaSuccess) return HPC_ERR_CUDA;
     hpc::prefill_tc_kernel<true><<<sms, hpc::tc::Cfg<true>::kThreads, hpc::tc::kSmemBytes, stream>>>(
-        map, q_map, num_tokens, kv_scale, query_start, seq_lens, batch, block_table, max_blocks,
+        map, q_map, num_tokens, static_cast<const uint8_t*>(kv_cache), kv_scale, query_start,
+        seq_lens, batch, block_table, max_blocks,
         num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
   } else {
     if (hpc::prefill_tc_smem_optin<false>() != cudaSuccess) return HPC_ERR_CUDA;
     hpc::prefill_tc_kernel<false><<<sms, hpc::tc::Cfg<false>::kThreads, hpc::tc::kSmemBytes, stream>>>(
-        map, q_map, num_tokens, kv_scale, query_start, seq_lens, batch, block_table, max_blocks,
+        map, q_map, num_tokens, static_cast<const uint8_t*>(kv_cache), kv_scale, query_start,
+        seq_lens, batch, block_table, max_blocks,
         num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
   }
   return HPC_LAUNCH_STATUS();

@@ -70,14 +70,14 @@ struct Cfg<false> {   // BF16 cache: the MMA reads the TMA ring itself
   static constexpr int kUnitReaders = 11;           // 2 MMA, Q loader, 8 softmax warps
 };
 template <>
-struct Cfg<true> {    // E4M3 cache: codes in the TMA ring, F16 tiles in a second ring
+struct Cfg<true> {    // E4M3 cache: the converter reads the codes itself into F16 tiles
   static constexpr int kThreads = 512;
-  static constexpr int kPStages = 3;
-  static constexpr int kPStageBytes = 2 * 64 * 128; // K codes + V codes
-  static constexpr int kMStages = 3;
-  static constexpr int kOffM = kPStages * kPStageBytes;
+  static constexpr int kPStages = 4;                // (no TMA ring: the producer loads no tile)
+  static constexpr int kPStageBytes = 0;
+  static constexpr int kMStages = 4;
+  static constexpr int kOffM = 0;
   static constexpr int kOffQ = kOffM + kMStages * kTileBytes;
-  static constexpr uint32_t kRegsSoftmax = 192, kRegsMid = 72, kRegsConv = 56;
+  static constexpr uint32_t kRegsSoftmax = 176, kRegsMid = 64, kRegsConv = 88;
   static constexpr int kUnitReaders = 15;           // + the 4 converter warps
 };
 static_assert(Cfg<false>::kOffQ + 2 * kQBytes <= kOffBar, "BF16 layout overlaps the barriers");
@@ -227,7 +227,8 @@ __device__ __forceinline__ void umma_pv_lane(uint32_t o, uint32_t p, uint64_t v,
 template <bool kFp8>
 __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-    int32_t num_tokens, const float* __restrict__ kv_scale, const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
+    int32_t num_tokens, const uint8_t* __restrict__ kv_codes, const float* __restrict__ kv_scale,
+    const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
     const int32_t* __restrict__ block_table, int32_t max_blocks, int32_t num_blocks,
     const int32_t* __restrict__ unit_ptr, int32_t* counters, void* __restrict__ out,
     int32_t out_dtype, float sm_scale, int32_t* __restrict__ status) {
@@ -374,7 +375,8 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       }
       ++n_pushed;
       if (!__shfl_sync(0xffffffffu, ok, 0) || b < 0) break;
-      for (int tb = 0; tb < ntiles && alive; tb += 32) {
+      // E4M3 caches: the converter reads the pages itself
+      for (int tb = 0; !kFp8 && tb < ntiles && alive; tb += 32) {
         const int t = tb + lane;
         const int bids = t < ntiles ? block_table[static_cast<int64_t>(b) * max_blocks + t] : 0;
         for (int jj = 0; jj < min(32, ntiles - tb) && alive; ++jj) {
@@ -730,9 +732,11 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   } else if (kFp8 && warp >= tc::kWarpConv0) {
     // ---------------------------------------------------------- converter (E4M3)
     // Per unit: each lane's Q tile BF16 -> F16 in place (thread = row), then
-    // each tile's K and V codes -> F16 into the MMA side's ring, in the
-    // layout a BF16 stage has (two 64-column boxes per page, 128-byte
-    // swizzle); V rows past the sequence length, or of a bad block, -> 0.
+    // each tile's K and V codes, read from the cache (global memory, the
+    // page two tiles on prefetched into L2), -> F16 into the MMA side's
+    // ring, in the layout a BF16 stage has (two 64-column boxes per page,
+    // 128-byte swizzle); V rows past the sequence length, or of a bad block
+    // (status set), -> 0.
     regs_dec<C::kRegsConv>();
     const int t = static_cast<int>(threadIdx.x) - 32 * tc::kWarpConv0;   // 0 .. 127
     uint32_t G = 0, U = 0, vq0 = 0, vq1 = 0;
@@ -768,62 +772,73 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         mbar_arrive(bar(tc::kBarQReady + l));
         ++vq;
       }
+      // the unit's pages, read here straight from the cache: row r of a page
+      // is 128 codes at r * 128; this thread's 16-byte chunks z = t + 128 k
+      const int64_t bt = static_cast<int64_t>(d.b) * max_blocks;
+      auto page = [&](int bid, int kv) {
+        return kv_codes + ((static_cast<int64_t>(bid) * 2 + kv) * kHkv + d.h) * (kPage * kD);
+      };
       for (int j = 0; j < nt && !dead; ++j) {
         const uint32_t g = G + j;
-        const int s = static_cast<int>(g % C::kPStages);
         const int c = static_cast<int>(g % C::kMStages);
-        if (!wait_all(tc::kBarRawFull + s, (g / C::kPStages) & 1) ||
-            (g >= static_cast<uint32_t>(C::kMStages) &&
-             (!wait_all(tc::kBarTEmpty + c, ((g - C::kMStages) / C::kMStages) & 1) ||
-              !wait_all(tc::kBarTEmpty + 4 + c, ((g - C::kMStages) / C::kMStages) & 1)))) {
+        // the page two tiles on into L2 (one 128-byte line per thread)
+        if (j + 2 < nt) {
+          const int bid2 = block_table[bt + j + 2];
+          if (bid2 >= 0 && bid2 < num_blocks)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(page(bid2, t >> 6) + (t & 63) * 128));
+        }
+        const int bid = block_table[bt + j];
+        const bool ok = bid >= 0 && bid < num_blocks;
+        if (!ok && t == 0) atomicOr(status, HPC_STATUS_BAD_BLOCK);
+        const int keep = ok ? max(0, min(64, L - 64 * j)) : 0;
+        uint4 kw[4], vw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int z = t + 128 * k;
+          kw[k] = ok ? *reinterpret_cast<const uint4*>(page(bid, 0) + z * 16) : make_uint4(0u, 0u, 0u, 0u);
+          vw[k] = (z >> 3) < keep ? *reinterpret_cast<const uint4*>(page(bid, 1) + z * 16)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (g >= static_cast<uint32_t>(C::kMStages) &&
+            (!wait_all(tc::kBarTEmpty + c, ((g - C::kMStages) / C::kMStages) & 1) ||
+             !wait_all(tc::kBarTEmpty + 4 + c, ((g - C::kMStages) / C::kMStages) & 1))) {
           dead = true;
           break;
         }
-        const bool ok = stage_ok[s] != 0;
-        const int keep = ok ? max(0, min(64, L - 64 * j)) : 0;
-        const uint8_t* raw = smem + s * C::kPStageBytes;
         uint8_t* dst = smem + C::kOffM + c * tc::kTileBytes;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          // source chunk: row r, 16 codes (d = 16 lc .. 16 lc + 15) at
-          // physical chunk sc; destination: half lc / 4 of d, logical
-          // chunks 2 (lc % 4) and the next, swizzled by the row
-          const int z = t + 128 * k, r = z >> 3, sc = z & 7, lc = sc ^ (r & 7);
+          // 16 codes of row r (d = 16 lc .. 16 lc + 15) -> half lc / 4 of d,
+          // logical chunks 2 (lc % 4) and the next, swizzled by the row
+          const int z = t + 128 * k, r = z >> 3, lc = z & 7;
           const int hd = lc >> 2, dl = (lc & 3) * 2;
           const int o0 = hd * tc::kBox + r * 128 + ((dl ^ (r & 7)) << 4);
           const int o1 = hd * tc::kBox + r * 128 + (((dl + 1) ^ (r & 7)) << 4);
-          if (ok) {
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + sc * 16);
-            *reinterpret_cast<uint4*>(dst + o0) =
-                make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
-            *reinterpret_cast<uint4*>(dst + o1) =
-                make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)),
-                           e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
-          }
-          uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
-          if (r < keep) {
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + C::kPStageBytes / 2 + r * 128 + sc * 16);
-            v0 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
-            v1 = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)),
-                            e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
-          }
-          *reinterpret_cast<uint4*>(dst + tc::kPage + o0) = v0;
-          *reinterpret_cast<uint4*>(dst + tc::kPage + o1) = v1;
+          const uint4 w = kw[k], v = vw[k];
+          *reinterpret_cast<uint4*>(dst + o0) =
+              make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.y)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
+          *reinterpret_cast<uint4*>(dst + o1) =
+              make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.z)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.z >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.w)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.w >> 16)));
+          *reinterpret_cast<uint4*>(dst + tc::kPage + o0) =
+              make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(v.x)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.y)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.y >> 16)));
+          *reinterpret_cast<uint4*>(dst + tc::kPage + o1) =
+              make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(v.z)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.z >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.w)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(v.w >> 16)));
         }
         if (t == 0) tile_ok_of[c] = ok ? 1 : 0;
         fence_proxy_async_smem();
         mbar_arrive(bar(tc::kBarMFull + c));
-        mbar_arrive(bar(tc::kBarRawEmpty + s));
       }
       G += nt;
     }
