@@ -77,7 +77,7 @@ struct Cfg<true> {    // E4M3 cache: the converter reads the codes itself into F
   static constexpr int kMStages = 4;
   static constexpr int kOffM = 0;
   static constexpr int kOffQ = kOffM + kMStages * kTileBytes;
-  static constexpr uint32_t kRegsSoftmax = 176, kRegsMid = 64, kRegsConv = 88;
+  static constexpr uint32_t kRegsSoftmax = 176, kRegsMid = 64, kRegsConv = 96;
   static constexpr int kUnitReaders = 15;           // + the 4 converter warps
 };
 static_assert(Cfg<false>::kOffQ + 2 * kQBytes <= kOffBar, "BF16 layout overlaps the barriers");
@@ -758,9 +758,13 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
           break;
         }
         uint8_t* qrow = smem + C::kOffQ + l * tc::kQBytes + t * 128;
+        // 8 BF16 -> 8 F16 per 16-byte chunk, in place; the chunk order is
+        // rotated by the row, so the eight rows of a quarter-warp touch eight
+        // different 16-byte bank groups at every step
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {   // 8 BF16 -> 8 F16 per 16-byte chunk, in place
-          uint4* p = reinterpret_cast<uint4*>(qrow + (c >> 3) * 2 * tc::kBox + (c & 7) * 16);
+        for (int c = 0; c < 16; ++c) {
+          const int cc = (c & 8) | ((c ^ t) & 7);
+          uint4* p = reinterpret_cast<uint4*>(qrow + (cc >> 3) * 2 * tc::kBox + (cc & 7) * 16);
           uint4 w = *p;
           w.x = pack_f16(bf16_lo(w.x), bf16_hi(w.x));
           w.y = pack_f16(bf16_lo(w.y), bf16_hi(w.y));
@@ -809,12 +813,17 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           // 16 codes of row r (d = 16 lc .. 16 lc + 15) -> half lc / 4 of d,
-          // logical chunks 2 (lc % 4) and the next, swizzled by the row
+          // logical chunks 2 (lc % 4) and the next, swizzled by the row.  The
+          // lanes of the second half store their odd chunk first, so the eight
+          // lanes of a row (a quarter-warp) write eight different 16-byte bank
+          // groups with each store
           const int z = t + 128 * k, r = z >> 3, lc = z & 7;
-          const int hd = lc >> 2, dl = (lc & 3) * 2;
+          const int hd = lc >> 2, dl = (lc & 3) * 2 + hd;
           const int o0 = hd * tc::kBox + r * 128 + ((dl ^ (r & 7)) << 4);
-          const int o1 = hd * tc::kBox + r * 128 + (((dl + 1) ^ (r & 7)) << 4);
-          const uint4 w = kw[k], v = vw[k];
+          const int o1 = hd * tc::kBox + r * 128 + (((dl ^ 1) ^ (r & 7)) << 4);
+          const uint4 wk = kw[k], wv = vw[k];
+          const uint4 w = hd ? make_uint4(wk.z, wk.w, wk.x, wk.y) : wk;
+          const uint4 v = hd ? make_uint4(wv.z, wv.w, wv.x, wv.y) : wv;
           *reinterpret_cast<uint4*>(dst + o0) =
               make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w.x)),
                          e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
