@@ -13,25 +13,28 @@
 // producer warp streams by TMA into a ring of stages (64-row x 128-byte
 // boxes, 128-byte swizzle).  Per 64-key tile and lane:
 //  * S = Q K^T (M 128, N 64, K 128: eight K-major steps, both operands in
-//    shared memory) into one of the lane's two TMEM score buffers; the
-//    producer loads each lane's Q tile by TMA (a 3-D map over [tokens, heads,
-//    d]) as soon as the lane's last Q K^T of the previous unit is done;
+//    shared memory) into one of the lane's two TMEM score buffers; a Q
+//    loader warp loads each lane's Q tile by TMA (a 3-D map over [tokens,
+//    heads, d]) as soon as the lane's last Q K^T of the previous unit is done;
 //  * its softmax warpgroup (thread = row) loads the row of S, masks it by
 //    position, keeps the running maximum until it grows by more than 2^8
 //    (only then rescaling the row of O in TMEM), and writes P as BF16 pairs
 //    back over the scores;
 //  * O += P V (M 128, N 128 = d, K 64: four steps, A = P read from TMEM, B =
 //    V MN-major in shared memory), O resident in TMEM for the whole unit.
-// One warp issues every MMA; the two lanes' softmax runs overlap the other
-// lane's products.  V rows past the sequence length (or of a tile whose
+// Each lane has its own MMA warp, so one lane's softmax runs overlap the
+// other lane's products and one warp's barrier waits never idle the tensor
+// core.  V rows past the sequence length (or of a tile whose
 // block id is bad) are zeroed before any P V reads them: the cache may hold
 // NaN there.  Every mbarrier wait is bounded; on a timeout the CTA winds
 // down, lets its copies and products finish, and frees its TMEM.
 //
-// E4M3 caches (kFp8): a converter warpgroup turns each landed page of codes
-// into F16 (every E4M3 value is an F16 value) in a second ring the MMA warp
-// reads, and turns each lane's BF16 Q tile into F16 in place (exact for
-// |q| in [2^-14, 65504]); both products then run on F16 operands.  The K
+// E4M3 caches (kFp8): no TMA ring of codes.  A converter warpgroup reads
+// each tile's codes straight from the cache (the page two tiles on
+// prefetched into L2), writes them as F16 (every E4M3 value is an F16 value)
+// into the ring the MMA warps read, and turns each lane's BF16 Q tile into
+// F16 in place (exact for |q| in [2^-14, 65504]); both products then run on
+// F16 operands.  The K
 // scale joins the softmax scale and the V scale the final division, so the
 // result is the attention over the dequantised cache.
 #pragma once
