@@ -94,8 +94,8 @@ constexpr int regs_needed() {   // per CTA, for the warpgroups' raised budgets
 }
 
 // mbarriers (index of the first of each kind; [l] per lane, [l][i] per lane and buffer)
-constexpr int kBarRawFull = 0;     // [4] producer stage landed (TMA)
-constexpr int kBarRawEmpty = 4;    // [4] E4M3: producer stage consumed (128 converter threads)
+constexpr int kBarRawFull = 0;     // [4] BF16: producer stage landed (TMA)
+                                   // (4 .. 7 unused)
 constexpr int kBarMFull = 8;       // [4] E4M3: F16 tile written (128 converter threads)
 constexpr int kBarTEmpty = 12;     // [2][4] the lane's P V of the tile the MMA side holds done
                                    //     (a lane without the tile commits for it at its unit end)
@@ -254,10 +254,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
   const uint32_t base = smem_u32(smem);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kPStages; ++s) {
-      mbar_init(bar(tc::kBarRawFull + s), 1);
-      mbar_init(bar(tc::kBarRawEmpty + s), 128);
-    }
+    for (int s = 0; s < C::kPStages; ++s) mbar_init(bar(tc::kBarRawFull + s), 1);
     for (int c = 0; c < C::kMStages; ++c) {
       mbar_init(bar(tc::kBarMFull + c), 128);
       mbar_init(bar(tc::kBarTEmpty + c), 1);
@@ -378,7 +375,8 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       }
       ++n_pushed;
       if (!__shfl_sync(0xffffffffu, ok, 0) || b < 0) break;
-      // E4M3 caches: the converter reads the pages itself
+      // the unit's tiles by TMA, BF16 caches only (for E4M3 caches the
+      // converter reads the pages itself)
       for (int tb = 0; !kFp8 && tb < ntiles && alive; tb += 32) {
         const int t = tb + lane;
         const int bids = t < ntiles ? block_table[static_cast<int64_t>(b) * max_blocks + t] : 0;
@@ -393,9 +391,9 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
               tok = 0;
             } else if (use > 0) {
               const uint32_t par = (use - 1) & 1;
-              const bool freed = kFp8 ? mbar_wait(bar(tc::kBarRawEmpty + s), par, status)
-                                      : mbar_wait(bar(tc::kBarTEmpty + s), par, status) &&
-                                            mbar_wait(bar(tc::kBarTEmpty + 4 + s), par, status);
+              // the MMA side reads the stage itself; both lanes release it
+              const bool freed = mbar_wait(bar(tc::kBarTEmpty + s), par, status) &&
+                                 mbar_wait(bar(tc::kBarTEmpty + 4 + s), par, status);
               if (!freed) {
                 *abort_flag = 1;
                 tok = 0;
@@ -408,27 +406,20 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
               const uint32_t dst = base + s * C::kPStageBytes;
               const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;
               const int yv = yk + kHkv * kPage;
-              if constexpr (kFp8) {   // one 64-row x 128-code box per page
-                tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-                tma_load_2d(dst + C::kPStageBytes / 2, &kv_map, 0, yv, fb, policy);
-              } else {                // two 64-row x 64-element boxes per page
-                tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
-                tma_load_2d(dst + tc::kBox, &kv_map, 64, yk, fb, policy);
-                tma_load_2d(dst + tc::kPage, &kv_map, 0, yv, fb, policy);
-                tma_load_2d(dst + tc::kPage + tc::kBox, &kv_map, 64, yv, fb, policy);
-              }
+              // two 64-row x 64-element boxes per page
+              tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
+              tma_load_2d(dst + tc::kBox, &kv_map, 64, yk, fb, policy);
+              tma_load_2d(dst + tc::kPage, &kv_map, 0, yv, fb, policy);
+              tma_load_2d(dst + tc::kPage + tc::kBox, &kv_map, 64, yv, fb, policy);
             }
           }
           tok = __shfl_sync(0xffffffffu, tok, 0);
           if (tok && !good) {
             // a bad block id: no copy; the stage is marked (its keys are
-            // masked, its V rows zeroed: here for BF16, by the converter for
-            // E4M3) and the status set
-            if constexpr (!kFp8) {
-              uint4* vst = reinterpret_cast<uint4*>(smem + s * C::kPStageBytes + tc::kPage);
-              for (int z = lane; z < tc::kPage / 16; z += 32) vst[z] = make_uint4(0u, 0u, 0u, 0u);
-              fence_proxy_async_smem();
-            }
+            // masked, its V rows zeroed) and the status set
+            uint4* vst = reinterpret_cast<uint4*>(smem + s * C::kPStageBytes + tc::kPage);
+            for (int z = lane; z < tc::kPage / 16; z += 32) vst[z] = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               atomicOr(status, HPC_STATUS_BAD_BLOCK);
