@@ -60,6 +60,26 @@ def test_attention_matches_oracle(name):
     assert np.all(np.isfinite(got)), "NaN/inf in outputs (read past a length?)"
 
 
+@pytest.mark.parametrize("kv", [0, 1])
+def test_attention_at_the_batch_limit(kv):
+    """HPC_MAX_BATCH (8192) sequences of ragged lengths 1 .. 129 (single
+    tiles, tile edges, two tiles) through the planner, the attention and the
+    fused merge in the benchmark's launch configuration: the largest batch the
+    planner takes, with 64K segments and more items than queues."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    lengths = np.random.default_rng(11 + kv).integers(1, 130, 8192).tolist()
+    wl = Workload("custom", seed=11 + kv, lengths=lengths, kv_dtype=kv, include_new_token=True)
+    out, st = _run(wl)
+    assert st == 0, st
+    got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got)), "NaN/inf in outputs (read past a length?)"
+    seqs = sorted(set(_sample(wl, k=8, seed=5)) | {0, wl.batch - 1})
+    want = gu.oracle_outputs(wl, wl.q, seqs)
+    for n, b in enumerate(seqs):
+        gu.compare(got[b], want[n], *_tol(wl), label="batch limit seq %d (L=%d)" % (b, wl.lengths[b]))
+
+
 @pytest.mark.parametrize("lengths", [
     [1], [63], [64], [65], [0, 1, 0], [129, 1, 2, 3, 640, 641, 639],
     list(np.random.default_rng(9).integers(1, 300, 1024)),

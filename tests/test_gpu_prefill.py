@@ -41,6 +41,28 @@ def _check(wl, q, qs, out, seqs=None, heads=None, tol=None):
         gu.compare(got[a:e], want, *tol, label="seq %d (L=%d, q_len=%d)" % (b, L, e - a))
 
 
+def test_prefill_at_the_batch_limit():
+    """HPC_MAX_BATCH (8192) sequences, each with 1 .. 3 new tokens after a
+    ragged history (the decode side of a mixed batch at its largest): 64K
+    units dealt to the persistent grid; sampled sequences against the oracle."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    rng = np.random.default_rng(21)
+    q_lens = rng.integers(1, 4, 8192)
+    lengths = (q_lens + rng.integers(0, 127, 8192)).tolist()
+    wl, q, qst, qs = _batch(lengths, q_lens.tolist(), 21)
+    pf = ops.PrefillAttention(wl.batch)
+    pf.plan(qst)
+    out = torch.empty_like(q)
+    pf(q, qst, wl.cache, 0, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) == 0
+    assert int(pf.counters.abs().sum().item()) == 0
+    assert torch.isfinite(out.float()).all()
+    seqs = sorted(set(rng.choice(8192, 8, replace=False).tolist()) | {0, 8191})
+    _check(wl, q, qs, out, seqs=seqs)
+
+
 def test_prefill_prompts_and_chunks():
     """Whole prompts (q_len = L, tile and block edges) and chunks after a
     history, one launch; a second launch of the same plan gives the same bits."""
