@@ -11,14 +11,11 @@ import gpu_util as gu
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,two_launch", [("tiny", True), ("tiny", False), ("mixed", True),
-                                             ("mixed", False), ("heavy_tail", True)])
-def test_decode_step_end_to_end(name, two_launch):
-    gu.require_gpu()
+def _step_vs_oracle(wl, seqs, two_launch, label):
+    """One step over the workload; the sampled sequences against the oracle's
+    prologue, cache write and attention on host copies of their pages taken
+    before the step."""
     from paged_gqa_decode_rope_gb300 import ops
-    from paged_gqa_decode_rope_gb300.workloads import Workload
-    wl = Workload(name, seed=0)                 # history holds tokens 0 .. L-2
-    seqs = list(range(wl.batch)) if name == "tiny" else [int(np.argmax(wl.lengths)), 3, 9]
     views = {b: gu.seq_view(wl.cache, wl.block_table_np[b], int(wl.lengths[b]), wl.kv_dtype)
              for b in seqs}
     cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
@@ -28,6 +25,7 @@ def test_decode_step_end_to_end(name, two_launch):
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got)), "%s: NaN/inf in outputs" % label
     q, k, v = gu.bf16_host(wl.q), gu.bf16_host(wl.k), gu.bf16_host(wl.v)
     qw, kw = gu.bf16_host(wl.q_norm_w), gu.bf16_host(wl.k_norm_w)
     scale = wl.kv_scale.cpu().numpy().astype(np.float64)
@@ -39,7 +37,30 @@ def test_decode_step_end_to_end(name, two_launch):
         heads = list(range(0, 64, 9)) if L > 65536 else None
         q_out, want = od.decode_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], [L - 1], qw, kw, sub,
                                      row[None, :], [L], [slot], wl.kv_dtype, scale, heads=heads)
-        gu.compare(got[b], want[0], *tol, label="%s seq %d" % (name, b))
+        gu.compare(got[b], want[0], *tol, label="%s seq %d" % (label, b))
+
+
+@pytest.mark.parametrize("name,two_launch", [("tiny", True), ("tiny", False), ("mixed", True),
+                                             ("mixed", False), ("heavy_tail", True)])
+def test_decode_step_end_to_end(name, two_launch):
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload(name, seed=0)                 # history holds tokens 0 .. L-2
+    seqs = list(range(wl.batch)) if name == "tiny" else [int(np.argmax(wl.lengths)), 3, 9]
+    _step_vs_oracle(wl, seqs, two_launch, name)
+
+
+@pytest.mark.parametrize("kv", [0, 1])
+def test_decode_step_at_the_batch_limit(kv):
+    """The whole step for HPC_MAX_BATCH (8192) sequences of ragged lengths
+    1 .. 129: 73 729 prologue blocks beside the planner block, 8192 new tokens
+    written into the cache, then the attention and merge."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    rng = np.random.default_rng(31 + kv)
+    wl = Workload("custom", seed=31 + kv, lengths=rng.integers(1, 130, 8192).tolist(), kv_dtype=kv)
+    seqs = sorted(set(rng.choice(8192, 6, replace=False).tolist()) | {0, 8191})
+    _step_vs_oracle(wl, seqs, True, "batch limit kv %d" % kv)
 
 
 @pytest.mark.parametrize("two_launch", [True, False])
