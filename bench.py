@@ -459,22 +459,27 @@ def _describe(wl):
 def prefill_times(ops, stream, reps=10):
     """Prefill attention: 4 whole prompts of 4096 tokens and 8 chunks of 512
     new tokens after 7680-token histories on a BF16 cache, and the prompts on
-    an E4M3 cache; CUDA events over ``reps`` launches.  Flops 4 * 64 * 128 per
-    query token and visible key (the causal triangle counted exactly)."""
+    an E4M3 cache, directly and with the pages staged to BF16 first (the
+    staging launches timed with the attention); CUDA events over ``reps``
+    calls.  Flops 4 * 64 * 128 per query token and visible key (the causal
+    triangle counted exactly)."""
     import torch
     from paged_gqa_decode_rope_gb300.workloads import Workload
     res = {}
     peaks = _load_peak_tflops()
-    for name, lengths, q_lens, kvd in (("4 prompts x 4096", [4096] * 4, [4096] * 4, 0),
-                                       ("8 chunks of 512 after 7680", [8192] * 8, [512] * 8, 0),
-                                       ("4 prompts x 4096, E4M3 cache", [4096] * 4, [4096] * 4, 1)):
+    for name, lengths, q_lens, kvd, staged in (
+            ("4 prompts x 4096", [4096] * 4, [4096] * 4, 0, False),
+            ("8 chunks of 512 after 7680", [8192] * 8, [512] * 8, 0, False),
+            ("4 prompts x 4096, E4M3 cache", [4096] * 4, [4096] * 4, 1, False),
+            ("4 prompts x 4096, E4M3 cache staged to BF16", [4096] * 4, [4096] * 4, 1, True)):
         wl = Workload("custom", seed=21, lengths=lengths, kv_dtype=kvd, include_new_token=True)
         qs = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
         g = torch.Generator(device="cuda").manual_seed(1)
         q = torch.randn((int(qs[-1]), 64, 128), generator=g, device="cuda").to(torch.bfloat16)
         qst = torch.as_tensor(qs, device="cuda")
         out = torch.empty_like(q)
-        pf = ops.PrefillAttention(wl.batch)
+        pf = ops.PrefillAttention(wl.batch, staging_pages=ops.PrefillAttention.pages_for(lengths)
+                                  if staged else 0)
         pf.plan(qst)
         for _ in range(2):
             pf(q, qst, wl.cache, kvd, wl.kv_scale, wl.block_table, wl.seq_lens, out)

@@ -489,6 +489,37 @@ int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t* query_sta
                      int32_t batch, const int32_t* unit_ptr, int32_t* counters, void* out,
                      int32_t out_dtype, float sm_scale, int32_t* status, cudaStream_t stream);
 
+/* hpc_prefill_attn with the pages of an E4M3 cache staged first.  Each tile
+ * of a sequence is read by every unit of 32 new tokens that sees it (about
+ * q_len / 64 units on average for a prompt), and the E4M3 kernel converts it
+ * each time; this call instead converts every page the batch reads once, into
+ * a caller-owned BF16 staging buffer (exact: every E4M3 value is a BF16
+ * value), and runs the BF16 kernel over the staged pages with the K and V
+ * scales.  Three launches: the page prefix, the conversion, the attention.
+ * The result is the attention over the dequantised cache, with P stored as
+ * BF16 (as for a BF16 cache) instead of F16.  For a BF16 cache this is
+ * hpc_prefill_attn (staging unused).
+ * Source: as hpc_prefill_attn.
+ * Arguments as hpc_prefill_attn, and:
+ *   staging        (device) [staging_pages][2][8][64][128] bf16, 16-byte
+ *                  aligned, written: staged page page_ptr[b] + j holds block
+ *                  block_table[b][j] of sequence b
+ *   staging_pages  pages staging holds; it needs sum_b ceil(seq_lens[b] / 64)
+ *   page_ptr       (device) int32 [batch + 1], written: page_ptr[b] = first
+ *                  staged page of sequence b, page_ptr[batch] = all pages
+ *   status         as hpc_prefill_attn, and PLAN_OVERFLOW for a sequence whose
+ *                  pages do not fit in staging (the sequence is skipped)
+ * Errors: as hpc_prefill_attn; HPC_ERR_INVALID_ARG for an E4M3 cache without
+ * staging or page_ptr, staging_pages < 1 or misaligned staging;
+ * HPC_ERR_UNSUPPORTED for staging_pages > HPC_MAX_NUM_BLOCKS. */
+int hpc_prefill_attn_staged(const void* q, int32_t num_tokens, const int32_t* query_start,
+                            const void* kv_cache, int32_t kv_dtype, const float* kv_scale,
+                            int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,
+                            const int32_t* seq_lens, int32_t batch, const int32_t* unit_ptr,
+                            int32_t* counters, void* out, int32_t out_dtype, float sm_scale,
+                            void* staging, int32_t staging_pages, int32_t* page_ptr,
+                            int32_t* status, cudaStream_t stream);
+
 /* Self-test of the bounded pipeline wait (no counterpart on the pages).
  * Every wait of the attention pipeline gives up after a time limit (1 s),
  * sets HPC_STATUS_WAIT_TIMEOUT and winds its CTA down, so a stuck pipeline

@@ -96,6 +96,9 @@ SIGNATURES = {
     "hpc_prefill_attn": (ctypes.c_int, [
         _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p,
         _c_i32, ctypes.c_float, _c_p, _c_p]),
+    "hpc_prefill_attn_staged": (ctypes.c_int, [
+        _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p,
+        _c_i32, ctypes.c_float, _c_p, _c_i32, _c_p, _c_p, _c_p]),
     "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }
 

@@ -55,6 +55,83 @@ __global__ void __launch_bounds__(kPfPlanThreads) prefill_plan_kernel(
   }
 }
 
+// Staged pages (hpc_prefill_attn_staged): page_ptr[b] = first staged page of
+// sequence b (its ceil(L_b / 64) pages in order), page_ptr[batch] = all of
+// them.  One CTA of kPfPlanThreads threads.
+__global__ void __launch_bounds__(kPfPlanThreads) stage_plan_kernel(
+    const int32_t* __restrict__ seq_lens, int32_t batch, int32_t max_blocks,
+    int32_t* __restrict__ page_ptr, int32_t* __restrict__ status) {
+  __shared__ int warp_sums[32];
+  const int per = (batch + kPfPlanThreads - 1) / kPfPlanThreads;
+  const int b0 = min(batch, static_cast<int>(threadIdx.x) * per);
+  const int b1 = min(batch, b0 + per);
+  auto pages = [&](int b) {
+    const int L = seq_lens[b];
+    if (L < 0 || L > max_blocks * kPage) return 0;   // the attention reports the sequence
+    return (L + kPage - 1) / kPage;
+  };
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += pages(b);
+  int total;
+  int run = cta_exclusive_scan<kPfPlanThreads>(local, warp_sums, &total);
+  for (int b = b0; b < b1; ++b) {
+    page_ptr[b] = run;
+    run += pages(b);
+  }
+  if (threadIdx.x == 0) page_ptr[batch] = total;
+}
+
+// Every page the batch reads, E4M3 codes -> BF16 (exact: every E4M3 value is
+// a BF16 value) into its staged page: staged page page_ptr[b] + j holds
+// block block_table[b][j] of sequence b.  The work is split into 8 KB pieces
+// (one K or V page of one KV head), dealt grid-stride, so a batch of few long
+// pages still spreads over every SM; 256 threads, 16 codes a thread and
+// step, both loads and stores coalesced.  Pages past the staging capacity are
+// left (their sequences are reported by the attention); a bad block id
+// stages nothing (the attention masks that tile by the real block table).
+constexpr int kStageThreads = 256;
+__global__ void __launch_bounds__(kStageThreads) stage_convert_kernel(
+    const uint8_t* __restrict__ cache, int32_t num_blocks, const int32_t* __restrict__ block_table,
+    int32_t max_blocks, int32_t batch, const int32_t* __restrict__ page_ptr, int32_t staged_pages,
+    uint16_t* __restrict__ staged) {
+  constexpr int kPieces = 2 * kHkv;                 // K and V of 8 heads per block
+  constexpr int kPieceChunks = kPage * kD / 16;     // 16-code chunks of a piece (512)
+  const int64_t total = static_cast<int64_t>(min(page_ptr[batch], staged_pages)) * kPieces;
+  for (int64_t u = blockIdx.x; u < total; u += gridDim.x) {
+    const int pg = static_cast<int>(u / kPieces), piece = static_cast<int>(u % kPieces);
+    int lo = 0, hi = batch;   // the last b with page_ptr[b] <= pg
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (page_ptr[mid] <= pg) lo = mid;
+      else hi = mid;
+    }
+    const int bid = block_table[static_cast<int64_t>(lo) * max_blocks + (pg - page_ptr[lo])];
+    if (bid < 0 || bid >= num_blocks) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        cache + (static_cast<int64_t>(bid) * kPieces + piece) * kPieceChunks * 16);
+    uint4* dst = reinterpret_cast<uint4*>(
+        staged + (static_cast<int64_t>(pg) * kPieces + piece) * kPieceChunks * 16);
+#pragma unroll
+    for (int z = threadIdx.x; z < kPieceChunks; z += kStageThreads) {
+      const uint4 w = src[z];
+      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // two codes -> f16x2 (exact) -> two floats -> bf16x2 (exact)
+        const uint32_t h0 = e4m3x2_to_f16x2(static_cast<uint16_t>(in[k]));
+        const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(in[k] >> 16));
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+        o[2 * k] = pack_bf16(f0.x, f0.y);
+        o[2 * k + 1] = pack_bf16(f1.x, f1.y);
+      }
+      dst[2 * z] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[2 * z + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
 template <bool kFp8>
 cudaError_t prefill_tc_smem_optin() {
   static std::mutex mu;
@@ -90,13 +167,17 @@ extern "C" int hpc_prefill_plan(const int32_t* query_start, int32_t batch, int32
   return HPC_LAUNCH_STATUS();
 }
 
-extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t* query_start,
-                                const void* kv_cache,
-                                int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
-                                const int32_t* block_table, int32_t max_blocks,
-                                const int32_t* seq_lens, int32_t batch, const int32_t* unit_ptr,
-                                int32_t* counters, void* out, int32_t out_dtype, float sm_scale,
-                                int32_t* status, cudaStream_t stream) {
+namespace hpc {
+namespace {
+
+// hpc_prefill_attn, or with staging set hpc_prefill_attn_staged: the checks,
+// the maps and the launches.
+int prefill_run(const void* q, int32_t num_tokens, const int32_t* query_start, const void* kv_cache,
+                int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
+                const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                int32_t batch, const int32_t* unit_ptr, int32_t* counters, void* out,
+                int32_t out_dtype, float sm_scale, void* staging, int32_t staging_pages,
+                int32_t* page_ptr, int32_t* status, cudaStream_t stream) {
   HPC_CHECK_ARG(q && query_start && kv_cache && block_table && seq_lens && unit_ptr && counters &&
                 out && status);
   HPC_CHECK_ARG(batch >= 0 && num_tokens >= 0 && num_blocks > 0 && max_blocks >= 1 && sm_scale > 0.f);
@@ -108,31 +189,41 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
   HPC_CHECK_ARG(!fp8 || kv_scale != nullptr);
   if (batch > HPC_MAX_BATCH || num_blocks > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(max_blocks) * hpc::kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks) * kPage >= (int64_t{1} << 31)) return HPC_ERR_UNSUPPORTED;
+  const bool staged = fp8 && staging != nullptr;
+  if (staged) {
+    HPC_CHECK_ARG(page_ptr != nullptr && staging_pages >= 1 &&
+                  (reinterpret_cast<uintptr_t>(staging) & 15) == 0);
+    if (staging_pages > HPC_MAX_NUM_BLOCKS) return HPC_ERR_UNSUPPORTED;
+  }
   if (batch == 0 || num_tokens == 0) return HPC_OK;
-  auto encode = hpc::tensor_map_encoder();
+  auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
+  // the pages the kernel streams: the cache, or its staged BF16 copy
+  const void* pages = staged ? staging : kv_cache;
+  const bool pages_fp8 = fp8 && !staged;
+  const int32_t map_blocks = staged ? staging_pages : num_blocks;
   CUtensorMap map;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(hpc::kD),
-                              static_cast<cuuint64_t>(num_blocks) * 2 * hpc::kHkv * hpc::kPage};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
+                              static_cast<cuuint64_t>(map_blocks) * 2 * kHkv * kPage};
   // rows of 128 BF16 (two 64-element boxes per page) or 128 E4M3 codes (one box)
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(hpc::kD) * (fp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(hpc::kPage)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * (pages_fp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {pages_fp8 ? 128u : 64u, static_cast<cuuint32_t>(kPage)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult cr = encode(&map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                             2, const_cast<void*>(kv_cache),
+  const CUresult cr = encode(&map, pages_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             2, const_cast<void*>(pages),
                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return HPC_ERR_INVALID_ARG;
   // q as [tokens][64 heads][128 d]: boxes of 16 tokens x 8 heads x 64 of d
   CUtensorMap q_map;
-  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(hpc::kD), static_cast<cuuint64_t>(hpc::kHq),
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kHq),
                                static_cast<cuuint64_t>(num_tokens)};
-  const cuuint64_t qstrides[2] = {static_cast<cuuint64_t>(hpc::kD) * 2,
-                                  static_cast<cuuint64_t>(hpc::kHq) * hpc::kD * 2};
-  const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(hpc::kGroup),
-                              static_cast<cuuint32_t>(hpc::tc::kLaneTokens)};
+  const cuuint64_t qstrides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                  static_cast<cuuint64_t>(kHq) * kD * 2};
+  const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(kGroup),
+                              static_cast<cuuint32_t>(tc::kLaneTokens)};
   const cuuint32_t qestr[3] = {1, 1, 1};
   const CUresult qr = encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims,
                              qstrides, qbox, qestr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -143,18 +234,58 @@ extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
-  if (fp8) {
-    if (hpc::prefill_tc_smem_optin<true>() != cudaSuccess) return HPC_ERR_CUDA;
-    hpc::prefill_tc_kernel<true><<<sms, hpc::tc::Cfg<true>::kThreads, hpc::tc::kSmemBytes, stream>>>(
+  if (staged) {
+    stage_plan_kernel<<<1, kPfPlanThreads, 0, stream>>>(seq_lens, batch, max_blocks, page_ptr, status);
+    stage_convert_kernel<<<8 * sms, kStageThreads, 0, stream>>>(
+        static_cast<const uint8_t*>(kv_cache), num_blocks, block_table, max_blocks, batch, page_ptr,
+        staging_pages, static_cast<uint16_t*>(staging));
+    if (cudaPeekAtLastError() != cudaSuccess) return HPC_ERR_CUDA;
+  }
+  if (pages_fp8) {
+    if (prefill_tc_smem_optin<true>() != cudaSuccess) return HPC_ERR_CUDA;
+    prefill_tc_kernel<true><<<sms, tc::Cfg<true>::kThreads, tc::kSmemBytes, stream>>>(
         map, q_map, num_tokens, static_cast<const uint8_t*>(kv_cache), kv_scale, query_start,
-        seq_lens, batch, block_table, max_blocks,
-        num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
+        seq_lens, batch, block_table, max_blocks, num_blocks, unit_ptr, counters, out, out_dtype,
+        sm_scale, status, nullptr, 0);
   } else {
-    if (hpc::prefill_tc_smem_optin<false>() != cudaSuccess) return HPC_ERR_CUDA;
-    hpc::prefill_tc_kernel<false><<<sms, hpc::tc::Cfg<false>::kThreads, hpc::tc::kSmemBytes, stream>>>(
-        map, q_map, num_tokens, static_cast<const uint8_t*>(kv_cache), kv_scale, query_start,
-        seq_lens, batch, block_table, max_blocks,
-        num_blocks, unit_ptr, counters, out, out_dtype, sm_scale, status);
+    // BF16 pages: the cache itself (no scales, whatever kv_scale points at),
+    // or the staged copy of an E4M3 cache (its scales; the real block table
+    // still says which tiles are bad)
+    if (prefill_tc_smem_optin<false>() != cudaSuccess) return HPC_ERR_CUDA;
+    prefill_tc_kernel<false><<<sms, tc::Cfg<false>::kThreads, tc::kSmemBytes, stream>>>(
+        map, q_map, num_tokens, static_cast<const uint8_t*>(pages), staged ? kv_scale : nullptr,
+        query_start, seq_lens, batch, block_table, max_blocks, num_blocks, unit_ptr, counters, out,
+        out_dtype, sm_scale, status, staged ? page_ptr : nullptr, staged ? staging_pages : 0);
   }
   return HPC_LAUNCH_STATUS();
+}
+
+}  // namespace
+}  // namespace hpc
+
+extern "C" int hpc_prefill_attn(const void* q, int32_t num_tokens, const int32_t* query_start,
+                                const void* kv_cache,
+                                int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
+                                const int32_t* block_table, int32_t max_blocks,
+                                const int32_t* seq_lens, int32_t batch, const int32_t* unit_ptr,
+                                int32_t* counters, void* out, int32_t out_dtype, float sm_scale,
+                                int32_t* status, cudaStream_t stream) {
+  return hpc::prefill_run(q, num_tokens, query_start, kv_cache, kv_dtype, kv_scale, num_blocks,
+                          block_table, max_blocks, seq_lens, batch, unit_ptr, counters, out,
+                          out_dtype, sm_scale, nullptr, 0, nullptr, status, stream);
+}
+
+extern "C" int hpc_prefill_attn_staged(const void* q, int32_t num_tokens,
+                                       const int32_t* query_start, const void* kv_cache,
+                                       int32_t kv_dtype, const float* kv_scale, int32_t num_blocks,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       const int32_t* seq_lens, int32_t batch,
+                                       const int32_t* unit_ptr, int32_t* counters, void* out,
+                                       int32_t out_dtype, float sm_scale, void* staging,
+                                       int32_t staging_pages, int32_t* page_ptr, int32_t* status,
+                                       cudaStream_t stream) {
+  if (kv_dtype == HPC_KV_FP8_E4M3) HPC_CHECK_ARG(staging != nullptr);
+  return hpc::prefill_run(q, num_tokens, query_start, kv_cache, kv_dtype, kv_scale, num_blocks,
+                          block_table, max_blocks, seq_lens, batch, unit_ptr, counters, out,
+                          out_dtype, sm_scale, staging, staging_pages, page_ptr, status, stream);
 }

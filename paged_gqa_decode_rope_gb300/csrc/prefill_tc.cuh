@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
     const int32_t* __restrict__ query_start, const int32_t* __restrict__ seq_lens, int32_t batch,
     const int32_t* __restrict__ block_table, int32_t max_blocks, int32_t num_blocks,
     const int32_t* __restrict__ unit_ptr, int32_t* counters, void* __restrict__ out,
-    int32_t out_dtype, float sm_scale, int32_t* __restrict__ status) {
+    int32_t out_dtype, float sm_scale, int32_t* __restrict__ status,
+    const int32_t* __restrict__ page_ptr, int32_t staged_pages) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -350,6 +351,11 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         } else {
           nt0 = tc::lane_tiles(qlen, L, pair * tc::kUnitTokens);
           nt1 = tc::lane_tiles(qlen, L, pair * tc::kUnitTokens + tc::kLaneTokens);
+          // staged pages: sequence b's pages are staged pages page_ptr[b] ..
+          if (page_ptr != nullptr && page_ptr[b + 1] > staged_pages) {
+            if (lane == 0) atomicOr(status, HPC_STATUS_PLAN_OVERFLOW);
+            nt0 = nt1 = -1;
+          }
         }
       }
       const int ntiles = max(nt0, nt1);
@@ -380,6 +386,7 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       for (int tb = 0; !kFp8 && tb < ntiles && alive; tb += 32) {
         const int t = tb + lane;
         const int bids = t < ntiles ? block_table[static_cast<int64_t>(b) * max_blocks + t] : 0;
+        const int page0 = page_ptr != nullptr ? page_ptr[b] + tb : 0;   // staged page of tile tb
         for (int jj = 0; jj < min(32, ntiles - tb) && alive; ++jj) {
           const int bid = __shfl_sync(0xffffffffu, bids, jj);
           const bool good = bid >= 0 && bid < num_blocks;
@@ -404,7 +411,9 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
               const uint32_t fb = bar(tc::kBarRawFull + s);
               mbar_arrive_expect_tx(fb, C::kPStageBytes);
               const uint32_t dst = base + s * C::kPStageBytes;
-              const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;
+              // the cache's block, or (staged) the staged copy of the sequence's page
+              const int yb = page_ptr != nullptr ? page0 + jj : bid;
+              const int yk = ((yb * 2 + 0) * kHkv + h) * kPage;
               const int yv = yk + kHkv * kPage;
               // two 64-row x 64-element boxes per page
               tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
@@ -547,8 +556,10 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
     const int tok = row >> 3, hl = row & 7;
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 * l;
     // E4M3: scores of the codes times the K scale, outputs times the V scale
-    const float scale_log2 = sm_scale * 1.4426950408889634f * (kFp8 ? kv_scale[0] : 1.f);
-    const float v_scale = kFp8 ? kv_scale[1] : 1.f;
+    // (also for BF16 pages staged from an E4M3 cache: the host passes the scales then)
+    const float scale_log2 =
+        sm_scale * 1.4426950408889634f * (kFp8 || kv_scale != nullptr ? kv_scale[0] : 1.f);
+    const float v_scale = kFp8 || kv_scale != nullptr ? kv_scale[1] : 1.f;
     uint32_t G = 0, U = 0, Gl = 0, Vl = 0;
     bool dead = false;
     Unit d;

@@ -611,11 +611,25 @@ class PrefillAttention:
     query_start[b+1]-1 of q and out and sees its history plus its new tokens
     up to each one.  The unit plan and counters are allocated once."""
 
-    def __init__(self, batch, device="cuda", out_dtype=OUT_BF16):
+    def __init__(self, batch, device="cuda", out_dtype=OUT_BF16, staging_pages=0):
+        """``staging_pages`` > 0: E4M3 caches go through hpc_prefill_attn_staged
+        with a BF16 staging buffer of that many pages (it needs the sum over
+        sequences of ceil(seq_len / 64); see ``pages_for``)."""
         self.batch, self.out_dtype = batch, out_dtype
         self.unit_ptr = torch.zeros(batch + 1, dtype=torch.int32, device=device)
         self.counters = torch.zeros(2, dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.staging_pages = int(staging_pages)
+        self.staging = self.page_ptr = None
+        if self.staging_pages > 0:
+            self.staging = torch.empty((self.staging_pages, 2, HKV, PAGE, D), dtype=torch.bfloat16,
+                                       device=device)
+            self.page_ptr = torch.zeros(batch + 1, dtype=torch.int32, device=device)
+
+    @staticmethod
+    def pages_for(seq_lens):
+        """Staged pages a batch needs: the sum of ceil(L / 64) over its lengths (host values)."""
+        return int(sum((int(L) + PAGE - 1) // PAGE for L in seq_lens))
 
     def plan(self, query_start):
         _want(query_start, "query_start", (torch.int32,), (self.batch + 1,))
@@ -636,6 +650,14 @@ class PrefillAttention:
         _want(seq_lens, "seq_lens", (torch.int32,), (B,))
         _want(out, "out", (_OUT_TORCH[self.out_dtype],), (T, HQ, D))
         scale = 1.0 / math.sqrt(D) if sm_scale is None else float(sm_scale)
+        if self.staging is not None and kv_dtype == KV_FP8:
+            check("hpc_prefill_attn_staged", _lib.lib().hpc_prefill_attn_staged(
+                _p(q), T, _p(query_start), _p(kv_cache), kv_dtype, _p(kv_scale),
+                kv_cache.shape[0], _p(block_table), block_table.shape[1], _p(seq_lens), B,
+                _p(self.unit_ptr), _p(self.counters), _p(out), int(self.out_dtype), scale,
+                _p(self.staging), self.staging_pages, _p(self.page_ptr), _p(self.status),
+                _stream()))
+            return out
         check("hpc_prefill_attn", _lib.lib().hpc_prefill_attn(
             _p(q), T, _p(query_start), _p(kv_cache), kv_dtype,
             _p(kv_scale if kv_dtype == KV_FP8 else None), kv_cache.shape[0], _p(block_table),

@@ -157,18 +157,23 @@ def test_prefill_bad_lengths_set_status_and_skip():
     _check(wl, q, qs, out, seqs=[1])
 
 
+@pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("kv_dtype", [0, 1])
-def test_prefill_bad_block_is_reported_and_skipped(kv_dtype):
+def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged):
     """A block id past the cache: the status says BAD_BLOCK, the page's keys
     are left out of that sequence's attention, the other sequences are
-    untouched (BF16 and E4M3 caches)."""
+    untouched (BF16 and E4M3 caches; E4M3 also through staged pages, where the
+    real block table still marks the tile)."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
+    if staged and kv_dtype == 0:
+        pytest.skip("staging applies to E4M3 caches")
     lengths = [300, 260, 100]
     q_lens = [40, 70, 100]
     wl, q, qst, qs = _batch(lengths, q_lens, 17, kv_dtype)
     wl.block_table[1, 2] = wl.num_blocks + 5           # page 2 (keys 128..191) of sequence 1
-    pf = ops.PrefillAttention(wl.batch)
+    pf = ops.PrefillAttention(wl.batch, staging_pages=ops.PrefillAttention.pages_for(lengths)
+                              if staged else 0)
     pf.plan(qst)
     out = torch.empty_like(q)
     pf(q, qst, wl.cache, kv_dtype, wl.kv_scale, wl.block_table, wl.seq_lens, out)
@@ -216,3 +221,59 @@ def test_prefill_fp8_cache_prompts_and_chunks():
     assert torch.equal(outs[ops.OUT_BF16], outs[ops.OUT_FP32].to(torch.bfloat16))
     _check(wl, q, qs, outs[ops.OUT_FP32])
     _check(wl, q, qs, outs[ops.OUT_BF16])
+
+
+def test_prefill_fp8_cache_staged_pages():
+    """An E4M3 cache through hpc_prefill_attn_staged: every page the batch
+    reads converted once into BF16 staging, then the BF16 kernel with the K and
+    V scales.  The page prefix is ceil(L / 64) per sequence; the output matches
+    the oracle over the device's codes, and the direct E4M3 kernel to within
+    the FP8 tolerance (P is BF16 here, F16 there); a second launch gives the
+    same bits."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [1, 16, 17, 64, 65, 130, 300, 1000, 2200]
+    q_lens = [1, 16, 17, 64, 65, 130, 37, 200, 33]
+    wl, q, qst, qs = _batch(lengths, q_lens, 23, kv_dtype=1)
+    need = ops.PrefillAttention.pages_for(lengths)
+    pf = ops.PrefillAttention(wl.batch, staging_pages=need)
+    pf.plan(qst)
+    out = torch.full_like(q, float("nan"))
+    pf(q, qst, wl.cache, 1, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    again = pf(q, qst, wl.cache, 1, wl.kv_scale, wl.block_table, wl.seq_lens, torch.empty_like(q))
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) == 0
+    assert int(pf.counters.abs().sum().item()) == 0
+    pages = [(L + 63) // 64 for L in lengths]
+    assert pf.page_ptr.cpu().tolist() == [0] + np.cumsum(pages).tolist()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    _check(wl, q, qs, out)
+    direct = ops.PrefillAttention(wl.batch)
+    direct.plan(qst)
+    ref = direct(q, qst, wl.cache, 1, wl.kv_scale, wl.block_table, wl.seq_lens, torch.empty_like(q))
+    torch.cuda.synchronize()
+    # both are within the oracle's FP8 tolerance; between them the BF16 P
+    # moves an output by at most a few BF16 ulps (1 ulp is 2^-6 at |x| in [2, 4))
+    diff = (out.float() - ref.float()).abs()
+    assert float(diff.max()) <= gu.TOL_FP8_MAX and float(diff.mean()) <= 5e-4, \
+        (float(diff.max()), float(diff.mean()))
+
+
+def test_prefill_staging_overflow_skips_the_sequences_that_do_not_fit():
+    """Staging with room for the first sequences' pages only: PLAN_OVERFLOW,
+    the sequences that fit are computed, the others skipped (left as they were)."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    lengths = [300, 130, 2200, 65]
+    q_lens = [37, 130, 33, 65]
+    wl, q, qst, qs = _batch(lengths, q_lens, 29, kv_dtype=1)
+    room = ops.PrefillAttention.pages_for(lengths[:2])    # sequences 0 and 1 fit, 2 and 3 do not
+    pf = ops.PrefillAttention(wl.batch, staging_pages=room)
+    pf.plan(qst)
+    out = torch.full_like(q, float("nan"))
+    pf(q, qst, wl.cache, 1, wl.kv_scale, wl.block_table, wl.seq_lens, out)
+    torch.cuda.synchronize()
+    assert int(pf.status.item()) & 16                    # HPC_STATUS_PLAN_OVERFLOW
+    assert int(pf.counters.abs().sum().item()) == 0
+    _check(wl, q, qs, out, seqs=[0, 1])
+    assert torch.isnan(out[int(qs[2]):].float()).all()
