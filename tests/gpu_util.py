@@ -8,7 +8,6 @@ import pytest
 import torch
 
 from oracle import decode as od
-from oracle import numerics as nx
 
 TOL_BF16_MAX = 2e-2
 TOL_BF16_MEAN = 2e-3

@@ -12,7 +12,6 @@ import pytest
 import torch
 
 from oracle import decode as od
-from oracle import numerics as nx
 import gpu_util as gu
 
 pytestmark = pytest.mark.gpu

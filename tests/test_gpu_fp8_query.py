@@ -2,7 +2,6 @@
 on the tensor cores) and the caller-chosen output type, against the float64
 oracle on the same dequantised values."""
 
-import math
 
 import numpy as np
 import pytest

@@ -2,7 +2,6 @@
 a barrier phase nothing completes, the kernel records WAIT_TIMEOUT and
 returns, and the same context then runs a decode step normally."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -7,7 +7,6 @@ defect: a wrong pairing, sign, exponent, index, scale, dropped term or
 rounding rule.
 """
 
-import math
 
 import numpy as np
 import pytest

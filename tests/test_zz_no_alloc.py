@@ -12,7 +12,6 @@ tests.  Collected last on purpose; it also passes alone in a fresh process.
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 
