@@ -8,7 +8,16 @@ KV in 64-token pages), whose KV (1.06 GB) is larger than L2, so no flush is
 needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-static] [--no-cpu]
+                    [--workload tiny|uniform|mixed|mixed_fp8|heavy_tail] [--seed S]
+                    [--no-static] [--no-cpu] [--cpu-seconds T] [--no-multi-token]
+                    [--no-prefill]
+    python bench.py --prefill-only
+
+The JSON line also carries the roofline of the dominant kernel (the attention
+with the merge fused in), the end-to-end rate through the public API with
+host buffers, the CPU oracle baseline, the SM clocks seen while timing, the
+dynamic-vs-static schedule comparison, and the multi-token and prefill
+timings (each section can be skipped with its flag).
 
 Prints ONE JSON line on rank 0.  ``value`` is the KV+Q+O bytes of all ranks'
 batches divided by the max-over-ranks device time of K steps (TB/s);
