@@ -41,6 +41,13 @@
 //    run over a fixed permutation of d (and the V rows over a permutation of
 //    d inside each 16-row tile) that makes each ldmatrix word feed the MMA
 //    directly; q uses the same permutation and the epilogue undoes it.
+//  * With an E4M3 q (kQ8; E4M3 caches only) Q K^T runs as E4M3 x E4M3
+//    products (m16n8k32) on the codes themselves, q_scale joining the
+//    softmax scale; P V stays f16.
+//  * With the merge fused in (out set), a segment of one item is written to
+//    the output directly; the queue that finishes the last item of a longer
+//    segment (a per-segment arrival counter) merges its partials in item
+//    order, so the result does not depend on which queue merges.
 //  * Tokens past a query's last visible key get p = 0 and their V entries
 //    are zeroed in registers (the cache may hold NaN there: 0 * NaN is NaN).
 //  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
