@@ -193,6 +193,8 @@ def _mt_mutant(kind):
                     seen = length
                 elif kind == "self_hidden":
                     seen = length - qn + t
+                elif kind == "from_start":              # positions counted from the sequence start
+                    seen = min(t + 1, length)
                 else:                                   # "reversed": new tokens in the wrong order
                     seen = length - t
                 for j in range(h * 8, h * 8 + 8):
@@ -206,3 +208,11 @@ def _mt_mutant(kind):
 def test_multi_token_mutants_fail_masked_sdpa(kind):
     with pytest.raises(AssertionError):
         pins.check_attention_mt_sdpa(_mt_mutant(kind), np.random.default_rng(3))
+
+
+def test_prefill_position_mutant_fails_chunk_pin():
+    """New tokens placed at positions 0 .. q_len-1 instead of L-q_len .. L-1:
+    the same as the right rule for a whole prompt, wrong for a chunk after a
+    history; the prefill pin (which has chunks) must catch it."""
+    with pytest.raises(AssertionError):
+        pins.check_attention_prefill_sdpa(_mt_mutant("from_start"), np.random.default_rng(5))
