@@ -88,6 +88,43 @@ def check_rms_norm_library(rms, rng):
     assert np.allclose(cos, 1.0, rtol=1e-13)
 
 
+# -------------------------------------------------------------- prologue --
+
+def check_prologue_order(prologue):
+    """prologue(q [64,128], k [8,128], v [8,128], pos, q_w, k_w) -> (q', k', v').
+
+    Hand-derived fixture (tests/golden/prologue_order.json): a unit vector
+    rotated by RoPE and then normalised with a weight that differs between
+    the two elements of its rotation pair.  Rotating first puts w[i] on the
+    cosine part and w[i+64] on the sine part; normalising first would put
+    one weight on both.  The q and k weight vectors differ at the checked
+    elements, so using one for the other also fails."""
+    g = load_golden("prologue_order.json")
+    for which in ("q", "k"):
+        q = np.zeros((64, D))
+        k = np.zeros((8, D))
+        v = np.arange(8 * D, dtype=np.float64).reshape(8, D) / 100.0
+        q_w, k_w = np.ones(D), np.ones(D)
+        for i, w in g["q_weight"].items():
+            q_w[int(i)] = float(w)
+        for i, w in g["k_weight"].items():
+            k_w[int(i)] = float(w)
+        head = g[which + "_head"]
+        x = q if which == "q" else k
+        x[head, g[which + "_in_index"]] = 1.0
+        qo, ko, vo = prologue(q, k, v, g[which + "_pos"], q_w, k_w)
+        got = qo if which == "q" else ko
+        other = ko if which == "q" else qo
+        want = np.zeros_like(got)
+        for i, val in g[which + "_expected"].items():
+            want[head, int(i)] = float(val)
+        # the angle is exactly 1 rad; float64 sin/cos and the norm's sqrt
+        # leave a few ulp of the ~30-sized results
+        assert np.max(np.abs(got - want)) <= 1e-13, (which, got[head][got[head] != 0])
+        assert not np.any(other), "a zero head stays zero"
+        assert np.array_equal(vo, v), "v passes through"
+
+
 # ------------------------------------------------------------- attention --
 
 def check_attention_closed_forms(attn, rng):

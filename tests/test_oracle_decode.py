@@ -31,6 +31,12 @@ def test_rms_norm_against_library(rng):
     pins.check_rms_norm_library(od.rms_norm, rng)
 
 
+def test_prologue_order_hand_derived():
+    """RoPE first, then the weighted RMSNorm: hand-derived values at an angle
+    of exactly 1 rad for a q head and a k head."""
+    pins.check_prologue_order(od.prologue_token)
+
+
 def test_prologue_order_only_matters_through_the_weight(rng):
     """The mean square is rotation invariant: with unit weights RoPE and the
     norm commute; with non-unit weights they do not."""

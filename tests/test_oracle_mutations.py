@@ -57,6 +57,30 @@ def test_rms_norm_mutants_fail(mutant):
         pins.check_rms_norm_library(mutant, np.random.default_rng(0))
 
 
+def _prologue_mutant(kind):
+    """Copies of the prologue with one defect each: the norm before RoPE, the
+    q and k weight vectors swapped, or the weight taken at the rotation
+    partner of each element."""
+    def f(q, k, v, pos, q_w, k_w):
+        q_w, k_w = np.asarray(q_w, np.float64), np.asarray(k_w, np.float64)
+        if kind == "norm_first":
+            return (od.rope_neox(od.rms_norm(q, q_w), pos), od.rope_neox(od.rms_norm(k, k_w), pos),
+                    np.asarray(v, np.float64).copy())
+        if kind == "weights_swapped":
+            q_w, k_w = k_w, q_w
+        if kind == "partner_weight":
+            q_w, k_w = np.roll(q_w, 64), np.roll(k_w, 64)
+        return (od.rms_norm(od.rope_neox(q, pos), q_w), od.rms_norm(od.rope_neox(k, pos), k_w),
+                np.asarray(v, np.float64).copy())
+    return f
+
+
+@pytest.mark.parametrize("kind", ["norm_first", "weights_swapped", "partner_weight"])
+def test_prologue_mutants_fail_order_pin(kind):
+    with pytest.raises(AssertionError):
+        pins.check_prologue_order(_prologue_mutant(kind))
+
+
 def _attn(q, K, V, scale, scale_mut=None, drop_last=False):
     if drop_last and len(K) > 1:
         K, V = K[:-1], V[:-1]
