@@ -483,9 +483,12 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       cur_bids = nxt_bids;
     }
     if (claiming && lane == 0) finish_claims();   // stopped early by a fault
-    // After a fault, copies may still be landing in stages nobody will wait
-    // on: wait for the last one issued into every stage before exiting.
-    if (lane == 0 && *abort_flag) {
+    // Wait for the last copy issued into every stage before this warp exits,
+    // on every path: a queue that stops on a fault (its own, or the abort of
+    // another queue of the CTA, seen after this producer finished issuing)
+    // leaves copies landing in stages nobody else waits on, and the CTA must
+    // not end while a copy still targets its shared memory.
+    if (lane == 0) {
       for (uint32_t s = 0; s < static_cast<uint32_t>(SG) && s < g; ++s) {
         const uint32_t last = s + SG * ((g - 1 - s) / SG);
         mbar_wait(smem_u32(&full[s]), (last / SG) & 1, status);

@@ -446,7 +446,10 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         counters[0] = 0;   // the last CTA resets the counters: the plan can run again
         counters[1] = 0;
       }
-      if (*abort_flag) {   // copies still landing in stages nobody waits on
+      // the last copy issued into every stage has landed before this warp
+      // leaves, on every path: after an abort seen by another warp once this
+      // one had finished issuing, nobody else waits on those stages
+      {
         for (uint32_t s = 0; s < static_cast<uint32_t>(C::kPStages) && s < g; ++s) {
           const uint32_t last = s + C::kPStages * ((g - 1 - s) / C::kPStages);
           mbar_wait(bar(tc::kBarRawFull + s), (last / C::kPStages) & 1, status);
@@ -728,8 +731,9 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       }
       if (!ok) break;
     }
-    // copies still landing after an abort
-    if (lane == 0 && *abort_flag) {
+    // the last Q copy of each lane has landed before this warp leaves (on
+    // every path: the MMA side may have stopped waiting on an abort)
+    if (lane == 0) {
       if (vq0 > 0) mbar_wait(bar(tc::kBarQFull + 0), (vq0 - 1) & 1, status);
       if (vq1 > 0) mbar_wait(bar(tc::kBarQFull + 1), (vq1 - 1) & 1, status);
     }
