@@ -156,9 +156,9 @@ def _cpu_worker(spec_path):
 
 
 def _oracle_item(wl, b, host):
-    import gpu_util as gu
+    from paged_gqa_decode_rope_gb300.workloads import host_pages
     L = int(wl.lengths[b])
-    sub, row = gu.seq_view(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
+    sub, row = host_pages(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
     q, k, v, qw, kw = host
     return {"q": q[b:b + 1], "k": k[b:b + 1], "v": v[b:b + 1], "qw": qw, "kw": kw,
             "cache": sub, "row": row, "L": L}
@@ -168,10 +168,9 @@ def run_oracle_steps(wl, steps, seconds):
     """Time the oracle on host cores over ``steps`` (lists of sequence ids)."""
     import pickle
     import tempfile
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import gpu_util as gu
-    host = (gu.bf16_host(wl.q), gu.bf16_host(wl.k), gu.bf16_host(wl.v),
-            gu.bf16_host(wl.q_norm_w), gu.bf16_host(wl.k_norm_w))
+    from paged_gqa_decode_rope_gb300.workloads import host_f64
+    host = (host_f64(wl.q), host_f64(wl.k), host_f64(wl.v), host_f64(wl.q_norm_w),
+            host_f64(wl.k_norm_w))
     cache = {}
     spec_steps = []
     for ids in steps:

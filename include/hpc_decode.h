@@ -169,7 +169,13 @@ typedef struct {
  * Errors: HPC_ERR_INVALID_ARG if cos_sin is null, max_pos <= 0 or theta <= 0. */
 int hpc_rope_cos_sin_cache(double theta, int32_t max_pos, float* cos_sin, cudaStream_t stream);
 
-/* Fused prologue, one pass per sequence b in [0, batch):
+/* Fused prologue, one pass per sequence b in [0, batch).
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", section "Why does dynamic scheduling matter for attention?" (RoPE
+ * rotation, QK-Norm and the KV write in one kernel pass, in that order), and
+ * page "[vllm] Introducing the HPC-Ops attention backend", "Code analysis"
+ * item 2 (the fused RoPE + QK-Norm + KV-cache-write op that writes into a
+ * caller-provided output).
  *   q'  = RMSNorm(RoPE(q[b], positions[b]), q_norm_w)   for each of 64 heads
  *   k'  = RMSNorm(RoPE(k[b], positions[b]), k_norm_w)   for each of 8 heads
  *   q_out[b] = bf16(q')                  (round to nearest even)
@@ -204,6 +210,11 @@ int hpc_rope_norm_kvwrite(const void* q, const void* k, const void* v,
                           void* q_out, int32_t batch, int32_t* status, cudaStream_t stream);
 
 /* Length-proportional split-KV plan (one CTA, on the device).
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", section "Why does dynamic scheduling matter for attention?": a
+ * static split-KV schedule leaves compute units idle on mixed lengths; the
+ * backend's scheduler deals 64-token KV tiles at every step in proportion to
+ * each sequence's current length.
  * With n_b = ceil(seq_lens[b] / 64) tiles per (b, kv_head) and
  * T = 8 * sum_b n_b, every CTA c < num_ctas owns the flat tile range
  * [c*q, min((c+1)*q, T)) of the (seq, kv_head, tile) order, where
@@ -236,8 +247,14 @@ int hpc_decode_plan(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
 int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_blocks,
                            int32_t splits, hpc_plan* plan, int32_t* status, cudaStream_t stream);
 
-/* Split-KV paged GQA decode attention.  For every work item i =
- * (b, h, t0, t1) and each of the 8 query heads j = 8h .. 8h+7:
+/* Split-KV paged GQA decode attention.
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", intro of "Two new HPC backends in the vLLM ecosystem" (64 query
+ * heads, 8 KV heads, head_dim 128) and "Why does dynamic scheduling matter
+ * for attention?" (split-KV over 64-token tiles, BF16 and FP8 caches); page
+ * "[vllm] Introducing the HPC-Ops attention backend", introduction (FP8 E4M3
+ * models).  For every work item i = (b, h, t0, t1) and each of the 8 query
+ * heads j = 8h .. 8h+7:
  *   s_t   = sm_scale * k_scale * q[b][j] . K[b][h][t]   for tokens t in tiles
  *           [t0, t1) with t < seq_lens[b]
  *   partial_o[i][j - 8h]   = v_scale * sum_t softmax(s)_t V[b][h][t]
@@ -295,7 +312,13 @@ int hpc_decode_attn_profiled(const void* q, const void* kv_cache, int32_t kv_dty
                              float* partial_o, float* partial_lse, float sm_scale,
                              int32_t* status, unsigned long long* cta_clock, cudaStream_t stream);
 
-/* Log-sum-exp merge: for each segment s = b*8 + h with items K_s =
+/* Log-sum-exp merge of the split partials.
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", section "Why does dynamic scheduling matter for attention?": a
+ * split-KV schedule cuts a sequence's KV across compute units, which implies
+ * combining their partial results into the sequence's output; the page does
+ * not spell the combination out.  For each segment s = b*8 + h with items
+ * K_s =
  * seg_ptr[s] .. seg_ptr[s+1]-1, in item order,
  *   M = max_k lse_k,  w_k = exp(lse_k - M),
  *   out[b][8h + r] = bf16( sum_k w_k partial_o[k][r] / sum_k w_k )
@@ -322,7 +345,10 @@ int hpc_merge(const float* partial_o, const float* partial_lse, const hpc_plan* 
  *     456 queues).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call before any
- *     stream capture.
+ *     stream capture.  The kept address belongs to the device's context of
+ *     that moment: after the context is torn down and created again
+ *     (cudaDeviceReset), the next call looks the address up anew, and that
+ *     call, too, should come before any stream capture.
  *   - All calls share the one array, which keeps the last call's contents;
  *     every item of a valid plan is rewritten before it is read, so nothing
  *     needs clearing.  Calls that overlap on the GPU (other streams, other

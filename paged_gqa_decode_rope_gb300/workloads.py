@@ -155,6 +155,27 @@ def make_cache(lengths, block_table, num_blocks, kv_dtype, seed=0, device="cuda"
     return cache, kv_scale
 
 
+def raw_cache_host(cache, kv_dtype):
+    """A cache (or some of its pages) as a host numpy array of raw codes:
+    uint16 BF16 bit patterns or uint8 E4M3 codes."""
+    if kv_dtype == KV_BF16:
+        return cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    return cache.view(torch.uint8).cpu().numpy()
+
+
+def host_pages(cache, block_row, length, kv_dtype):
+    """(sub_cache, row): a host copy of the raw codes of one sequence's pages,
+    renumbered 0 .. n-1, and the block row that reads them in order."""
+    n = pages_of(length)
+    pages = torch.as_tensor(np.asarray(block_row[:n], dtype=np.int64), device=cache.device)
+    return raw_cache_host(cache[pages], kv_dtype), np.arange(n)
+
+
+def host_f64(t):
+    """A BF16 (or any float) tensor as a float64 host array."""
+    return t.float().cpu().numpy().astype(np.float64)
+
+
 class Workload:
     """Everything one decode step of a named workload needs, on ``device``."""
 

@@ -8,6 +8,7 @@ import pytest
 import torch
 
 from oracle import decode as od
+from paged_gqa_decode_rope_gb300 import workloads
 
 TOL_BF16_MAX = 2e-2
 TOL_BF16_MEAN = 2e-3
@@ -21,23 +22,10 @@ def require_gpu():
     build_library()
 
 
-def raw_cache_host(cache, kv_dtype):
-    """Whole cache as a host numpy array of raw codes (uint16 BF16 bits / uint8)."""
-    if kv_dtype == od.KV_BF16:
-        return cache.view(torch.int16).cpu().numpy().view(np.uint16)
-    return cache.view(torch.uint8).cpu().numpy()
-
-
-def seq_view(cache, block_row, length, kv_dtype):
-    """(sub_cache, row): host raw copy of one sequence's pages, renumbered 0..n-1."""
-    n = -(-int(length) // 64)
-    pages = torch.as_tensor(np.asarray(block_row[:n], dtype=np.int64), device=cache.device)
-    sub = cache[pages]
-    return raw_cache_host(sub, kv_dtype), np.arange(n)
-
-
-def bf16_host(t):
-    return t.float().cpu().numpy().astype(np.float64)
+# host copies of device tensors (shared with the benchmark's CPU leg)
+raw_cache_host = workloads.raw_cache_host
+seq_view = workloads.host_pages
+bf16_host = workloads.host_f64
 
 
 def oracle_outputs(wl, q_bf16, seqs, heads=None, cache=None, kv_scale=None):
