@@ -71,9 +71,10 @@ _E4M3_MIN_NORMAL_EXP = 1 - _E4M3_BIAS      # -6
 _E4M3_SUBNORMAL_STEP = 2.0 ** (_E4M3_MIN_NORMAL_EXP - 3)   # 2^-9
 
 
-def e4m3_decode(codes):
-    """float64 values of E4M3 codes (uint8); S.1111.111 decodes to NaN."""
-    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+def _e4m3_value(c):
+    """float64 value of each E4M3 code in the int64 array c, from the fields:
+    sign S, exponent E (bias 7) and mantissa M; E = 0 is subnormal
+    (M/8 * 2^-6), otherwise (1 + M/8) * 2^(E-7); S.1111.111 is NaN."""
     sign = np.where(c & 0x80, -1.0, 1.0)
     e = (c >> 3) & 0xF
     m = c & 0x7
@@ -81,6 +82,16 @@ def e4m3_decode(codes):
     sub = np.ldexp(m / 8.0, _E4M3_MIN_NORMAL_EXP)
     val = sign * np.where(e == 0, sub, normal)
     return np.where((c & 0x7F) == 0x7F, np.nan, val)
+
+
+# the value of every one of the 256 codes, each formed once by _e4m3_value
+_E4M3_VALUES = _e4m3_value(np.arange(256, dtype=np.int64))
+
+
+def e4m3_decode(codes):
+    """float64 values of E4M3 codes (uint8); S.1111.111 decodes to NaN.
+    Each code's value is the field formula of ``_e4m3_value``, looked up."""
+    return _E4M3_VALUES[np.asarray(codes, dtype=np.uint8)]
 
 
 def e4m3_encode(x):
