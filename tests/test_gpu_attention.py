@@ -2,9 +2,11 @@
 
 Every workload runs at its full size in the launch configuration the
 benchmark uses (persistent grid, length-proportional plan); the oracle
-recomputes sampled output rows one by one from host copies of the same cache
-pages.  Unused cache entries are NaN, so any read past a sequence's length or
-any 0 * NaN in the PV product shows up as a non-finite output.
+recomputes every output row (every sequence, every query head) from host
+copies of the same cache pages, and the max-abs and mean-abs errors are taken
+over all batch x 64 x 128 outputs.  Unused cache entries are NaN, so any read
+past a sequence's length or any 0 * NaN in the PV product shows up as a
+non-finite output.
 """
 
 import numpy as np
@@ -45,18 +47,19 @@ def _tol(wl):
 
 @pytest.mark.parametrize("name", ["tiny", "uniform", "mixed", "mixed_fp8", "heavy_tail"])
 def test_attention_matches_oracle(name):
+    """Every output of the workload against the oracle; the bounds hold over
+    the whole [batch, 64, 128] output (BF16: max 2e-2 and mean 2e-3; FP8: max
+    3e-2 against the oracle on the same dequantised cache codes)."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300.workloads import Workload
     wl = Workload(name, seed=0, include_new_token=True)
     out, st = _run(wl)
     assert st == 0, st
     got = gu.bf16_host(out)
-    seqs = list(range(wl.batch)) if name == "tiny" else _sample(wl)
-    for b in seqs:
-        heads = None if wl.lengths[b] <= 65536 else list(range(0, 64, 9))   # one per KV head
-        want = gu.oracle_outputs(wl, wl.q, [b], heads=heads)[0]
-        mx, mean = gu.compare(got[b], want, *_tol(wl), label="%s seq %d (L=%d)" % (name, b, wl.lengths[b]))
     assert np.all(np.isfinite(got)), "NaN/inf in outputs (read past a length?)"
+    want = gu.oracle_outputs(wl, wl.q, range(wl.batch))
+    assert np.all(np.isfinite(want)), "the oracle covers every output"
+    gu.compare(got, want, *_tol(wl), label="%s, all %d sequences" % (name, wl.batch))
 
 
 @pytest.mark.parametrize("kv", [0, 1])
@@ -156,9 +159,8 @@ def test_fp8_against_oracle_quantised_history():
         gpu_raw, _ = gu.seq_view(wl.cache, wl.block_table_np[b], L, od.KV_FP8)
         diff = np.count_nonzero(gpu_raw[:, :, :, :, :][..., :] != sub)
         assert diff <= max(8, sub.size // 10000), "history codes differ at %d places" % diff
-        heads = list(range(0, 64, 9)) if L > 65536 else None
         q = gu.bf16_host(wl.q)[b]
-        want = od.decode_attention(q, sub, np.arange(n), L, od.KV_FP8, scale[0], scale[1], heads=heads)
+        want = od.decode_attention(q, sub, np.arange(n), L, od.KV_FP8, scale[0], scale[1])
         gu.compare(got[b], want, gu.TOL_FP8_MAX, label="seq %d" % b)
 
 

@@ -6,7 +6,8 @@ through the C ABI, twice in a row on different batches (so that anything the
 first call left in the shared array would show up in the second), its output
 must match the allocating path (hpc_decode_attn + hpc_merge with
 caller-owned partials) within the attention tolerance used by the other
-tests.  Collected last on purpose; it also passes alone in a fresh process.
+tests, and the float64 oracle on every output row.  Collected last on
+purpose; it also passes alone in a fresh process.
 """
 
 import ctypes
@@ -61,6 +62,8 @@ def test_noalloc_matches_allocating_path_on_two_calls_in_a_row():
         got, want = gu.bf16_host(out), gu.bf16_host(ref)
         tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if wl.kv_dtype == 0 else (gu.TOL_FP8_MAX, None)
         gu.compare(got, want, *tol, label="noalloc vs allocating, %s" % wl.name)
+        gu.compare(got, gu.oracle_outputs(wl, wl.q, range(wl.batch)), *tol,
+                   label="noalloc vs oracle, %s" % wl.name)
 
 
 def test_noalloc_rejects_a_plan_beyond_its_array():
