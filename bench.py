@@ -10,14 +10,17 @@ needed between steps.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload tiny|uniform|mixed|mixed_fp8|heavy_tail] [--seed S]
                     [--no-static] [--no-cpu] [--cpu-seconds T] [--no-multi-token]
-                    [--no-prefill]
+                    [--no-prefill] [--no-configs]
     python bench.py --prefill-only
+    python bench.py --attn-only dynamic|static:S [--workload W] [--steps K] [--warmup W]
 
 The JSON line also carries the roofline of the dominant kernel (the attention
 with the merge fused in), the end-to-end rate through the public API with
 host buffers, the CPU oracle baseline, the SM clocks seen while timing, the
-dynamic-vs-static schedule comparison, and the multi-token and prefill
-timings (each section can be skipped with its flag).
+dynamic-vs-static schedule comparison, the multi-token and prefill timings,
+and every listed decode configuration (tiny, uniform, mixed, mixed FP8, heavy
+tail) timed as a whole step, as a graph-replayed step and as the attention
+alone (each section can be skipped with its flag).
 
 Prints ONE JSON line on rank 0.  ``value`` is the KV+Q+O bytes of all ranks'
 batches divided by the max-over-ranks device time of K steps (TB/s);
@@ -61,8 +64,14 @@ def _parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-multi-token", action="store_true", help="skip the multi-token decode timings")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill timings")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the timings of every listed decode configuration")
     p.add_argument("--prefill-only", action="store_true",
                    help="run only the prefill timings and print them as one JSON line")
+    p.add_argument("--attn-only", default=None, metavar="SCHEDULE",
+                   help="plan once under SCHEDULE ('dynamic' or 'static:S'), then time only the "
+                        "attention launch (merge fused in) on the workload; one JSON line "
+                        "(the form profiles are captured with)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
@@ -126,89 +135,150 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle -----
 
+def host_cores():
+    """Host CPU cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def _cpu_worker(spec_path):
-    """Run the float64 oracle (prologue + attention of each listed sequence) on
-    the host, one thread.  Each entry of spec["steps"] is a list of sequences;
-    a step stops early once spec["seconds"] (if > 0) of work is done.  Prints
-    per-step bytes, seconds, tokens and sequence counts as JSON."""
+    """Run the float64 oracle (prologue + attention) on this worker's units,
+    one BLAS thread.  A unit is one (sequence, KV head): the prologue of the
+    sequence and the attention of that KV head's 8 query heads.  The cache
+    pages of every sequence sit in one shared-memory block written by the
+    parent.  spec["steps"][s] lists this worker's units of step s; a step
+    stops early once spec["seconds"] (if > 0) of its work is done.  Prints
+    per-step bytes, seconds, tokens and unit counts as JSON."""
     import pickle
+    from multiprocessing import shared_memory
     from oracle import decode as od
     with open(spec_path, "rb") as f:
         spec = pickle.load(f)
-    elem = 2 if spec["kv_dtype"] == 0 else 1
-    res = []
-    for step in spec["steps"]:
-        done_bytes = done_tok = seqs = 0
-        t_total = 0.0
-        for item in step:
-            t0 = time.perf_counter()
-            od.decode_step(item["q"], item["k"], item["v"], [item["L"] - 1], item["qw"], item["kw"],
-                           item["cache"], item["row"][None, :], [item["L"]], [item["L"] - 1],
-                           spec["kv_dtype"], spec["scale"])
-            t_total += time.perf_counter() - t0
-            done_tok += item["L"]
-            done_bytes += item["L"] * 8 * 128 * 2 * elem
-            seqs += 1
-            if 0 < spec["seconds"] <= t_total:
-                break
-        res.append({"bytes": done_bytes, "seconds": t_total, "tokens": done_tok, "seqs": seqs})
-    print(json.dumps(res))
+    shm = shared_memory.SharedMemory(name=spec["shm"])
+    # the parent owns the block: attaching must not make this process's
+    # resource tracker unlink it at exit
+    from multiprocessing import resource_tracker
+    resource_tracker.unregister(shm._name, "shared_memory")
+    try:
+        elem = 2 if spec["kv_dtype"] == 0 else 1
+        dt = np.uint16 if spec["kv_dtype"] == 0 else np.uint8
+        seqs = {}
+        for b, (off, shape) in spec["pages"].items():
+            seqs[b] = np.ndarray(shape, dtype=dt, buffer=shm.buf, offset=off)
+        res = []
+        for units in spec["steps"]:
+            done_bytes = done_tok = n = 0
+            t_total = 0.0
+            for b, h in units:
+                it = spec["seqs"][b]
+                L = it["L"]
+                cache = seqs[b]
+                t0 = time.perf_counter()
+                od.decode_step(it["q"], it["k"], it["v"], [L - 1], spec["qw"], spec["kw"], cache,
+                               np.arange(cache.shape[0])[None, :], [L], [L - 1], spec["kv_dtype"],
+                               spec["scale"], heads=range(8 * h, 8 * h + 8))
+                t_total += time.perf_counter() - t0
+                done_tok += L
+                done_bytes += L * 128 * 2 * elem           # one KV head's K and V
+                n += 1
+                if 0 < spec["seconds"] <= t_total:
+                    break
+            res.append({"bytes": done_bytes, "seconds": t_total, "tokens": done_tok, "units": n})
+        print(json.dumps(res))
+    finally:
+        del seqs
+        shm.close()
 
 
-def _oracle_item(wl, b, host):
-    from paged_gqa_decode_rope_gb300.workloads import host_pages
-    L = int(wl.lengths[b])
-    sub, row = host_pages(wl.cache, wl.block_table_np[b], L, wl.kv_dtype)
-    q, k, v, qw, kw = host
-    return {"q": q[b:b + 1], "k": k[b:b + 1], "v": v[b:b + 1], "qw": qw, "kw": kw,
-            "cache": sub, "row": row, "L": L}
+def run_oracle_steps(wl, steps, seconds, workers=None):
+    """Time the oracle on the host cores over ``steps`` (lists of sequence ids).
 
-
-def run_oracle_steps(wl, steps, seconds):
-    """Time the oracle on host cores over ``steps`` (lists of sequence ids)."""
+    Every sequence of a step is cut into its 8 KV heads; the units are dealt,
+    longest first, to the least-loaded of ``workers`` processes (default: all
+    host cores), each with one BLAS thread, which run concurrently.  A step's
+    time is its slowest worker's time; its bytes, tokens and units are summed.
+    Returns one dict per step and the number of workers used."""
     import pickle
     import tempfile
-    from paged_gqa_decode_rope_gb300.workloads import host_f64
-    host = (host_f64(wl.q), host_f64(wl.k), host_f64(wl.v), host_f64(wl.q_norm_w),
-            host_f64(wl.k_norm_w))
-    cache = {}
-    spec_steps = []
-    for ids in steps:
-        items = []
-        for b in ids:
-            if int(wl.lengths[b]) == 0:
-                continue
-            if b not in cache:
-                cache[b] = _oracle_item(wl, b, host)
-            items.append(cache[b])
-        spec_steps.append(items)
-    spec = {"steps": spec_steps, "kv_dtype": wl.kv_dtype, "seconds": seconds,
-            "scale": wl.kv_scale.cpu().numpy().astype(np.float64)}
-    with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
-        pickle.dump(spec, f)
-        path = f.name
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    from multiprocessing import shared_memory
+    from paged_gqa_decode_rope_gb300.workloads import host_f64, host_pages
+    workers = max(1, workers or host_cores())
+    q, k, v = host_f64(wl.q), host_f64(wl.k), host_f64(wl.v)
+    ids = sorted({b for ids in steps for b in ids if int(wl.lengths[b]) > 0})
+    raw = {b: host_pages(wl.cache, wl.block_table_np[b], int(wl.lengths[b]), wl.kv_dtype)[0]
+           for b in ids}
+    total = sum(r.nbytes for r in raw.values())
+    shm = shared_memory.SharedMemory(create=True, size=max(total, 1))
+    paths, procs = [], []
     try:
-        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", path],
-                             capture_output=True, text=True, env=env, timeout=900)
+        pages, off = {}, 0
+        for b in ids:
+            dst = np.ndarray(raw[b].shape, dtype=raw[b].dtype, buffer=shm.buf, offset=off)
+            dst[...] = raw[b]
+            pages[b] = (off, raw[b].shape)
+            off += raw[b].nbytes
+            del dst
+        del raw
+        per_worker = [[[] for _ in steps] for _ in range(workers)]
+        for s, step_ids in enumerate(steps):
+            load = [0] * workers
+            units = sorted(((b, h) for b in step_ids if b in pages for h in range(8)),
+                           key=lambda u: -int(wl.lengths[u[0]]))
+            for b, h in units:
+                w = load.index(min(load))
+                per_worker[w][s].append((b, h))
+                load[w] += int(wl.lengths[b])
+        common = {"kv_dtype": wl.kv_dtype, "seconds": seconds, "shm": shm.name,
+                  "scale": wl.kv_scale.cpu().numpy().astype(np.float64),
+                  "qw": host_f64(wl.q_norm_w), "kw": host_f64(wl.k_norm_w)}
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        for w in range(workers):
+            mine = sorted({b for st in per_worker[w] for b, _ in st})
+            spec = dict(common, steps=per_worker[w], pages={b: pages[b] for b in mine},
+                        seqs={b: {"L": int(wl.lengths[b]), "q": q[b:b + 1], "k": k[b:b + 1],
+                                  "v": v[b:b + 1]} for b in mine})
+            with tempfile.NamedTemporaryFile(suffix=".pkl", delete=False) as f:
+                pickle.dump(spec, f)
+                paths.append(f.name)
+            procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-worker",
+                                           f.name], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                          text=True, env=env))
+        outs = []
+        for p in procs:
+            o, e = p.communicate(timeout=900)
+            if p.returncode != 0:
+                raise RuntimeError("oracle worker failed: " + e[-2000:])
+            outs.append(json.loads(o.strip().splitlines()[-1]))
     finally:
-        os.unlink(path)
-    if out.returncode != 0:
-        raise RuntimeError("oracle worker failed: " + out.stderr[-2000:])
-    return json.loads(out.stdout.strip().splitlines()[-1])
+        for p in procs:
+            if p.poll() is None:
+                p.kill()
+        for path in paths:
+            os.unlink(path)
+        shm.close()
+        shm.unlink()
+    res = []
+    for s in range(len(steps)):
+        rows = [o[s] for o in outs]
+        res.append({"bytes": sum(r["bytes"] for r in rows), "seconds": max(r["seconds"] for r in rows),
+                    "tokens": sum(r["tokens"] for r in rows) // 8, "units": sum(r["units"] for r in rows)})
+    return res, workers
 
 
 def cpu_baseline(wl, seconds):
     """The oracle on a bounded, seeded random sample of the workload's
-    sequences, about ``seconds`` of single-thread CPU work."""
+    sequences, on all host cores (about ``seconds`` of work per core at most)."""
     order = np.random.default_rng(123).permutation(wl.batch).tolist()
     picked, est = [], 0
     for b in order:                  # enough sequences for the time budget
         picked.append(b)
         est += int(wl.lengths[b])
-        if est > 400000:
+        if est > 400000 * host_cores():
             break
-    return run_oracle_steps(wl, [picked], seconds)[0]
+    res, workers = run_oracle_steps(wl, [picked], seconds)
+    return dict(res[0], workers=workers, seqs=len(picked))
 
 
 # ------------------------------------------------------------ helpers --------
@@ -285,7 +355,8 @@ def run_reference(args):
     # of at most 8192 tokens, round-robin (float64, one thread)
     short = [b for b in range(wl.batch) if 0 < wl.lengths[b] <= 8192] or [int(np.argmin(wl.lengths))]
     steps = [[short[s % len(short)]] for s in range(args.warmup + args.steps)]
-    res = run_oracle_steps(wl, steps, 0.0)[args.warmup:]
+    res, workers = run_oracle_steps(wl, steps, 0.0, workers=min(8, host_cores()))
+    res = res[args.warmup:]
     t = sum(r["seconds"] for r in res)
     value = sum(r["bytes"] for r in res) / t / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": ws,
@@ -294,8 +365,10 @@ def run_reference(args):
             "data": "synthetic",
             "config": {"workload": args.workload + ": " + _describe(wl),
                        "sample": "one sequence of <= 8192 tokens per step"},
-            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": 1, "kind": "oracle",
-                             "sample": "one <=8192-token sequence per step, prologue + attention"},
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": workers, "host_cores": host_cores(),
+                             "kind": "oracle",
+                             "sample": "one <=8192-token sequence per step, prologue + attention, its 8 "
+                                       "KV heads on %d processes (one BLAS thread each)" % workers},
             "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -404,6 +477,7 @@ def run_ours(args):
         sched = schedule_comparison(ops, wl, stream)
     mt = multi_token_times(ops, wl, stream) if rank == 0 and not args.no_multi_token else None
     pre = prefill_times(ops, stream) if rank == 0 and not args.no_prefill else None
+    cfgs = config_times(ops, stream) if rank == 0 and not args.no_configs else None
 
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -424,9 +498,11 @@ def run_ours(args):
     if ws == 1 and not args.no_cpu:
         r = cpu_baseline(wl, args.cpu_seconds)
         cpu_tbps = r["bytes"] / r["seconds"] / 1e12
-        cpu = {"value": cpu_tbps, "unit": "TB/s", "cores": 1, "kind": "oracle",
-               "sample": "%d of %d sequences (%d tokens), float64 prologue + attention, one thread"
-                         % (r["seqs"], wl.batch, r["tokens"]),
+        cpu = {"value": cpu_tbps, "unit": "TB/s", "cores": r["workers"], "host_cores": host_cores(),
+               "kind": "oracle",
+               "sample": "%d of %d sequences (%d tokens), float64 prologue + attention, (sequence, "
+                         "KV head) units on %d processes of one BLAS thread each"
+                         % (r["seqs"], wl.batch, r["tokens"], r["workers"]),
                "seconds": round(r["seconds"], 2),
                "us_per_layer_step_extrapolated": round(wl.kv_bytes() / (r["bytes"] / r["seconds"]) * 1e6, 1)}
     line = {
@@ -449,6 +525,7 @@ def run_ours(args):
         "schedules": sched,
         "multi_token": mt,
         "prefill": pre,
+        "configs": cfgs,
     }
     print(json.dumps(line))
 
@@ -520,6 +597,46 @@ def run_prefill_only():
     print(json.dumps({"prefill": prefill_times(ops, torch.cuda.current_stream())}))
 
 
+def run_attn_only(args):
+    """One workload, one plan, W + K attention launches (merge fused in):
+    the launches a profile of one schedule captures."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import __graft_entry__
+    __graft_entry__.build()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    torch.cuda.set_device(0)
+    sched = args.attn_only
+    if sched.startswith("static:"):
+        schedule = ("static", int(sched.split(":", 1)[1]))
+    elif sched == "dynamic":
+        schedule = "dynamic"
+    else:
+        raise SystemExit("--attn-only takes 'dynamic' or 'static:S'")
+    wl = Workload(args.workload, seed=args.seed, include_new_token=True)
+    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=schedule)
+    step.plan_step(wl.seq_lens)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    b.record(stream)
+    torch.cuda.synchronize()
+    st = int(step.status.item())
+    if st != 0:
+        raise RuntimeError("device status %d" % st)
+    us = a.elapsed_time(b) / args.steps * 1e3
+    nbytes = wl.kv_bytes() + wl.qo_bytes()
+    print(json.dumps({"attn_only": sched, "workload": args.workload + ": " + _describe(wl),
+                      "queues": step.plan.num_ctas, "attn_us": round(us, 2),
+                      "TBps": round(nbytes / us / 1e6, 4), "launches": args.warmup + args.steps}))
+
+
 def _load_peak_tflops():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -573,6 +690,98 @@ def multi_token_times(ops, wl, stream, reps=200):
                                 "frac": round(nbytes / us / 1e3 / peak_gbs, 4),
                                 "TFLOP/s": round(flops / us / 1e6, 2)}
     return out
+
+
+CONFIGS = ("tiny", "uniform", "mixed", "mixed_fp8", "heavy_tail")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def config_times(ops, stream, seed=0, reps=100):
+    """Every listed decode configuration at its full size, in the launch
+    configuration of the headline: the whole step (prologue + plan in one
+    launch, attention with the merge fused in as its programmatic dependent),
+    eagerly and replayed from a CUDA graph, and the attention launch alone;
+    CUDA events over ``reps`` back-to-back calls each.  A batch whose bytes
+    fit twice in L2 (the tiny one) is timed call by call with a write of
+    twice the L2 size between calls, outside the events.  Bytes are the
+    KV + Q + O bytes of the batch; ``frac`` is the attention's rate over the
+    measured copy bandwidth."""
+    import torch
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    peak_gbs, peak_kind = _load_peaks()
+    res = {}
+    for name in CONFIGS:
+        wl = Workload(name, seed=seed)
+        cos_sin = ops.rope_cos_sin_cache(wl.max_pos + 1)
+        step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks)
+        nbytes = wl.kv_bytes() + wl.qo_bytes()
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") \
+            if nbytes < 2 * L2_BYTES else None
+
+        def one_step():
+            step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
+                 wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
+
+        def attend():
+            step.attend(step.q_out, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+
+        def timed(fn):
+            """Mean µs per call of fn over ``reps`` calls."""
+            if flush is None:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(reps):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                return a.elapsed_time(b) / reps * 1e3
+            total = 0.0
+            for _ in range(reps):
+                flush.fill_(1.0)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                total += a.elapsed_time(b)
+            return total / reps * 1e3
+
+        for _ in range(3):
+            one_step()
+        torch.cuda.synchronize()
+        step_us = timed(one_step)
+        attn_us = timed(attend)
+        # the same step captured once in a CUDA graph and replayed
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cs):
+            one_step()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cs):
+                one_step()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        graph_us = timed(g.replay)
+        st = int(step.status.item())
+        if st != 0:
+            raise RuntimeError("device status %d in config %s" % (st, name))
+        res[name] = {
+            "workload": _describe(wl), "tokens": wl.tokens, "bytes": nbytes,
+            "step_us": round(step_us, 2), "step_graph_us": round(graph_us, 2),
+            "attn_us": round(attn_us, 2),
+            "step_TBps": round(nbytes / step_us / 1e6, 4),
+            "attn_TBps": round(nbytes / attn_us / 1e6, 4),
+            "frac": round(nbytes / attn_us / 1e3 / peak_gbs, 4),
+            "step_frac": round(nbytes / step_us / 1e3 / peak_gbs, 4),
+            "frac_of_8TBps": round(nbytes / attn_us / 8e6, 4),
+            "l2": "flushed between calls" if flush is not None else "inputs larger than L2",
+        }
+        del g, step, wl, cos_sin, flush
+        torch.cuda.empty_cache()
+    return {"unit": "us", "peak_GBps": peak_gbs, "peak_kind": peak_kind, "reps": reps, "seed": seed,
+            "step": "prologue + plan (one launch) -> attention + merge (PDL launch)", "by_config": res}
 
 
 def schedule_comparison(ops, wl, stream):
@@ -640,6 +849,9 @@ def main():
         return
     if args.prefill_only:
         run_prefill_only()
+        return
+    if args.attn_only:
+        run_attn_only(args)
         return
     run_ours(args)
 
