@@ -72,6 +72,10 @@ def _parse():
                    help="plan once under SCHEDULE ('dynamic' or 'static:S'), then time only the "
                         "attention launch (merge fused in) on the workload; one JSON line "
                         "(the form profiles are captured with)")
+    p.add_argument("--q-len", type=int, default=1,
+                   help="--attn-only: new tokens per sequence (multi-token decode, 1 .. 4)")
+    p.add_argument("--q-dtype", default="bf16", choices=["bf16", "e4m3"],
+                   help="--attn-only: the stored q (e4m3 needs an FP8 cache)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--cpu-worker", default=None, help=argparse.SUPPRESS)
     return p.parse_args()
@@ -615,24 +619,38 @@ def run_attn_only(args):
     else:
         raise SystemExit("--attn-only takes 'dynamic' or 'static:S'")
     wl = Workload(args.workload, seed=args.seed, include_new_token=True)
-    step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=schedule)
+    qn = args.q_len
+    if qn == 1 and args.q_dtype == "bf16":
+        step = ops.DecodeStep(wl.batch, wl.kv_dtype, wl.max_blocks, schedule=schedule)
+        q = wl.q
+    else:
+        if schedule != "dynamic":
+            raise SystemExit("multi-token and E4M3-q runs take the dynamic plan")
+        # random q of the multi-token layout (E4M3: codes of q / (max|q| / 448))
+        g = torch.Generator(device="cuda").manual_seed(qn)
+        q = torch.randn((wl.batch, qn, 64, 128), generator=g, device="cuda")
+        qs = float(q.abs().max()) / 448.0
+        qd = ops.Q_FP8 if args.q_dtype == "e4m3" else ops.Q_BF16
+        q = (q / qs).to(torch.float8_e4m3fn).view(torch.uint8) if qd == ops.Q_FP8 else q.to(torch.bfloat16)
+        step = ops.DecodeStepEx(wl.batch, wl.kv_dtype, wl.max_blocks, q_len=qn, q_dtype=qd, q_scale=qs)
     step.plan_step(wl.seq_lens)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(args.steps):
-        step.attend(wl.q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+        step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
     b.record(stream)
     torch.cuda.synchronize()
     st = int(step.status.item())
     if st != 0:
         raise RuntimeError("device status %d" % st)
     us = a.elapsed_time(b) / args.steps * 1e3
-    nbytes = wl.kv_bytes() + wl.qo_bytes()
-    print(json.dumps({"attn_only": sched, "workload": args.workload + ": " + _describe(wl),
+    nbytes = wl.kv_bytes() + qn * wl.qo_bytes()
+    print(json.dumps({"attn_only": sched, "q_len": qn, "q_dtype": args.q_dtype,
+                      "workload": args.workload + ": " + _describe(wl),
                       "queues": step.plan.num_ctas, "attn_us": round(us, 2),
                       "TBps": round(nbytes / us / 1e6, 4), "launches": args.warmup + args.steps}))
 

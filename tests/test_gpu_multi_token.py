@@ -59,21 +59,22 @@ def test_multi_token_attention_matches_oracle(q_len, kv, fused):
                 assert np.all(got[b, t] == 0.0)
 
 
+@pytest.mark.parametrize("kv", [0, 1])
 @pytest.mark.parametrize("q_len", [2, 4])
-def test_multi_token_pooled_plan_and_reproducible(q_len):
+def test_multi_token_pooled_plan_and_reproducible(q_len, kv):
     """A plan with many pooled chunks (many items per segment, merged by the
     last queue to finish) gives the unpooled result within the split
     tolerance, and two runs of one plan are bit-identical."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
-    wl = Workload("custom", seed=61, lengths=[20000, 300, 7, 4096, 1], kv_dtype=0,
+    wl = Workload("custom", seed=61, lengths=[20000, 300, 7, 4096, 1], kv_dtype=kv,
                   include_new_token=True)
     q = _q(wl.batch, q_len, 99)
-    ref = ops.DecodeStepMT(wl.batch, q_len, 0, wl.max_blocks, pool_chunks=0)
+    ref = ops.DecodeStepMT(wl.batch, q_len, kv, wl.max_blocks, pool_chunks=0)
     ref.plan_step(wl.seq_lens)
     a = ref.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens).clone()
-    pooled = ops.DecodeStepMT(wl.batch, q_len, 0, wl.max_blocks, pool_chunks=3, pool_min_tiles=1)
+    pooled = ops.DecodeStepMT(wl.batch, q_len, kv, wl.max_blocks, pool_chunks=3, pool_min_tiles=1)
     pooled.plan_step(wl.seq_lens)
     b1 = pooled.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens).clone()
     b2 = pooled.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens).clone()
@@ -84,27 +85,31 @@ def test_multi_token_pooled_plan_and_reproducible(q_len):
     d = (a.float() - b1.float()).abs()
     assert float(d.max()) <= 4e-3 and float(d.mean()) <= 2e-4
     got = gu.bf16_host(b1)
-    gu.compare(got[0], _oracle(wl, q, 0, heads=list(range(0, 64, 7))), *_tol(0), label="seq 0")
+    gu.compare(got[0], _oracle(wl, q, 0, heads=list(range(0, 64, 7))), *_tol(kv), label="seq 0")
+    gu.compare(got[1:], np.stack([_oracle(wl, q, b) for b in range(1, wl.batch)]), *_tol(kv),
+               label="seqs 1..")
 
 
-def test_multi_token_mixed_full_size():
-    """q_len = 2 on the full mixed batch (1 x 128K + 31 x 4K tokens, BF16), in
-    the launch configuration of the single-token bench; sampled rows."""
+@pytest.mark.parametrize("name,q_len", [("mixed", 2), ("mixed_fp8", 4)])
+def test_multi_token_mixed_full_size(name, q_len):
+    """Multi-token decode on the full mixed batch (1 x 128K + 31 x 4K tokens),
+    BF16 at q_len 2 and FP8 at q_len 4, in the launch configuration of the
+    benchmark; every output row against the oracle, the bounds over all of
+    them."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
-    wl = Workload("mixed", seed=3, include_new_token=True)
-    q = _q(wl.batch, 2, 5)
-    step = ops.DecodeStepMT(wl.batch, 2, wl.kv_dtype, wl.max_blocks)
+    wl = Workload(name, seed=3, include_new_token=True)
+    q = _q(wl.batch, q_len, 5)
+    step = ops.DecodeStepMT(wl.batch, q_len, wl.kv_dtype, wl.max_blocks)
     step.plan_step(wl.seq_lens)
     out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0
     got = gu.bf16_host(out)
     assert np.all(np.isfinite(got))
-    for b in (0, 1, 17, 31):
-        heads = list(range(0, 64, 9)) if wl.lengths[b] > 65536 else None
-        gu.compare(got[b], _oracle(wl, q, b, heads=heads), *_tol(0), label="mixed seq %d" % b)
+    want = np.stack([_oracle(wl, q, b) for b in range(wl.batch)])
+    gu.compare(got, want, *_tol(wl.kv_dtype), label="%s q_len %d" % (name, q_len))
 
 
 @pytest.mark.parametrize("kv", [0, 1])
