@@ -75,6 +75,9 @@ struct AttnTraits {
   // half the bytes, so FP8 keeps three queues in flight.
   static constexpr int kGroups = kFp8 ? 3 : 2;
   static constexpr int kGroupStages = 3;                      // stage ring of one queue
+  // tiles per queue pulled into L2 while a programmatic dependent launch
+  // waits for the plan (about 29 MB in all on a 152-SM part)
+  static constexpr int kL2PrefetchTiles = kFp8 ? 4 : 3;
   static constexpr int kStages = kGroups * kGroupStages;
   static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
   static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
@@ -127,6 +130,83 @@ __device__ __forceinline__ void record_cta_clock(unsigned long long* cta_clock,
   cta_clock[3 * blockIdx.x + 0] = t_start;
   cta_clock[3 * blockIdx.x + 1] = globaltimer_ns();
   cta_clock[3 * blockIdx.x + 2] = smid;
+}
+
+// Tiles of a sequence length (0 for a length out of range).
+__device__ __forceinline__ int tiles_of_len(int L, int max_blocks) {
+  return (L > 0 && L <= max_blocks * kPage) ? (L + kPage - 1) / kPage : 0;
+}
+
+// The first `ntiles` tiles of work queue vq under the length-proportional
+// plan, pulled into L2 by one warp.  The plan gives queue vq the flat tiles
+// (in (sequence, kv_head, tile) order) from vq * q, with q = ceil(T /
+// queues), or at least the common tile count when every sequence has the
+// same one and there are no more segments than queues; this is worked out
+// here from the lengths and the block table alone.  Only tiles of the
+// sequence holding the queue's first tile are taken.  A prefetch only warms
+// L2: a guess that misses the plan (another min_tiles, say) costs
+// bandwidth, never correctness, and L2 stays coherent with later writes.
+template <bool kFp8>
+__device__ void l2_prefetch_queue_start(const CUtensorMap* map, const int32_t* seq_lens, int batch,
+                                        const int32_t* block_table, int max_blocks, int num_blocks,
+                                        int vq, int num_queues, int ntiles) {
+  const int lane = threadIdx.x & 31;
+  const int n0 = batch > 0 ? tiles_of_len(seq_lens[0], max_blocks) : 0;
+  int tot = 0;
+  bool same = true;
+  for (int b = lane; b < batch; b += 32) {
+    const int n = tiles_of_len(seq_lens[b], max_blocks);
+    tot += n;
+    same = same && n == n0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  same = __all_sync(0xffffffffu, same);
+  const int64_t T = int64_t{kHkv} * tot;
+  if (T == 0 || num_queues < 1) return;
+  int64_t q = (T + num_queues - 1) / num_queues;
+  if (same && static_cast<int64_t>(batch) * kHkv <= num_queues && n0 > q) q = n0;
+  const int64_t f0 = static_cast<int64_t>(vq) * q;
+  if (f0 >= T) return;
+  const int64_t fend = min(T, f0 + q);
+  // the sequence whose segments hold flat tile f0, 32 sequences at a time
+  int64_t base = 0;   // tiles of the sequences before the chunk
+  int bsel = -1, nsel = 0;
+  int64_t start = 0;  // flat tile of sequence bsel's first segment
+  for (int cb = 0; cb < batch && bsel < 0; cb += 32) {
+    const int b = cb + lane;
+    const int n = b < batch ? tiles_of_len(seq_lens[b], max_blocks) : 0;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, b < batch && kHkv * (base + incl) > f0);
+    if (m != 0u) {
+      const int src = __ffs(m) - 1;
+      bsel = cb + src;
+      nsel = __shfl_sync(0xffffffffu, n, src);
+      start = kHkv * (base + __shfl_sync(0xffffffffu, incl, src) - nsel);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (bsel < 0 || nsel <= 0) return;
+  const int64_t r = f0 - start + lane;   // lane's tile within the sequence's segments
+  if (lane < ntiles && f0 + lane < fend && r < int64_t{kHkv} * nsel) {
+    const int h = static_cast<int>(r / nsel), t = static_cast<int>(r % nsel);
+    const int bid = block_table[static_cast<int64_t>(bsel) * max_blocks + t];
+    if (bid >= 0 && bid < num_blocks) {
+      const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
+      const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
+      tma_prefetch_l2_2d(map, 0, yk);
+      tma_prefetch_l2_2d(map, 0, yv);
+      if constexpr (!kFp8) {
+        tma_prefetch_l2_2d(map, 64, yk);
+        tma_prefetch_l2_2d(map, 64, yv);
+      }
+    }
+  }
 }
 
 // O^T += V^T P^T for one warp's 16 tokens (rows: d, cols: 8 heads).  With
@@ -200,7 +280,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     int32_t capacity, int32_t num_queues, float* __restrict__ partial_o,
     float* __restrict__ partial_lse,
     float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
-    const int32_t* seg_ptr, int32_t* seg_done, void* __restrict__ out, int32_t out_dtype) {
+    const int32_t* seg_ptr, int32_t* seg_done, void* __restrict__ out, int32_t out_dtype,
+    int32_t l2_prefetch_tiles) {
   using T = AttnTraits<kFp8>;
   static_assert(kQ == 1 || kQ == 2 || kQ == 4, "query layouts of 1, 2 or 4 tokens");
   static_assert(kFp8 || !kQ8, "an E4M3 q needs an E4M3 cache");
@@ -252,6 +333,13 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     mbar_fence_init();
   }
   if (warp == T::kConsumerWarps && lane == 0) tma_prefetch_desc(&kv_map);
+  // As a programmatic dependent of the step's prologue + planner launch the
+  // CTAs are resident while the plan is made: each producer warp uses that
+  // wait to pull its queue's first tiles into L2.
+  if (l2_prefetch_tiles > 0 && is_producer)
+    l2_prefetch_queue_start<kFp8>(&kv_map, seq_lens, batch, block_table, max_blocks, num_blocks,
+                                  static_cast<int>(blockIdx.x) * G + grp, num_queues,
+                                  l2_prefetch_tiles);
   // everything above is independent of the previous kernel on the stream;
   // from here on the plan, q and the cache are read
   pdl_wait();
@@ -1026,7 +1114,8 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
       static_cast<const hpc_work_item*>(plan->items),
       static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
       plan->pool, plan->capacity, plan->num_ctas, partial_o, partial_lse, sm_scale, status, cta_clock,
-      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out, opts.out_dtype);
+      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out, opts.out_dtype,
+      pdl ? T::kL2PrefetchTiles : 0);
   return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
 

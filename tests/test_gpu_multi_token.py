@@ -68,7 +68,8 @@ def test_multi_token_pooled_plan_and_reproducible(q_len, kv):
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
-    wl = Workload("custom", seed=61, lengths=[20000, 300, 7, 4096, 1], kv_dtype=kv,
+    # long enough for pooled chunks on either grid (304 BF16 or 456 FP8 queues)
+    wl = Workload("custom", seed=61, lengths=[60000, 300, 7, 4096, 1], kv_dtype=kv,
                   include_new_token=True)
     q = _q(wl.batch, q_len, 99)
     ref = ops.DecodeStepMT(wl.batch, q_len, kv, wl.max_blocks, pool_chunks=0)
