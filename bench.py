@@ -403,16 +403,17 @@ def run_ours(args):
         step(wl.q, wl.k, wl.v, wl.positions, cos_sin, wl.q_norm_w, wl.k_norm_w, wl.cache,
              wl.slot_mapping, wl.kv_scale, wl.block_table, wl.seq_lens)
 
+    # the clock sampler starts before the warm-up, so that the timed steps
+    # follow warm steps directly (no idle gap in which the clocks could drop)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     for _ in range(max(3, args.warmup)):
         one_step()
     torch.cuda.synchronize()
     if int(step.status.item()) != 0:
         raise RuntimeError("device status %d during warm-up" % int(step.status.item()))
-
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
