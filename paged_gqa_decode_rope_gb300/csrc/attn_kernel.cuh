@@ -779,17 +779,12 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
             for (int k4 = 0; k4 < 4; ++k4) x[mb][k4] = (sa[k4] + sb[k4]) * scale_log2;
           }
           // keys past the query's last visible one: p = 0, V entries zeroed
-          uint32_t mask01[kMB], mask23[kMB];
 #pragma unroll
           for (int mb = 0; mb < kMB; ++mb) {
             const int nv = nvalid - 16 * mb;
-            mask01[mb] = 0xffffffffu;
-            mask23[mb] = 0xffffffffu;
             if (nv < 16) {
               if (r >= nv) x[mb][0] = x[mb][1] = -INFINITY;
               if (r + 8 >= nv) x[mb][2] = x[mb][3] = -INFINITY;
-              mask01[mb] = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
-              mask23[mb] = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
             }
           }
           float mt0 = -INFINITY, mt1 = -INFINITY;
@@ -832,23 +827,31 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
               o[mi][3] *= al1;
             }
           }
+          // P^T fragments -> B operands (k = token, n = head) by 8x8
+          // transposes, all blocks first (the scores are then dead)
+          uint32_t pb[kMB][2];
 #pragma unroll
           for (int mb = 0; mb < kMB; ++mb) {
-            // P^T fragment -> B operand (k = token, n = head) by an 8x8 transpose
-            uint32_t pb0, pb1;
             if constexpr (kFp8) {
-              pb0 = movmatrix_t(pack_f16(x[mb][0], x[mb][1]));
-              pb1 = movmatrix_t(pack_f16(x[mb][2], x[mb][3]));
+              pb[mb][0] = movmatrix_t(pack_f16(x[mb][0], x[mb][1]));
+              pb[mb][1] = movmatrix_t(pack_f16(x[mb][2], x[mb][3]));
             } else {
-              pb0 = movmatrix_t(pack_bf16(x[mb][0], x[mb][1]));
-              pb1 = movmatrix_t(pack_bf16(x[mb][2], x[mb][3]));
+              pb[mb][0] = movmatrix_t(pack_bf16(x[mb][0], x[mb][1]));
+              pb[mb][1] = movmatrix_t(pack_bf16(x[mb][2], x[mb][3]));
             }
-            if (nvalid - 16 * mb < 16)
-              pv_tile<kFp8, true>(vb, row + 16 * mb, vtok_bf16 + 16 * mb, vsel_bf16, hi, sw, pb0, pb1,
-                                  mask01[mb], mask23[mb], o);
-            else
-              pv_tile<kFp8, false>(vb, row + 16 * mb, vtok_bf16 + 16 * mb, vsel_bf16, hi, sw, pb0,
-                                   pb1, mask01[mb], mask23[mb], o);
+          }
+#pragma unroll
+          for (int mb = 0; mb < kMB; ++mb) {
+            const int nv = nvalid - 16 * mb;   // V rows of tokens past it are zeroed
+            if (nv < 16) {
+              const uint32_t m01 = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+              const uint32_t m23 = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+              pv_tile<kFp8, true>(vb, row + 16 * mb, vtok_bf16 + 16 * mb, vsel_bf16, hi, sw, pb[mb][0],
+                                  pb[mb][1], m01, m23, o);
+            } else {
+              pv_tile<kFp8, false>(vb, row + 16 * mb, vtok_bf16 + 16 * mb, vsel_bf16, hi, sw,
+                                   pb[mb][0], pb[mb][1], 0xffffffffu, 0xffffffffu, o);
+            }
           }
         }
         __syncwarp();
