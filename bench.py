@@ -480,7 +480,15 @@ def run_ours(args):
     sched = None
     if rank == 0 and not args.no_static:
         sched = schedule_comparison(ops, wl, stream)
-    mt = multi_token_times(ops, wl, stream) if rank == 0 and not args.no_multi_token else None
+    mt = None
+    if rank == 0 and not args.no_multi_token:
+        mt = multi_token_times(ops, wl, stream)
+        if wl.kv_dtype == 0 and args.workload == "mixed":
+            # the same mix over an E4M3 cache, so that both cache types are in the line
+            wl8 = Workload("mixed_fp8", seed=rank_seed(args.seed, rank))
+            mt = {"mixed BF16": mt, "mixed FP8": multi_token_times(ops, wl8, stream)}
+            del wl8
+            torch.cuda.empty_cache()
     pre = prefill_times(ops, stream) if rank == 0 and not args.no_prefill else None
     cfgs = config_times(ops, stream) if rank == 0 and not args.no_configs else None
 
