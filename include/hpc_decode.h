@@ -129,9 +129,11 @@ typedef struct {
  *                              left at zero by every run)
  * num_ctas is the number of work queues ("CTA ranges") the plan deals to.
  * hpc_decode_attn runs each queue on one group of 4 consumer warps fed by its
- * own producer warp; a CTA hosts 2 queues (BF16) or 3 (FP8), so the grid is
- * ceil(num_ctas / 2) or ceil(num_ctas / 3) CTAs.  For the length-proportional
- * plan use hpc_decode_num_ctas() (SMs x queues per CTA).  A
+ * own producer warp; a CTA hosts 2 queues (BF16) or 3 (FP8; 2 when q_len is 3
+ * or 4), so the grid is ceil(num_ctas / queues per CTA) CTAs.  For the
+ * length-proportional plan use hpc_decode_num_ctas() (q_len 1) or
+ * hpc_decode_num_queues() (SMs x queues per CTA).  Any num_ctas >= 1 runs
+ * correctly; another count than these leaves SMs idle or runs in waves.  A
  * length-proportional plan with J pool chunks needs
  * capacity >= num_ctas * (1 + J) + 8 * batch (hpc_plan_capacity).
  * items must be 16-byte aligned. */
@@ -387,6 +389,17 @@ int hpc_decode_step(const void* q, const void* k, const void* v, const int32_t* 
  * for the given KV dtype: SM count x queues per CTA (2 for BF16, 3 for FP8),
  * one CTA per SM.  The num_ctas to plan for. */
 int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
+
+/* The num_ctas to plan for when each sequence has q_len new tokens
+ * (1 <= q_len <= HPC_MAX_Q_LEN): hpc_decode_num_ctas() except for E4M3 pages
+ * with q_len 3 or 4, whose tensor-core form runs 2 queues per CTA (SMs x 2).
+ * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
+ * Hopper", "Why does dynamic scheduling matter for attention?" (work dealt to
+ * compute units in proportion to length).  Writes *num_queues; returns
+ * HPC_ERR_INVALID_ARG for a null pointer or q_len out of range,
+ * HPC_ERR_UNSUPPORTED for another kv_dtype, HPC_ERR_CUDA if the device cannot
+ * be queried. */
+int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t* num_queues);
 
 /* Items a length-proportional plan may need:
  * num_ctas * (1 + pool_chunks) + 8 * batch. */

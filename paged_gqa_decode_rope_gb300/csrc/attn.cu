@@ -82,6 +82,18 @@ extern "C" int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas) {
   return HPC_OK;
 }
 
+extern "C" int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t* num_queues) {
+  HPC_CHECK_ARG(num_queues != nullptr && q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
+  // q_len 3 and 4 run the tensor-core form: two queues per CTA on both cache types
+  if (kv_dtype != HPC_KV_FP8_E4M3 || q_len < 3) return hpc_decode_num_ctas(kv_dtype, num_queues);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return HPC_ERR_CUDA;
+  *num_queues = sms * hpc::AttnTraits<true, true>::kGroups;
+  return HPC_OK;
+}
+
 extern "C" int hpc_decode_attn_ex(const void* q, const void* kv_cache, int32_t kv_dtype,
                                   const float* kv_scale, int32_t num_blocks,
                                   const int32_t* block_table, int32_t max_blocks,

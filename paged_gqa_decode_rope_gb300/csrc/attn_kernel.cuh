@@ -50,6 +50,14 @@
 //    order, so the result does not depend on which queue merges.
 //  * Tokens past a query's last visible key get p = 0 and their V entries
 //    are zeroed in registers (the cache may hold NaN there: 0 * NaN is NaN).
+//  * The 4-token layout (q_len 3, 4) runs the tensor-core form (kTC): its
+//    q_len x 8 query rows are one M = 128 tcgen05 operand, so per 64-token
+//    tile a single Q K^T (N 64) into tensor memory, a softmax warp with one
+//    row per thread, and one P V (N 128, P read from tensor memory) serve
+//    all new tokens; an MMA warp per queue issues the products of two tiles
+//    in flight, whichever is ready first.  E4M3 pages are widened to F16 in
+//    their stage by two converter warps (K first, so that Q K^T can start).
+//    Its partials are merged by the merge pass after the kernel.
 //  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
 //    HPC_STATUS_WAIT_TIMEOUT and winds down, waiting for its own copies.
 #include <mutex>
@@ -62,18 +70,26 @@
 namespace hpc {
 namespace {
 
-template <bool kFp8>
+// kTC: the tensor-core form of the 4-token layout: per queue one MMA warp
+// issuing tcgen05 products into tensor memory, one softmax warp and (E4M3
+// pages) two converter warps; the Q tiles sit ahead of the stage rings.
+template <bool kFp8, bool kTC = false>
 struct AttnTraits {
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
-  static constexpr int kStageBytes = 2 * kPageBytes;          // K page + V page
+  static constexpr int kTmaStageBytes = 2 * kPageBytes;       // K page + V page as loaded
+  // a stage of the tensor-core form holds the tile as the products read it:
+  // F16 / BF16 K and V pages (an E4M3 tile is loaded into its first half and
+  // widened in place)
+  static constexpr int kF16Page = kPage * kD * 2;
+  static constexpr int kStageBytes = kTC ? 2 * kF16Page : kTmaStageBytes;
   // A CTA hosts kGroups independent work queues.  A queue has its own producer
   // warp, stage ring, item ring and 4 consumer warps, and runs whole work
   // items, so one queue's epilogue and merge overlap the other queues'
   // streaming.  FP8 tiles carry a longer per-tile chain (the conversions) at
   // half the bytes, so FP8 keeps three queues in flight.
-  static constexpr int kGroups = kFp8 ? 3 : 2;
+  static constexpr int kGroups = (kFp8 && !kTC) ? 3 : 2;
   static constexpr int kGroupStages = 3;                      // stage ring of one queue
   // tiles per queue pulled into L2 while a programmatic dependent launch
   // waits for the plan (about 29 MB in all on a 152-SM part)
@@ -84,19 +100,29 @@ struct AttnTraits {
   static constexpr int kGroupThreads = 32 * kWarpsPerGroup;
   static constexpr int kThreads = 32 * (kConsumerWarps + kGroups);   // + a producer warp per queue
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
-  static constexpr int kOffO = kStages * kStageBytes;                 // [warps][8][kOStride]
-  static constexpr int kOffM = kOffO + kConsumerWarps * kGroup * kOStride * 4;
-  static constexpr int kOffL = kOffM + kConsumerWarps * kGroup * 4;
-  static constexpr int kOffBar = kOffL + kConsumerWarps * kGroup * 4;
+  // tensor-core form: per queue a 16 KB Q tile (two 64-column halves of 64
+  // rows; the M = 128 operand's rows past 64 read whatever follows, which the
+  // products ignore), ahead of the rings so that those rows stay in bounds
+  static constexpr int kQtBytes = 16384;
+  static constexpr int kOffQt = 0;
+  static constexpr int kOffStages = kTC ? kGroups * kQtBytes : 0;
+  static constexpr int kSliceWarps = kTC ? 0 : kConsumerWarps;   // merge slices (the mma.sync form)
+  static constexpr int kOffO = kOffStages + kStages * kStageBytes;    // [warps][8][kOStride]
+  static constexpr int kOffM = kOffO + kSliceWarps * kGroup * kOStride * 4;
+  static constexpr int kOffL = kOffM + kSliceWarps * kGroup * 4;
+  static constexpr int kOffBar = kOffL + kSliceWarps * kGroup * 4;
   static constexpr int kItemRing = 2;                         // items queued ahead, per queue
-  // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier
-  static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1;
+  // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier,
+  // and for the tensor-core form s_full[2], p_full[2], q_full, q_free, o_final, o_free, drain,
+  // and over E4M3 pages conv_k[SG] and conv_v[SG] (the stage's K, V widened to F16)
+  static constexpr int kTcBars = kTC ? 9 + (kFp8 ? 2 * kGroupStages : 0) : 0;
+  static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1 + kTcBars;
   static constexpr int kOffOk = kOffBar + kGroups * kGroupBars * 8;
   static constexpr int kOffRing = kOffOk + kStages * 4;
   static constexpr int kRingInts = 8;                         // idx, seq, h, t0, t1, len
-  // flags: the CTA's abort flag, then one merge flag per queue
+  // flags: the CTA's abort flag, one merge flag per queue, the TMEM address
   static constexpr int kOffFlags = kOffRing + kGroups * kItemRing * kRingInts * 4;
-  static constexpr int kSmemUsed = kOffFlags + 4 * (1 + kGroups);
+  static constexpr int kSmemUsed = kOffFlags + 4 * (2 + kGroups);
   static constexpr int kSmemBytes = kSmemUsed + 1024;         // slack for 1024-byte alignment
   static_assert(kOffBar % 8 == 0, "mbarriers need 8-byte alignment");
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-CTA shared memory");
@@ -250,6 +276,60 @@ __device__ __forceinline__ void pv_tile(uint32_t vb, int row, int vtok_bf16, int
   }
 }
 
+// S = Q K^T of one queue for one tile (tensor-core form): eight K-major steps
+// of 16 d, the second 64-column halves of both operands 8 KB on; a commit on
+// s_full, and on q_free too after the item's last tile (its Q tile may then
+// be replaced).  Run by the whole converged MMA warp; one elected thread
+// issues the chain.
+__device__ __forceinline__ void umma_qk_tile(uint32_t d, uint64_t q, uint64_t k, uint32_t idesc,
+                                             uint32_t s_full, bool last, uint32_t q_free) {
+#define HPC_DQK_STEP(O) \
+  "add.s64 a, %1, " O ";\n\tadd.s64 b, %2, " O ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+  asm volatile(
+      "{\n\t.reg .pred e, f, pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 f, %5, 0, e;\n\t"
+      "setp.ne.b32 pf, %5, %5;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      HPC_DQK_STEP("2") HPC_DQK_STEP("4") HPC_DQK_STEP("6")
+      HPC_DQK_STEP("512") HPC_DQK_STEP("514") HPC_DQK_STEP("516") HPC_DQK_STEP("518")
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+      ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free)
+      : "memory");
+#undef HPC_DQK_STEP
+}
+
+// One 128-code row of an E4M3 page (128-byte swizzled, as TMA lands it),
+// read into registers (zeros when !live), and written back as 128 F16 values
+// in two 128-byte swizzled rows, d 0..63 and 64..127 (the layout of a 16-bit
+// stage).
+__device__ __forceinline__ void load_e4m3_row(const uint8_t* raw, int r, bool live, uint4 (&w)[8]) {
+  const int sw = r & 7;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    w[c] = live ? *reinterpret_cast<const uint4*>(raw + ((c ^ sw) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+}
+__device__ __forceinline__ void store_f16_row(const uint4 (&w)[8], uint8_t* lo_row, uint8_t* hi_row, int r) {
+  const int sw = r & 7;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint8_t* dst = c < 4 ? lo_row : hi_row;
+    const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;   // 16-byte F16 chunks of codes 16c ..
+    *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) =
+        make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].x)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].x >> 16)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].y)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].y >> 16)));
+    *reinterpret_cast<uint4*>(dst + ((c1 ^ sw) << 4)) =
+        make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].z)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].z >> 16)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].w)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(w[c].w >> 16)));
+  }
+}
+
 // Four consecutive output elements (index a multiple of 4) in the caller's
 // output type.
 __device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, float b, float c,
@@ -267,8 +347,8 @@ __device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, floa
 // kQ: query layout, 1 (decode), 2 or 4 new tokens per sequence (q_len = 3
 // runs the 4-token layout with the fourth query's warp idle).  kQ8: q is E4M3
 // codes (FP8 cache only) and QK^T runs as E4M3 x E4M3 products.
-template <bool kFp8, int kQ, bool kQ8>
-__global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_kernel(
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
+__global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_attn_kernel(
     // q, the plan arrays and the cache may be written by the kernel this one
     // is a programmatic dependent of: they are read with plain (coherent)
     // loads, never as restrict/read-only data, so that no load of them can be
@@ -282,8 +362,9 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
     const int32_t* seg_ptr, int32_t* seg_done, void* __restrict__ out, int32_t out_dtype,
     int32_t l2_prefetch_tiles) {
-  using T = AttnTraits<kFp8>;
+  using T = AttnTraits<kFp8, kTC>;
   static_assert(kQ == 1 || kQ == 2 || kQ == 4, "query layouts of 1, 2 or 4 tokens");
+  static_assert(!kTC || T::kGroups == 2, "tensor-core form: two queues");
   static_assert(kFp8 || !kQ8, "an E4M3 q needs an E4M3 cache");
   constexpr int kWq = T::kWarpsPerGroup / kQ;   // warps per query
   constexpr int kMB = kQ;                       // 16-token blocks per warp and tile
@@ -312,7 +393,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   volatile int* stage_ok = reinterpret_cast<volatile int*>(smem + T::kOffOk) + grp * SG;
   volatile int* ring = reinterpret_cast<volatile int*>(smem + T::kOffRing) + grp * R * T::kRingInts;
   volatile int* merge_flag = abort_flag + 1 + grp;
-  const uint32_t stage_base = smem_u32(smem) + grp * SG * T::kStageBytes;   // this queue's stages
+  const uint32_t stage_base =
+      smem_u32(smem) + T::kOffStages + grp * SG * T::kStageBytes;   // this queue's stages
 
   const unsigned long long t_start = cta_clock != nullptr ? globaltimer_ns() : 0ull;
   if (threadIdx.x == 0) {
@@ -321,13 +403,18 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
       uint64_t* b = bars + k * T::kGroupBars;
       for (int st = 0; st < SG; ++st) {
         mbar_init(smem_u32(&b[st]), 1);                           // full
-        mbar_init(smem_u32(&b[SG + st]), T::kWarpsPerGroup);      // empty
+        // empty: the consumer warps, or the commit of the tile's P V
+        mbar_init(smem_u32(&b[SG + st]), kTC ? 1 : T::kWarpsPerGroup);
       }
       for (int r = 0; r < R; ++r) {
         mbar_init(smem_u32(&b[2 * SG + r]), 1);                   // item_full
-        mbar_init(smem_u32(&b[2 * SG + R + r]), T::kWarpsPerGroup);   // item_empty
+        // item_empty: every reading warp (tensor-core form: the MMA and softmax
+        // warps, and over E4M3 pages the two converter warps)
+        mbar_init(smem_u32(&b[2 * SG + R + r]), kTC ? (kFp8 ? 4 : 2) : T::kWarpsPerGroup);
       }
       mbar_init(smem_u32(&b[2 * SG + 2 * R]), T::kGroupThreads);  // the queue's consumer barrier
+      for (int x = 0; x < T::kTcBars; ++x)   // conv_k, conv_v: one arrival per converter warp
+        mbar_init(smem_u32(&b[2 * SG + 2 * R + 1 + x]), x >= 9 ? 2 : 1);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -379,7 +466,16 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
   const int home_begin = vq < num_queues ? cta_ptr[vq] : 0;
   const int home_stop = vq < num_queues ? home_end[vq] : 0;
 
+  // tensor-core form: 512 TMEM columns, 256 per queue (scores 0 / 64, O 128),
+  // allocated by an idle warp, freed by it after every warp's final barrier
+  constexpr int kTmemWarp = 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffFlags) + 1 + G;
+  if constexpr (kTC) {
+    if (warp == kTmemWarp) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+  }
   __syncthreads();
+  if constexpr (kTC) tc_fence_after();
 
   // ------------------------------------------------------------ producer
   // The producer does not wait on a global load in its issue loop: the home
@@ -505,7 +601,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
           const uint32_t fb = smem_u32(&full[s]);
           if (data && bid >= 0 && bid < num_blocks) {
             stage_ok[s] = 1;
-            mbar_arrive_expect_tx(fb, T::kStageBytes);
+            mbar_arrive_expect_tx(fb, T::kTmaStageBytes);
             const uint32_t dst = stage_base + s * T::kStageBytes;
             const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
             const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
@@ -582,6 +678,10 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
         mbar_wait(smem_u32(&full[s]), (last / SG) & 1, status);
       }
     }
+    if constexpr (kTC) {
+      __syncwarp();
+      named_bar_sync(2, T::kThreads);   // every warp done; TMEM is freed after this
+    }
     return;
   }
 
@@ -648,6 +748,350 @@ __global__ void __launch_bounds__(AttnTraits<kFp8>::kThreads, 1) decode_attn_ker
     if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
     return true;
   };
+  if constexpr (kTC) {
+    // ---------------------------------------------------- tensor-core form
+    // Multi-token decode over BF16 pages on the 5th-generation tensor cores.
+    // The item's q_len x 8 query rows (row 8 t + head, zeros for t >= q_len)
+    // are rows 32 k .. 32 k + 31 of queue k's M = 128 Q tile, so that queue
+    // k's softmax warp is the one whose TMEM lanes those rows are (warp w
+    // reaches lanes 32 (w % 4) ..): warp 0 for queue 0, warp 5 for queue 1.
+    // Per 64-key tile: S = Q K^T (N 64) into one of two score buffers; the
+    // softmax warp (thread = row) masks each row at its token's position,
+    // keeps a running maximum that moves only when it grows by more than
+    // 2^8 (then O is rescaled in TMEM), and writes P as BF16 pairs over the
+    // scores; O += P V (N 128, P from TMEM, V MN-major), O in TMEM for the
+    // item.  The item's partial (O / l and lse per row) goes to the partial
+    // buffers; a merge pass combines the items of every segment.
+    uint64_t* tb = full + 2 * SG + 2 * R + 1;   // this queue's tensor-core barriers
+    const uint32_t b_sfull = smem_u32(&tb[0]), b_pfull = smem_u32(&tb[2]);
+    const uint32_t b_qfull = smem_u32(&tb[4]), b_qfree = smem_u32(&tb[5]);
+    const uint32_t b_ofinal = smem_u32(&tb[6]), b_ofree = smem_u32(&tb[7]);
+    const uint32_t b_drain = smem_u32(&tb[8]);
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tq = tmem + 256u * static_cast<uint32_t>(grp);   // the queue's columns
+    uint8_t* qtile = smem + T::kOffQt + grp * T::kQtBytes;
+    auto wait_warp = [&](uint32_t bar, uint32_t parity) -> bool {
+      bool ok = !*abort_flag && mbar_wait(bar, parity, status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) *abort_flag = 1;
+      return ok;
+    };
+
+    if (wq == 2) {
+      // ------------------------------------------------ MMA warp of the queue
+      constexpr uint32_t kIdescS = kFp8 ? umma_idesc_f16(128, 64, false) : umma_idesc_bf16(128, 64, false);
+      constexpr uint32_t kIdescO = kFp8 ? umma_idesc_f16(128, 128, true) : umma_idesc_bf16(128, 128, true);
+      constexpr uint64_t kStageStep = T::kStageBytes >> 4;
+      const uint64_t desc_q = umma_smem_desc(smem_u32(qtile), 1024, 1024);
+      const uint64_t desc_k = umma_smem_desc(stage_base, 1024, 1024);
+      const uint64_t desc_v = umma_smem_desc(stage_base + T::kF16Page, T::kBoxBytes, 1024);
+      uint32_t gl = 0, nq = 0;   // tiles and items of the queue so far
+      bool stop = false;
+      for (uint32_t n = 0; !stop; ++n) {
+        Desc d;
+        if (!fetch_desc(n, d) || d.i < 0) break;
+        if (!d.it.ok) continue;
+        const int nt = d.it.t1 - d.it.t0;
+        if (!wait_warp(b_qfull, nq & 1)) break;
+        tc_fence_after();
+        // Issue Q K^T of tile jq once its K is in place (at most two ahead of
+        // P V: two score buffers) and P V of tile jp once its P is written,
+        // whichever is ready first, so that neither waits on the other's tile.
+        int jq = 0, jp = 0;
+        unsigned long long idle_since = 0ull;
+        while (jp < nt) {
+          bool did = false;
+          if (jp < jq) {
+            const uint32_t gg = g + jp, st = gg % SG, pb = (gl + jp) & 1u;
+            bool ready = mbar_test_wait(b_pfull + 8u * pb, ((gl + jp) >> 1) & 1u);
+            if (kFp8) ready = ready && mbar_test_wait(smem_u32(&tb[9 + SG + st]), (gg / SG) & 1);
+            if (jp == 0 && nq > 0) ready = ready && mbar_test_wait(b_ofree, (nq - 1) & 1);
+            if (__all_sync(0xffffffffu, ready)) {
+              tc_fence_after();
+              umma_pv_lane(tq + 128, tq + 64u * pb, desc_v + st * kStageStep, kIdescO, jp != 0,
+                           jp == nt - 1, b_ofinal, smem_u32(&empty[st]));
+              ++jp;
+              did = true;
+            }
+          }
+          if (jq < nt && jq - jp < 2) {
+            const uint32_t gg = g + jq, st = gg % SG;
+            // the tile as the products read it: landed (BF16) or K widened (E4M3)
+            const bool ready = mbar_test_wait(kFp8 ? smem_u32(&tb[9 + st]) : smem_u32(&full[st]),
+                                              (gg / SG) & 1);
+            if (__all_sync(0xffffffffu, ready)) {
+              // V rows the products must not see (the cache may hold NaN
+              // there): past the length on the sequence's last tile, all of a
+              // bad block's (the converter zeroes them for E4M3 pages)
+              const int keep = stage_ok[st] ? min(kPage, d.it.len - (d.it.t0 + jq) * kPage) : 0;
+              if (!kFp8 && keep < kPage) {
+                uint4* v0 = reinterpret_cast<uint4*>(smem + (stage_base - smem_u32(smem)) +
+                                                     st * T::kStageBytes + T::kF16Page);
+                uint4* v1 = v0 + T::kBoxBytes / 16;
+                for (int z = keep * 8 + lane; z < kPage * 8; z += 32) {
+                  v0[z] = make_uint4(0u, 0u, 0u, 0u);
+                  v1[z] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+              }
+              tc_fence_after();
+              umma_qk_tile(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
+                           b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree);
+              ++jq;
+              did = true;
+            }
+          }
+          if (did) {
+            idle_since = 0ull;
+            continue;
+          }
+          // nothing ready: bounded like every other wait of the kernel (lane
+          // 0 decides, so that the warp leaves the loop as one)
+          int give_up = 0;
+          if (lane == 0) {
+            const unsigned long long now = globaltimer_ns();
+            if (*abort_flag) {
+              give_up = 1;
+            } else if (idle_since == 0ull) {
+              idle_since = now;
+            } else if (now - idle_since > kWaitLimitNs) {
+              atomicOr(status, HPC_STATUS_WAIT_TIMEOUT);
+              *abort_flag = 1;
+              give_up = 1;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, give_up, 0)) {
+            stop = true;
+            break;
+          }
+        }
+        if (stop) break;
+        g += nt;
+        gl += nt;
+        ++nq;
+      }
+      // every product issued here has completed before TMEM is freed
+      umma_commit_elect(b_drain);
+      mbar_wait(b_drain, 0, status);
+      __syncwarp();
+    } else if (wq == grp) {
+      // ------------------------------------------------ softmax warp of the queue
+      const int rr = lane, row = 32 * grp + rr;   // row of the Q tile = TMEM lane
+      const int tok = rr >> 3, hl = rr & 7;
+      const uint32_t trow = tq + (static_cast<uint32_t>(32 * grp) << 16);
+      uint32_t gl = 0, nq = 0;
+      bool stop = false;
+      for (uint32_t n = 0; !stop; ++n) {
+        Desc d;
+        if (!fetch_desc(n, d) || d.i < 0) break;
+        const Item it = d.it;
+        const bool valid = tok < q_len;
+        const int64_t prow = (static_cast<int64_t>(d.i) * q_len + tok) * kGroup + hl;
+        if (!it.ok) {   // no products: an empty partial
+          if (valid) {
+            for (int e = 0; e < kD; e += 4)
+              *reinterpret_cast<float4*>(partial_o + prow * kD + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+            partial_lse[prow] = -INFINITY;
+          }
+          continue;
+        }
+        const int nt = it.t1 - it.t0;
+        // the item's Q rows, once the previous item's last Q K^T has read the tile
+        if (nq > 0 && !wait_warp(b_qfree, (nq - 1) & 1)) break;
+        {
+          // one row: 16 chunks of 8 values, d 0..63 then 64..127; over E4M3
+          // pages the products take F16, so a BF16 q is rounded to F16 and an
+          // E4M3 q widened (exactly)
+          const int64_t qr = (static_cast<int64_t>(it.seq) * q_len + (valid ? tok : 0)) * kHq +
+                             it.h * kGroup + hl;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (valid) {
+              if constexpr (kQ8) {
+                const uint2 c8v = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(q) + qr * kD)[ch];
+                v = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.x)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.x >> 16)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.y)),
+                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.y >> 16)));
+              } else {
+                v = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + qr * kD)[ch];
+                if constexpr (kFp8)
+                  v = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
+                                 pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
+              }
+            }
+            const int half = ch >> 3, c8 = ch & 7;
+            *reinterpret_cast<uint4*>(qtile + half * (T::kQtBytes / 2) + (row >> 3) * 1024 +
+                                      (row & 7) * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_qfull);
+        }
+        const int pos = it.len - q_len + tok;   // the row's token position
+        float m_used = -INFINITY, lsum = 0.f;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t gg = g + j, st = gg % SG, b = (gl + j) & 1u;
+          if (!wait_warp(b_sfull + 8u * b, ((gl + j) >> 1) & 1u)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          uint32_t sr[64];
+          tmem_ld64(trow + 64u * b, sr);
+          tmem_wait_ld();
+          const int key0 = (it.t0 + j) * kPage;
+          const int lim = (valid && stage_ok[st]) ? min(kPage - 1, pos - key0) : -1;
+          float x[64];
+          if (__all_sync(0xffffffffu, lim == kPage - 1)) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(sr[k]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) x[k] = k <= lim ? __uint_as_float(sr[k]) : -INFINITY;
+          }
+          // the row maximum in 8 independent chains of three-input maxima;
+          // the scale is positive, so it commutes with the maximum
+          float m8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+          for (int k = 8; k < 64; k += 2) m8[(k >> 1) & 7] = max3f(m8[(k >> 1) & 7], x[k], x[k + 1]);
+          const float mx =
+              max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+              scale_log2;
+          // the running maximum moves only when it grows by more than 2^8
+          // (weights stay <= 2^8); the row's O is then rescaled in TMEM
+          const bool grow = mx > m_used + 8.f;
+          const float alpha = grow ? exp2_ftz(m_used - mx) : 1.f;   // 0 while m_used = -inf
+          if (grow) {
+            lsum *= alpha;
+            m_used = mx;
+          }
+          if (j > 0 && __any_sync(0xffffffffu, grow)) {
+            // the previous tile's P V must be in O before it is rescaled: its
+            // stage's empty barrier completes with it
+            const uint32_t gp = gg - 1;
+            if (!wait_warp(smem_u32(&empty[gp % SG]), (gp / SG) & 1)) {
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int qc = 0; qc < 4; ++qc) {
+              uint32_t ov[32];
+              tmem_ld32(trow + 128 + 32 * qc, ov);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha);
+              tmem_st32(trow + 128 + 32 * qc, ov);
+            }
+          }
+          // p = 2^(s scale - m): one packed FMA per pair and an exponential
+          // each; the row sum in 4 independent chains of packed adds
+          const float nms = m_used == -INFINITY ? 0.f : -m_used;
+          const uint64_t scale2 = f32x2(scale_log2, scale_log2), nms2 = f32x2(nms, nms);
+          uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
+          uint32_t pk[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            float a0, a1;
+            f32x2_split(fma_f32x2(f32x2(x[2 * k], x[2 * k + 1]), scale2, nms2), a0, a1);
+            const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
+            ps2[k & 3] = add_f32x2(ps2[k & 3], f32x2(p0, p1));
+            pk[k] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+          }
+          float s0, s1;
+          f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+          lsum += s0 + s1;
+          tmem_st32(trow + 64u * b, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_pfull + 8u * b);
+        }
+        if (stop) break;
+        // the item's partial once its last P V is done: this row of O
+        if (!wait_warp(b_ofinal, nq & 1)) break;
+        tc_fence_after();
+        const float inv = lsum > 0.f ? v_scale / lsum : 0.f;
+#pragma unroll
+        for (int qc = 0; qc < 4; ++qc) {
+          uint32_t ov[32];
+          tmem_ld32(trow + 128 + 32 * qc, ov);
+          tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              *reinterpret_cast<float4*>(partial_o + prow * kD + 32 * qc + k) =
+                  make_float4(__uint_as_float(ov[k]) * inv, __uint_as_float(ov[k + 1]) * inv,
+                              __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv);
+          }
+        }
+        if (valid)
+          partial_lse[prow] = lsum > 0.f ? (m_used + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ofree);
+        g += nt;
+        gl += nt;
+        ++nq;
+      }
+    }
+    if constexpr (kFp8) {
+      if (wq != 2 && wq != grp) {
+        // -------------------------------------------- converter warps of the queue
+        // Each landed E4M3 tile is widened to F16 in its own stage: thread ct
+        // reads raw K row ct and raw V row ct, writes K row ct in place (so
+        // that Q K^T can start), then V row ct into the stage's second half
+        // (zeros past the length or on a bad block).  The only bytes a
+        // thread's outputs share with codes still to read are its own rows
+        // (K's first half is its raw K row, K's second half its raw V row,
+        // both read before), so the widening needs no barrier.
+        const int ct = (wq == 3 ? 32 : 0) + lane;
+        bool stop = false;
+        for (uint32_t n = 0; !stop; ++n) {
+          Desc d;
+          if (!fetch_desc(n, d) || d.i < 0) break;
+          if (!d.it.ok) continue;
+          const int nt = d.it.t1 - d.it.t0;
+          for (int j = 0; j < nt; ++j) {
+            const uint32_t gg = g + j, st = gg % SG;
+            if (!wait_warp(smem_u32(&full[st]), (gg / SG) & 1)) {
+              stop = true;
+              break;
+            }
+            uint8_t* stg = smem + T::kOffStages + (grp * SG + st) * T::kStageBytes;
+            const int keep = stage_ok[st] ? min(kPage, d.it.len - (d.it.t0 + j) * kPage) : 0;
+            uint4 kw[8], vw[8];
+            load_e4m3_row(stg + ct * 128, ct, true, kw);
+            load_e4m3_row(stg + T::kPageBytes + ct * 128, ct, ct < keep, vw);
+            store_f16_row(kw, stg + ct * 128, stg + T::kBoxBytes + ct * 128, ct);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tb[9 + st]));
+            store_f16_row(vw, stg + T::kF16Page + ct * 128, stg + T::kF16Page + T::kBoxBytes + ct * 128, ct);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tb[9 + SG + st]));
+          }
+          g += nt;
+        }
+      }
+    }
+    // every warp of the CTA meets here; then the allocating warp frees TMEM
+    tc_fence_before();
+    __syncwarp();
+    named_bar_sync(2, T::kThreads);
+    if (warp == kTmemWarp) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    return;
+  }
+
   // The item's q words (this lane's share of the B operand Q^T of the 8 query
   // heads of its KV head, head = r) and, with the merge fused in, its
   // segment's first item and item count.  Issued one item ahead, so the
@@ -1063,7 +1507,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-template <bool kFp8, int kQ, bool kQ8>
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
 cudaError_t ensure_smem_attr() {
   // once per device: the dynamic shared memory opt-in is a per-device setting
   static std::mutex mu;
@@ -1073,22 +1517,26 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ, kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           AttnTraits<kFp8>::kSmemBytes);
+  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ, kQ8, kTC>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           AttnTraits<kFp8, kTC>::kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <bool kFp8, int kQ, bool kQ8>
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
 int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int32_t num_blocks,
                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
                 int32_t batch, const hpc_attn_options& opts, const hpc_plan* plan,
                 float* partial_o, float* partial_lse, float sm_scale, int32_t* status,
                 unsigned long long* cta_clock, void* out, bool pdl, cudaStream_t stream) {
-  using T = AttnTraits<kFp8>;
+  using T = AttnTraits<kFp8, kTC>;
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
-  if (ensure_smem_attr<kFp8, kQ, kQ8>() != cudaSuccess) return HPC_ERR_CUDA;
+  if (ensure_smem_attr<kFp8, kQ, kQ8, kTC>() != cudaSuccess) return HPC_ERR_CUDA;
+  // the tensor-core form writes every item's partial; the merge runs after it
+  void* fused_out = kTC ? nullptr : out;
+  if (kTC && cta_clock != nullptr) return HPC_ERR_UNSUPPORTED;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
                               static_cast<cuuint64_t>(num_blocks) * 2 * kHkv * kPage};
@@ -1112,14 +1560,17 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, decode_attn_kernel<kFp8, kQ, kQ8>, map, q, opts.q_scale, kv_scale, block_table,
+      &cfg, decode_attn_kernel<kFp8, kQ, kQ8, kTC>, map, q, opts.q_scale, kv_scale, block_table,
       max_blocks, num_blocks, seq_lens, batch, opts.q_len,
       static_cast<const hpc_work_item*>(plan->items),
       static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
       plan->pool, plan->capacity, plan->num_ctas, partial_o, partial_lse, sm_scale, status, cta_clock,
-      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, out, opts.out_dtype,
+      static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, fused_out, opts.out_dtype,
       pdl ? T::kL2PrefetchTiles : 0);
-  return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+  if (e != cudaSuccess) return HPC_ERR_CUDA;
+  if (kTC && out != nullptr)
+    return hpc_merge_ex(partial_o, partial_lse, plan, batch, &opts, out, stream);
+  return HPC_OK;
 }
 
 // The kernel instances of one query layout: BF16 cache, E4M3 cache with a
@@ -1131,10 +1582,27 @@ int launch_attn_layout(const void* q, const void* kv_cache, int32_t kv_dtype, co
                        const hpc_plan* plan, float* partial_o, float* partial_lse, float sm_scale,
                        int32_t* status, unsigned long long* cta_clock, void* out, bool pdl,
                        cudaStream_t stream) {
-  if (kv_dtype == HPC_KV_BF16)
+  if (kv_dtype == HPC_KV_BF16) {
+    if constexpr (kQ == 4)
+      return launch_attn<false, kQ, false, true>(q, kv_cache, kv_scale, num_blocks, block_table,
+                                                 max_blocks, seq_lens, batch, opts, plan,
+                                                 partial_o, partial_lse, sm_scale, status,
+                                                 cta_clock, out, pdl, stream);
     return launch_attn<false, kQ, false>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
                                          seq_lens, batch, opts, plan, partial_o, partial_lse,
                                          sm_scale, status, cta_clock, out, pdl, stream);
+  }
+  if constexpr (kQ == 4) {
+    if (opts.q_dtype == HPC_Q_FP8_E4M3)
+      return launch_attn<true, kQ, true, true>(q, kv_cache, kv_scale, num_blocks, block_table,
+                                               max_blocks, seq_lens, batch, opts, plan, partial_o,
+                                               partial_lse, sm_scale, status, cta_clock, out, pdl,
+                                               stream);
+    return launch_attn<true, kQ, false, true>(q, kv_cache, kv_scale, num_blocks, block_table,
+                                              max_blocks, seq_lens, batch, opts, plan, partial_o,
+                                              partial_lse, sm_scale, status, cta_clock, out, pdl,
+                                              stream);
+  }
   if (opts.q_dtype == HPC_Q_FP8_E4M3)
     return launch_attn<true, kQ, true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
                                        seq_lens, batch, opts, plan, partial_o, partial_lse,

@@ -128,32 +128,6 @@ __device__ __forceinline__ int lane_tiles(int qlen, int L, int first_token) {
 
 }  // namespace tc
 
-// Softmax arithmetic on two fp32 lanes at once (FMA2 / ADD2: one issue slot
-// for two elements) and the three-input maximum.
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-  uint64_t d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-  return d;
-}
-__device__ __forceinline__ void f32x2_split(uint64_t x, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 // Eight consecutive output elements (index a multiple of 8) in the caller's type.
 __device__ __forceinline__ void store_out8(void* out, int64_t idx, const float (&v)[8],
                                            int32_t out_dtype) {
@@ -201,30 +175,6 @@ __device__ __forceinline__ void umma_qk_lane(uint32_t d, uint64_t q, uint64_t k,
       ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free)
       : "memory");
 #undef HPC_QK_STEP
-}
-
-// O += P V of one lane for one tile: four steps of 16 keys (P from TMEM, 8
-// columns a step; V MN-major, 2048 bytes a step; the first step overwrites O
-// unless `acc`), a commit on fin if it was the lane's last tile of the unit,
-// then a commit on the tile's empty barrier (which counts both lanes).
-__device__ __forceinline__ void umma_pv_lane(uint32_t o, uint32_t p, uint64_t v, uint32_t idesc,
-                                             bool acc, bool last, uint32_t fin, uint32_t empty) {
-#define HPC_PV_STEP(PO, VO) \
-  "add.u32 a, %1, " PO ";\n\tadd.s64 b, %2, " VO ";\n\t" \
-  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, pt;\n\t"
-  const uint32_t flags = (acc ? 1u : 0u) | (last ? 2u : 0u);
-  asm volatile(
-      "{\n\t.reg .pred e, f, pa, pt;\n\t.reg .b64 b;\n\t.reg .b32 a, t;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "and.b32 t, %4, 1;\n\tsetp.ne.b32 pa, t, 0;\n\tsetp.eq.b32 pt, t, t;\n\t"
-      "and.b32 t, %4, 2;\n\tsetp.ne.and.b32 f, t, 0, e;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t"
-      HPC_PV_STEP("8", "128") HPC_PV_STEP("16", "256") HPC_PV_STEP("24", "384")
-      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
-      ::"r"(o), "r"(p), "l"(v), "r"(idesc), "r"(flags), "r"(fin), "r"(empty)
-      : "memory");
-#undef HPC_PV_STEP
 }
 
 template <bool kFp8>

@@ -56,10 +56,15 @@ def _cache_dtypes(kv_dtype):
     raise ValueError("kv_dtype must be KV_BF16 (0) or KV_FP8 (1)")
 
 
-def num_ctas(kv_dtype=KV_BF16):
-    """Persistent grid of the attention kernel on the current device."""
+def num_ctas(kv_dtype=KV_BF16, q_len=1):
+    """Work queues of the persistent attention grid on the current device for
+    the KV dtype and the new tokens per sequence: the plan's num_ctas."""
     n = ctypes.c_int32(0)
-    check("hpc_decode_num_ctas", _lib.lib().hpc_decode_num_ctas(kv_dtype, ctypes.byref(n)))
+    if q_len == 1:
+        check("hpc_decode_num_ctas", _lib.lib().hpc_decode_num_ctas(kv_dtype, ctypes.byref(n)))
+    else:
+        check("hpc_decode_num_queues",
+              _lib.lib().hpc_decode_num_queues(kv_dtype, int(q_len), ctypes.byref(n)))
     return n.value
 
 
@@ -81,8 +86,8 @@ class DecodePlan:
 
     @classmethod
     def dynamic(cls, batch, device="cuda", n_ctas=None, kv_dtype=KV_BF16, pool_chunks=POOL_CHUNKS,
-                pool_min_tiles=POOL_MIN_TILES):
-        n_ctas = num_ctas(kv_dtype) if n_ctas is None else n_ctas
+                pool_min_tiles=POOL_MIN_TILES, q_len=1):
+        n_ctas = num_ctas(kv_dtype, q_len) if n_ctas is None else n_ctas
         cap = _lib.lib().hpc_plan_capacity(batch, n_ctas, pool_chunks)
         return cls(batch, n_ctas, cap, device, pool_chunks, pool_min_tiles)
 
@@ -437,7 +442,8 @@ class DecodeStepMT:
                  pool_chunks=POOL_CHUNKS, pool_min_tiles=POOL_MIN_TILES, fused=True, min_tiles=1):
         self.batch, self.q_len, self.kv_dtype, self.max_blocks = batch, q_len, kv_dtype, max_blocks
         self.fused, self.min_tiles = fused, min_tiles
-        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles)
+        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles,
+                                       q_len)
         cap = max(self.plan.capacity, 1)
         self.partial_o = torch.empty((cap, q_len, HKV, D), dtype=torch.float32, device=device)
         self.partial_lse = torch.empty((cap, q_len, HKV), dtype=torch.float32, device=device)
@@ -562,7 +568,8 @@ class DecodeStepEx:
         self.batch, self.kv_dtype, self.max_blocks = batch, kv_dtype, max_blocks
         self.q_len, self.q_dtype, self.q_scale, self.out_dtype = q_len, q_dtype, q_scale, out_dtype
         self.fused, self.min_tiles = fused, min_tiles
-        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles)
+        self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles,
+                                       q_len)
         cap = max(self.plan.capacity, 1)
         self.partial_o = torch.empty((cap, q_len, HKV, D), dtype=torch.float32, device=device)
         self.partial_lse = torch.empty((cap, q_len, HKV), dtype=torch.float32, device=device)
