@@ -90,8 +90,7 @@ extern "C" int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t* n
   if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return HPC_ERR_CUDA;
-  *num_queues = sms * (hpc::tt_enabled() ? hpc::AttnTraits<true, 2>::kGroups
-                                          : hpc::AttnTraits<true, 1>::kGroups);
+  *num_queues = sms * hpc::AttnTraits<true, true>::kGroups;
   return HPC_OK;
 }
 

@@ -60,7 +60,6 @@
 //    Its partials are merged by the merge pass after the kernel.
 //  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
 //    HPC_STATUS_WAIT_TIMEOUT and winds down, waiting for its own copies.
-#include <cstdlib>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -71,17 +70,11 @@
 namespace hpc {
 namespace {
 
-// kForm 0: the mma.sync form.  kForm 1 (kTC): the tensor-core form of the
-// 4-token layout: per queue one MMA warp issuing tcgen05 products into
-// tensor memory, one softmax warp and (E4M3 pages) two converter warps; the
-// Q tiles sit ahead of the stage rings.  kForm 2 (kTT): the transposed
-// tensor-core form of the 4-token layout over E4M3 pages, keys on M: one
-// queue per CTA, four softmax warps (one per tensor-memory lane quarter),
-// an MMA warp and two converter warps.
-template <bool kFp8, int kForm = 0>
+// kTC: the tensor-core form of the 4-token layout: per queue one MMA warp
+// issuing tcgen05 products into tensor memory, one softmax warp and (E4M3
+// pages) two converter warps; the Q tiles sit ahead of the stage rings.
+template <bool kFp8, bool kTC = false>
 struct AttnTraits {
-  static constexpr bool kTC = kForm == 1;
-  static constexpr bool kTT = kForm == 2;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kPageBytes = kPage * kD * kElem;      // one K or V page of one KV head
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
@@ -96,15 +89,13 @@ struct AttnTraits {
   // items, so one queue's epilogue and merge overlap the other queues'
   // streaming.  FP8 tiles carry a longer per-tile chain (the conversions) at
   // half the bytes, so FP8 keeps three queues in flight.
-  static constexpr int kGroups = kTT ? 1 : (kFp8 && !kTC) ? 3 : 2;
-  // stage ring of one queue (the transposed form: 2 pairs of pages)
-  static constexpr int kGroupStages = kTT ? 4 : 3;
+  static constexpr int kGroups = (kFp8 && !kTC) ? 3 : 2;
+  static constexpr int kGroupStages = 3;                      // stage ring of one queue
   // tiles per queue pulled into L2 while a programmatic dependent launch
   // waits for the plan (about 29 MB in all on a 152-SM part)
   static constexpr int kL2PrefetchTiles = kFp8 ? 4 : 3;
   static constexpr int kStages = kGroups * kGroupStages;
-  // 16 tokens of a tile each (the transposed form: 4 softmax, MMA, 2 converters)
-  static constexpr int kWarpsPerGroup = kTT ? 7 : 4;
+  static constexpr int kWarpsPerGroup = 4;                    // 16 tokens of a tile each
   static constexpr int kConsumerWarps = kGroups * kWarpsPerGroup;
   static constexpr int kGroupThreads = 32 * kWarpsPerGroup;
   static constexpr int kThreads = 32 * (kConsumerWarps + kGroups);   // + a producer warp per queue
@@ -112,21 +103,11 @@ struct AttnTraits {
   // tensor-core form: per queue a 16 KB Q tile (two 64-column halves of 64
   // rows; the M = 128 operand's rows past 64 read whatever follows, which the
   // products ignore), ahead of the rings so that those rows stay in bounds
-  // (the transposed form: the N = 64 B operand of Q K^T, 64 rows of 128 codes)
-  static constexpr int kQtBytes = kTT ? 8192 : 16384;
+  static constexpr int kQtBytes = 16384;
   static constexpr int kOffQt = 0;
-  static constexpr int kOffStages = kTT ? kQtBytes : kTC ? kGroups * kQtBytes : 0;
-  // transposed form: three F16 V buffers of a pair ([d half][128 keys][128
-  // B]), three P^T buffers ([128 keys][64 rows], rows 32.. unused), the
-  // softmax warps' exchange area
-  static constexpr int kOffV16 = kOffStages + kStages * kStageBytes;
-  static constexpr int kV16Bytes = kTT ? 3 * 32768 : 0;
-  static constexpr int kOffP = kOffV16 + kV16Bytes;
-  static constexpr int kPBytes = kTT ? 3 * 16384 : 0;
-  static constexpr int kOffX = kOffP + kPBytes;
-  static constexpr int kXBytes = kTT ? 4096 : 0;
-  static constexpr int kSliceWarps = (kTC || kTT) ? 0 : kConsumerWarps;   // merge slices (mma.sync)
-  static constexpr int kOffO = kOffX + kXBytes;                       // [warps][8][kOStride]
+  static constexpr int kOffStages = kTC ? kGroups * kQtBytes : 0;
+  static constexpr int kSliceWarps = kTC ? 0 : kConsumerWarps;   // merge slices (the mma.sync form)
+  static constexpr int kOffO = kOffStages + kStages * kStageBytes;    // [warps][8][kOStride]
   static constexpr int kOffM = kOffO + kSliceWarps * kGroup * kOStride * 4;
   static constexpr int kOffL = kOffM + kSliceWarps * kGroup * 4;
   static constexpr int kOffBar = kOffL + kSliceWarps * kGroup * 4;
@@ -134,7 +115,7 @@ struct AttnTraits {
   // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier,
   // and for the tensor-core form s_full[2], p_full[2], q_full, q_free, o_final, o_free, drain,
   // and over E4M3 pages conv_k[SG] and conv_v[SG] (the stage's K, V widened to F16)
-  static constexpr int kTcBars = kTC ? 9 + (kFp8 ? 2 * kGroupStages : 0) : kTT ? 19 : 0;
+  static constexpr int kTcBars = kTC ? 9 + (kFp8 ? 2 * kGroupStages : 0) : 0;
   static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1 + kTcBars;
   static constexpr int kOffOk = kOffBar + kGroups * kGroupBars * 8;
   static constexpr int kOffRing = kOffOk + kStages * 4;
@@ -349,118 +330,6 @@ __device__ __forceinline__ void store_f16_row(const uint4 (&w)[8], uint8_t* lo_r
   }
 }
 
-// ---------------------------------------------------------------------------
-// Transposed tensor-core form (E4M3 pages, 4-token layout).  Per pair of
-// pages (128 keys) of an item:
-//   S^T[128 keys x N] = K[128 x 128 codes] . Qb^T      (kind::f8f6f4, E4M3)
-//   O^T[128 d x 64]  += V^T[128 d x 128 keys] . P^T    (kind::f16, F16)
-// Qb is the item's q_len x 8 query rows as E4M3: the codes of an E4M3 q (N =
-// 32), or a BF16 q split exactly into two E4M3 terms per row (N = 64: rows
-// 0..31 the leading term, 32..63 the remainder) under a power-of-two row
-// scale.  K is read by the products as TMA landed it; V is widened to F16
-// into its own buffer.  Thread k of the four softmax warps holds key k's
-// scores of all 32 rows (tensor-memory lane = key).
-namespace tt {
-// Score buffers (and the row-maximum exchange) go by pair p & 1; the P^T
-// and V buffers by p % kNB, so that the widening of pair p + kNB - 1 and the
-// softmax of pair p + kNB - 1 need only P V of pair p - 1 done.
-constexpr int kNB = 3;
-constexpr int kSFull = 0;             // [2] Q K^T of a pair done (commit)
-constexpr int kPFull = 2;             // [kNB] P^T of a pair written (4 softmax warps)
-constexpr int kPvDone = kPFull + kNB; // [kNB] P V of a pair done (commit): its P^T and V buffers are free
-constexpr int kVFull = kPvDone + kNB; // [kNB] V of a pair widened (2 converter warps)
-constexpr int kQFull = kVFull + kNB;  // the item's Q operand and row scales written (4 softmax warps)
-constexpr int kQFree = kQFull + 1;    // the item's last Q K^T done (commit)
-constexpr int kOFinal = kQFree + 1;   // the item's last P V done (commit)
-constexpr int kOFree = kOFinal + 1;   // O^T read out (4 softmax warps)
-constexpr int kDrain = kOFree + 1;    // every product of the queue done (commit)
-constexpr int kXMax = kDrain + 1;     // [2] row maxima of a pair exchanged (4 softmax warps)
-constexpr int kXSum = kXMax + 2;      // row sums of an item exchanged (4 softmax warps)
-constexpr int kBars = kXSum + 1;
-__host__ __device__ constexpr int arrivals(int x) {
-  return ((x >= kPFull && x < kPFull + kNB) || x == kQFull || x == kOFree ||
-          (x >= kXMax && x < kXMax + 2) || x == kXSum) ? 4
-         : (x >= kVFull && x < kVFull + kNB) ? 2 : 1;
-}
-}  // namespace tt
-
-// S^T = K . Qb^T over d: four kind::f8f6f4 steps of 32 codes (32 bytes of
-// each 128-byte swizzled row), then commits: the pair's score buffer, the
-// pair's two page stages (their K is read), and at the item's last pair the
-// Q operand.
-__device__ __forceinline__ void umma_qk_tt(uint32_t d, uint64_t k, uint64_t q, uint32_t idesc,
-                                           uint32_t s_full, uint32_t empty0, uint32_t empty1,
-                                           bool last, uint32_t q_free) {
-#define HPC_TQK_STEP(O) \
-  "add.s64 a, %1, " O ";\n\tadd.s64 b, %2, " O ";\n\t" \
-  "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
-  asm volatile(
-      "{\n\t.reg .pred e, f, pf, pt;\n\t.reg .b64 a, b;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.and.b32 f, %7, 0, e;\n\t"
-      "setp.ne.b32 pf, %7, %7;\n\tsetp.eq.b32 pt, %7, %7;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
-      HPC_TQK_STEP("2") HPC_TQK_STEP("4") HPC_TQK_STEP("6")
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t}"
-      ::"r"(d), "l"(k), "l"(q), "r"(idesc), "r"(s_full), "r"(empty0), "r"(empty1),
-        "r"(last ? 1u : 0u), "r"(q_free)
-      : "memory");
-#undef HPC_TQK_STEP
-}
-
-// O^T (+)= V^T . P^T over the pair's 128 keys: eight kind::f16 steps of 16
-// keys (2048 bytes of both MN-major operands), then commits: the pair's P^T
-// and V buffers, and at the item's last pair the accumulator.
-__device__ __forceinline__ void umma_pv_tt(uint32_t o, uint64_t v, uint64_t p, uint32_t idesc,
-                                           bool acc, bool last, uint32_t done, uint32_t fin) {
-#define HPC_TPV_STEP(O) \
-  "add.s64 a, %1, " O ";\n\tadd.s64 b, %2, " O ";\n\t" \
-  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
-  asm volatile(
-      "{\n\t.reg .pred e, f, pa, pt;\n\t.reg .b64 a, b;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 pa, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\t"
-      "setp.ne.and.b32 f, %5, 0, e;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pa;\n\t"
-      HPC_TPV_STEP("128") HPC_TPV_STEP("256") HPC_TPV_STEP("384") HPC_TPV_STEP("512")
-      HPC_TPV_STEP("640") HPC_TPV_STEP("768") HPC_TPV_STEP("896")
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
-      ::"r"(o), "l"(v), "l"(p), "r"(idesc), "r"(acc ? 1u : 0u), "r"(last ? 1u : 0u),
-        "r"(done), "r"(fin)
-      : "memory");
-#undef HPC_TPV_STEP
-}
-
-// Across the warp, for 32 values per lane (index = row): lane l ends with the
-// reduction (maximum or sum) of row l over the 32 lanes.  Five halving
-// exchanges, 31 shuffles in all.
-template <bool kMax>
-__device__ __forceinline__ float warp_rows_reduce32(float (&v)[32], int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) {
-    const bool up = (lane & h) != 0;
-#pragma unroll
-    for (int i = 0; i < h; ++i) {
-      const float send = up ? v[i] : v[i + h];
-      const float keep = up ? v[i + h] : v[i];
-      v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, h));
-    }
-  }
-  return v[0];
-}
-
-// The maximum of x over the warp, in every lane (-inf entries allowed).
-__device__ __forceinline__ float warp_max_f32(float x) {
-  float y;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Four consecutive output elements (index a multiple of 4) in the caller's
 // output type.
 __device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, float b, float c,
@@ -478,8 +347,8 @@ __device__ __forceinline__ void store_out4(void* out, int64_t idx, float a, floa
 // kQ: query layout, 1 (decode), 2 or 4 new tokens per sequence (q_len = 3
 // runs the 4-token layout with the fourth query's warp idle).  kQ8: q is E4M3
 // codes (FP8 cache only) and QK^T runs as E4M3 x E4M3 products.
-template <bool kFp8, int kQ, bool kQ8, int kForm = 0>
-__global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_attn_kernel(
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
+__global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_attn_kernel(
     // q, the plan arrays and the cache may be written by the kernel this one
     // is a programmatic dependent of: they are read with plain (coherent)
     // loads, never as restrict/read-only data, so that no load of them can be
@@ -493,12 +362,9 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
     float sm_scale, int32_t* __restrict__ status, unsigned long long* __restrict__ cta_clock,
     const int32_t* seg_ptr, int32_t* seg_done, void* __restrict__ out, int32_t out_dtype,
     int32_t l2_prefetch_tiles) {
-  using T = AttnTraits<kFp8, kForm>;
-  constexpr bool kTC = T::kTC, kTT = T::kTT;
+  using T = AttnTraits<kFp8, kTC>;
   static_assert(kQ == 1 || kQ == 2 || kQ == 4, "query layouts of 1, 2 or 4 tokens");
   static_assert(!kTC || T::kGroups == 2, "tensor-core form: two queues");
-  static_assert(!kTT || (kFp8 && kQ == 4 && T::kGroups == 1 && T::kGroupStages % 2 == 0),
-                "transposed form: E4M3 pages, the 4-token layout, one queue, pairs of stages");
   static_assert(kFp8 || !kQ8, "an E4M3 q needs an E4M3 cache");
   constexpr int kWq = T::kWarpsPerGroup / kQ;   // warps per query
   constexpr int kMB = kQ;                       // 16-token blocks per warp and tile
@@ -537,20 +403,18 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
       uint64_t* b = bars + k * T::kGroupBars;
       for (int st = 0; st < SG; ++st) {
         mbar_init(smem_u32(&b[st]), 1);                           // full
-        // empty: the consumer warps, or the commit of the tile's P V, or (the
-        // transposed form) the commit of its Q K^T and the two converter warps
-        mbar_init(smem_u32(&b[SG + st]), kTT ? 3 : kTC ? 1 : T::kWarpsPerGroup);
+        // empty: the consumer warps, or the commit of the tile's P V
+        mbar_init(smem_u32(&b[SG + st]), kTC ? 1 : T::kWarpsPerGroup);
       }
       for (int r = 0; r < R; ++r) {
         mbar_init(smem_u32(&b[2 * SG + r]), 1);                   // item_full
         // item_empty: every reading warp (tensor-core form: the MMA and softmax
         // warps, and over E4M3 pages the two converter warps)
-        mbar_init(smem_u32(&b[2 * SG + R + r]),
-                  kTT ? T::kWarpsPerGroup : kTC ? (kFp8 ? 4 : 2) : T::kWarpsPerGroup);
+        mbar_init(smem_u32(&b[2 * SG + R + r]), kTC ? (kFp8 ? 4 : 2) : T::kWarpsPerGroup);
       }
       mbar_init(smem_u32(&b[2 * SG + 2 * R]), T::kGroupThreads);  // the queue's consumer barrier
       for (int x = 0; x < T::kTcBars; ++x)   // conv_k, conv_v: one arrival per converter warp
-        mbar_init(smem_u32(&b[2 * SG + 2 * R + 1 + x]), kTT ? tt::arrivals(x) : x >= 9 ? 2 : 1);
+        mbar_init(smem_u32(&b[2 * SG + 2 * R + 1 + x]), x >= 9 ? 2 : 1);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -604,16 +468,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
 
   // tensor-core form: 512 TMEM columns, 256 per queue (scores 0 / 64, O 128),
   // allocated by an idle warp, freed by it after every warp's final barrier
-  // (the transposed form: 256, scores 0 / 64, O^T 128)
   constexpr int kTmemWarp = 3;
-  constexpr uint32_t kTmemCols = kTT ? 256 : 512;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffFlags) + 1 + G;
-  if constexpr (kTC || kTT) {
-    if (warp == kTmemWarp) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if constexpr (kTC) {
+    if (warp == kTmemWarp) tmem_alloc(smem_u32(tmem_slot), 512);
     tc_fence_before();
   }
   __syncthreads();
-  if constexpr (kTC || kTT) tc_fence_after();
+  if constexpr (kTC) tc_fence_after();
 
   // ------------------------------------------------------------ producer
   // The producer does not wait on a global load in its issue loop: the home
@@ -743,12 +605,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
             const uint32_t dst = stage_base + s * T::kStageBytes;
             const int yk = ((bid * 2 + 0) * kHkv + h) * kPage;   // row of [bid][0][h][0]
             const int yv = yk + kHkv * kPage;                     // row of [bid][1][h][0]
-            if constexpr (kTT) {
-              // K pages and V pages in two regions, so that the K pages of a
-              // pair of stages are one 128-row operand
-              tma_load_2d(stage_base + s * T::kPageBytes, &kv_map, 0, yk, fb, policy);
-              tma_load_2d(stage_base + (SG + s) * T::kPageBytes, &kv_map, 0, yv, fb, policy);
-            } else if constexpr (kFp8) {
+            if constexpr (kFp8) {
               tma_load_2d(dst, &kv_map, 0, yk, fb, policy);
               tma_load_2d(dst + T::kPageBytes, &kv_map, 0, yv, fb, policy);
             } else {
@@ -799,11 +656,6 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
           alive = issue(__shfl_sync(0xffffffffu, cur_bids, j), it.h, true);
         cur_bids = pre;
       }
-      // the transposed form takes pages in pairs: an item of an odd page
-      // count ends with a stage without data
-      if constexpr (kTT) {
-        if (it.ok && alive && ((it.t1 - it.t0) & 1)) alive = issue(0, it.h, false);
-      }
       if (!alive) break;
       if (!have_next) {
         nxt = next_item();
@@ -826,7 +678,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
         mbar_wait(smem_u32(&full[s]), (last / SG) & 1, status);
       }
     }
-    if constexpr (kTC || kTT) {
+    if constexpr (kTC) {
       __syncwarp();
       named_bar_sync(2, T::kThreads);   // every warp done; TMEM is freed after this
     }
@@ -896,432 +748,6 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
     if (lane == 0) mbar_arrive(smem_u32(&item_empty[rslot]));
     return true;
   };
-  if constexpr (kTT) {
-    // ------------------------------------------- transposed tensor-core form
-    // Warps 0..3 softmax (warp w: keys 32w.. of a pair's scores, d 32w.. of
-    // O^T), warp 4 the products, warps 5..6 widen V.  Pair p of the queue
-    // (counted across items) uses page stages 2p, 2p+1 (mod SG), score
-    // buffer p & 1, P^T and V buffers p % tt::kNB.
-    uint64_t* xb = full + 2 * SG + 2 * R + 1;   // the transposed form's barriers
-    auto bar = [&](int x) { return smem_u32(&xb[x]); };
-    const uint32_t tmem = *tmem_slot;
-    constexpr int kNS = kQ8 ? 32 : 64;   // score columns: the rows of the Q operand
-    uint8_t* qtile = smem + T::kOffQt;
-    uint8_t* v16 = smem + T::kOffV16;
-    uint8_t* pbuf = smem + T::kOffP;
-    float* xred = reinterpret_cast<float*>(smem + T::kOffX);   // [2][4][32] row maxima
-    float* xsum = xred + 2 * 4 * 32;                            // [4][32] row sums
-    float* cs = xsum + 4 * 32;                                  // [32] row scales
-    // [kNB] which pages of a pair hold data (bit 0, bit 1), published by the
-    // converters with the pair's V: a page stage may be refilled (and its
-    // stage_ok rewritten) once its K and V are read, before the softmax
-    volatile int* pok = reinterpret_cast<volatile int*>(cs + 32);
-    float* xm = cs + 64;                                        // [4][32] each warp's -m of every row
-    auto wait_warp = [&](uint32_t b, uint32_t parity) -> bool {
-      bool ok = !*abort_flag && mbar_wait(b, parity, status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok && lane == 0) *abort_flag = 1;
-      return ok;
-    };
-    auto pair_stage = [&](uint32_t p) { return (2u * p) % static_cast<uint32_t>(SG); };
-    auto pair_phase = [&](uint32_t p) { return ((2u * p) / static_cast<uint32_t>(SG)) & 1u; };
-
-    if (warp == 4) {
-      // ---------------------------------------------------------- products
-      constexpr uint32_t kIdescS = umma_idesc_e4m3(128, kNS);
-      constexpr uint32_t kIdescO = umma_idesc_f16_mn(128, 64);
-      const uint64_t desc_q = umma_smem_desc(smem_u32(qtile), 1024, 1024);
-      const uint64_t desc_k = umma_smem_desc(stage_base, 1024, 1024);
-      const uint64_t desc_v = umma_smem_desc(smem_u32(v16), 16384, 1024);
-      const uint64_t desc_p = umma_smem_desc(smem_u32(pbuf), 16384, 1024);
-      uint32_t gp = 0, nq = 0;
-      bool stop = false;
-      for (uint32_t n = 0; !stop; ++n) {
-        Desc d;
-        if (!fetch_desc(n, d) || d.i < 0) break;
-        if (!d.it.ok) continue;
-        const int np = (d.it.t1 - d.it.t0 + 1) / 2;
-        if (!wait_warp(bar(tt::kQFull), nq & 1)) break;
-        tc_fence_after();
-        // Q K^T of pair jq once both its pages have landed (at most two
-        // ahead of P V: two score buffers), P V of pair jp once its P^T and
-        // V are written, whichever is ready first
-        int jq = 0, jp = 0;
-        unsigned long long idle_since = 0ull;
-        while (jp < np) {
-          bool did = false;
-          if (jp < jq) {
-            const uint32_t p = gp + jp, u = p % tt::kNB, uph = (p / tt::kNB) & 1u;
-            bool ready = mbar_test_wait(bar(tt::kPFull + u), uph) &&
-                         mbar_test_wait(bar(tt::kVFull + u), uph);
-            if (jp == 0 && nq > 0) ready = ready && mbar_test_wait(bar(tt::kOFree), (nq - 1) & 1);
-            if (__all_sync(0xffffffffu, ready)) {
-              tc_fence_after();
-              umma_pv_tt(tmem + 128, desc_v + u * (32768 >> 4), desc_p + u * (16384 >> 4), kIdescO,
-                         jp != 0, jp == np - 1, bar(tt::kPvDone + u), bar(tt::kOFinal));
-              ++jp;
-              did = true;
-            }
-          }
-          if (jq < np && jq - jp < 2) {
-            const uint32_t p = gp + jq, b = p & 1u, s0 = pair_stage(p), ph = pair_phase(p);
-            const bool ready = mbar_test_wait(smem_u32(&full[s0]), ph) &&
-                               mbar_test_wait(smem_u32(&full[s0 + 1]), ph);
-            if (__all_sync(0xffffffffu, ready)) {
-              tc_fence_after();
-              umma_qk_tt(tmem + 64u * b, desc_k + s0 * (T::kPageBytes >> 4), desc_q, kIdescS,
-                         bar(tt::kSFull + b), smem_u32(&empty[s0]), smem_u32(&empty[s0 + 1]),
-                         jq == np - 1, bar(tt::kQFree));
-              ++jq;
-              did = true;
-            }
-          }
-          if (did) {
-            idle_since = 0ull;
-            continue;
-          }
-          // nothing ready: bounded like every other wait of the kernel (lane
-          // 0 decides, so that the warp leaves the loop as one)
-          int give_up = 0;
-          if (lane == 0) {
-            const unsigned long long now = globaltimer_ns();
-            if (*abort_flag) {
-              give_up = 1;
-            } else if (idle_since == 0ull) {
-              idle_since = now;
-            } else if (now - idle_since > kWaitLimitNs) {
-              atomicOr(status, HPC_STATUS_WAIT_TIMEOUT);
-              *abort_flag = 1;
-              give_up = 1;
-            }
-          }
-          if (__shfl_sync(0xffffffffu, give_up, 0)) {
-            stop = true;
-            break;
-          }
-          // this warp shares its scheduler with a softmax warp: poll gently
-          __nanosleep(32);
-        }
-        if (stop) break;
-        gp += np;
-        ++nq;
-      }
-      // every product issued here has completed before TMEM is freed
-      umma_commit_elect(bar(tt::kDrain));
-      mbar_wait(bar(tt::kDrain), 0, status);
-      __syncwarp();
-    } else if (warp < 4) {
-      // ----------------------------------------------------------- softmax
-      const int w = warp;
-      const int kk = 32 * w + lane;                                   // key of a pair, d of O^T
-      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * w) << 16);   // this warp's lanes
-      uint32_t gp = 0, nq = 0;
-      bool stop = false;
-      for (uint32_t n = 0; !stop; ++n) {
-        Desc d;
-        if (!fetch_desc(n, d) || d.i < 0) break;
-        const Item it = d.it;
-        const int rows = q_len * kGroup;   // valid rows: 8 t + head for t < q_len
-        if (!it.ok) {   // no products: an empty partial
-          for (int r = 0; r < rows; ++r)
-            partial_o[((static_cast<int64_t>(d.i) * q_len + (r >> 3)) * kGroup + (r & 7)) * kD + kk] = 0.f;
-          if (w == 0 && lane < rows)
-            partial_lse[(static_cast<int64_t>(d.i) * q_len + (lane >> 3)) * kGroup + (lane & 7)] = -INFINITY;
-          continue;
-        }
-        const int np = (it.t1 - it.t0 + 1) / 2;
-        // the item's Q operand once the previous item's last Q K^T has read it:
-        // warp w writes rows 8w .. 8w+7, four lanes a row, 32 values a lane
-        if (nq > 0 && !wait_warp(bar(tt::kQFree), (nq - 1) & 1)) break;
-        {
-          const int r = 8 * w + (lane >> 2), qd = lane & 3;
-          const int tok = r >> 3;
-          const bool valid = tok < q_len;
-          const int64_t qr = (static_cast<int64_t>(it.seq) * q_len + (valid ? tok : 0)) * kHq +
-                             it.h * kGroup + (r & 7);
-          auto put = [&](int row, int c, uint4 v) {
-            *reinterpret_cast<uint4*>(qtile + row * 128 + ((c ^ (row & 7)) << 4)) = v;
-          };
-          if constexpr (kQ8) {
-            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-            if (valid) {
-              const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(q) + qr * kD) + 2 * qd;
-              a = src[0];
-              b = src[1];
-            }
-            put(r, 2 * qd, a);
-            put(r, 2 * qd + 1, b);
-            if (qd == 0) cs[r] = scale_log2;
-          } else {
-            // q = 2^-se (hi + lo): hi the row-scaled q rounded to E4M3, lo the
-            // remainder rounded to E4M3 (exact for every element within 2^10
-            // of the row's largest); se puts the row's largest in [2^7, 2^8)
-            float x[32];
-            if (valid) {
-              const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + qr * kD) + 4 * qd;
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint4 u = src[c];
-                x[8 * c + 0] = bf16_lo(u.x); x[8 * c + 1] = bf16_hi(u.x);
-                x[8 * c + 2] = bf16_lo(u.y); x[8 * c + 3] = bf16_hi(u.y);
-                x[8 * c + 4] = bf16_lo(u.z); x[8 * c + 5] = bf16_hi(u.z);
-                x[8 * c + 6] = bf16_lo(u.w); x[8 * c + 7] = bf16_hi(u.w);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) x[e] = 0.f;
-            }
-            float amax = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(x[e]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const int e2 = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 : 0;
-            const int se = 7 - max(e2, -119);   // in [-120, 126]
-            const float sc = __uint_as_float(static_cast<uint32_t>(127 + se) << 23);
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float a0 = x[e] * sc, a1 = x[e + 1] * sc, a2 = x[e + 2] * sc, a3 = x[e + 3] * sc;
-              const uint16_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
-              uint32_t f01 = e4m3x2_to_f16x2(h01), f23 = e4m3x2_to_f16x2(h23);
-              const float2 d01 = __half22float2(*reinterpret_cast<__half2*>(&f01));
-              const float2 d23 = __half22float2(*reinterpret_cast<__half2*>(&f23));
-              const uint16_t l01 = f32x2_to_e4m3x2(a0 - d01.x, a1 - d01.y);
-              const uint16_t l23 = f32x2_to_e4m3x2(a2 - d23.x, a3 - d23.y);
-              hi[e >> 2] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-              lo[e >> 2] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-            }
-            put(r, 2 * qd, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-            put(r, 2 * qd + 1, make_uint4(hi[4], hi[5], hi[6], hi[7]));
-            put(32 + r, 2 * qd, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-            put(32 + r, 2 * qd + 1, make_uint4(lo[4], lo[5], lo[6], lo[7]));
-            if (qd == 0) cs[r] = scale_log2 * __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(tt::kQFull));
-        }
-        // every row's scale is written once all four warps have arrived
-        if (!wait_warp(bar(tt::kQFull), nq & 1)) break;
-        float c[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) c[r] = cs[r];
-        const float c_l = cs[lane];
-        // row `lane`'s running maximum; this thread's key sums of every row
-        // (reduced over keys once, at the item's end)
-        float m_l = -INFINITY;
-        float lsp[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) lsp[r] = 0.f;
-        const int iend = min(it.len, it.t1 * kPage);   // keys of the item end here
-        int lim[4];                                    // last visible key of each token
-#pragma unroll
-        for (int t = 0; t < 4; ++t) lim[t] = t < q_len ? min(it.len - q_len + t, iend - 1) : -1;
-        for (int jj = 0; jj < np; ++jj) {
-          const uint32_t p = gp + jj, b = p & 1u, u = p % tt::kNB, uph = (p / tt::kNB) & 1u;
-          if (!wait_warp(bar(tt::kSFull + b), (p >> 1) & 1u)) {
-            stop = true;
-            break;
-          }
-          // the pair's page mask, published with its V
-          if (!wait_warp(bar(tt::kVFull + u), uph)) {
-            stop = true;
-            break;
-          }
-          const int pmask = pok[u];
-          tc_fence_after();
-          float v[32];
-          if constexpr (kQ8) {
-            uint32_t sr[32];
-            tmem_ld32(tl + 64u * b, sr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < 32; ++r) v[r] = __uint_as_float(sr[r]);
-          } else {
-            uint32_t sr[64];
-            tmem_ld64(tl + 64u * b, sr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < 32; r += 2)
-              f32x2_split(add_f32x2(f32x2(__uint_as_float(sr[r]), __uint_as_float(sr[r + 1])),
-                                    f32x2(__uint_as_float(sr[32 + r]), __uint_as_float(sr[33 + r]))),
-                          v[r], v[r + 1]);
-          }
-          // keys the rows do not see: past each token's position, past the
-          // item, on a page without data
-          // (a pair every row sees whole, the common case, needs none)
-          const int key0 = (it.t0 + 2 * jj) * kPage;
-          if (!(pmask == 3 && key0 + 2 * kPage - 1 <= lim[0])) {
-            const int key = key0 + kk;
-            const bool page_ok = ((pmask >> (kk >> 6)) & 1) != 0;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const bool vis = page_ok && key <= lim[t];
-#pragma unroll
-              for (int h = 0; h < 8; ++h) v[8 * t + h] = vis ? v[8 * t + h] : -INFINITY;
-            }
-          }
-          // the pair's row maxima: within the warp (one reduction a row), then
-          // over the four warps
-          float wm[32];
-#pragma unroll
-          for (int r = 0; r < 32; ++r) wm[r] = warp_max_f32(v[r]);
-          if (lane == 0) {
-            float4* dst = reinterpret_cast<float4*>(xred + (b * 4 + w) * 32);
-#pragma unroll
-            for (int r = 0; r < 32; r += 4) dst[r >> 2] = make_float4(wm[r], wm[r + 1], wm[r + 2], wm[r + 3]);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(tt::kXMax + b));
-          if (!wait_warp(bar(tt::kXMax + b), (p >> 1) & 1u)) {
-            stop = true;
-            break;
-          }
-          const float* xr = xred + b * 4 * 32;
-          const float mx = fmaxf(fmaxf(xr[lane], xr[32 + lane]), fmaxf(xr[64 + lane], xr[96 + lane])) * c_l;
-          // the running maximum moves only when it grows by more than 2^8
-          // (weights stay <= 2^8); O^T is then rescaled in TMEM
-          const bool grow = mx > m_l + 8.f;
-          const float alpha = grow ? exp2_ftz(m_l - mx) : 1.f;   // 0 while m_l = -inf
-          if (grow) m_l = mx;
-          if (jj > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll
-            for (int r = 0; r < 32; ++r) lsp[r] *= __shfl_sync(0xffffffffu, alpha, r);
-            // the previous pair's P V must be in O^T before it is rescaled
-            if (!wait_warp(bar(tt::kPvDone + (p - 1) % tt::kNB), ((p - 1) / tt::kNB) & 1u)) {
-              stop = true;
-              break;
-            }
-            tc_fence_after();
-            uint32_t ov[32];
-            tmem_ld32(tl + 128, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < 32; ++r)
-              ov[r] = __float_as_uint(__uint_as_float(ov[r]) * __shfl_sync(0xffffffffu, alpha, r));
-            tmem_st32(tl + 128, ov);
-            tmem_wait_st();
-          }
-          // this key's P^T row once the pair two back has been multiplied
-          if (p >= tt::kNB && !wait_warp(bar(tt::kPvDone + u), ((p - tt::kNB) / tt::kNB) & 1u)) {
-            stop = true;
-            break;
-          }
-          // every row's -m to every lane, through this warp's slot
-          xm[w * 32 + lane] = m_l == -INFINITY ? 0.f : -m_l;
-          __syncwarp();
-          float nm[32];
-#pragma unroll
-          for (int r = 0; r < 32; r += 4) {
-            const float4 t4 = *reinterpret_cast<const float4*>(xm + w * 32 + r);
-            nm[r] = t4.x;
-            nm[r + 1] = t4.y;
-            nm[r + 2] = t4.z;
-            nm[r + 3] = t4.w;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int r = 0; r < 32; r += 2) {
-            float a0, a1;
-            f32x2_split(fma_f32x2(f32x2(v[r], v[r + 1]), f32x2(c[r], c[r + 1]), f32x2(nm[r], nm[r + 1])),
-                        a0, a1);
-            const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
-            f32x2_split(add_f32x2(f32x2(lsp[r], lsp[r + 1]), f32x2(p0, p1)), lsp[r], lsp[r + 1]);
-            pk[r >> 1] = pack_f16(p0, p1);
-          }
-          uint8_t* prow = pbuf + u * 16384 + kk * 128;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(prow + ((cc ^ (kk & 7)) << 4)) =
-                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-          fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(tt::kPFull + u));
-        }
-        if (stop) break;
-        gp += np;
-        // the item's partial once its last P V is done: row sums over the
-        // four warps, then this warp's d quarter of every row
-        if (!wait_warp(bar(tt::kOFinal), nq & 1)) break;
-        xsum[w * 32 + lane] = warp_rows_reduce32<false>(lsp, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(tt::kXSum));
-        if (!wait_warp(bar(tt::kXSum), nq & 1)) break;
-        const float lt = xsum[lane] + xsum[32 + lane] + xsum[64 + lane] + xsum[96 + lane];
-        const float inv = lt > 0.f ? v_scale / lt : 0.f;
-        tc_fence_after();
-        uint32_t ov[32];
-        tmem_ld32(tl + 128, ov);
-        tmem_wait_ld();
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const float ir = __shfl_sync(0xffffffffu, inv, r);
-          if (r < rows)
-            partial_o[((static_cast<int64_t>(d.i) * q_len + (r >> 3)) * kGroup + (r & 7)) * kD + kk] =
-                __uint_as_float(ov[r]) * ir;
-        }
-        if (w == 0 && lane < rows)
-          partial_lse[(static_cast<int64_t>(d.i) * q_len + (lane >> 3)) * kGroup + (lane & 7)] =
-              lt > 0.f ? (m_l + log2f(lt)) * 0.6931471805599453f : -INFINITY;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(tt::kOFree));
-        ++nq;
-      }
-    } else if (warp == 5 || warp == 6) {
-      // ------------------------------------------------- V widening warps
-      // thread ct widens V row ct of both pages of a pair (zeros past the
-      // item or on a page without data) into the pair's F16 V buffer
-      const int ct = (warp - 5) * 32 + lane;
-      uint32_t gp = 0;
-      bool stop = false;
-      for (uint32_t n = 0; !stop; ++n) {
-        Desc d;
-        if (!fetch_desc(n, d) || d.i < 0) break;
-        if (!d.it.ok) continue;
-        const int np = (d.it.t1 - d.it.t0 + 1) / 2;
-        const int iend = min(d.it.len, d.it.t1 * kPage);
-        for (int jj = 0; jj < np; ++jj) {
-          const uint32_t p = gp + jj, u = p % tt::kNB, s0 = pair_stage(p), ph = pair_phase(p);
-          if (!wait_warp(smem_u32(&full[s0]), ph) || !wait_warp(smem_u32(&full[s0 + 1]), ph) ||
-              (p >= tt::kNB && !wait_warp(bar(tt::kPvDone + u), ((p - tt::kNB) / tt::kNB) & 1u))) {
-            stop = true;
-            break;
-          }
-          const int key0 = (d.it.t0 + 2 * jj) * kPage;
-          uint8_t* vb = v16 + u * 32768;
-          if (warp == 5 && lane == 0) pok[u] = (stage_ok[s0] != 0 ? 1 : 0) | (stage_ok[s0 + 1] != 0 ? 2 : 0);
-#pragma unroll
-          for (int pg = 0; pg < 2; ++pg) {
-            const int kr = 64 * pg + ct;
-            const bool live = stage_ok[s0 + pg] != 0 && key0 + kr < iend;
-            uint4 vw[8];
-            load_e4m3_row(smem + T::kOffStages + (SG + s0 + pg) * T::kPageBytes + ct * 128, ct, live, vw);
-            store_f16_row(vw, vb + kr * 128, vb + 16384 + kr * 128, kr);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(bar(tt::kVFull + u));
-            mbar_arrive(smem_u32(&empty[s0]));
-            mbar_arrive(smem_u32(&empty[s0 + 1]));
-          }
-        }
-        gp += (d.it.t1 - d.it.t0 + 1) / 2;
-      }
-    }
-    // every warp of the CTA meets here; then the allocating warp frees TMEM
-    tc_fence_before();
-    __syncwarp();
-    named_bar_sync(2, T::kThreads);
-    if (warp == kTmemWarp) {
-      tc_fence_after();
-      tmem_dealloc(tmem, kTmemCols);
-    }
-    return;
-  }
   if constexpr (kTC) {
     // ---------------------------------------------------- tensor-core form
     // Multi-token decode over BF16 pages on the 5th-generation tensor cores.
@@ -1661,7 +1087,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
     named_bar_sync(2, T::kThreads);
     if (warp == kTmemWarp) {
       tc_fence_after();
-      tmem_dealloc(tmem, kTmemCols);
+      tmem_dealloc(tmem, 512);
     }
     return;
   }
@@ -1985,10 +1411,9 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kForm>::kThreads, 1) decode_a
         // kMergeChunk items are taken chunk by chunk with an online rescale.
         constexpr int kMergeChunk = 512 / kQ;
         constexpr int kOuts = kQ * kGroup * kD / (4 * T::kGroupThreads);   // float4 outputs per thread
-        // (the transposed form never reaches this code; it has returned above)
-        static_assert(kTT || kMergeChunk * kQ * kGroup <= T::kWarpsPerGroup * kGroup * T::kOStride,
+        static_assert(kMergeChunk * kQ * kGroup <= T::kWarpsPerGroup * kGroup * T::kOStride,
                       "the lse staging area must fit in the queue's merge slices");
-        static_assert(kTT || kOuts * 4 * T::kGroupThreads == kQ * kGroup * kD, "outputs split evenly");
+        static_assert(kOuts * 4 * T::kGroupThreads == kQ * kGroup * kD, "outputs split evenly");
         float* lse_s = sm_o + w0 * kGroup * T::kOStride;
         const int i0 = seg_first;
         const int rows = q_len * kGroup;          // lse values per item
@@ -2082,10 +1507,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// experiment switch while the transposed form is measured against the other
-inline bool tt_enabled() { return std::getenv("HPC_EXPERIMENT_TT") != nullptr; }
-
-template <bool kFp8, int kQ, bool kQ8, int kForm = 0>
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
 cudaError_t ensure_smem_attr() {
   // once per device: the dynamic shared memory opt-in is a per-device setting
   static std::mutex mu;
@@ -2095,27 +1517,26 @@ cudaError_t ensure_smem_attr() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ, kQ8, kForm>,
+  e = cudaFuncSetAttribute(decode_attn_kernel<kFp8, kQ, kQ8, kTC>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           AttnTraits<kFp8, kForm>::kSmemBytes);
+                           AttnTraits<kFp8, kTC>::kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <bool kFp8, int kQ, bool kQ8, int kForm = 0>
+template <bool kFp8, int kQ, bool kQ8, bool kTC = false>
 int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int32_t num_blocks,
                 const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
                 int32_t batch, const hpc_attn_options& opts, const hpc_plan* plan,
                 float* partial_o, float* partial_lse, float sm_scale, int32_t* status,
                 unsigned long long* cta_clock, void* out, bool pdl, cudaStream_t stream) {
-  using T = AttnTraits<kFp8, kForm>;
-  constexpr bool kTensorForm = T::kTC || T::kTT;
+  using T = AttnTraits<kFp8, kTC>;
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
-  if (ensure_smem_attr<kFp8, kQ, kQ8, kForm>() != cudaSuccess) return HPC_ERR_CUDA;
-  // the tensor-core forms write every item's partial; the merge runs after them
-  void* fused_out = kTensorForm ? nullptr : out;
-  if (kTensorForm && cta_clock != nullptr) return HPC_ERR_UNSUPPORTED;
+  if (ensure_smem_attr<kFp8, kQ, kQ8, kTC>() != cudaSuccess) return HPC_ERR_CUDA;
+  // the tensor-core form writes every item's partial; the merge runs after it
+  void* fused_out = kTC ? nullptr : out;
+  if (kTC && cta_clock != nullptr) return HPC_ERR_UNSUPPORTED;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
                               static_cast<cuuint64_t>(num_blocks) * 2 * kHkv * kPage};
@@ -2139,7 +1560,7 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, decode_attn_kernel<kFp8, kQ, kQ8, kForm>, map, q, opts.q_scale, kv_scale, block_table,
+      &cfg, decode_attn_kernel<kFp8, kQ, kQ8, kTC>, map, q, opts.q_scale, kv_scale, block_table,
       max_blocks, num_blocks, seq_lens, batch, opts.q_len,
       static_cast<const hpc_work_item*>(plan->items),
       static_cast<const int32_t*>(plan->cta_ptr), static_cast<const int32_t*>(plan->home_end),
@@ -2147,7 +1568,7 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
       static_cast<const int32_t*>(plan->seg_ptr), plan->seg_done, fused_out, opts.out_dtype,
       pdl ? T::kL2PrefetchTiles : 0);
   if (e != cudaSuccess) return HPC_ERR_CUDA;
-  if (kTensorForm && out != nullptr)
+  if (kTC && out != nullptr)
     return hpc_merge_ex(partial_o, partial_lse, plan, batch, &opts, out, stream);
   return HPC_OK;
 }
@@ -2163,7 +1584,7 @@ int launch_attn_layout(const void* q, const void* kv_cache, int32_t kv_dtype, co
                        cudaStream_t stream) {
   if (kv_dtype == HPC_KV_BF16) {
     if constexpr (kQ == 4)
-      return launch_attn<false, kQ, false, 1>(q, kv_cache, kv_scale, num_blocks, block_table,
+      return launch_attn<false, kQ, false, true>(q, kv_cache, kv_scale, num_blocks, block_table,
                                                  max_blocks, seq_lens, batch, opts, plan,
                                                  partial_o, partial_lse, sm_scale, status,
                                                  cta_clock, out, pdl, stream);
@@ -2172,26 +1593,15 @@ int launch_attn_layout(const void* q, const void* kv_cache, int32_t kv_dtype, co
                                          sm_scale, status, cta_clock, out, pdl, stream);
   }
   if constexpr (kQ == 4) {
-    if (tt_enabled()) {
-      if (opts.q_dtype == HPC_Q_FP8_E4M3)
-        return launch_attn<true, kQ, true, 2>(q, kv_cache, kv_scale, num_blocks, block_table,
+    if (opts.q_dtype == HPC_Q_FP8_E4M3)
+      return launch_attn<true, kQ, true, true>(q, kv_cache, kv_scale, num_blocks, block_table,
+                                               max_blocks, seq_lens, batch, opts, plan, partial_o,
+                                               partial_lse, sm_scale, status, cta_clock, out, pdl,
+                                               stream);
+    return launch_attn<true, kQ, false, true>(q, kv_cache, kv_scale, num_blocks, block_table,
                                               max_blocks, seq_lens, batch, opts, plan, partial_o,
                                               partial_lse, sm_scale, status, cta_clock, out, pdl,
                                               stream);
-      return launch_attn<true, kQ, false, 2>(q, kv_cache, kv_scale, num_blocks, block_table,
-                                             max_blocks, seq_lens, batch, opts, plan, partial_o,
-                                             partial_lse, sm_scale, status, cta_clock, out, pdl,
-                                             stream);
-    }
-    if (opts.q_dtype == HPC_Q_FP8_E4M3)
-      return launch_attn<true, kQ, true, 1>(q, kv_cache, kv_scale, num_blocks, block_table,
-                                            max_blocks, seq_lens, batch, opts, plan, partial_o,
-                                            partial_lse, sm_scale, status, cta_clock, out, pdl,
-                                            stream);
-    return launch_attn<true, kQ, false, 1>(q, kv_cache, kv_scale, num_blocks, block_table,
-                                           max_blocks, seq_lens, batch, opts, plan, partial_o,
-                                           partial_lse, sm_scale, status, cta_clock, out, pdl,
-                                           stream);
   }
   if (opts.q_dtype == HPC_Q_FP8_E4M3)
     return launch_attn<true, kQ, true>(q, kv_cache, kv_scale, num_blocks, block_table, max_blocks,
