@@ -573,6 +573,16 @@ int hpc_prefill_attn_staged(const void* q, int32_t num_tokens, const int32_t* qu
 int hpc_selftest_wait_timeout(uint64_t limit_ns, int32_t* status, uint64_t* waited_ns,
                               cudaStream_t stream);
 
+/* Self-test of the bounded polling wait (no counterpart on the pages).  The
+ * tensor-core form of the 4-token attention layout has a warp that tests
+ * several barriers without blocking on any; when none is ready for the time
+ * limit (1 s) it gives up the same way: HPC_STATUS_WAIT_TIMEOUT, the CTA's
+ * abort flag, wind-down.  This call runs that polling loop over two mbarrier
+ * phases that never complete, with the given limit; arguments, results and
+ * errors as hpc_selftest_wait_timeout. */
+int hpc_selftest_poll_timeout(uint64_t limit_ns, int32_t* status, uint64_t* waited_ns,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

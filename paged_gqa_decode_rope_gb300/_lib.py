@@ -101,6 +101,7 @@ SIGNATURES = {
         _c_p, _c_i32, _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p,
         _c_i32, ctypes.c_float, _c_p, _c_i32, _c_p, _c_p, _c_p]),
     "hpc_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
+    "hpc_selftest_poll_timeout": (ctypes.c_int, [ctypes.c_uint64, _c_p, _c_p, _c_p]),
 }
 
 _lib = None

@@ -846,22 +846,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
             idle_since = 0ull;
             continue;
           }
-          // nothing ready: bounded like every other wait of the kernel (lane
-          // 0 decides, so that the warp leaves the loop as one)
-          int give_up = 0;
-          if (lane == 0) {
-            const unsigned long long now = globaltimer_ns();
-            if (*abort_flag) {
-              give_up = 1;
-            } else if (idle_since == 0ull) {
-              idle_since = now;
-            } else if (now - idle_since > kWaitLimitNs) {
-              atomicOr(status, HPC_STATUS_WAIT_TIMEOUT);
-              *abort_flag = 1;
-              give_up = 1;
-            }
-          }
-          if (__shfl_sync(0xffffffffu, give_up, 0)) {
+          // nothing ready: bounded like every other wait of the kernel
+          if (poll_give_up(idle_since, abort_flag, status, kWaitLimitNs)) {
             stop = true;
             break;
           }

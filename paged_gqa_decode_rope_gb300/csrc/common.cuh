@@ -78,6 +78,30 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One idle round of a warp's polling loop (a loop that tests several
+// barriers without blocking on any): lane 0 starts the clock on the first
+// idle round after progress (idle_since == 0) and gives up once limit_ns
+// has passed, recording HPC_STATUS_WAIT_TIMEOUT and raising the CTA's abort
+// flag; another warp's abort ends the loop too.  Returns the same answer in
+// every lane; the caller resets idle_since to 0 whenever it makes progress.
+__device__ __forceinline__ bool poll_give_up(unsigned long long& idle_since, volatile int* abort_flag,
+                                             int32_t* status, unsigned long long limit_ns) {
+  int give_up = 0;
+  if ((threadIdx.x & 31) == 0) {
+    const unsigned long long now = globaltimer_ns();
+    if (*abort_flag) {
+      give_up = 1;
+    } else if (idle_since == 0ull) {
+      idle_since = now;
+    } else if (now - idle_since > limit_ns) {
+      atomicOr(status, HPC_STATUS_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      give_up = 1;
+    }
+  }
+  return __shfl_sync(0xffffffffu, give_up, 0) != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most
 // kWaitLimitNs.  Returns false (after recording the timeout) if it did not.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,

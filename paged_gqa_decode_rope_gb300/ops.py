@@ -263,6 +263,16 @@ def selftest_wait_timeout(limit_ns, status, waited_ns=None):
         int(limit_ns), _p(status), _p(waited_ns), _stream()))
 
 
+def selftest_poll_timeout(limit_ns, status, waited_ns=None):
+    """Run the pipeline's bounded polling wait over phases that never complete
+    (see hpc_selftest_poll_timeout): sets HPC_STATUS_WAIT_TIMEOUT in ``status``."""
+    _want(status, "status", (torch.int32,), (1,))
+    if waited_ns is not None:
+        _want(waited_ns, "waited_ns", (torch.int64,), (1,))
+    check("hpc_selftest_poll_timeout", _lib.lib().hpc_selftest_poll_timeout(
+        int(limit_ns), _p(status), _p(waited_ns), _stream()))
+
+
 def decode_step(q, k, v, positions, cos_sin, q_norm_w, k_norm_w, kv_cache, kv_dtype, slot_mapping,
                 kv_scale, block_table, seq_lens, plan, partial_o, partial_lse, q_out, out, status,
                 min_tiles=1, eps=EPS, sm_scale=None):

@@ -175,3 +175,28 @@ def test_multi_token_step_end_to_end(kv):
         gu.compare(got[b], att, *_tol(kv), label="attention kv %d seq %d (L=%d)" % (kv, b, L))
         if kv == od.KV_BF16:
             gu.compare(got[b], want[0], *_tol(kv), label="step seq %d (L=%d)" % (b, L))
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("kv", [0, 1])
+@pytest.mark.parametrize("q_len", [3, 4])
+def test_multi_token_bad_block_is_reported_and_skipped(q_len, kv, fused):
+    """A block id past the cache (the 4-token layout's tensor-core form): the
+    status says BAD_BLOCK, the other sequences are exact to the oracle, and
+    the bad sequence's outputs stay finite."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=60 + q_len, lengths=[300, 200, 4097, 70], kv_dtype=kv,
+                  include_new_token=True)
+    wl.block_table[1, 2] = wl.num_blocks + 5          # tile 2 of sequence 1 points past the cache
+    q = _q(wl.batch, q_len, 70 + q_len)
+    step = ops.DecodeStepMT(wl.batch, q_len, kv, wl.max_blocks, fused=fused)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) & 1, "BAD_BLOCK"
+    got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got[1]))
+    for b in (0, 2, 3):
+        gu.compare(got[b], _oracle(wl, q, b), *_tol(kv), label="seq %d" % b)
