@@ -80,17 +80,18 @@ struct AttnTraits {
   static constexpr int kBoxBytes = 64 * 128;                  // one 64-row x 128-byte TMA box
   static constexpr int kTmaStageBytes = 2 * kPageBytes;       // K page + V page as loaded
   // a stage of the tensor-core form holds the tile as the products read it:
-  // F16 / BF16 K and V pages (an E4M3 tile is loaded into its first half and
-  // widened in place)
+  // BF16 K and V pages, or over E4M3 pages the K page of codes as it landed
+  // (Q K^T runs on E4M3 products) and the V page widened to F16 in place
   static constexpr int kF16Page = kPage * kD * 2;
-  static constexpr int kStageBytes = kTC ? 2 * kF16Page : kTmaStageBytes;
+  // (over E4M3 pages: the K page as landed, then V widened in place, 24 KB)
+  static constexpr int kStageBytes = kTC ? (kFp8 ? kPageBytes + kF16Page : 2 * kF16Page) : kTmaStageBytes;
   // A CTA hosts kGroups independent work queues.  A queue has its own producer
   // warp, stage ring, item ring and 4 consumer warps, and runs whole work
   // items, so one queue's epilogue and merge overlap the other queues'
   // streaming.  FP8 tiles carry a longer per-tile chain (the conversions) at
   // half the bytes, so FP8 keeps three queues in flight.
   static constexpr int kGroups = (kFp8 && !kTC) ? 3 : 2;
-  static constexpr int kGroupStages = 3;                      // stage ring of one queue
+  static constexpr int kGroupStages = (kTC && kFp8) ? 4 : 3;   // stage ring of one queue
   // tiles per queue pulled into L2 while a programmatic dependent launch
   // waits for the plan (about 29 MB in all on a 152-SM part)
   static constexpr int kL2PrefetchTiles = kFp8 ? 4 : 3;
@@ -100,9 +101,11 @@ struct AttnTraits {
   static constexpr int kGroupThreads = 32 * kWarpsPerGroup;
   static constexpr int kThreads = 32 * (kConsumerWarps + kGroups);   // + a producer warp per queue
   static constexpr int kOStride = kD + 4;                     // padded row of the merge buffer
-  // tensor-core form: per queue a 16 KB Q tile (two 64-column halves of 64
-  // rows; the M = 128 operand's rows past 64 read whatever follows, which the
-  // products ignore), ahead of the rings so that those rows stay in bounds
+  // tensor-core form: per queue a 16 KB Q tile of 64 rows (BF16 pages: two
+  // 64-column halves; E4M3 pages: the rows' leading E4M3 terms, then their
+  // remainders, 128 codes a row); the M = 128 operand's rows past 64 read
+  // whatever follows, which the products ignore, and the tiles sit ahead of
+  // the rings so that those rows stay in bounds
   static constexpr int kQtBytes = 16384;
   static constexpr int kOffQt = 0;
   static constexpr int kOffStages = kTC ? kGroups * kQtBytes : 0;
@@ -114,8 +117,8 @@ struct AttnTraits {
   static constexpr int kItemRing = 2;                         // items queued ahead, per queue
   // barriers of one queue: full[SG], empty[SG], item_full[R], item_empty[R], consumer barrier,
   // and for the tensor-core form s_full[2], p_full[2], q_full, q_free, o_final, o_free, drain,
-  // and over E4M3 pages conv_k[SG] and conv_v[SG] (the stage's K, V widened to F16)
-  static constexpr int kTcBars = kTC ? 9 + (kFp8 ? 2 * kGroupStages : 0) : 0;
+  // and over E4M3 pages conv_v[SG] (the stage's V widened to F16)
+  static constexpr int kTcBars = kTC ? 9 + (kFp8 ? kGroupStages : 0) : 0;
   static constexpr int kGroupBars = 2 * kGroupStages + 2 * kItemRing + 1 + kTcBars;
   static constexpr int kOffOk = kOffBar + kGroups * kGroupBars * 8;
   static constexpr int kOffRing = kOffOk + kStages * 4;
@@ -301,6 +304,37 @@ __device__ __forceinline__ void umma_qk_tile(uint32_t d, uint64_t q, uint64_t k,
 #undef HPC_DQK_STEP
 }
 
+// S = Q K^T over E4M3 pages on E4M3 products (kind::f8f6f4): four steps of 32
+// codes of each 128-byte swizzled row; with two_terms a second chain over
+// the remainder terms (q_lo, 8 KB after q) accumulates into the same S.
+// Then the commits of umma_qk_tile.
+__device__ __forceinline__ void umma_qk_tile_e4m3(uint32_t d, uint64_t q, uint64_t k, uint32_t idesc,
+                                                  uint32_t s_full, bool last, uint32_t q_free,
+                                                  bool two_terms) {
+#define HPC_EQK_STEP(QO, KO) \
+  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+#define HPC_EQK_LO(QO, KO) \
+  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
+  "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+  asm volatile(
+      "{\n\t.reg .pred e, f, g, pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 f, %5, 0, e;\n\t"
+      "setp.ne.and.b32 g, %7, 0, e;\n\t"
+      "setp.ne.b32 pf, %5, %5;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
+      HPC_EQK_STEP("2", "2") HPC_EQK_STEP("4", "4") HPC_EQK_STEP("6", "6")
+      HPC_EQK_LO("512", "0") HPC_EQK_LO("514", "2") HPC_EQK_LO("516", "4") HPC_EQK_LO("518", "6")
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+      ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free),
+        "r"(two_terms ? 1u : 0u)
+      : "memory");
+#undef HPC_EQK_STEP
+#undef HPC_EQK_LO
+}
+
 // One 128-code row of an E4M3 page (128-byte swizzled, as TMA lands it),
 // read into registers (zeros when !live), and written back as 128 F16 values
 // in two 128-byte swizzled rows, d 0..63 and 64..127 (the layout of a 16-bit
@@ -413,7 +447,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         mbar_init(smem_u32(&b[2 * SG + R + r]), kTC ? (kFp8 ? 4 : 2) : T::kWarpsPerGroup);
       }
       mbar_init(smem_u32(&b[2 * SG + 2 * R]), T::kGroupThreads);  // the queue's consumer barrier
-      for (int x = 0; x < T::kTcBars; ++x)   // conv_k, conv_v: one arrival per converter warp
+      for (int x = 0; x < T::kTcBars; ++x)   // conv_v: one arrival per converter warp
         mbar_init(smem_u32(&b[2 * SG + 2 * R + 1 + x]), x >= 9 ? 2 : 1);
     }
     *abort_flag = 0;
@@ -779,12 +813,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
 
     if (wq == 2) {
       // ------------------------------------------------ MMA warp of the queue
-      constexpr uint32_t kIdescS = kFp8 ? umma_idesc_f16(128, 64, false) : umma_idesc_bf16(128, 64, false);
+      constexpr uint32_t kIdescS = kFp8 ? umma_idesc_e4m3(128, 64) : umma_idesc_bf16(128, 64, false);
       constexpr uint32_t kIdescO = kFp8 ? umma_idesc_f16(128, 128, true) : umma_idesc_bf16(128, 128, true);
       constexpr uint64_t kStageStep = T::kStageBytes >> 4;
+      // V: the stage's second part (E4M3 pages: after the 8 KB K page of codes)
+      constexpr uint32_t kOffV = kFp8 ? T::kPageBytes : T::kF16Page;
       const uint64_t desc_q = umma_smem_desc(smem_u32(qtile), 1024, 1024);
       const uint64_t desc_k = umma_smem_desc(stage_base, 1024, 1024);
-      const uint64_t desc_v = umma_smem_desc(stage_base + T::kF16Page, T::kBoxBytes, 1024);
+      const uint64_t desc_v = umma_smem_desc(stage_base + kOffV, T::kBoxBytes, 1024);
       uint32_t gl = 0, nq = 0;   // tiles and items of the queue so far
       bool stop = false;
       for (uint32_t n = 0; !stop; ++n) {
@@ -804,7 +840,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           if (jp < jq) {
             const uint32_t gg = g + jp, st = gg % SG, pb = (gl + jp) & 1u;
             bool ready = mbar_test_wait(b_pfull + 8u * pb, ((gl + jp) >> 1) & 1u);
-            if (kFp8) ready = ready && mbar_test_wait(smem_u32(&tb[9 + SG + st]), (gg / SG) & 1);
+            if (kFp8) ready = ready && mbar_test_wait(smem_u32(&tb[9 + st]), (gg / SG) & 1);
             if (jp == 0 && nq > 0) ready = ready && mbar_test_wait(b_ofree, (nq - 1) & 1);
             if (__all_sync(0xffffffffu, ready)) {
               tc_fence_after();
@@ -816,9 +852,8 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           }
           if (jq < nt && jq - jp < 2) {
             const uint32_t gg = g + jq, st = gg % SG;
-            // the tile as the products read it: landed (BF16) or K widened (E4M3)
-            const bool ready = mbar_test_wait(kFp8 ? smem_u32(&tb[9 + st]) : smem_u32(&full[st]),
-                                              (gg / SG) & 1);
+            // Q K^T reads K as landed (E4M3 codes, or BF16)
+            const bool ready = mbar_test_wait(smem_u32(&full[st]), (gg / SG) & 1);
             if (__all_sync(0xffffffffu, ready)) {
               // V rows the products must not see (the cache may hold NaN
               // there): past the length on the sequence's last tile, all of a
@@ -836,8 +871,12 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
                 __syncwarp();
               }
               tc_fence_after();
-              umma_qk_tile(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
-                           b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree);
+              if constexpr (kFp8)
+                umma_qk_tile_e4m3(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
+                                  b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree, !kQ8);
+              else
+                umma_qk_tile(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
+                             b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree);
               ++jq;
               did = true;
             }
@@ -885,32 +924,74 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         const int nt = it.t1 - it.t0;
         // the item's Q rows, once the previous item's last Q K^T has read the tile
         if (nq > 0 && !wait_warp(b_qfree, (nq - 1) & 1)) break;
+        // this row's factor from raw scores to log2 units (over E4M3 pages with
+        // a BF16 q: divided by the row's power-of-two scale)
+        float c_row = scale_log2;
         {
-          // one row: 16 chunks of 8 values, d 0..63 then 64..127; over E4M3
-          // pages the products take F16, so a BF16 q is rounded to F16 and an
-          // E4M3 q widened (exactly)
           const int64_t qr = (static_cast<int64_t>(it.seq) * q_len + (valid ? tok : 0)) * kHq +
                              it.h * kGroup + hl;
+          if constexpr (!kFp8) {
+            // one row: 16 chunks of 8 BF16 values, d 0..63 then 64..127
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (valid) {
-              if constexpr (kQ8) {
-                const uint2 c8v = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(q) + qr * kD)[ch];
-                v = make_uint4(e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.x)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.x >> 16)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.y)),
-                               e4m3x2_to_f16x2(static_cast<uint16_t>(c8v.y >> 16)));
-              } else {
-                v = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + qr * kD)[ch];
-                if constexpr (kFp8)
-                  v = make_uint4(pack_f16(bf16_lo(v.x), bf16_hi(v.x)), pack_f16(bf16_lo(v.y), bf16_hi(v.y)),
-                                 pack_f16(bf16_lo(v.z), bf16_hi(v.z)), pack_f16(bf16_lo(v.w), bf16_hi(v.w)));
-              }
+            for (int ch = 0; ch < 16; ++ch) {
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (valid) v = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + qr * kD)[ch];
+              const int half = ch >> 3, c8 = ch & 7;
+              *reinterpret_cast<uint4*>(qtile + half * (T::kQtBytes / 2) + (row >> 3) * 1024 +
+                                        (row & 7) * 128 + ((c8 ^ (row & 7)) << 4)) = v;
             }
-            const int half = ch >> 3, c8 = ch & 7;
-            *reinterpret_cast<uint4*>(qtile + half * (T::kQtBytes / 2) + (row >> 3) * 1024 +
-                                      (row & 7) * 128 + ((c8 ^ (row & 7)) << 4)) = v;
+          } else if constexpr (kQ8) {
+            // one row of 128 codes: 8 chunks of 16
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (valid) v = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(q) + qr * kD)[ch];
+              *reinterpret_cast<uint4*>(qtile + (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) = v;
+            }
+          } else {
+            // q = 2^-se (hi + lo): hi the row-scaled q rounded to E4M3, lo the
+            // remainder rounded to E4M3, exact for every element within 2^10
+            // of the row's largest; se puts the row's largest in [2^7, 2^8).
+            // Leading terms in the tile's first 8 KB, remainders in its second.
+            uint4 w[16];
+            float amax = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) {
+              w[ch] = valid ? reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + qr * kD)[ch]
+                            : make_uint4(0u, 0u, 0u, 0u);
+              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w[ch].x)), fabsf(bf16_hi(w[ch].x))),
+                                       fmaxf(fabsf(bf16_lo(w[ch].y)), fabsf(bf16_hi(w[ch].y)))));
+              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w[ch].z)), fabsf(bf16_hi(w[ch].z))),
+                                       fmaxf(fabsf(bf16_lo(w[ch].w)), fabsf(bf16_hi(w[ch].w)))));
+            }
+            const int e2 = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127 : 0;
+            const int se = 7 - max(e2, -119);   // in [-120, 126]
+            const float sc = __uint_as_float(static_cast<uint32_t>(127 + se) << 23);
+            c_row = scale_log2 * __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
+            // codes of 4 values (a 32-bit word), leading term and remainder
+            auto split4 = [&](uint32_t u0, uint32_t u1, uint32_t& hi, uint32_t& lo) {
+              const float a0 = bf16_lo(u0) * sc, a1 = bf16_hi(u0) * sc;
+              const float a2 = bf16_lo(u1) * sc, a3 = bf16_hi(u1) * sc;
+              const uint16_t h01 = f32x2_to_e4m3x2(a0, a1), h23 = f32x2_to_e4m3x2(a2, a3);
+              uint32_t f01 = e4m3x2_to_f16x2(h01), f23 = e4m3x2_to_f16x2(h23);
+              const float2 d01 = __half22float2(*reinterpret_cast<__half2*>(&f01));
+              const float2 d23 = __half22float2(*reinterpret_cast<__half2*>(&f23));
+              const uint16_t l01 = f32x2_to_e4m3x2(a0 - d01.x, a1 - d01.y);
+              const uint16_t l23 = f32x2_to_e4m3x2(a2 - d23.x, a3 - d23.y);
+              hi = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
+              lo = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
+            };
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {   // 16 codes: BF16 chunks 2ch, 2ch+1
+              uint4 hi, lo;
+              split4(w[2 * ch].x, w[2 * ch].y, hi.x, lo.x);
+              split4(w[2 * ch].z, w[2 * ch].w, hi.y, lo.y);
+              split4(w[2 * ch + 1].x, w[2 * ch + 1].y, hi.z, lo.z);
+              split4(w[2 * ch + 1].z, w[2 * ch + 1].w, hi.w, lo.w);
+              const int off = (row >> 3) * 1024 + (row & 7) * 128 + ((ch ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(qtile + off) = hi;
+              *reinterpret_cast<uint4*>(qtile + T::kQtBytes / 2 + off) = lo;
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -946,8 +1027,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
 #pragma unroll
           for (int k = 8; k < 64; k += 2) m8[(k >> 1) & 7] = max3f(m8[(k >> 1) & 7], x[k], x[k + 1]);
           const float mx =
-              max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
-              scale_log2;
+              max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
           // the running maximum moves only when it grows by more than 2^8
           // (weights stay <= 2^8); the row's O is then rescaled in TMEM
           const bool grow = mx > m_used + 8.f;
@@ -978,7 +1058,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           // p = 2^(s scale - m): one packed FMA per pair and an exponential
           // each; the row sum in 4 independent chains of packed adds
           const float nms = m_used == -INFINITY ? 0.f : -m_used;
-          const uint64_t scale2 = f32x2(scale_log2, scale_log2), nms2 = f32x2(nms, nms);
+          const uint64_t scale2 = f32x2(c_row, c_row), nms2 = f32x2(nms, nms);
           uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
           uint32_t pk[32];
 #pragma unroll
@@ -1029,13 +1109,12 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
     if constexpr (kFp8) {
       if (wq != 2 && wq != grp) {
         // -------------------------------------------- converter warps of the queue
-        // Each landed E4M3 tile is widened to F16 in its own stage: thread ct
-        // reads raw K row ct and raw V row ct, writes K row ct in place (so
-        // that Q K^T can start), then V row ct into the stage's second half
-        // (zeros past the length or on a bad block).  The only bytes a
-        // thread's outputs share with codes still to read are its own rows
-        // (K's first half is its raw K row, K's second half its raw V row,
-        // both read before), so the widening needs no barrier.
+        // Each landed tile's V page is widened to F16 in its own stage (Q K^T
+        // reads the K codes as they landed): thread ct reads raw V row ct and
+        // writes F16 row ct, d 0..63 over the raw row itself and d 64..127
+        // into the stage's last 8 KB (zeros past the length or on a bad
+        // block).  A thread's output shares bytes only with its own raw row,
+        // read before, so the widening needs no barrier.
         const int ct = (wq == 3 ? 32 : 0) + lane;
         bool stop = false;
         for (uint32_t n = 0; !stop; ++n) {
@@ -1049,19 +1128,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
               stop = true;
               break;
             }
-            uint8_t* stg = smem + T::kOffStages + (grp * SG + st) * T::kStageBytes;
+            uint8_t* vst = smem + T::kOffStages + (grp * SG + st) * T::kStageBytes + T::kPageBytes;
             const int keep = stage_ok[st] ? min(kPage, d.it.len - (d.it.t0 + j) * kPage) : 0;
-            uint4 kw[8], vw[8];
-            load_e4m3_row(stg + ct * 128, ct, true, kw);
-            load_e4m3_row(stg + T::kPageBytes + ct * 128, ct, ct < keep, vw);
-            store_f16_row(kw, stg + ct * 128, stg + T::kBoxBytes + ct * 128, ct);
+            uint4 vw[8];
+            load_e4m3_row(vst + ct * 128, ct, ct < keep, vw);
+            store_f16_row(vw, vst + ct * 128, vst + T::kBoxBytes + ct * 128, ct);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tb[9 + st]));
-            store_f16_row(vw, stg + T::kF16Page + ct * 128, stg + T::kF16Page + T::kBoxBytes + ct * 128, ct);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tb[9 + SG + st]));
           }
           g += nt;
         }

@@ -330,6 +330,13 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n, bool b_mn) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (type code 0 in
+// both fields) and an F32 accumulator, M x N, both K-major: the same bits as
+// umma_idesc_f16(m, n, false), named for what it describes.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // tcgen05.commit by one elected thread of a converged warp.
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
