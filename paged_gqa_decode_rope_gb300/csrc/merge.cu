@@ -10,7 +10,8 @@
 // One CTA per (sequence, kv_head) segment and new token, 256 threads: warp r
 // handles query head 8h + r and each lane 4 consecutive elements, so every
 // partial row is one coalesced 512-byte read.  Items are combined in item
-// order (that is, tile order), which makes the output bit-reproducible.  With
+// order (that is, tile order), which makes the output bit-reproducible.  A
+// segment whose every partial is empty (lse = -inf) merges to zeros.  With
 // q_len new tokens per sequence the partial of item i for token j is row
 // (i*q_len + j)*8 + r, and the output row is (b*q_len + j)*64 + 8h + r.
 #include "common.cuh"
@@ -18,7 +19,7 @@
 namespace hpc {
 namespace {
 
-__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ partial_o,
+__global__ void __launch_bounds__(256, 4) merge_kernel(const float* __restrict__ partial_o,
                                                     const float* __restrict__ partial_lse,
                                                     const int32_t* __restrict__ seg_ptr,
                                                     int32_t capacity, int32_t q_len,
@@ -37,23 +38,43 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   if (i1 - i0 == 1) {
     acc = *reinterpret_cast<const float4*>(partial_o + prow(i0) * kD + d);
   } else if (i1 > i0) {
-    // both loops are unrolled so that several partials are in flight at once
-    // (a long sequence's segment holds tens of items)
-    float M = -INFINITY;
+    // The segment's log-sum-exps of this warp's head are staged in shared
+    // memory by one parallel load per chunk of kChunk items, so the maximum
+    // comes from shared memory and the weighted sum is one pass of
+    // independent partial loads (a long sequence's segment holds tens of
+    // items).  Chunks after the first rescale what came before (online).
+    constexpr int kChunk = 256;
+    __shared__ float lse_s[kGroup][kChunk];
+    const int lane = threadIdx.x & 31;
+    float M = -INFINITY, wsum = 0.f;
+    for (int c0 = i0; c0 < i1; c0 += kChunk) {
+      const int cn = min(kChunk, i1 - c0);
+      __syncwarp();   // the previous chunk's values are read
+      for (int k = lane; k < cn; k += 32) lse_s[r][k] = partial_lse[prow(c0 + k)];
+      __syncwarp();
+      float Mc = -INFINITY;
+      for (int k = 0; k < cn; ++k) Mc = fmaxf(Mc, lse_s[r][k]);
+      const float Mn = fmaxf(M, Mc);
+      if (Mn == -INFINITY) continue;   // nothing but empty partials so far
+      const float sc = M == -INFINITY ? 0.f : expf(M - Mn);
+      acc.x *= sc;
+      acc.y *= sc;
+      acc.z *= sc;
+      acc.w *= sc;
+      wsum *= sc;
 #pragma unroll 8
-    for (int i = i0; i < i1; ++i) M = fmaxf(M, partial_lse[prow(i)]);
-    if (M != -INFINITY) {
-      float wsum = 0.f;
-#pragma unroll 8
-      for (int i = i0; i < i1; ++i) {
-        const float w = expf(partial_lse[prow(i)] - M);
-        const float4 o = *reinterpret_cast<const float4*>(partial_o + prow(i) * kD + d);
+      for (int k = 0; k < cn; ++k) {
+        const float w = expf(lse_s[r][k] - Mn);
+        const float4 o = *reinterpret_cast<const float4*>(partial_o + prow(c0 + k) * kD + d);
         acc.x += w * o.x;
         acc.y += w * o.y;
         acc.z += w * o.z;
         acc.w += w * o.w;
         wsum += w;
       }
+      M = Mn;
+    }
+    if (wsum > 0.f) {
       const float inv = 1.0f / wsum;
       acc.x *= inv;
       acc.y *= inv;
