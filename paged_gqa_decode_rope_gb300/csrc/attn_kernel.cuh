@@ -57,7 +57,8 @@
 //    all new tokens; an MMA warp per queue issues the products of two tiles
 //    in flight, whichever is ready first.  E4M3 pages are widened to F16 in
 //    their stage by two converter warps (K first, so that Q K^T can start).
-//    Its partials are merged by the merge pass after the kernel.
+//    A segment of one item is written to the output directly; the other
+//    items' partials are combined by the merge pass after the kernel.
 //  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
 //    HPC_STATUS_WAIT_TIMEOUT and winds down, waiting for its own copies.
 #include <mutex>
@@ -302,37 +303,6 @@ __device__ __forceinline__ void umma_qk_tile(uint32_t d, uint64_t q, uint64_t k,
       ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free)
       : "memory");
 #undef HPC_DQK_STEP
-}
-
-// S = Q K^T over E4M3 pages on E4M3 products (kind::f8f6f4): four steps of 32
-// codes of each 128-byte swizzled row; with two_terms a second chain over
-// the remainder terms (q_lo, 8 KB after q) accumulates into the same S.
-// Then the commits of umma_qk_tile.
-__device__ __forceinline__ void umma_qk_tile_e4m3(uint32_t d, uint64_t q, uint64_t k, uint32_t idesc,
-                                                  uint32_t s_full, bool last, uint32_t q_free,
-                                                  bool two_terms) {
-#define HPC_EQK_STEP(QO, KO) \
-  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
-  "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
-#define HPC_EQK_LO(QO, KO) \
-  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
-  "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
-  asm volatile(
-      "{\n\t.reg .pred e, f, g, pf, pt;\n\t.reg .b64 a, b;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.and.b32 f, %5, 0, e;\n\t"
-      "setp.ne.and.b32 g, %7, 0, e;\n\t"
-      "setp.ne.b32 pf, %5, %5;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
-      HPC_EQK_STEP("2", "2") HPC_EQK_STEP("4", "4") HPC_EQK_STEP("6", "6")
-      HPC_EQK_LO("512", "0") HPC_EQK_LO("514", "2") HPC_EQK_LO("516", "4") HPC_EQK_LO("518", "6")
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
-      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
-      ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free),
-        "r"(two_terms ? 1u : 0u)
-      : "memory");
-#undef HPC_EQK_STEP
-#undef HPC_EQK_LO
 }
 
 // One 128-code row of an E4M3 page (128-byte swizzled, as TMA lands it),
@@ -872,8 +842,9 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
               }
               tc_fence_after();
               if constexpr (kFp8)
-                umma_qk_tile_e4m3(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
-                                  b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree, !kQ8);
+                umma_qk_e4m3(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
+                             b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree, !kQ8,
+                             (T::kQtBytes / 2) >> 4);
               else
                 umma_qk_tile(tq + 64u * ((gl + jq) & 1u), desc_q, desc_k + st * kStageStep, kIdescS,
                              b_sfull + 8u * ((gl + jq) & 1u), jq == nt - 1, b_qfree);
@@ -913,11 +884,22 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         const Item it = d.it;
         const bool valid = tok < q_len;
         const int64_t prow = (static_cast<int64_t>(d.i) * q_len + tok) * kGroup + hl;
-        if (!it.ok) {   // no products: an empty partial
+        // With the output given, a segment of one item is written to it
+        // directly (the merge pass after the kernel leaves such segments
+        // alone); other items write their partial.
+        const bool seg_known = it.seq >= 0 && it.seq < batch && it.h >= 0 && it.h < kHkv;
+        const int seg = seg_known ? it.seq * kHkv + it.h : 0;
+        const bool direct = fuse && seg_known && seg_ptr[seg + 1] - seg_ptr[seg] == 1;
+        const int64_t orow = ((static_cast<int64_t>(it.seq) * q_len + tok) * kHq + it.h * kGroup + hl) * kD;
+        if (!it.ok) {   // no products: an empty partial, or zeros
           if (valid) {
-            for (int e = 0; e < kD; e += 4)
-              *reinterpret_cast<float4*>(partial_o + prow * kD + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-            partial_lse[prow] = -INFINITY;
+            if (direct) {
+              for (int e = 0; e < kD; e += 4) store_out4(out, orow + e, 0.f, 0.f, 0.f, 0.f, out_dtype);
+            } else {
+              for (int e = 0; e < kD; e += 4)
+                *reinterpret_cast<float4*>(partial_o + prow * kD + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+              partial_lse[prow] = -INFINITY;
+            }
           }
           continue;
         }
@@ -1088,7 +1070,13 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           uint32_t ov[32];
           tmem_ld32(trow + 128 + 32 * qc, ov);
           tmem_wait_ld();
-          if (valid) {
+          if (valid && direct) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              store_out4(out, orow + 32 * qc + k, __uint_as_float(ov[k]) * inv,
+                         __uint_as_float(ov[k + 1]) * inv, __uint_as_float(ov[k + 2]) * inv,
+                         __uint_as_float(ov[k + 3]) * inv, out_dtype);
+          } else if (valid) {
 #pragma unroll
             for (int k = 0; k < 32; k += 4)
               *reinterpret_cast<float4*>(partial_o + prow * kD + 32 * qc + k) =
@@ -1096,7 +1084,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
                               __uint_as_float(ov[k + 2]) * inv, __uint_as_float(ov[k + 3]) * inv);
           }
         }
-        if (valid)
+        if (valid && !direct)
           partial_lse[prow] = lsum > 0.f ? (m_used + log2f(lsum)) * 0.6931471805599453f : -INFINITY;
         tc_fence_before();
         __syncwarp();
@@ -1594,8 +1582,9 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return HPC_ERR_CUDA;
   if (ensure_smem_attr<kFp8, kQ, kQ8, kTC>() != cudaSuccess) return HPC_ERR_CUDA;
-  // the tensor-core form writes every item's partial; the merge runs after it
-  void* fused_out = kTC ? nullptr : out;
+  // the tensor-core form writes single-item segments to the output and the
+  // other items' partials; the merge pass after it combines the latter
+  void* fused_out = out;
   if (kTC && cta_clock != nullptr) return HPC_ERR_UNSUPPORTED;
   CUtensorMap map;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD),
@@ -1629,7 +1618,7 @@ int launch_attn(const void* q, const void* kv_cache, const float* kv_scale, int3
       pdl ? T::kL2PrefetchTiles : 0);
   if (e != cudaSuccess) return HPC_ERR_CUDA;
   if (kTC && out != nullptr)
-    return hpc_merge_ex(partial_o, partial_lse, plan, batch, &opts, out, stream);
+    return launch_merge(partial_o, partial_lse, plan, batch, &opts, out, true, stream);
   return HPC_OK;
 }
 

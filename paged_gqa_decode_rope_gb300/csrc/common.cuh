@@ -337,6 +337,40 @@ __host__ __device__ constexpr uint32_t umma_idesc_e4m3(int m, int n) {
   return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// S = Q K^T on E4M3 products (kind::f8f6f4) with an M = 128 Q operand and an
+// N = 64 K operand, both K-major 128-byte swizzled rows of 128 codes: four
+// steps of 32 codes.  With two_terms a second chain over the remainder terms
+// (the Q operand lo_off 16-byte units further on) accumulates into the same
+// S.  Then commits: the score buffer's barrier, and at the unit's last tile
+// the Q operand's.
+__device__ __forceinline__ void umma_qk_e4m3(uint32_t d, uint64_t q, uint64_t k, uint32_t idesc,
+                                             uint32_t s_full, bool last, uint32_t q_free,
+                                             bool two_terms, uint32_t lo_off) {
+#define HPC_EQK_STEP(QO, KO) \
+  "add.s64 a, %1, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+#define HPC_EQK_LO(QO, KO) \
+  "add.s64 a, c, " QO ";\n\tadd.s64 b, %2, " KO ";\n\t" \
+  "@g tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, pt;\n\t"
+  asm volatile(
+      "{\n\t.reg .pred e, f, g, pf, pt;\n\t.reg .b64 a, b, c;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.b32 f, %5, 0, e;\n\t"
+      "setp.ne.and.b32 g, %7, 0, e;\n\t"
+      "setp.ne.b32 pf, %5, %5;\n\tsetp.eq.b32 pt, %5, %5;\n\t"
+      "cvt.u64.u32 c, %8;\n\tadd.s64 c, c, %1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
+      HPC_EQK_STEP("2", "2") HPC_EQK_STEP("4", "4") HPC_EQK_STEP("6", "6")
+      HPC_EQK_LO("0", "0") HPC_EQK_LO("2", "2") HPC_EQK_LO("4", "4") HPC_EQK_LO("6", "6")
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t"
+      "@f tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}"
+      ::"r"(d), "l"(q), "l"(k), "r"(idesc), "r"(s_full), "r"(last ? 1u : 0u), "r"(q_free),
+        "r"(two_terms ? 1u : 0u), "r"(lo_off)
+      : "memory");
+#undef HPC_EQK_STEP
+#undef HPC_EQK_LO
+}
+
 // tcgen05.commit by one elected thread of a converged warp.
 __device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"

@@ -28,6 +28,12 @@ int launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, co
 int launch_decode_attn_q2(HPC_LAYOUT_LAUNCH_ARGS);
 int launch_decode_attn_q4(HPC_LAYOUT_LAUNCH_ARGS);
 
+// hpc_merge_ex with its checks; skip_single leaves the output rows of
+// single-item segments alone (the attention kernel wrote them directly).
+int launch_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                 int32_t batch, const hpc_attn_options* opts, void* out, bool skip_single,
+                 cudaStream_t stream);
+
 // The single-token BF16 options: {1, HPC_Q_BF16, 1.0f, HPC_OUT_BF16}.
 inline hpc_attn_options default_attn_options() {
   hpc_attn_options o;

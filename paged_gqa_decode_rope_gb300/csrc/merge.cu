@@ -15,6 +15,7 @@
 // q_len new tokens per sequence the partial of item i for token j is row
 // (i*q_len + j)*8 + r, and the output row is (b*q_len + j)*64 + 8h + r.
 #include "common.cuh"
+#include "internal.h"
 
 namespace hpc {
 namespace {
@@ -23,7 +24,8 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const float* __restrict__
                                                     const float* __restrict__ partial_lse,
                                                     const int32_t* __restrict__ seg_ptr,
                                                     int32_t capacity, int32_t q_len,
-                                                    void* __restrict__ out, int32_t out_dtype) {
+                                                    void* __restrict__ out, int32_t out_dtype,
+                                                    bool skip_single) {
   const int s = blockIdx.x;            // segment = seq * 8 + kv_head
   const int j = blockIdx.y;            // new token
   const int r = threadIdx.x >> 5;      // query head within the group
@@ -33,6 +35,7 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const float* __restrict__
   const int64_t orow = (static_cast<int64_t>(s / kHkv) * q_len + j) * kHq + (s % kHkv) * kGroup + r;
   int i0 = seg_ptr[s], i1 = seg_ptr[s + 1];
   if (i0 < 0 || i1 < i0 || i1 > capacity) i1 = i0;   // a corrupt plan merges to zeros
+  if (skip_single && i1 - i0 == 1) return;            // written by the attention kernel
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (i1 - i0 == 1) {
@@ -95,9 +98,9 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const float* __restrict__
 }  // namespace
 }  // namespace hpc
 
-extern "C" int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
-                            int32_t batch, const hpc_attn_options* opts, void* out,
-                            cudaStream_t stream) {
+int hpc::launch_merge(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                      int32_t batch, const hpc_attn_options* opts, void* out, bool skip_single,
+                      cudaStream_t stream) {
   HPC_CHECK_ARG(partial_o && partial_lse && plan && plan->seg_ptr && out);
   hpc_attn_options o;
   o.q_len = 1;
@@ -112,8 +115,14 @@ extern "C" int hpc_merge_ex(const float* partial_o, const float* partial_lse, co
   if (batch == 0) return HPC_OK;
   if (static_cast<int64_t>(batch) * hpc::kHkv > 0x7fffffff) return HPC_ERR_UNSUPPORTED;
   hpc::merge_kernel<<<dim3(batch * hpc::kHkv, o.q_len), 256, 0, stream>>>(
-      partial_o, partial_lse, plan->seg_ptr, plan->capacity, o.q_len, out, o.out_dtype);
+      partial_o, partial_lse, plan->seg_ptr, plan->capacity, o.q_len, out, o.out_dtype, skip_single);
   return HPC_LAUNCH_STATUS();
+}
+
+extern "C" int hpc_merge_ex(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
+                            int32_t batch, const hpc_attn_options* opts, void* out,
+                            cudaStream_t stream) {
+  return hpc::launch_merge(partial_o, partial_lse, plan, batch, opts, out, false, stream);
 }
 
 extern "C" int hpc_merge_mt(const float* partial_o, const float* partial_lse, const hpc_plan* plan,
