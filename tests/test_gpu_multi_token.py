@@ -200,3 +200,32 @@ def test_multi_token_bad_block_is_reported_and_skipped(q_len, kv, fused):
     assert np.all(np.isfinite(got[1]))
     for b in (0, 2, 3):
         gu.compare(got[b], _oracle(wl, q, b), *_tol(kv), label="seq %d" % b)
+
+
+@pytest.mark.parametrize("q_len", [3, 4])
+def test_multi_token_e4m3_pages_wide_range_q(q_len):
+    """Over E4M3 pages the 4-token layout's Q K^T runs on E4M3 products, a BF16
+    q split per row into two E4M3 terms under a power-of-two row scale.  The
+    split is exact for elements within 2^10 of the row's largest and off by at
+    most 2^-17 of it below that.  Rows whose elements span 2^-20 .. 2^4 (and
+    whole rows of zeros) must still match the float64 oracle within the FP8
+    tolerance."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=80 + q_len, lengths=[300, 4097, 65, 1], kv_dtype=1,
+                  include_new_token=True)
+    rng = np.random.default_rng(90 + q_len)
+    mag = np.exp2(rng.uniform(-20.0, 4.0, size=(wl.batch, q_len, 64, 128)))
+    qf = rng.standard_normal((wl.batch, q_len, 64, 128)) * mag
+    qf[0, 0, 3, :] = 0.0                        # a row of zeros
+    q = torch.as_tensor(qf, dtype=torch.float32, device="cuda").to(torch.bfloat16)
+    step = ops.DecodeStepMT(wl.batch, q_len, 1, wl.max_blocks)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got))
+    for b in range(wl.batch):
+        gu.compare(got[b], _oracle(wl, q, b), *_tol(1), label="seq %d (L=%d)" % (b, wl.lengths[b]))
