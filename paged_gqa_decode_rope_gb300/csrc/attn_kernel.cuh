@@ -55,10 +55,13 @@
 //    tile a single Q K^T (N 64) into tensor memory, a softmax warp with one
 //    row per thread, and one P V (N 128, P read from tensor memory) serve
 //    all new tokens; an MMA warp per queue issues the products of two tiles
-//    in flight, whichever is ready first.  E4M3 pages are widened to F16 in
-//    their stage by two converter warps (K first, so that Q K^T can start).
-//    A segment of one item is written to the output directly; the other
-//    items' partials are combined by the merge pass after the kernel.
+//    in flight, whichever is ready first.  Over E4M3 pages Q K^T runs on
+//    E4M3 products (kind::f8f6f4) directly on the landed K codes, a BF16 q
+//    split per row into two E4M3 terms under a power-of-two row scale (exact
+//    for every element within 2^10 of the row's largest); two converter
+//    warps widen only the V page to F16, in place.  A segment of one item is
+//    written to the output directly; the other items' partials are combined
+//    by the merge pass after the kernel.
 //  * Every wait is bounded (kWaitLimitNs): a stuck pipeline records
 //    HPC_STATUS_WAIT_TIMEOUT and winds down, waiting for its own copies.
 #include <mutex>
