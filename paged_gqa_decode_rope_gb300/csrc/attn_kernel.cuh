@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
   const int home_stop = vq < num_queues ? home_end[vq] : 0;
 
   // tensor-core form: 512 TMEM columns, 256 per queue (scores 0 / 64, O 128),
-  // allocated by an idle warp, freed by it after every warp's final barrier
+  // allocated by warp 3, freed by it after every warp's final barrier
   constexpr int kTmemWarp = 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffFlags) + 1 + G;
   if constexpr (kTC) {
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
   };
   if constexpr (kTC) {
     // ---------------------------------------------------- tensor-core form
-    // Multi-token decode over BF16 pages on the 5th-generation tensor cores.
+    // Multi-token decode on the 5th-generation tensor cores.
     // The item's q_len x 8 query rows (row 8 t + head, zeros for t >= q_len)
     // are rows 32 k .. 32 k + 31 of queue k's M = 128 Q tile, so that queue
     // k's softmax warp is the one whose TMEM lanes those rows are (warp w
