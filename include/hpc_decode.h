@@ -391,15 +391,17 @@ int hpc_decode_step(const void* q, const void* k, const void* v, const int32_t* 
 int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas);
 
 /* The num_ctas to plan for when each sequence has q_len new tokens
- * (1 <= q_len <= HPC_MAX_Q_LEN): hpc_decode_num_ctas() except for E4M3 pages
- * with q_len 3 or 4, whose tensor-core form runs 2 queues per CTA (SMs x 2).
+ * (1 <= q_len <= HPC_MAX_Q_LEN) of the given q_dtype (HPC_Q_BF16 or
+ * HPC_Q_FP8_E4M3): hpc_decode_num_ctas() except for E4M3 pages with q_len 3
+ * or 4, or q_len 2 with an E4M3 q, which run the tensor-core form of the
+ * attention at 2 queues per CTA (SMs x 2).
  * Source: page "vLLM and Tencent Hunyuan upstream two HPC backends for NVIDIA
  * Hopper", "Why does dynamic scheduling matter for attention?" (work dealt to
  * compute units in proportion to length).  Writes *num_queues; returns
- * HPC_ERR_INVALID_ARG for a null pointer or q_len out of range,
+ * HPC_ERR_INVALID_ARG for a null pointer, q_len out of range or another q_dtype,
  * HPC_ERR_UNSUPPORTED for another kv_dtype, HPC_ERR_CUDA if the device cannot
  * be queried. */
-int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t* num_queues);
+int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t q_dtype, int32_t* num_queues);
 
 /* Items a length-proportional plan may need:
  * num_ctas * (1 + pool_chunks) + 8 * batch. */

@@ -73,7 +73,7 @@ SIGNATURES = {
         _c_p, _c_p, _c_p, _c_i32, _c_p, _c_i32, ctypes.POINTER(PlanParams), ctypes.POINTER(Plan),
         _c_p, _c_p, _c_p, _c_p, ctypes.c_float, _c_p, _c_p]),
     "hpc_decode_num_ctas": (ctypes.c_int, [_c_i32, ctypes.POINTER(_c_i32)]),
-    "hpc_decode_num_queues": (ctypes.c_int, [_c_i32, _c_i32, ctypes.POINTER(_c_i32)]),
+    "hpc_decode_num_queues": (ctypes.c_int, [_c_i32, _c_i32, _c_i32, ctypes.POINTER(_c_i32)]),
     "hpc_plan_capacity": (_c_i32, [_c_i32, _c_i32, _c_i32]),
     "hpc_decode_attn_mt": (ctypes.c_int, [
         _c_p, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_p, _c_i32, _c_i32, ctypes.POINTER(Plan),

@@ -20,7 +20,7 @@ int hpc::launch_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtyp
     return hpc::launch_attn_layout<1>(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
                                       max_blocks, seq_lens, batch, opts, plan, partial_o,
                                       partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
-  if (opts.q_len == 2)
+  if (opts.q_len == 2 && !hpc::uses_tensor_form(kv_dtype, opts.q_len, opts.q_dtype))
     return hpc::launch_decode_attn_q2(q, kv_cache, kv_dtype, kv_scale, num_blocks, block_table,
                                       max_blocks, seq_lens, batch, opts, plan, partial_o,
                                       partial_lse, sm_scale, status, cta_clock, out, pdl, stream);
@@ -82,10 +82,14 @@ extern "C" int hpc_decode_num_ctas(int32_t kv_dtype, int32_t* num_ctas) {
   return HPC_OK;
 }
 
-extern "C" int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t* num_queues) {
+extern "C" int hpc_decode_num_queues(int32_t kv_dtype, int32_t q_len, int32_t q_dtype,
+                                     int32_t* num_queues) {
   HPC_CHECK_ARG(num_queues != nullptr && q_len >= 1 && q_len <= HPC_MAX_Q_LEN);
-  // q_len 3 and 4 run the tensor-core form: two queues per CTA on both cache types
-  if (kv_dtype != HPC_KV_FP8_E4M3 || q_len < 3) return hpc_decode_num_ctas(kv_dtype, num_queues);
+  HPC_CHECK_ARG(q_dtype == HPC_Q_BF16 || q_dtype == HPC_Q_FP8_E4M3);
+  // the tensor-core form runs two queues per CTA on both cache types, like
+  // the BF16 cache's other layouts; the E4M3 cache's mma.sync layouts run three
+  if (kv_dtype != HPC_KV_FP8_E4M3 || !hpc::uses_tensor_form(kv_dtype, q_len, q_dtype))
+    return hpc_decode_num_ctas(kv_dtype, num_queues);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

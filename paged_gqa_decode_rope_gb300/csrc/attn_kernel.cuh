@@ -50,7 +50,9 @@
 //    order, so the result does not depend on which queue merges.
 //  * Tokens past a query's last visible key get p = 0 and their V entries
 //    are zeroed in registers (the cache may hold NaN there: 0 * NaN is NaN).
-//  * The 4-token layout (q_len 3, 4) runs the tensor-core form (kTC): its
+//  * The 4-token layout (q_len 3, 4; and q_len 2 with an E4M3 q on an E4M3
+//    cache, where the rows of the third and fourth tokens stay empty) runs
+//    the tensor-core form (kTC): its
 //    q_len x 8 query rows are one M = 128 tcgen05 operand, so per 64-token
 //    tile a single Q K^T (N 64) into tensor memory, a softmax warp with one
 //    row per thread, and one P V (N 128, P read from tensor memory) serve

@@ -34,6 +34,14 @@ int launch_merge(const float* partial_o, const float* partial_lse, const hpc_pla
                  int32_t batch, const hpc_attn_options* opts, void* out, bool skip_single,
                  cudaStream_t stream);
 
+// Whether the attention runs the tensor-core form (the 4-token layout's
+// kernel, two queues per CTA): every call with q_len 3 or 4, and q_len 2
+// with an E4M3 q on an E4M3 cache.  hpc_decode_num_queues and the dispatch
+// both follow it.
+inline bool uses_tensor_form(int32_t kv_dtype, int32_t q_len, int32_t q_dtype) {
+  return q_len >= 3 || (q_len == 2 && kv_dtype == HPC_KV_FP8_E4M3 && q_dtype == HPC_Q_FP8_E4M3);
+}
+
 // The single-token BF16 options: {1, HPC_Q_BF16, 1.0f, HPC_OUT_BF16}.
 inline hpc_attn_options default_attn_options() {
   hpc_attn_options o;

@@ -56,15 +56,17 @@ def _cache_dtypes(kv_dtype):
     raise ValueError("kv_dtype must be KV_BF16 (0) or KV_FP8 (1)")
 
 
-def num_ctas(kv_dtype=KV_BF16, q_len=1):
+def num_ctas(kv_dtype=KV_BF16, q_len=1, q_dtype=None):
     """Work queues of the persistent attention grid on the current device for
-    the KV dtype and the new tokens per sequence: the plan's num_ctas."""
+    the KV dtype, the new tokens per sequence and the q dtype: the plan's
+    num_ctas."""
     n = ctypes.c_int32(0)
-    if q_len == 1:
+    qd = Q_BF16 if q_dtype is None else int(q_dtype)
+    if q_len == 1 and qd == Q_BF16:
         check("hpc_decode_num_ctas", _lib.lib().hpc_decode_num_ctas(kv_dtype, ctypes.byref(n)))
     else:
         check("hpc_decode_num_queues",
-              _lib.lib().hpc_decode_num_queues(kv_dtype, int(q_len), ctypes.byref(n)))
+              _lib.lib().hpc_decode_num_queues(kv_dtype, int(q_len), qd, ctypes.byref(n)))
     return n.value
 
 
@@ -86,8 +88,8 @@ class DecodePlan:
 
     @classmethod
     def dynamic(cls, batch, device="cuda", n_ctas=None, kv_dtype=KV_BF16, pool_chunks=POOL_CHUNKS,
-                pool_min_tiles=POOL_MIN_TILES, q_len=1):
-        n_ctas = num_ctas(kv_dtype, q_len) if n_ctas is None else n_ctas
+                pool_min_tiles=POOL_MIN_TILES, q_len=1, q_dtype=None):
+        n_ctas = num_ctas(kv_dtype, q_len, q_dtype) if n_ctas is None else n_ctas
         cap = _lib.lib().hpc_plan_capacity(batch, n_ctas, pool_chunks)
         return cls(batch, n_ctas, cap, device, pool_chunks, pool_min_tiles)
 
@@ -579,7 +581,7 @@ class DecodeStepEx:
         self.q_len, self.q_dtype, self.q_scale, self.out_dtype = q_len, q_dtype, q_scale, out_dtype
         self.fused, self.min_tiles = fused, min_tiles
         self.plan = DecodePlan.dynamic(batch, device, n_ctas, kv_dtype, pool_chunks, pool_min_tiles,
-                                       q_len)
+                                       q_len, q_dtype)
         cap = max(self.plan.capacity, 1)
         self.partial_o = torch.empty((cap, q_len, HKV, D), dtype=torch.float32, device=device)
         self.partial_lse = torch.empty((cap, q_len, HKV), dtype=torch.float32, device=device)

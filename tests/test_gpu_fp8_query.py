@@ -33,7 +33,7 @@ def _oracle_mt(wl, qvals, b, heads=None):
 
 
 @pytest.mark.parametrize("fused", [True, False])
-@pytest.mark.parametrize("q_len", [1, 2, 4])
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4])
 def test_fp8_query_attention_matches_oracle(q_len, fused):
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
@@ -54,6 +54,49 @@ def test_fp8_query_attention_matches_oracle(q_len, fused):
     for b in range(wl.batch):
         gu.compare(got[b], _oracle_mt(wl, qvals, b), gu.TOL_FP8_MAX, None,
                    label="q_len %d seq %d (L=%d)" % (q_len, b, wl.lengths[b]))
+
+
+def test_fp8_query_queue_count_follows_the_form():
+    """An E4M3 q at q_len 2 on an E4M3 cache runs the tensor-core form (two
+    queues per CTA), a BF16 q at q_len 2 the 2-token mma.sync layout (three),
+    and q_len 3-4 the tensor-core form for both q types."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ops.num_ctas(od.KV_FP8, 2, ops.Q_FP8) == 2 * sms
+    assert ops.num_ctas(od.KV_FP8, 2, ops.Q_BF16) == 3 * sms
+    assert ops.num_ctas(od.KV_FP8, 1, ops.Q_FP8) == 3 * sms
+    for qn in (3, 4):
+        for qd in (ops.Q_BF16, ops.Q_FP8):
+            assert ops.num_ctas(od.KV_FP8, qn, qd) == 2 * sms
+    assert ops.num_ctas(od.KV_BF16, 2, ops.Q_BF16) == 2 * sms
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_fp8_query_bad_block_is_reported_and_skipped(q_len, fused):
+    """A block id past the cache under an E4M3 q (the tensor-core form): the
+    status says BAD_BLOCK, the other sequences match the oracle and the bad
+    sequence's outputs stay finite."""
+    gu.require_gpu()
+    from paged_gqa_decode_rope_gb300 import ops
+    from paged_gqa_decode_rope_gb300.workloads import Workload
+    wl = Workload("custom", seed=40 + q_len, lengths=[300, 200, 4097, 70], kv_dtype=od.KV_FP8,
+                  include_new_token=True)
+    wl.block_table[1, 2] = wl.num_blocks + 5          # tile 2 of sequence 1 points past the cache
+    codes, qs = _q_codes(wl.batch, q_len, 50 + q_len)
+    q = torch.as_tensor(codes, device="cuda")
+    qvals = od.decode_kv(codes, od.KV_FP8, qs)
+    step = ops.DecodeStepEx(wl.batch, od.KV_FP8, wl.max_blocks, q_len=q_len, q_dtype=ops.Q_FP8,
+                            q_scale=qs, fused=fused)
+    step.plan_step(wl.seq_lens)
+    out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) & 1, "BAD_BLOCK"
+    got = gu.bf16_host(out)
+    assert np.all(np.isfinite(got[1]))
+    for b in (0, 2, 3):
+        gu.compare(got[b], _oracle_mt(wl, qvals, b), gu.TOL_FP8_MAX, None, label="seq %d" % b)
 
 
 def test_fp8_query_full_mixed():
