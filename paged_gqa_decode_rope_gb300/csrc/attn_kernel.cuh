@@ -998,21 +998,23 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           tmem_wait_ld();
           const int key0 = (it.t0 + j) * kPage;
           const int lim = (valid && stage_ok[st]) ? min(kPage - 1, pos - key0) : -1;
-          float x[64];
-          if (__all_sync(0xffffffffu, lim == kPage - 1)) {
+          // the mask sets the scores past lim to -inf in place (a copy of
+          // the row would cost a move per score on the unmasked tiles)
+          if (!__all_sync(0xffffffffu, lim == kPage - 1)) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(sr[k]);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 64; ++k) x[k] = k <= lim ? __uint_as_float(sr[k]) : -INFINITY;
+            for (int k = 0; k < 64; ++k)
+              if (k > lim) sr[k] = 0xff800000u;
           }
-          // the row maximum in 8 independent chains of three-input maxima;
-          // the scale is positive, so it commutes with the maximum
+          const float* x = reinterpret_cast<const float*>(sr);
+          // the row maximum in 8 independent chains of three-input maxima,
+          // each started from a pair; the scale is positive, so it commutes
+          // with the maximum
           float m8[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = x[k];
-#pragma unroll
-          for (int k = 8; k < 64; k += 2) m8[(k >> 1) & 7] = max3f(m8[(k >> 1) & 7], x[k], x[k + 1]);
+          for (int k = 0; k < 64; k += 2) {
+            const int c = (k >> 1) & 7;
+            m8[c] = k < 16 ? fmaxf(x[k], x[k + 1]) : max3f(m8[c], x[k], x[k + 1]);
+          }
           const float mx =
               max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
           // the running maximum moves only when it grows by more than 2^8

@@ -548,24 +548,25 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         const bool tile_ok = tile_ok_of[s] != 0;
         const int key0 = j * kPage;
         // keys of this tile the row sees: 0 .. lim (none for lim < 0); only
-        // the tiles on a row's diagonal (or a bad tile) need the mask
+        // the tiles on a row's diagonal (or a bad tile) need the mask, which
+        // sets the other scores to -inf in place (a copy of the row would
+        // cost a move per score on the unmasked tiles)
         const int lim = (valid && tile_ok) ? min(63, pos - key0) : -1;
-        float x[64];
-        if (__all_sync(0xffffffffu, lim == 63)) {
+        if (!__all_sync(0xffffffffu, lim == 63)) {
 #pragma unroll
-          for (int jk = 0; jk < 64; ++jk) x[jk] = __uint_as_float(sr[jk]);
-        } else {
-#pragma unroll
-          for (int jk = 0; jk < 64; ++jk) x[jk] = jk <= lim ? __uint_as_float(sr[jk]) : -INFINITY;
+          for (int jk = 0; jk < 64; ++jk)
+            if (jk > lim) sr[jk] = 0xff800000u;
         }
         // the row maximum of the raw scores, three-input maxima in 8
-        // independent chains; the scale is positive, so it commutes with the
-        // maximum
+        // independent chains (each started from a pair); the scale is
+        // positive, so it commutes with the maximum
         float m8[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) m8[c] = x[c];
-#pragma unroll
-        for (int jk = 8; jk < 64; jk += 2) m8[(jk >> 1) & 7] = max3f(m8[(jk >> 1) & 7], x[jk], x[jk + 1]);
+        for (int jk = 0; jk < 64; jk += 2) {
+          const int c = (jk >> 1) & 7;
+          const float a = __uint_as_float(sr[jk]), b = __uint_as_float(sr[jk + 1]);
+          m8[c] = jk < 16 ? fmaxf(a, b) : max3f(m8[c], a, b);
+        }
         const float mx =
             max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
             scale_log2;
@@ -599,22 +600,26 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
         // p = 2^(s * scale - m) as one FMA and one exponential, packed as
         // BF16 (F16 for E4M3 caches) pairs over the scores; the row sum in 4
         // independent chains
-        const float nms = m_used == -INFINITY ? 0.f : -m_used;
-        const uint64_t scale2 = f32x2(scale_log2, scale_log2), nms2 = f32x2(nms, nms);
-        uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // pairs of row sums
-        uint32_t pk[32];
+        {
+          const float nms = m_used == -INFINITY ? 0.f : -m_used;
+          const uint64_t scale2 = f32x2(scale_log2, scale_log2), nms2 = f32x2(nms, nms);
+          uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};   // pairs of row sums
+          uint32_t pk[32];
 #pragma unroll
-        for (int jk = 0; jk < 32; ++jk) {
-          float a0, a1;
-          f32x2_split(fma_f32x2(f32x2(x[2 * jk], x[2 * jk + 1]), scale2, nms2), a0, a1);
-          const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
-          ps2[jk & 3] = add_f32x2(ps2[jk & 3], f32x2(p0, p1));
-          pk[jk] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+          for (int jk = 0; jk < 32; ++jk) {
+            float a0, a1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[2 * jk]), __uint_as_float(sr[2 * jk + 1])),
+                                  scale2, nms2),
+                        a0, a1);
+            const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
+            ps2[jk & 3] = add_f32x2(ps2[jk & 3], f32x2(p0, p1));
+            pk[jk] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+          }
+          tmem_st32(trow + 64 * (gl & 1), pk);
+          float s0, s1;
+          f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
+          lsum += s0 + s1;
         }
-        float s0, s1;
-        f32x2_split(add_f32x2(add_f32x2(ps2[0], ps2[1]), add_f32x2(ps2[2], ps2[3])), s0, s1);
-        lsum += s0 + s1;
-        tmem_st32(trow + 64 * (gl & 1), pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(tc::kBarPFull + 2 * l + (gl & 1)));

@@ -157,13 +157,15 @@ def test_prefill_bad_lengths_set_status_and_skip():
     _check(wl, q, qs, out, seqs=[1])
 
 
+@pytest.mark.parametrize("bad_page", [2, 3])
 @pytest.mark.parametrize("staged", [False, True])
 @pytest.mark.parametrize("kv_dtype", [0, 1])
-def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged):
+def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged, bad_page):
     """A block id past the cache: the status says BAD_BLOCK, the page's keys
     are left out of that sequence's attention, the other sequences are
     untouched (BF16 and E4M3 caches; E4M3 also through staged pages, where the
-    real block table still marks the tile)."""
+    real block table still marks the tile).  Pages 2 and 3 are the first and
+    the second page of a BF16 cache's 128-key tile."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     if staged and kv_dtype == 0:
@@ -171,7 +173,7 @@ def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged):
     lengths = [300, 260, 100]
     q_lens = [40, 70, 100]
     wl, q, qst, qs = _batch(lengths, q_lens, 17, kv_dtype)
-    wl.block_table[1, 2] = wl.num_blocks + 5           # page 2 (keys 128..191) of sequence 1
+    wl.block_table[1, bad_page] = wl.num_blocks + 5    # keys 64 p .. 64 p + 63 of sequence 1
     pf = ops.PrefillAttention(wl.batch, staging_pages=ops.PrefillAttention.pages_for(lengths)
                               if staged else 0)
     pf.plan(qst)
@@ -184,7 +186,7 @@ def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged):
     sub, row = gu.seq_view(wl.cache, wl.block_table_np[1], L, kv_dtype)
     ks, vs = [float(x) for x in wl.kv_scale.cpu().numpy()] if kv_dtype == 1 else (1.0, 1.0)
     qh = gu.bf16_host(q)[int(qs[1]):int(qs[2])]
-    keep = np.r_[0:128, 192:L]
+    keep = np.r_[0:64 * bad_page, 64 * bad_page + 64:L]
     want = np.zeros((n, 64, 128))
     for h in range(8):
         K, V = od.gather_kv(sub, row, L, h, kv_dtype, ks, vs)
@@ -194,7 +196,7 @@ def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged):
                 want[t, j] = od.attention_head(qh[t, j], K[vis], V[vis], 1.0 / np.sqrt(128))
     tol = (gu.TOL_BF16_MAX, gu.TOL_BF16_MEAN) if kv_dtype == 0 else (gu.TOL_FP8_MAX, None)
     gu.compare(out[int(qs[1]):int(qs[2])].float().cpu().numpy().astype(np.float64), want,
-               *tol, label="seq 1 without page 2")
+               *tol, label="seq 1 without page %d" % bad_page)
 
 
 def test_prefill_fp8_cache_prompts_and_chunks():
