@@ -164,8 +164,8 @@ def test_prefill_bad_block_is_reported_and_skipped(kv_dtype, staged, bad_page):
     """A block id past the cache: the status says BAD_BLOCK, the page's keys
     are left out of that sequence's attention, the other sequences are
     untouched (BF16 and E4M3 caches; E4M3 also through staged pages, where the
-    real block table still marks the tile).  Pages 2 and 3 are the first and
-    the second page of a BF16 cache's 128-key tile."""
+    real block table still marks the tile).  The bad page is page 2 or page 3
+    of sequence 1, an even and an odd page of its pages 0..4."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     if staged and kv_dtype == 0:
