@@ -1005,7 +1005,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
             for (int k = 0; k < 64; ++k)
               if (k > lim) sr[k] = 0xff800000u;
           }
-          const float* x = reinterpret_cast<const float*>(sr);
+          auto x = [&](int k) { return __uint_as_float(sr[k]); };
           // the row maximum in 8 independent chains of three-input maxima,
           // each started from a pair; the scale is positive, so it commutes
           // with the maximum
@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
 #pragma unroll
           for (int k = 0; k < 64; k += 2) {
             const int c = (k >> 1) & 7;
-            m8[c] = k < 16 ? fmaxf(x[k], x[k + 1]) : max3f(m8[c], x[k], x[k + 1]);
+            m8[c] = k < 16 ? fmaxf(x(k), x(k + 1)) : max3f(m8[c], x(k), x(k + 1));
           }
           const float mx =
               max3f(max3f(m8[0], m8[1], m8[2]), max3f(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * c_row;
@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
             float a0, a1;
-            f32x2_split(fma_f32x2(f32x2(x[2 * k], x[2 * k + 1]), scale2, nms2), a0, a1);
+            f32x2_split(fma_f32x2(f32x2(x(2 * k), x(2 * k + 1)), scale2, nms2), a0, a1);
             const float p0 = exp2_ftz(a0), p1 = exp2_ftz(a1);
             ps2[k & 3] = add_f32x2(ps2[k & 3], f32x2(p0, p1));
             pk[k] = kFp8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
