@@ -91,3 +91,9 @@ def test_host_argument_checks(lib):
     assert lib.hpc_selftest_wait_timeout(10, fake, NULL, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_selftest_wait_timeout(2 * 10 ** 9, fake, NULL, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_selftest_wait_timeout(10 ** 6, NULL, NULL, NULL) == HPC_ERR_INVALID_ARG
+    # the queue count for multi-token decode: q_len 1 .. 4, a q dtype it knows, a result slot
+    n = ctypes.c_int32(0)
+    assert lib.hpc_decode_num_queues(1, 0, 0, ctypes.byref(n)) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_num_queues(1, 5, 0, ctypes.byref(n)) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_num_queues(1, 2, 7, ctypes.byref(n)) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_decode_num_queues(1, 2, 1, NULL) == HPC_ERR_INVALID_ARG
