@@ -99,16 +99,19 @@ def test_fp8_query_bad_block_is_reported_and_skipped(q_len, fused):
         gu.compare(got[b], _oracle_mt(wl, qvals, b), gu.TOL_FP8_MAX, None, label="seq %d" % b)
 
 
-def test_fp8_query_full_mixed():
-    """The E4M3 q on the full mixed FP8 batch, sampled rows."""
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_fp8_query_full_mixed(q_len):
+    """The E4M3 q on the full mixed FP8 batch, sampled rows (q_len 2 runs the
+    tensor-core form)."""
     gu.require_gpu()
     from paged_gqa_decode_rope_gb300 import ops
     from paged_gqa_decode_rope_gb300.workloads import Workload
     wl = Workload("mixed_fp8", seed=4, include_new_token=True)
-    codes, qs = _q_codes(wl.batch, 1, 17)
+    codes, qs = _q_codes(wl.batch, q_len, 17 + q_len)
     q = torch.as_tensor(codes, device="cuda")
     qvals = od.decode_kv(codes, od.KV_FP8, qs)
-    step = ops.DecodeStepEx(wl.batch, od.KV_FP8, wl.max_blocks, q_dtype=ops.Q_FP8, q_scale=qs)
+    step = ops.DecodeStepEx(wl.batch, od.KV_FP8, wl.max_blocks, q_len=q_len, q_dtype=ops.Q_FP8,
+                            q_scale=qs)
     step.plan_step(wl.seq_lens)
     out = step.attend(q, wl.cache, wl.kv_scale, wl.block_table, wl.seq_lens)
     torch.cuda.synchronize()
