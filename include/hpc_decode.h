@@ -273,9 +273,13 @@ int hpc_decode_plan_static(const int32_t* seq_lens, int32_t batch, int32_t max_b
  *                seq_lens; its num_ctas queues set the grid.  A plan may be run any
  *                number of times, but launches that share one plan must not
  *                overlap on the GPU (they share its pool counters).
- *   partial_o    (device) float32 [plan->capacity, 8, 128], written per item
- *   partial_lse  (device) float32 [plan->capacity, 8], written per item
- * Errors: HPC_ERR_INVALID_ARG for null pointers or bad sizes;
+ *   partial_o    (device) float32 [plan->capacity, 8, 128], written per item,
+ *                16-byte aligned
+ *   partial_lse  (device) float32 [plan->capacity, 8], written per item,
+ *                16-byte aligned (both alignments hold for every call that
+ *                takes partial buffers: the attention writes and reads them,
+ *                and the merges read them, 16 bytes at a time)
+ * Errors: HPC_ERR_INVALID_ARG for null pointers, bad sizes or misaligned partials;
  * HPC_ERR_UNSUPPORTED for num_blocks > HPC_MAX_NUM_BLOCKS or unknown dtype. */
 int hpc_decode_attn(const void* q, const void* kv_cache, int32_t kv_dtype, const float* kv_scale,
                     int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,

@@ -1464,6 +1464,14 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         // by one parallel load, so the per-thread loop is a single pass of
         // independent float4 loads through L2; segments of more than
         // kMergeChunk items are taken chunk by chunk with an online rescale.
+        // With no next item the queue's stages hold nothing more, and the
+        // partials land there too, by cp.async (no registers held while in
+        // flight): a chunk of up to ring_items items is one round through L2
+        // instead of a few, which matters most for the merges of long
+        // segments, run after their queues' last items at the launch's end.
+        // Not in the 2-token layout over E4M3 pages, whose 128 registers
+        // would then spill in the streaming loop.
+        constexpr bool kRingMerge = !(kFp8 && kQ == 2);
         constexpr int kMergeChunk = 512 / kQ;
         constexpr int kOuts = kQ * kGroup * kD / (4 * T::kGroupThreads);   // float4 outputs per thread
         static_assert(kMergeChunk * kQ * kGroup <= T::kWarpsPerGroup * kGroup * T::kOStride,
@@ -1472,6 +1480,11 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         float* lse_s = sm_o + w0 * kGroup * T::kOStride;
         const int i0 = seg_first;
         const int rows = q_len * kGroup;          // lse values per item
+        const int item_floats = q_len * kGroup * kD;
+        const int ring_items = kRingMerge && nxt.i < 0 ? SG * T::kStageBytes / (item_floats * 4) : 0;
+        const int chunk = ring_items > 0 ? min(ring_items, kMergeChunk) : kMergeChunk;
+        const float* ring_o = reinterpret_cast<const float*>(smem + T::kOffStages +
+                                                             grp * SG * T::kStageBytes);
         float M[kOuts], W[kOuts];
         float4 acc[kOuts];
 #pragma unroll
@@ -1481,10 +1494,20 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
           acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         bool synced = true;
-        for (int base = 0; base < seg_items && synced; base += kMergeChunk) {
-          const int m = min(kMergeChunk, seg_items - base);
-          for (int x = gt; x < m * rows; x += T::kGroupThreads)
-            lse_s[x] = __ldcg(partial_lse + static_cast<int64_t>(i0 + base) * rows + x);
+        for (int base = 0; base < seg_items && synced; base += chunk) {
+          const int m = min(chunk, seg_items - base);
+          if (kRingMerge && ring_items > 0) {
+            const float* lsrc = partial_lse + static_cast<int64_t>(i0 + base) * rows;
+            for (int x = gt; x < m * rows / 4; x += T::kGroupThreads)
+              cp_async16_cg(smem_u32(lse_s) + 16 * x, lsrc + 4 * x);
+            const float* psrc = partial_o + static_cast<int64_t>(i0 + base) * item_floats;
+            for (int x = gt; x < m * item_floats / 4; x += T::kGroupThreads)
+              cp_async16_cg(stage_base + 16 * x, psrc + 4 * x);
+            cp_async_wait_all();
+          } else {
+            for (int x = gt; x < m * rows; x += T::kGroupThreads)
+              lse_s[x] = __ldcg(partial_lse + static_cast<int64_t>(i0 + base) * rows + x);
+          }
           if (!(synced = cons_sync())) break;
 #pragma unroll
           for (int u = 0; u < kOuts; ++u) {
@@ -1499,18 +1522,32 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
               const float sc = __expf(M[u] - Mn);   // 0 while M is still -inf
               acc[u].x *= sc; acc[u].y *= sc; acc[u].z *= sc; acc[u].w *= sc;
               W[u] *= sc;
-              const float* po =
-                  partial_o + (static_cast<int64_t>(i0 + base) * q_len + j) * kGroup * kD + e;
+              if (kRingMerge && ring_items > 0) {
+                const float* ro = ring_o + j * kGroup * kD + e;
 #pragma unroll 8
-              for (int k = 0; k < m; ++k) {
-                const float w = __expf(lse_s[k * rows + row_l] - Mn);
-                const float4 x = __ldcg(
-                    reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * q_len * kGroup * kD));
-                acc[u].x += w * x.x;
-                acc[u].y += w * x.y;
-                acc[u].z += w * x.z;
-                acc[u].w += w * x.w;
-                W[u] += w;
+                for (int k = 0; k < m; ++k) {
+                  const float w = __expf(lse_s[k * rows + row_l] - Mn);
+                  const float4 x = *reinterpret_cast<const float4*>(ro + k * item_floats);
+                  acc[u].x += w * x.x;
+                  acc[u].y += w * x.y;
+                  acc[u].z += w * x.z;
+                  acc[u].w += w * x.w;
+                  W[u] += w;
+                }
+              } else {
+                const float* po =
+                    partial_o + (static_cast<int64_t>(i0 + base) * q_len + j) * kGroup * kD + e;
+#pragma unroll 8
+                for (int k = 0; k < m; ++k) {
+                  const float w = __expf(lse_s[k * rows + row_l] - Mn);
+                  const float4 x = __ldcg(
+                      reinterpret_cast<const float4*>(po + static_cast<int64_t>(k) * q_len * kGroup * kD));
+                  acc[u].x += w * x.x;
+                  acc[u].y += w * x.y;
+                  acc[u].z += w * x.z;
+                  acc[u].w += w * x.w;
+                  W[u] += w;
+                }
               }
               M[u] = Mn;
             }
@@ -1680,6 +1717,9 @@ inline int check_attn_args(const void* q, const void* kv_cache, int32_t kv_dtype
                 plan->capacity >= 0);
   HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(kv_cache) & 15) == 0);
   HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(plan->items) & 15) == 0);
+  // partials are written and read 16 bytes at a time
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(partial_o) & 15) == 0 &&
+                (reinterpret_cast<uintptr_t>(partial_lse) & 15) == 0);
   if (out != nullptr) HPC_CHECK_ARG(plan->seg_ptr && plan->seg_done);
   if (kv_dtype == HPC_KV_FP8_E4M3) HPC_CHECK_ARG(kv_scale != nullptr);
   else if (kv_dtype != HPC_KV_BF16) return HPC_ERR_UNSUPPORTED;

@@ -294,6 +294,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// 16 bytes from global to shared memory, asynchronously and through L2 only
+// (data other SMs wrote during this launch); complete for this thread after
+// cp_async_wait_all, for the others after a barrier.
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Programmatic dependent launch: the primary grid lets its dependent grid be
 // scheduled early (trigger); the dependent waits for the primary grid to have
 // completed and its memory to be visible before touching its outputs (wait).

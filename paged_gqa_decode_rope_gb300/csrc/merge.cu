@@ -102,6 +102,7 @@ int hpc::launch_merge(const float* partial_o, const float* partial_lse, const hp
                       int32_t batch, const hpc_attn_options* opts, void* out, bool skip_single,
                       cudaStream_t stream) {
   HPC_CHECK_ARG(partial_o && partial_lse && plan && plan->seg_ptr && out);
+  HPC_CHECK_ARG((reinterpret_cast<uintptr_t>(partial_o) & 15) == 0);   // read 16 bytes at a time
   hpc_attn_options o;
   o.q_len = 1;
   o.q_dtype = HPC_Q_BF16;

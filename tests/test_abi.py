@@ -85,6 +85,14 @@ def test_host_argument_checks(lib):
     a[4] = 100
     a[2] = 3
     assert lib.hpc_decode_attn(*a) == HPC_ERR_UNSUPPORTED
+    # partial buffers not 16-byte aligned (they are written and read 16 bytes at a time)
+    a[2] = 0
+    for k in (10, 11):
+        b = list(a)
+        b[k] = ctypes.c_void_p(fake.value + 4)
+        assert lib.hpc_decode_attn(*b) == HPC_ERR_INVALID_ARG
+    assert lib.hpc_merge(ctypes.c_void_p(fake.value + 4), fake, ctypes.byref(plan), 4, fake,
+                         NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_merge(NULL, fake, ctypes.byref(plan), 4, fake, NULL) == HPC_ERR_INVALID_ARG
     assert lib.hpc_merge(fake, fake, ctypes.byref(plan), 0, fake, NULL) == 0
     # the wait self-test: limit outside 1 us .. 1 s, or no status word
