@@ -1449,13 +1449,12 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
     if (fuse && it.ok && !direct) {
       if (!cons_sync()) break;     // every thread's share of the partial is written
       if (gt == 0) {
-        __threadfence();           // the partial is visible device-wide before the count
-        const int done = atomicAdd(&seg_done[seg], 1);
+        // release: the queue's partial (ordered before by the barrier) is
+        // visible device-wide before the count; acquire: the last arrival
+        // sees every other item's partial
+        const int done = atomic_add_acq_rel_gpu(&seg_done[seg], 1);
         *merge_flag = done == seg_items - 1;
-        if (done == seg_items - 1) {
-          seg_done[seg] = 0;       // reset for the next run of this plan
-          __threadfence();
-        }
+        if (done == seg_items - 1) seg_done[seg] = 0;   // reset for the next run of this plan
       }
       if (!cons_sync()) break;
       if (*merge_flag) {

@@ -294,6 +294,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
+// Atomic add at GPU scope with acquire-release order: this thread's writes,
+// and those it has observed (the CTA's, after a barrier), are visible before
+// the add, and what other threads released before their adds is visible
+// after it.  Returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // 16 bytes from global to shared memory, asynchronously and through L2 only
 // (data other SMs wrote during this launch); complete for this thread after
 // cp_async_wait_all, for the others after a barrier.
