@@ -114,7 +114,12 @@ constexpr int kRingInts = 8;       // b, h, pair, ntiles lane 0, ntiles lane 1
 constexpr int kOffRing = kOffBar + kNumBars * 8;
 constexpr int kOffOk = kOffRing + 2 * kRingInts * 4;   // [4] producer stages, [2] F16 tiles
 constexpr int kOffMisc = kOffOk + 8 * 4;            // [0] abort flag, [1] TMEM address
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;    // + slack for the 1024-byte alignment
+// [8 softmax warps][32 rows][64 bytes]: one 32-column chunk of a warp's O rows
+// in a 16-bit output type, on its way to global memory
+constexpr int kEpiWarpBytes = 32 * 64;
+constexpr int kOffEpi = (kOffMisc + 16 + 127) / 128 * 128;
+constexpr int kSmemBytes = kOffEpi + 8 * kEpiWarpBytes + 1024;   // + slack for the 1024-byte alignment
+static_assert(kSmemBytes <= 227 * 1024, "the prefill layout exceeds a CTA's shared memory");
 constexpr uint32_t kTmemCols = 512;                 // lane l: S 256l + {0, 64}, O 256l + 128
 constexpr int kLaneTokens = 16;
 constexpr int kUnitTokens = 32;
@@ -630,19 +635,64 @@ __global__ void __launch_bounds__(tc::Cfg<kFp8>::kThreads, 1) prefill_tc_kernel(
       tc_fence_after();
       const float inv = lsum > 0.f ? v_scale / lsum : 0.f;
       const int64_t orow = (static_cast<int64_t>(qs + i) * kHq + head) * kD;
+      if (out_dtype == HPC_OUT_FP32) {
 #pragma unroll
-      for (int qc = 0; qc < 4; ++qc) {
-        uint32_t ov[32];
-        tmem_ld32(trow + 128 + 32 * qc, ov);
-        tmem_wait_ld();
-        if (valid) {
+        for (int qc = 0; qc < 4; ++qc) {
+          uint32_t ov[32];
+          tmem_ld32(trow + 128 + 32 * qc, ov);
+          tmem_wait_ld();
+          if (valid) {
 #pragma unroll
-          for (int jk = 0; jk < 32; jk += 8) {
-            float v8[8];
+            for (int jk = 0; jk < 32; jk += 8) {
+              float v8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(ov[jk + e]) * inv;
-            store_out8(out, orow + 32 * qc + jk, v8, out_dtype);
+              for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(ov[jk + e]) * inv;
+              store_out8(out, orow + 32 * qc + jk, v8, out_dtype);
+            }
           }
+        }
+      } else {
+        // 16-bit outputs: each 32-column chunk of the warp's 32 rows goes
+        // through shared memory, so that a store instruction writes 64
+        // contiguous bytes of each of 8 rows (a thread's own row, stored 16
+        // bytes at a time, would make every store 32 separate requests on
+        // this chain).  The 16-byte pieces of row r are rotated by (r / 2) % 4:
+        // both the row-wise writes and the piece-wise reads are free of bank
+        // conflicts.
+        const bool h16 = out_dtype == HPC_OUT_FP16;
+        uint8_t* ebuf = smem + tc::kOffEpi + warp * tc::kEpiWarpBytes;
+        const int rr0 = lane >> 2, pp = lane & 3;   // read side: rows 8 s + rr0, piece pp
+#pragma unroll
+        for (int qc = 0; qc < 4; ++qc) {
+          uint32_t ov[32];
+          tmem_ld32(trow + 128 + 32 * qc, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float a = __uint_as_float(ov[8 * pc + 2 * k]) * inv;
+              const float b = __uint_as_float(ov[8 * pc + 2 * k + 1]) * inv;
+              w[k] = h16 ? pack_f16(a, b) : pack_bf16(a, b);
+            }
+            *reinterpret_cast<uint4*>(ebuf + lane * 64 + 16 * (pc ^ ((lane >> 1) & 3))) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int st = 0; st < 4; ++st) {
+            const int rr = 8 * st + rr0;                         // the warp's row read here
+            const int rrow = (warp & 3) * 32 + rr;               // its row of the lane's tile
+            const int ri = d.pair * tc::kUnitTokens + l * tc::kLaneTokens + (rrow >> 3);
+            const uint4 v = *reinterpret_cast<const uint4*>(ebuf + rr * 64 + 16 * (pp ^ ((rr >> 1) & 3)));
+            if (ri < qlen) {
+              const int64_t o = (static_cast<int64_t>(qs + ri) * kHq + d.h * kGroup + (rrow & 7)) * kD +
+                                32 * qc + 8 * pp;
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = v;
+            }
+          }
+          __syncwarp();   // the chunk is read before the next one is written
         }
       }
       tc_fence_before();
