@@ -46,8 +46,10 @@
 //    softmax scale; P V stays f16.
 //  * With the merge fused in (out set), a segment of one item is written to
 //    the output directly; the queue that finishes the last item of a longer
-//    segment (a per-segment arrival counter) merges its partials in item
-//    order, so the result does not depend on which queue merges.
+//    segment (a per-segment arrival counter, one acquire-release atomic)
+//    merges its partials in item order, so the result does not depend on
+//    which queue merges.  A queue merging after its own last item lands the
+//    partials in its idle stages by cp.async first.
 //  * Tokens past a query's last visible key get p = 0 and their V entries
 //    are zeroed in registers (the cache may hold NaN there: 0 * NaN is NaN).
 //  * The 4-token layout (q_len 3, 4; and q_len 2 with an E4M3 q on an E4M3
