@@ -503,7 +503,16 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
     bool alive = true;
     int ticket = -1;         // lane 0: an unresolved pool claim (its counter value)
 
-    // home items, 32 at a time: lane j holds item hb_next - hb_cnt + j
+    // Home items in the order: the first, the last, then the others.  A
+    // range's first and last items are the pieces of segments it shares with
+    // the ranges before and after it, which run them first as well; so those
+    // segments' merges come early instead of at the end of the launch.
+    const int home_n = home_stop - home_begin;
+    auto home_index = [&](int p) {   // the item at position p of that order
+      return home_n >= 3 && p >= 1 ? (p == 1 ? home_stop - 1 : home_begin + p - 1) : home_begin + p;
+    };
+    // home items, 32 at a time: lane j holds the item at position
+    // hb_next - home_begin - hb_cnt + j
     int hb_next = home_begin, hb_cnt = 0, hb_pos = 0;
     int4 hw = make_int4(-1, -1, 0, 0);
     int hlen = -1;
@@ -513,7 +522,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
       hw = make_int4(-1, -1, 0, 0);
       hlen = -1;
       if (lane < hb_cnt) {
-        hw = items4[hb_next + lane];
+        hw = items4[home_index(hb_next - home_begin + lane)];
         hlen = (hw.x >= 0 && hw.x < batch) ? __ldg(seq_lens + hw.x) : -1;
       }
       hb_next += hb_cnt;
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(AttnTraits<kFp8, kTC>::kThreads, 1) decode_att
         if (hb_pos == hb_cnt && hb_next < home_stop) load_home_batch();
         if (hb_pos < hb_cnt) {
           Next n;
-          n.idx = hb_next - hb_cnt + hb_pos;
+          n.idx = home_index(hb_next - hb_cnt + hb_pos - home_begin);
           n.w.x = __shfl_sync(0xffffffffu, hw.x, hb_pos);
           n.w.y = __shfl_sync(0xffffffffu, hw.y, hb_pos);
           n.w.z = __shfl_sync(0xffffffffu, hw.z, hb_pos);
